@@ -1,0 +1,92 @@
+/*
+ * Oracle for the paged KV cache decode path -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded CPU restatement of what the pages describe:
+ *   - the bf16 and FP8-E4M3 number formats, from their definitions;
+ *   - the paged KV write (each new token's K/V scattered to its slot);
+ *   - paged decode attention, evaluated in fp64 by walking the block table;
+ *   - the host block pool: LRU free queue, ref_cnt, touch, reverse-order
+ *     free, chained SHA-256 block hashes, lazy eviction, preemption.
+ *
+ * Only the test suite, the smoke check and the CPU-baseline leg of the bench
+ * may load this library.  It shares no source, header, table or helper with
+ * the CUDA library, and its pool uses the pages' own block shape
+ * [2, block_size, num_kv_heads, head_dim] rather than the GPU pool layout.
+ *
+ * Return codes: 0 ok, 1 invalid argument, 2 out of blocks, 5 bad block id.
+ */
+#ifndef PAGEDKV_ORACLE_H
+#define PAGEDKV_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- number formats ------------------------------------------------------ */
+double  oracle_bf16_to_double(uint16_t bits);
+double  oracle_e4m3_to_double(uint8_t code);
+uint8_t oracle_e4m3_from_float(float x);                 /* RNE, saturate to +-448 */
+uint8_t oracle_e4m3_quantize(uint16_t bf16_bits, float scale); /* e4m3(float(x)/scale) */
+
+/* ---- host KV pool in the pages' block shape ----------------------------- */
+/* element (blk, kv, off, h, d) lives at ((((blk*2+kv)*BS+off)*Hkv+h)*D+d)  */
+typedef struct oracle_pool oracle_pool;
+oracle_pool* oracle_pool_create(int64_t num_blocks, int32_t block_size,
+                                int32_t n_kv_heads, int32_t head_dim,
+                                int32_t dtype /* 0 bf16, 1 e4m3 */);
+void     oracle_pool_destroy(oracle_pool* p);
+void*    oracle_pool_data(oracle_pool* p);
+uint64_t oracle_pool_bytes(const oracle_pool* p);
+int      oracle_pool_set_scales(oracle_pool* p, const float* k_scale, const float* v_scale);
+
+/* k, v: [T, Hkv, D] bf16 bits; slot < 0 = padded token (skipped). */
+int oracle_kv_write(oracle_pool* p, const uint16_t* k, const uint16_t* v,
+                    const int64_t* slot_mapping, int64_t num_tokens);
+
+/* q: [B, Hq, D] bf16 bits; block_tables: [B, max_blocks_per_seq];
+ * out: [B, Hq, D] float.  Only the sequences listed in `seqs` are computed
+ * (all of them when seqs == NULL).  window <= 0 disables the sliding window. */
+int oracle_paged_decode(const oracle_pool* p, const uint16_t* q, int32_t n_q_heads,
+                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* context_lens, int32_t batch,
+                        double scale, int32_t window,
+                        const int32_t* seqs, int32_t n_seqs, float* out);
+
+/* ---- SHA-256 (FIPS 180-4) ------------------------------------------------ */
+void oracle_sha256(const uint8_t* msg, uint64_t len, uint8_t digest[32]);
+
+/* ---- block pool bookkeeping --------------------------------------------- */
+typedef struct oracle_alloc oracle_alloc;
+oracle_alloc* oracle_alloc_create(int32_t num_blocks, int32_t block_size);
+void    oracle_alloc_destroy(oracle_alloc* a);
+/* Admit a request.  tokens may be NULL (content unknown: no prefix lookup and
+ * no hashes).  salt goes into block 0's hash only; extra into every block's. */
+int     oracle_alloc_admit(oracle_alloc* a, int64_t req_id, const int32_t* tokens,
+                           int64_t num_tokens, const uint8_t* salt, int32_t salt_len,
+                           const uint8_t* extra, int32_t extra_len,
+                           int64_t* cached_tokens);
+/* Grow a request by n tokens (tokens may be NULL). All-or-nothing. */
+int     oracle_alloc_append(oracle_alloc* a, int64_t req_id, const int32_t* tokens, int64_t n);
+int     oracle_alloc_free(oracle_alloc* a, int64_t req_id);
+int     oracle_alloc_preempt_newest(oracle_alloc* a, int64_t* req_id);
+int     oracle_alloc_table(const oracle_alloc* a, int64_t req_id, int32_t* out,
+                           int64_t cap, int64_t* n);
+int64_t oracle_alloc_num_tokens(const oracle_alloc* a, int64_t req_id);
+int32_t oracle_alloc_num_free(const oracle_alloc* a);
+int32_t oracle_alloc_free_queue(const oracle_alloc* a, int32_t* out, int32_t cap);
+int     oracle_alloc_block_info(const oracle_alloc* a, int32_t id, int32_t* ref_cnt,
+                                int32_t* has_hash, uint8_t hash[32]);
+int32_t oracle_alloc_lookup(const oracle_alloc* a, const uint8_t hash[32]);
+int32_t oracle_alloc_map_size(const oracle_alloc* a);
+int32_t oracle_alloc_map_entries(const oracle_alloc* a, uint8_t* hashes, int32_t* ids, int32_t cap);
+/* stats: [0] prefix queries (blocks looked up), [1] prefix hits (blocks),
+ *        [2] evictions, [3] preemptions, [4] running requests */
+void    oracle_alloc_stats(const oracle_alloc* a, int64_t out[5]);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
