@@ -1,0 +1,183 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) paged KV cache decode path.
+ *
+ * What it computes (sources by page title and section):
+ *  - "PagedAttention" (zhangchitc.github.io/posts/paged-attention), "What a
+ *    physical block looks like": one preallocated pool per layer, split into
+ *    num_blocks physical blocks of block_size tokens, each holding K and V for
+ *    every KV head.
+ *  - "Optimizing KV Cache Memory Management in vLLM with PagedAttention and
+ *    Dynamic Block Allocation":
+ *      "PagedAttention: Virtual Memory for LLMs" -- token i of a sequence is in
+ *      logical block floor(i / block_size) at offset i mod block_size; the
+ *      sequence's block table maps logical to physical blocks; the kernel
+ *      resolves K_i and V_i through the table.
+ *      "The Decode Phase" -- each step writes the new token's K/V into the
+ *      free slot of the last block; one query token per sequence attends.
+ *      "The Math of the KV Cache Bottleneck" -- GQA: several query heads per
+ *      KV head; BF16 (2 bytes) or FP8 (1 byte) elements.
+ *  - "How the block pool manages KV memory", "Hybrid models get groups": a
+ *    sliding-window layer needs only the blocks inside the last window.
+ *
+ * Conventions used by every call:
+ *  - Pointers named *_dev, and all tensor arguments, are DEVICE pointers on
+ *    the pool's device, owned by the caller, unless stated otherwise.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls that
+ *    take a stream are asynchronous: they validate their host-side arguments,
+ *    enqueue kernels and return.  Device-side problems (a table entry outside
+ *    [0, num_blocks), a slot outside the pool, a context length above the
+ *    bound, a wait that ran out) never trap: the kernel records them in the
+ *    pool's error word and skips the offending work; kv_pool_check_status()
+ *    reports and clears that word.
+ *  - A query attends to positions [lo, ctx) of its sequence, where ctx =
+ *    context_lens[b] counts the token written this step and lo = max(0, ctx -
+ *    sliding_window) when sliding_window > 0, else 0.  A sequence with ctx = 0
+ *    gets an all-zero output row.
+ *  - Pool layout (this library's, not the pages'): elements are stored as
+ *    [num_blocks][n_kv_heads][2 (K, V)][block_size][head_dim], head_dim
+ *    contiguous, so the K tile and the V tile of one (block, KV head) are one
+ *    contiguous run (8 KB for bf16, head_dim 128).  The base is 256-byte
+ *    aligned; every row is 16-byte aligned.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KV_OK = 0,
+  KV_ERR_INVALID_ARG = 1,   /* a host-side argument is out of range          */
+  KV_ERR_OOM = 2,           /* device memory allocation failed               */
+  KV_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed          */
+  KV_ERR_UNSUPPORTED = 4,   /* valid, but a shape this build does not cover  */
+  KV_ERR_BAD_BLOCK_ID = 5,  /* device: a block-table entry outside the pool  */
+  KV_ERR_TIMEOUT = 6,       /* device: a bounded wait on a copy ran out      */
+  KV_ERR_BAD_SLOT = 7,      /* device: a slot_mapping entry outside the pool */
+  KV_ERR_BAD_CONTEXT = 8    /* device: context_lens[b] < 0 or above a bound  */
+} kv_status;
+
+typedef enum { KV_BF16 = 0, KV_FP8_E4M3 = 1 } kv_dtype;
+
+typedef struct kv_pool kv_pool; /* opaque */
+
+typedef struct {
+  void* base_dev;         /* device address of element (0,0,0,0,0)                  */
+  int64_t num_blocks;
+  int32_t block_size, n_kv_heads, head_dim;
+  int32_t dtype;          /* kv_dtype                                                */
+  int64_t strides[5];     /* element strides of [num_blocks][Hkv][2][block_size][D]  */
+  uint64_t bytes;         /* total pool bytes                                        */
+  int32_t device;         /* CUDA device ordinal the pool lives on                   */
+  float* scales_dev;      /* fp8: device float[2 * Hkv], K scales then V scales      */
+} kv_pool_desc;
+
+/*
+ * kv_pool_create -- allocate one layer's block pool on the current device.
+ *   num_blocks > 0, block_size == 16, n_kv_heads >= 1, head_dim in {64, 128}
+ *   (FP8: head_dim 128).  The pool owns its memory (cudaMalloc here, cudaFree
+ *   in kv_pool_destroy); its contents start undefined.  FP8 scales start at
+ *   1.0.  Returns KV_ERR_INVALID_ARG / KV_ERR_UNSUPPORTED for bad shapes,
+ *   KV_ERR_OOM when the allocation fails, KV_ERR_CUDA when no device works.
+ */
+kv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_heads,
+                         int32_t head_dim, kv_dtype dtype, kv_pool** out);
+
+/* kv_pool_destroy -- synchronise the pool's device, free its memory and the handle. */
+kv_status kv_pool_destroy(kv_pool* pool);
+
+/* kv_pool_info -- describe the pool (a test or a framework can view its memory). */
+kv_status kv_pool_info(const kv_pool* pool, kv_pool_desc* out);
+
+/*
+ * kv_pool_set_scales -- FP8 pools: copy per-KV-head scales (device float[Hkv]
+ * each) into the pool, ordered on `stream`.  A stored FP8 code c of KV head h
+ * stands for c * k_scale[h] (K) or c * v_scale[h] (V); the write quantises
+ * x to E4M3(float(x) / scale) with round-to-nearest-even and saturation to
+ * +-448.  Scales must be finite and > 0 (not checked on the device).
+ */
+kv_status kv_pool_set_scales(kv_pool* pool, const float* k_scale_dev, const float* v_scale_dev,
+                             void* stream);
+
+/*
+ * paged_kv_write -- scatter new tokens' K/V into their slots ("The Decode
+ * Phase" / "The Prefill Phase": the kernel writes the computed states into
+ * the physical blocks).
+ *   k_dev, v_dev:        bf16 [num_tokens][n_kv_heads][head_dim], 16-byte aligned.
+ *   slot_mapping_dev:    int64 [num_tokens]; slot = physical_block * block_size
+ *                        + offset; slot < 0 marks a padded token (skipped);
+ *                        slot >= num_blocks * block_size sets KV_ERR_BAD_SLOT.
+ * BF16 pools receive a bit copy; FP8 pools the quantised codes.  Two tokens
+ * with the same slot in one call is undefined.  num_tokens == 0 is a no-op.
+ */
+kv_status paged_kv_write(kv_pool* pool, const void* k_dev, const void* v_dev,
+                         const int64_t* slot_mapping_dev, int64_t num_tokens, void* stream);
+
+/*
+ * paged_decode_workspace_bytes -- bytes of device scratch that
+ * paged_decode_attention needs for these sizes (split-K partial results).
+ * Depends on the pool's partition setting; 0 for invalid arguments.
+ */
+size_t paged_decode_workspace_bytes(const kv_pool* pool, int32_t batch, int32_t n_q_heads,
+                                    int32_t max_context_len, int32_t sliding_window);
+
+/*
+ * paged_decode_attention -- one decode step of attention over the pool.
+ *   q_dev:               bf16 [batch][n_q_heads][head_dim]; query head hq uses
+ *                        KV head hq / (n_q_heads / n_kv_heads); n_q_heads must
+ *                        be a multiple of n_kv_heads with a group of at most 8.
+ *   block_tables_dev:    int32 [batch][max_blocks_per_seq]; only entries of
+ *                        blocks holding an attended position are read.
+ *   context_lens_dev:    int32 [batch]; each in [0, max_context_len] and
+ *                        <= max_blocks_per_seq * block_size.
+ *   max_context_len:     host-side upper bound of context_lens (sizes the grid).
+ *   scale:               softmax scale applied to q.k.
+ *   sliding_window:      <= 0 disables the window.
+ *   out_dev:             fp32 [batch][n_q_heads][head_dim], softmax(scale q K^T) V.
+ *   workspace_dev:       at least paged_decode_workspace_bytes(...) bytes,
+ *                        16-byte aligned; contents need no initialisation.
+ * The split-K decode kernel and its reduce run on `stream` in order.  Calls
+ * that share a workspace must not overlap in time.
+ */
+kv_status paged_decode_attention(kv_pool* pool, const void* q_dev, int32_t n_q_heads,
+                                 const int32_t* block_tables_dev, int32_t max_blocks_per_seq,
+                                 const int32_t* context_lens_dev, int32_t batch,
+                                 int32_t max_context_len, float scale, int32_t sliding_window,
+                                 float* out_dev, void* workspace_dev, size_t workspace_bytes,
+                                 void* stream);
+
+/*
+ * kv_pool_set_partition_blocks -- split-K partition size, in blocks (a
+ * multiple of 4, 4..1024); 0 restores the automatic choice.  Tuning and tests
+ * only: results are the same for every setting up to rounding.
+ */
+kv_status kv_pool_set_partition_blocks(kv_pool* pool, int32_t blocks_per_partition);
+
+/*
+ * kv_pool_set_timing_events -- instrumentation: when both are non-NULL, each
+ * paged_decode_attention records `start_event` just before its split-K decode
+ * kernel and `stop_event` just after it (before the reduce), on its stream.
+ * The events (cudaEvent_t) stay owned by the caller; NULL, NULL turns it off.
+ */
+kv_status kv_pool_set_timing_events(kv_pool* pool, void* start_event, void* stop_event);
+
+/*
+ * kv_pool_check_status -- synchronise `stream`, read and clear the pool's
+ * device error word.  Returns KV_OK, or the first recorded problem in the
+ * order KV_ERR_TIMEOUT, KV_ERR_BAD_BLOCK_ID, KV_ERR_BAD_SLOT,
+ * KV_ERR_BAD_CONTEXT; KV_ERR_CUDA if the stream itself failed.
+ */
+kv_status kv_pool_check_status(kv_pool* pool, void* stream);
+
+/* kv_status_str -- static, human-readable name of a status code. */
+const char* kv_status_str(kv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

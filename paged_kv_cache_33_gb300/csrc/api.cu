@@ -1,0 +1,329 @@
+// C ABI of the paged KV cache decode path: pool lifetime, argument checks,
+// split-K planning and kernel launches.  Declarations and the contract of
+// every entry point are in include/pagedkv.h.
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s bound on any copy wait
+
+// Make the pool's device current for the duration of a call.
+struct DeviceGuard {
+  int prev = -1, want;
+  explicit DeviceGuard(int d) : want(d) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != want) cudaSetDevice(want);
+  }
+  ~DeviceGuard() {
+    if (prev >= 0 && prev != want) cudaSetDevice(prev);
+  }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// The pool as a 4-D tensor (D, BS, 2, NB*Hkv) with a box of one (block, head)
+// K+V pair: 64 bf16 columns (head_dim 128 takes two boxes) or 128 E4M3
+// columns, 16 token rows, both K and V; 128-byte swizzle in shared memory.
+bool encode_pool_map(kv_pool* p) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return false;
+  const uint64_t esz = p->dtype == KV_BF16 ? 2 : 1;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(p->head_dim),
+                        static_cast<cuuint64_t>(p->block_size), 2,
+                        static_cast<cuuint64_t>(p->num_blocks) * p->n_kv_heads};
+  cuuint64_t strides[3] = {p->head_dim * esz, p->block_size * p->head_dim * esz,
+                           2 * p->block_size * p->head_dim * esz};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(p->block_size),
+                       2, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(&p->tmap,
+                      p->dtype == KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                      4, p->base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int32_t blocks_for(int64_t tokens) { return static_cast<int32_t>((tokens + 15) / 16); }
+
+}  // namespace
+
+namespace pkv {
+
+DecodePlan plan_decode(const kv_pool* pool, int32_t batch, int32_t n_q_heads,
+                       int32_t max_context_len, int32_t sliding_window) {
+  DecodePlan plan{};
+  int32_t max_nblk = blocks_for(max_context_len);
+  if (sliding_window > 0) max_nblk = std::min(max_nblk, (sliding_window - 1) / 16 + 2);
+  int32_t pb = pool->partition_blocks;
+  if (pb <= 0) {
+    // Enough partitions to give every SM several CTAs over the whole grid,
+    // assuming the average sequence is about half the longest one.
+    const int64_t total_blocks = static_cast<int64_t>(batch) * pool->n_kv_heads *
+                                 std::max<int64_t>(1, max_nblk / 2);
+    const int64_t target_ctas = static_cast<int64_t>(std::max(pool->sm_count, 1)) * 8;
+    int64_t want = (total_blocks + target_ctas - 1) / target_ctas;
+    want = std::max<int64_t>(16, std::min<int64_t>(want, 128));
+    pb = static_cast<int32_t>((want + 3) / 4 * 4);
+  }
+  plan.part_blocks = pb;
+  plan.max_parts = std::max(1, (max_nblk + pb - 1) / pb);
+  if (plan.max_parts > 1) {
+    const size_t rows = static_cast<size_t>(batch) * n_q_heads * plan.max_parts;
+    plan.workspace_bytes = rows * pool->head_dim * sizeof(float) + rows * 2 * sizeof(float);
+  }
+  return plan;
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+const char* kv_status_str(kv_status s) {
+  switch (s) {
+    case KV_OK: return "KV_OK";
+    case KV_ERR_INVALID_ARG: return "KV_ERR_INVALID_ARG";
+    case KV_ERR_OOM: return "KV_ERR_OOM";
+    case KV_ERR_CUDA: return "KV_ERR_CUDA";
+    case KV_ERR_UNSUPPORTED: return "KV_ERR_UNSUPPORTED";
+    case KV_ERR_BAD_BLOCK_ID: return "KV_ERR_BAD_BLOCK_ID";
+    case KV_ERR_TIMEOUT: return "KV_ERR_TIMEOUT";
+    case KV_ERR_BAD_SLOT: return "KV_ERR_BAD_SLOT";
+    case KV_ERR_BAD_CONTEXT: return "KV_ERR_BAD_CONTEXT";
+  }
+  return "KV_ERR_UNKNOWN";
+}
+
+kv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_heads,
+                         int32_t head_dim, kv_dtype dtype, kv_pool** out) {
+  if (!out) return KV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (num_blocks <= 0 || n_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
+    return KV_ERR_INVALID_ARG;
+  if (dtype != KV_BF16 && dtype != KV_FP8_E4M3) return KV_ERR_INVALID_ARG;
+  if (block_size != 16) return KV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return KV_ERR_UNSUPPORTED;
+  if (dtype == KV_FP8_E4M3 && head_dim != 128) return KV_ERR_UNSUPPORTED;
+  if (num_blocks * n_kv_heads >= (int64_t(1) << 31)) return KV_ERR_UNSUPPORTED;
+
+  kv_pool* p = new (std::nothrow) kv_pool;
+  if (!p) return KV_ERR_OOM;
+  p->num_blocks = num_blocks;
+  p->block_size = block_size;
+  p->n_kv_heads = n_kv_heads;
+  p->head_dim = head_dim;
+  p->dtype = dtype;
+  const uint64_t esz = dtype == KV_BF16 ? 2 : 1;
+  p->bytes = static_cast<uint64_t>(num_blocks) * n_kv_heads * 2 * block_size * head_dim * esz;
+  if (cudaGetDevice(&p->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    delete p;
+    return KV_ERR_CUDA;
+  }
+  if (cudaMalloc(&p->base, p->bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete p;
+    return KV_ERR_OOM;
+  }
+  float ones[2 * 256];
+  const int ns = 2 * n_kv_heads;
+  bool ok = cudaMalloc(reinterpret_cast<void**>(&p->scales), ns * sizeof(float)) == cudaSuccess &&
+            cudaMalloc(reinterpret_cast<void**>(&p->err), sizeof(uint32_t)) == cudaSuccess;
+  if (ok) {
+    for (int i = 0; i < ns && i < 512; ++i) ones[i] = 1.0f;
+    for (int i = 0; i < ns && ok; i += 512)
+      ok = cudaMemcpy(p->scales + i, ones, std::min(512, ns - i) * sizeof(float),
+                      cudaMemcpyHostToDevice) == cudaSuccess;
+    ok = ok && cudaMemset(p->err, 0, sizeof(uint32_t)) == cudaSuccess;
+  }
+  ok = ok && encode_pool_map(p);
+  if (!ok) {
+    cudaGetLastError();
+    cudaFree(p->base);
+    cudaFree(p->scales);
+    cudaFree(p->err);
+    delete p;
+    return KV_ERR_CUDA;
+  }
+  *out = p;
+  return KV_OK;
+}
+
+kv_status kv_pool_destroy(kv_pool* p) {
+  if (!p) return KV_ERR_INVALID_ARG;
+  DeviceGuard guard(p->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  cudaFree(p->base);
+  cudaFree(p->scales);
+  cudaFree(p->err);
+  delete p;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+kv_status kv_pool_info(const kv_pool* p, kv_pool_desc* out) {
+  if (!p || !out) return KV_ERR_INVALID_ARG;
+  out->base_dev = p->base;
+  out->num_blocks = p->num_blocks;
+  out->block_size = p->block_size;
+  out->n_kv_heads = p->n_kv_heads;
+  out->head_dim = p->head_dim;
+  out->dtype = p->dtype;
+  out->strides[4] = 1;
+  out->strides[3] = p->head_dim;
+  out->strides[2] = static_cast<int64_t>(p->block_size) * p->head_dim;
+  out->strides[1] = 2 * out->strides[2];
+  out->strides[0] = static_cast<int64_t>(p->n_kv_heads) * out->strides[1];
+  out->bytes = p->bytes;
+  out->device = p->device;
+  out->scales_dev = p->scales;
+  return KV_OK;
+}
+
+kv_status kv_pool_set_scales(kv_pool* p, const float* k_scale, const float* v_scale,
+                             void* stream) {
+  if (!p || !k_scale || !v_scale) return KV_ERR_INVALID_ARG;
+  DeviceGuard guard(p->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t n = p->n_kv_heads * sizeof(float);
+  if (cudaMemcpyAsync(p->scales, k_scale, n, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(p->scales + p->n_kv_heads, v_scale, n, cudaMemcpyDeviceToDevice, s) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return KV_ERR_CUDA;
+  }
+  return KV_OK;
+}
+
+kv_status paged_kv_write(kv_pool* p, const void* k, const void* v, const int64_t* slots,
+                         int64_t num_tokens, void* stream) {
+  if (!p || num_tokens < 0) return KV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KV_OK;
+  if (!k || !v || !slots || !aligned16(k) || !aligned16(v)) return KV_ERR_INVALID_ARG;
+  if (num_tokens > (int64_t(1) << 40)) return KV_ERR_INVALID_ARG;
+  DeviceGuard guard(p->device);
+  cudaError_t e = pkv::launch_kv_write(p, k, v, slots, num_tokens, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+size_t paged_decode_workspace_bytes(const kv_pool* p, int32_t batch, int32_t n_q_heads,
+                                    int32_t max_context_len, int32_t sliding_window) {
+  if (!p || batch < 0 || n_q_heads <= 0 || max_context_len < 0) return 0;
+  return pkv::plan_decode(p, batch, n_q_heads, max_context_len, sliding_window).workspace_bytes;
+}
+
+kv_status paged_decode_attention(kv_pool* p, const void* q, int32_t n_q_heads,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* context_lens, int32_t batch,
+                                 int32_t max_context_len, float scale, int32_t sliding_window,
+                                 float* out, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  if (!p || batch < 0 || n_q_heads <= 0) return KV_ERR_INVALID_ARG;
+  if (n_q_heads % p->n_kv_heads != 0) return KV_ERR_INVALID_ARG;
+  const int32_t g = n_q_heads / p->n_kv_heads;
+  if (g > 8) return KV_ERR_UNSUPPORTED;
+  if (batch == 0) return KV_OK;
+  if (!q || !block_tables || !context_lens || !out || !aligned16(q)) return KV_ERR_INVALID_ARG;
+  if (max_blocks_per_seq <= 0 || max_context_len < 0 ||
+      static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * 16)
+    return KV_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return KV_ERR_INVALID_ARG;
+  if (batch > 65535 || p->n_kv_heads > 65535) return KV_ERR_UNSUPPORTED;
+
+  const pkv::DecodePlan plan = pkv::plan_decode(p, batch, n_q_heads, max_context_len, sliding_window);
+  if (plan.workspace_bytes > 0 &&
+      (!workspace || workspace_bytes < plan.workspace_bytes || !aligned16(workspace)))
+    return KV_ERR_INVALID_ARG;
+
+  pkv::DecodeParams d{};
+  d.q = q;
+  d.block_tables = block_tables;
+  d.context_lens = context_lens;
+  d.out = out;
+  const size_t rows = static_cast<size_t>(batch) * n_q_heads * plan.max_parts;
+  d.part_o = plan.workspace_bytes ? static_cast<float*>(workspace) : nullptr;
+  d.part_ml = plan.workspace_bytes ? d.part_o + rows * p->head_dim : nullptr;
+  d.err = p->err;
+  d.k_scale = p->scales;
+  d.v_scale = p->scales + p->n_kv_heads;
+  d.num_blocks = p->num_blocks;
+  d.mbs = max_blocks_per_seq;
+  d.batch = batch;
+  d.n_q_heads = n_q_heads;
+  d.n_kv_heads = p->n_kv_heads;
+  d.group = g;
+  d.max_ctx = max_context_len;
+  d.window = sliding_window > 0 ? sliding_window : 0;
+  d.part_blocks = plan.part_blocks;
+  d.max_parts = plan.max_parts;
+  d.scale_log2 = scale * 1.4426950408889634f;
+  d.wait_limit_ns = kWaitLimitNs;
+
+  DeviceGuard guard(p->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p->ev_start && cudaEventRecord(p->ev_start, s) != cudaSuccess) return KV_ERR_CUDA;
+  if (pkv::launch_decode(p, d, s) != cudaSuccess) return KV_ERR_CUDA;
+  if (p->ev_stop && cudaEventRecord(p->ev_stop, s) != cudaSuccess) return KV_ERR_CUDA;
+  if (plan.max_parts > 1 && pkv::launch_reduce(p, d, s) != cudaSuccess) return KV_ERR_CUDA;
+  return KV_OK;
+}
+
+kv_status kv_pool_set_partition_blocks(kv_pool* p, int32_t blocks_per_partition) {
+  if (!p) return KV_ERR_INVALID_ARG;
+  if (blocks_per_partition != 0 &&
+      (blocks_per_partition < 4 || blocks_per_partition > 1024 || blocks_per_partition % 4 != 0))
+    return KV_ERR_INVALID_ARG;
+  p->partition_blocks = blocks_per_partition;
+  return KV_OK;
+}
+
+kv_status kv_pool_set_timing_events(kv_pool* p, void* start_event, void* stop_event) {
+  if (!p || (!start_event) != (!stop_event)) return KV_ERR_INVALID_ARG;
+  p->ev_start = static_cast<cudaEvent_t>(start_event);
+  p->ev_stop = static_cast<cudaEvent_t>(stop_event);
+  return KV_OK;
+}
+
+kv_status kv_pool_check_status(kv_pool* p, void* stream) {
+  if (!p) return KV_ERR_INVALID_ARG;
+  DeviceGuard guard(p->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, p->err, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess ||
+      cudaMemsetAsync(p->err, 0, sizeof word, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return KV_ERR_CUDA;
+  }
+  if (word & pkv::kErrTimeout) return KV_ERR_TIMEOUT;
+  if (word & pkv::kErrBadBlock) return KV_ERR_BAD_BLOCK_ID;
+  if (word & pkv::kErrBadSlot) return KV_ERR_BAD_SLOT;
+  if (word & pkv::kErrBadContext) return KV_ERR_BAD_CONTEXT;
+  return KV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,126 @@
+// Paged KV write: scatter each new token's K and V rows into its slot.
+//
+// "Optimizing KV Cache Memory Management in vLLM with PagedAttention and
+// Dynamic Block Allocation", sections "The Prefill Phase" and "The Decode
+// Phase": the kernel writes the computed key/value states into the physical
+// blocks; in decode the new token goes to the free slot of the last block.
+// Slot s names physical block s / block_size and offset s mod block_size
+// (section "PagedAttention: Virtual Memory for LLMs").
+//
+// Pool layout: [num_blocks][Hkv][2][16][D], D contiguous.  One thread moves
+// 16 bytes of destination; consecutive threads cover one destination row, so
+// every store is a full, coalesced 16-byte vector.
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+// BF16 pool: bit copy.  Thread i handles chunk c of row (t, h, kv).
+template <int D>
+__global__ void __launch_bounds__(256) kv_write_bf16_kernel(
+    const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
+    int64_t num_tokens, int hkv, int64_t num_slots, uint4* __restrict__ pool,
+    uint32_t* __restrict__ err) {
+  constexpr int kChunks = D / 8;  // 16-byte chunks per row
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t total = num_tokens * hkv * 2 * kChunks;
+  if (i >= total) return;
+  const int c = static_cast<int>(i % kChunks);
+  int64_t rest = i / kChunks;
+  const int kv = static_cast<int>(rest % 2);
+  rest /= 2;
+  const int h = static_cast<int>(rest % hkv);
+  const int64_t t = rest / hkv;
+  const int64_t s = slots[t];
+  if (s < 0) return;
+  if (s >= num_slots) {
+    if (c == 0 && kv == 0 && h == 0) atomicOr(err, kErrBadSlot);
+    return;
+  }
+  const int64_t blk = s / kBlockSize;
+  const int off = static_cast<int>(s % kBlockSize);
+  const uint4 val = (kv ? v : k)[(t * hkv + h) * kChunks + c];
+  const int64_t row = ((blk * hkv + h) * 2 + kv) * kBlockSize + off;
+  pool[row * kChunks + c] = val;
+}
+
+// FP8 pool: code = E4M3(float(x) / scale[h]) with round-to-nearest-even and
+// saturation to +-448 (the cvt.rn.satfinite conversion).  Thread i makes 16
+// codes (one 16-byte store) from 16 bf16 inputs.
+template <int D>
+__global__ void __launch_bounds__(256) kv_write_fp8_kernel(
+    const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
+    int64_t num_tokens, int hkv, int64_t num_slots, const float* __restrict__ scales,
+    uint4* __restrict__ pool, uint32_t* __restrict__ err) {
+  constexpr int kChunks = D / 16;  // 16-code chunks per row
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t total = num_tokens * hkv * 2 * kChunks;
+  if (i >= total) return;
+  const int c = static_cast<int>(i % kChunks);
+  int64_t rest = i / kChunks;
+  const int kv = static_cast<int>(rest % 2);
+  rest /= 2;
+  const int h = static_cast<int>(rest % hkv);
+  const int64_t t = rest / hkv;
+  const int64_t s = slots[t];
+  if (s < 0) return;
+  if (s >= num_slots) {
+    if (c == 0 && kv == 0 && h == 0) atomicOr(err, kErrBadSlot);
+    return;
+  }
+  const float sc = scales[kv * hkv + h];
+  const uint4* src = (kv ? v : k) + ((t * hkv + h) * D) / 8 + 2 * c;
+  const uint4 x0 = src[0], x1 = src[1];
+  const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  uint32_t packed[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const uint32_t pair = w[2 * q + e];
+      const float a = __fdiv_rn(bf16_lo(pair), sc);
+      const float b = __fdiv_rn(bf16_hi(pair), sc);
+      const __nv_fp8x2_storage_t two =
+          __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+      word |= static_cast<uint32_t>(two) << (16 * e);
+    }
+    packed[q] = word;
+  }
+  const int64_t blk = s / kBlockSize;
+  const int off = static_cast<int>(s % kBlockSize);
+  const int64_t row = ((blk * hkv + h) * 2 + kv) * kBlockSize + off;
+  pool[row * kChunks + c] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
+
+}  // namespace
+
+cudaError_t launch_kv_write(const kv_pool* pool, const void* k, const void* v,
+                            const int64_t* slots, int64_t num_tokens, cudaStream_t stream) {
+  const int hkv = pool->n_kv_heads;
+  const int64_t num_slots = pool->num_blocks * pool->block_size;
+  const int threads = 256;
+  if (pool->dtype == KV_BF16) {
+    const int64_t total = num_tokens * hkv * 2 * (pool->head_dim / 8);
+    const int64_t blocks = (total + threads - 1) / threads;
+    if (pool->head_dim == 128)
+      kv_write_bf16_kernel<128><<<blocks, threads, 0, stream>>>(
+          static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, hkv,
+          num_slots, static_cast<uint4*>(pool->base), pool->err);
+    else
+      kv_write_bf16_kernel<64><<<blocks, threads, 0, stream>>>(
+          static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, hkv,
+          num_slots, static_cast<uint4*>(pool->base), pool->err);
+  } else {
+    const int64_t total = num_tokens * hkv * 2 * (pool->head_dim / 16);
+    const int64_t blocks = (total + threads - 1) / threads;
+    kv_write_fp8_kernel<128><<<blocks, threads, 0, stream>>>(
+        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, hkv,
+        num_slots, pool->scales, static_cast<uint4*>(pool->base), pool->err);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,252 @@
+"""ctypes binding of libpagedkv.so (include/pagedkv.h): argument marshalling only.
+
+Every computation runs in the library's CUDA kernels; this module checks
+tensor dtypes/devices, passes raw device pointers and the current torch
+stream, and raises KVError on a non-OK status.  There is no CPU fallback: if
+the library is missing or cannot load, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+KV_OK = 0
+STATUS = {0: "KV_OK", 1: "KV_ERR_INVALID_ARG", 2: "KV_ERR_OOM", 3: "KV_ERR_CUDA",
+          4: "KV_ERR_UNSUPPORTED", 5: "KV_ERR_BAD_BLOCK_ID", 6: "KV_ERR_TIMEOUT",
+          7: "KV_ERR_BAD_SLOT", 8: "KV_ERR_BAD_CONTEXT"}
+DTYPES = {"bf16": 0, "fp8": 1}
+
+LIB_PATH = _build.LIB_PATH
+
+
+class KVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [("base_dev", ctypes.c_void_p), ("num_blocks", ctypes.c_int64),
+                ("block_size", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("strides", ctypes.c_int64 * 5), ("bytes", ctypes.c_uint64),
+                ("device", ctypes.c_int32), ("scales_dev", ctypes.c_void_p)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load() -> ctypes.CDLL:
+    """Load libpagedkv.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if _build.stale():
+            _build.build()
+        L = ctypes.CDLL(LIB_PATH)
+        c, P = ctypes, ctypes.c_void_p
+        sig = {
+            "kv_pool_create": (c.c_int, [c.c_int64, c.c_int32, c.c_int32, c.c_int32, c.c_int,
+                                         c.POINTER(P)]),
+            "kv_pool_destroy": (c.c_int, [P]),
+            "kv_pool_info": (c.c_int, [P, c.POINTER(_Desc)]),
+            "kv_pool_set_scales": (c.c_int, [P, P, P, P]),
+            "paged_kv_write": (c.c_int, [P, P, P, P, c.c_int64, P]),
+            "paged_decode_workspace_bytes": (c.c_size_t, [P, c.c_int32, c.c_int32, c.c_int32,
+                                                          c.c_int32]),
+            "paged_decode_attention": (c.c_int, [P, P, c.c_int32, P, c.c_int32, P, c.c_int32,
+                                                 c.c_int32, c.c_float, c.c_int32, P, P,
+                                                 c.c_size_t, P]),
+            "kv_pool_set_partition_blocks": (c.c_int, [P, c.c_int32]),
+            "kv_pool_set_timing_events": (c.c_int, [P, P, P]),
+            "kv_pool_check_status": (c.c_int, [P, P]),
+            "kv_status_str": (c.c_char_p, [c.c_int]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _lib = L
+        return L
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != KV_OK:
+        raise KVError(rc, where)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, dtype: torch.dtype, name: str) -> ctypes.c_void_p:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+class KVPool:
+    """One layer's block pool on the current CUDA device (owns its memory)."""
+
+    def __init__(self, num_blocks: int, block_size: int, n_kv_heads: int, head_dim: int,
+                 dtype: str = "bf16"):
+        L = load()
+        h = ctypes.c_void_p()
+        _check(L.kv_pool_create(int(num_blocks), int(block_size), int(n_kv_heads),
+                                int(head_dim), DTYPES[dtype], ctypes.byref(h)), "kv_pool_create")
+        self._h = h
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+        self.n_kv_heads, self.head_dim, self.dtype = int(n_kv_heads), int(head_dim), dtype
+        self._events = None
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if self._h is None:
+            raise RuntimeError("pool destroyed")
+        return self._h
+
+    def destroy(self) -> None:
+        if getattr(self, "_h", None) is not None and _lib is not None:
+            _check(_lib.kv_pool_destroy(self._h), "kv_pool_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+    def info(self) -> dict:
+        d = _Desc()
+        _check(load().kv_pool_info(self.handle, ctypes.byref(d)), "kv_pool_info")
+        return {"base_dev": d.base_dev, "num_blocks": d.num_blocks, "block_size": d.block_size,
+                "n_kv_heads": d.n_kv_heads, "head_dim": d.head_dim, "dtype": d.dtype,
+                "strides": list(d.strides), "bytes": d.bytes, "device": d.device,
+                "scales_dev": d.scales_dev}
+
+    def view(self) -> torch.Tensor:
+        """The pool memory as a torch tensor [NB, Hkv, 2, BS, D] (bf16 or uint8), no copy."""
+        i = self.info()
+        tdt, typestr = (torch.bfloat16, "<V2") if self.dtype == "bf16" else (torch.uint8, "|u1")
+        shape = (self.num_blocks, self.n_kv_heads, 2, self.block_size, self.head_dim)
+
+        class _Buf:
+            __cuda_array_interface__ = {"shape": shape, "typestr": "|u1" if tdt == torch.uint8
+                                        else "<i2", "data": (i["base_dev"], False),
+                                        "version": 3, "strides": None}
+        t = torch.as_tensor(_Buf(), device=f"cuda:{i['device']}")
+        return t.view(tdt) if tdt == torch.bfloat16 else t
+
+    def set_scales(self, k_scale: torch.Tensor, v_scale: torch.Tensor, stream=None) -> None:
+        _check(load().kv_pool_set_scales(self.handle, _dev(k_scale, torch.float32, "k_scale"),
+                                         _dev(v_scale, torch.float32, "v_scale"),
+                                         _stream(stream)), "kv_pool_set_scales")
+
+    def set_partition_blocks(self, n: int) -> None:
+        _check(load().kv_pool_set_partition_blocks(self.handle, int(n)),
+               "kv_pool_set_partition_blocks")
+
+    def set_timing_events(self, start, stop) -> None:
+        """Record CUDA events around each decode kernel (None, None disables)."""
+        if start is None:
+            _check(load().kv_pool_set_timing_events(self.handle, None, None), "timing")
+            self._events = None
+            return
+        for ev in (start, stop):
+            if ev.cuda_event == 0:
+                ev.record()   # torch creates the event lazily
+        torch.cuda.synchronize()
+        _check(load().kv_pool_set_timing_events(self.handle, ctypes.c_void_p(start.cuda_event),
+                                                ctypes.c_void_p(stop.cuda_event)), "timing")
+        self._events = (start, stop)
+
+    def check_status(self, stream=None) -> int:
+        """Read and clear the device error word; returns the status code."""
+        return int(load().kv_pool_check_status(self.handle, _stream(stream)))
+
+
+# ----------------------------------------------------- C ABI named functions --
+
+def kv_pool_create(num_blocks: int, block_size: int, n_kv_heads: int, head_dim: int,
+                   dtype: str = "bf16") -> KVPool:
+    return KVPool(num_blocks, block_size, n_kv_heads, head_dim, dtype)
+
+
+def kv_pool_destroy(pool: KVPool) -> None:
+    pool.destroy()
+
+
+def kv_pool_set_scales(pool: KVPool, k_scale, v_scale, stream=None) -> None:
+    pool.set_scales(k_scale, v_scale, stream)
+
+
+def kv_pool_check_status(pool: KVPool, stream=None) -> int:
+    return pool.check_status(stream)
+
+
+def paged_kv_write(pool: KVPool, k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                   stream=None) -> None:
+    """Scatter k, v ([T, Hkv, D] bf16) to the slots in slot_mapping ([T] int64; <0 = skip)."""
+    T = slot_mapping.shape[0]
+    shape = (T, pool.n_kv_heads, pool.head_dim)
+    if tuple(k.shape) != shape or tuple(v.shape) != shape:
+        raise ValueError(f"k and v must be {shape}")
+    _check(load().paged_kv_write(pool.handle, _dev(k, torch.bfloat16, "k"),
+                                 _dev(v, torch.bfloat16, "v"),
+                                 _dev(slot_mapping, torch.int64, "slot_mapping"), T,
+                                 _stream(stream)), "paged_kv_write")
+
+
+def paged_decode_workspace_bytes(pool: KVPool, batch: int, n_q_heads: int, max_context_len: int,
+                                 sliding_window: int = 0) -> int:
+    return int(load().paged_decode_workspace_bytes(pool.handle, int(batch), int(n_q_heads),
+                                                   int(max_context_len), int(sliding_window)))
+
+
+def paged_decode_attention(pool: KVPool, q: torch.Tensor, block_tables: torch.Tensor,
+                           context_lens: torch.Tensor, scale: float, sliding_window: int = 0,
+                           max_context_len: int | None = None, out: torch.Tensor | None = None,
+                           workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Decode attention: q [B, Hq, D] bf16 -> out [B, Hq, D] fp32.
+
+    `max_context_len` bounds context_lens (the host side sizes the launch with
+    it); when omitted it is read from context_lens, which synchronises."""
+    B, Hq, D = q.shape
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if B else 0
+    if out is None:
+        out = torch.empty(B, Hq, D, dtype=torch.float32, device=q.device)
+    need = paged_decode_workspace_bytes(pool, B, Hq, max_context_len, sliding_window)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be [B, max_blocks_per_seq]")
+    _check(load().paged_decode_attention(
+        pool.handle, _dev(q, torch.bfloat16, "q"), Hq,
+        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _dev(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
+        int(sliding_window), _dev(out, torch.float32, "out"), ws_ptr, ws_bytes, _stream(stream)),
+        "paged_decode_attention")
+    return out
+
+
+def kv_status_str(status: int) -> str:
+    return load().kv_status_str(int(status)).decode()
+
+
+def library_path() -> str:
+    return os.path.abspath(LIB_PATH)

@@ -1,0 +1,76 @@
+"""The C-ABI library builds, loads and exports every entry point the header
+declares; host-side argument checks answer without touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_33_gb300 import pagedkv
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "pagedkv.h")
+
+
+def declared_functions() -> list[str]:
+    text = open(HEADER).read()
+    return re.findall(r"^(?:kv_status|size_t|const char\*)\s+(\w+)\(", text, re.M)
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ("kv_pool_create", "paged_kv_write", "paged_decode_attention",
+              "kv_pool_check_status", "kv_status_str"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = pagedkv.load()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings():
+    assert pagedkv.kv_status_str(0) == "KV_OK"
+    assert pagedkv.kv_status_str(5) == "KV_ERR_BAD_BLOCK_ID"
+    assert pagedkv.kv_status_str(99) == "KV_ERR_UNKNOWN"
+    for code, name in pagedkv.STATUS.items():
+        assert pagedkv.kv_status_str(code) == name
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 16, 8, 128, 0), 1),        # no blocks
+    ((10, 0, 8, 128, 0), 1),        # no block size
+    ((10, 16, 0, 128, 0), 1),       # no heads
+    ((10, 16, 8, 128, 7), 1),       # unknown dtype
+    ((10, 32, 8, 128, 0), 4),       # block size other than 16
+    ((10, 16, 8, 96, 0), 4),        # head_dim not 64/128
+    ((10, 16, 8, 64, 1), 4),        # FP8 needs head_dim 128
+])
+def test_create_rejects_bad_shapes_before_any_cuda_call(args, status):
+    L = pagedkv.load()
+    h = ctypes.c_void_p()
+    assert L.kv_pool_create(*args, ctypes.byref(h)) == status
+    assert not h.value
+
+
+def test_null_handles_are_rejected():
+    L = pagedkv.load()
+    assert L.kv_pool_destroy(None) == 1
+    assert L.paged_kv_write(None, None, None, None, 1, None) == 1
+    assert L.paged_decode_attention(None, None, 8, None, 4, None, 1, 64, 1.0, 0, None, None, 0,
+                                    None) == 1
+    assert L.paged_decode_workspace_bytes(None, 1, 8, 64, 0) == 0
+    assert L.kv_pool_check_status(None, None) == 1
+    assert L.kv_pool_set_partition_blocks(None, 8) == 1
+
+
+def test_create_without_a_device_fails_cleanly():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    L = pagedkv.load()
+    h = ctypes.c_void_p()
+    assert L.kv_pool_create(10, 16, 8, 128, 0, ctypes.byref(h)) in (2, 3)
+    assert not h.value
