@@ -1,0 +1,462 @@
+"""Benchmark of the paged decode hot path: one step = paged KV write of this
+step's token per sequence + split-K paged decode attention (+ its reduce).
+
+Prints ONE JSON line (rank 0).  `value` is KV-read GB/s: K+V bytes of the
+attended tokens (exact context, per layer) of all ranks / the max-over-ranks
+time of the timed steps, with every input resident in HBM.  `e2e` is the same
+metric through the public API with the step's inputs copied from pinned host
+memory and the output read back inside the timed region.  `roofline` gives the
+decode kernel alone against the measured HBM copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 8b|70b|sw|tiny]
+                  [--impl ours|reference] [--part-blocks P]
+
+Under torchrun every rank runs an independent replica on its own GPU (the
+path has no exchange step); ranks meet at barriers around the timed region.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention KV-read GB/s and % of GB300 HBM peak; decode tokens/s/layer"
+L2_BYTES = 129 * 1024 * 1024
+DESCRIPTIONS = {
+    "tiny": "tiny paged decode: 4 seqs ctx {5,16,33,70}, 2 q / 1 KV heads, head_dim 64, "
+            "64-block permuted pool, 4-token write",
+    "8b": "Llama-3-8B-shaped layer decode: batch 64, 32 q / 8 KV heads, head_dim 128, "
+          "16-token blocks, ctx U[128,4096], pool 1.2x needed with shuffled ids, "
+          "1-token KV write per seq before attention",
+    "70b": "Llama-3-70B-shaped layer decode: batch 128, 64 q / 8 KV heads, head_dim 128, "
+           "ctx log-uniform [256,8192], 64-block shared prefix (ref_cnt 128)",
+    "sw": "sliding-window layer decode: batch 32, 32 q / 8 KV heads, head_dim 128, "
+          "window 4096, ctx U[4096,32768], only window blocks mapped",
+}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="8b", choices=["tiny", "8b", "70b", "sw"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--part-blocks", type=int, default=0, help="split-K partition size (0 = auto)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------- host helpers --
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_33_gb300", "csrc")
+    for name in ("decode.cu", "common.cuh", "internal.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config: str) -> float | None:
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on this exact kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(config)
+    if not rec or rec.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples at 100 ms while running."""
+
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        self.dev = device_index
+        self.marks: dict[str, float] = {}
+        if shutil.which("nvidia-smi") is None:
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.out = open(self.path, "w")
+        self.proc = subprocess.Popen(
+            ["nvidia-smi", f"--id={device_index}", f"--query-gpu={self.FIELDS}",
+             "--format=csv,noheader,nounits", "-lms", "100"],
+            stdout=self.out, stderr=subprocess.DEVNULL)
+
+    def mark(self, name: str) -> None:
+        self.marks[name] = time.time()
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[1].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    rows.append({"t": ts, "sm": float(parts[2]), "max": float(parts[3]),
+                                 "reasons": {"hw_slowdown": parts[6], "hw_thermal_slowdown": parts[7],
+                                             "sw_thermal_slowdown": parts[8],
+                                             "sw_power_cap": parts[9]}})
+                except (ValueError, IndexError):
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        t0, t1 = self.marks.get("timed_start"), self.marks.get("timed_end")
+        window = "timed"
+        sel = [r for r in rows if t0 is not None and t0 - 1 <= r["t"] <= t1 + 1]
+        if len(sel) < 3:
+            sel, window = rows, "run"
+        reasons = sorted({k for r in sel for k, v in r["reasons"].items() if v == "Active"})
+        return {"sm_mhz": statistics.median(r["sm"] for r in sel),
+                "sm_max_mhz": max(r["max"] for r in sel), "reasons": reasons,
+                "samples": len(sel), "window": window}
+
+
+# ----------------------------------------------------------------- the step --
+
+class Step:
+    """Device-resident inputs of one decode step and the calls that run it."""
+
+    def __init__(self, w, device, part_blocks: int = 0):
+        import torch
+        from paged_kv_cache_33_gb300 import pagedkv
+
+        self.torch, self.pk, self.w = torch, pagedkv, w
+        self.pool = pagedkv.KVPool(w.num_blocks, w.block_size, w.n_kv_heads, w.head_dim, w.dtype)
+        if part_blocks:
+            self.pool.set_partition_blocks(part_blocks)
+        setup, (k_new, v_new, s_new) = w.fill_plan(device=device)
+        for k, v, s in setup:
+            pagedkv.paged_kv_write(self.pool, k, v, s.to(device))
+        self.k_new, self.v_new = k_new, v_new
+        self.slots = s_new.to(device)
+        self.q = w.query(device=device)
+        self.tables = torch.from_numpy(w.block_tables).to(device)
+        self.lens = torch.from_numpy(w.context_lens).to(device)
+        self.out = torch.empty(w.batch, w.n_q_heads, w.head_dim, dtype=torch.float32, device=device)
+        need = pagedkv.paged_decode_workspace_bytes(self.pool, w.batch, w.n_q_heads,
+                                                    w.max_context_len, w.window)
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+        self.launches = 2 + (1 if need > 0 else 0)
+        torch.cuda.synchronize()
+        if self.pool.check_status() != pagedkv.KV_OK:
+            raise RuntimeError("pool fill reported a device error")
+
+    def run(self, q=None, tables=None, lens=None, k=None, v=None, slots=None, out=None):
+        pk, w = self.pk, self.w
+        pk.paged_kv_write(self.pool, self.k_new if k is None else k, self.v_new if v is None else v,
+                          self.slots if slots is None else slots)
+        pk.paged_decode_attention(self.pool, self.q if q is None else q,
+                                  self.tables if tables is None else tables,
+                                  self.lens if lens is None else lens, w.scale, w.window,
+                                  max_context_len=w.max_context_len,
+                                  out=self.out if out is None else out, workspace=self.ws)
+
+
+def timed_device(step: Step, steps: int, warmup: int, dist_ctx, sampler) -> dict:
+    """K steps with all inputs resident; per-step decode-kernel events via the pool hook."""
+    torch = step.torch
+    for _ in range(warmup):
+        step.run()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    sampler.mark("timed_start")
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall = time.perf_counter()
+    torch.cuda.nvtx.range_push("timed_steps")
+    start.record()
+    for i in range(steps):
+        step.pool.set_timing_events(*ev[i])
+        step.run()
+    stop.record()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    sampler.mark("timed_end")
+    dist_ctx.barrier()
+    step.pool.set_timing_events(None, None)
+    status = step.pool.check_status()
+    if status != step.pk.KV_OK:
+        raise RuntimeError(f"device error during the timed steps: {step.pk.STATUS[status]}")
+    elapsed = start.elapsed_time(stop) / 1e3
+    kernel = sum(a.elapsed_time(b) for a, b in ev) / 1e3 / steps
+    return {"elapsed_s": elapsed, "wall_s": wall, "decode_kernel_s": kernel}
+
+
+def timed_e2e(step: Step, steps: int, warmup: int, dist_ctx) -> dict:
+    """Same steps through the public API with host inputs: every step copies q,
+    the new K/V, slots, block tables and context lengths from pinned memory
+    and reads the output back."""
+    torch, w = step.torch, step.w
+    host = {
+        "q": step.q.cpu().pin_memory(), "k": step.k_new.cpu().pin_memory(),
+        "v": step.v_new.cpu().pin_memory(), "slots": step.slots.cpu().pin_memory(),
+        "tables": step.tables.cpu().pin_memory(), "lens": step.lens.cpu().pin_memory(),
+    }
+    dev = {k: torch.empty_like(v, device=step.q.device) for k, v in host.items()}
+    out_host = torch.empty(step.out.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        step.run(q=dev["q"], tables=dev["tables"], lens=dev["lens"], k=dev["k"], v=dev["v"],
+                 slots=dev["slots"])
+        out_host.copy_(step.out, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    dist_ctx.barrier()
+    return {"elapsed_s": elapsed, "h2d": h2d, "d2h": d2h}
+
+
+# ------------------------------------------------------------ distributed --
+
+class DistCtx:
+    def __init__(self, want: int):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = os.environ.get("PAGEDKV_DIST_BACKEND", "nccl")
+            if backend == "nccl":
+                import torch
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        return self._reduce(x, "max")
+
+    def sum(self, x: float) -> float:
+        return self._reduce(x, "sum")
+
+    def _reduce(self, x: float, op: str) -> float:
+        if self.dist is None:
+            return x
+        import torch
+        backend = self.dist.get_backend()
+        t = torch.tensor([float(x)], dtype=torch.float64,
+                         device="cuda" if backend == "nccl" else "cpu")
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX if op == "max" else self.dist.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+
+
+def aggregate(dist_ctx: DistCtx, units: float, elapsed: float) -> tuple[float, float]:
+    """Whole-job throughput: units of all ranks / the slowest rank's time."""
+    return dist_ctx.sum(units), dist_ctx.max(elapsed)
+
+
+# ------------------------------------------------------------ CPU baseline --
+
+def oracle_sample(w, budget_s: float) -> dict:
+    """Time the oracle (single-threaded fp64) on a bounded sample of the
+    workload: sequences in seeded order until ~budget_s of CPU work."""
+    import numpy as np
+
+    import oracle
+
+    rng = np.random.default_rng(0)
+    order = rng.permutation(w.batch)
+    op = oracle.Pool(w.num_blocks, w.block_size, w.n_kv_heads, w.head_dim, w.dtype)
+    q = w.query()
+    done_bytes, t_total, seqs_done = 0, 0.0, []
+    elem = 2 if w.dtype == "bf16" else 1
+    for b in order:
+        setup, (k_new, v_new, s_new) = w.fill_plan(seqs=[int(b)])
+        for k, v, s in setup:
+            op.write(k, v, s.numpy())
+        keep = s_new.clone()
+        keep[[i for i in range(w.batch) if i != b]] = -1
+        op.write(k_new, v_new, keep.numpy())
+        t0 = time.perf_counter()
+        op.decode(q, w.block_tables, w.context_lens, w.scale, w.window, seqs=[int(b)])
+        t_total += time.perf_counter() - t0
+        lo, ctx = w.attended_range(int(b))
+        done_bytes += (ctx - lo) * w.n_kv_heads * 2 * w.head_dim * elem
+        seqs_done.append(int(b))
+        if t_total >= budget_s:
+            break
+    return {"value": done_bytes / t_total / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(seqs_done)} of {w.batch} sequences ({done_bytes / 1e6:.1f} MB of "
+                      f"K/V), single-threaded fp64 oracle, {t_total:.1f} s",
+            "seconds": t_total, "bytes": done_bytes}
+
+
+def run_reference(args) -> None:
+    """The reference arm: the oracle itself, timed on this host's cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from paged_kv_cache_33_gb300 import workloads as W
+    w = W.make(args.config, "full")
+    per_step_budget = max(0.5, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step_budget)
+    tot_b, tot_t = 0, 0.0
+    for _ in range(args.steps):
+        r = oracle_sample(w, per_step_budget)
+        tot_b += r["bytes"]
+        tot_t += r["seconds"]
+    value = tot_b / tot_t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": DESCRIPTIONS[args.config], "name": args.config,
+                       "batch": w.batch, "parallelism": "none (host oracle)"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step: sequences of the {args.config} workload in "
+                                       f"seeded order for ~{per_step_budget:.1f} s of "
+                                       "single-threaded fp64 oracle work"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------- main --
+
+def main(argv=None) -> None:
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+
+    from paged_kv_cache_33_gb300 import pagedkv
+    from paged_kv_cache_33_gb300 import workloads as W
+
+    dist_ctx = DistCtx(args.gpus)
+    torch.cuda.set_device(dist_ctx.local_rank)
+    device = torch.device("cuda", dist_ctx.local_rank)
+    pagedkv.load()
+    w = W.make(args.config, "full")
+    step = Step(w, device, args.part_blocks)
+    sampler = ClockSampler(dist_ctx.local_rank)
+    dev = timed_device(step, args.steps, args.warmup, dist_ctx, sampler)
+    clocks = sampler.stop()
+    e2e = timed_e2e(step, max(10, min(args.steps, 500)), min(args.warmup, 10), dist_ctx)
+
+    kv_bytes = w.kv_bytes_attended()
+    unique = w.kv_bytes_unique()
+    total_bytes, elapsed = aggregate(dist_ctx, kv_bytes * args.steps, dev["elapsed_s"])
+    e2e_steps = max(10, min(args.steps, 500))
+    e2e_bytes, e2e_elapsed = aggregate(dist_ctx, kv_bytes * e2e_steps, e2e["elapsed_s"])
+    kernel_s = dist_ctx.max(dev["decode_kernel_s"])
+    peaks = measured_peaks()
+    # algorithmic bytes of one decode launch: attended K/V (shared prefix once),
+    # the queries, the outputs and the block-table entries read
+    tables_read = 4 * w.n_kv_heads * sum(
+        (hi - 1) // 16 - lo // 16 + 1 for lo, hi in map(w.attended_range, range(w.batch)) if hi > lo)
+    algo = unique + w.batch * w.n_q_heads * w.head_dim * (2 + 4) + tables_read
+    achieved = algo / kernel_s / 1e9
+    step_s = elapsed / args.steps
+    result = {
+        "metric": METRIC, "value": total_bytes / elapsed / 1e9, "unit": "GB/s",
+        "n_gpus": dist_ctx.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[args.config], "name": args.config,
+                   "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+                   "head_dim": w.head_dim, "block_size": w.block_size,
+                   "num_blocks": w.num_blocks, "window": w.window,
+                   "kv_bytes_attended_per_step": kv_bytes, "kv_bytes_unique_per_step": unique,
+                   "l2": f"inputs larger than L2: {unique / 1e6:.0f} MB of distinct K/V per "
+                         f"step vs {L2_BYTES / 1e6:.0f} MB L2, no flush",
+                   "parallelism": f"replicas x{dist_ctx.world} (no collective on the path)"},
+        "pct_of_hbm_peak": 100.0 * achieved / peaks["hbm_gbs"],
+        "tokens_per_s_per_layer": dist_ctx.world * w.batch / step_s,
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy)",
+                     "algorithmic_bytes_per_launch": algo,
+                     "kernel_ms": kernel_s * 1e3,
+                     "traffic": recorded_traffic(args.config)},
+        "e2e": {"value": e2e_bytes / e2e_elapsed / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "steps": e2e_steps},
+        "clocks": clocks,
+        "gpu_launches": step.launches * args.steps,
+    }
+    if dist_ctx.rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = oracle_sample(w, args.cpu_baseline_seconds)
+        for k in ("seconds", "bytes"):
+            result["cpu_baseline"].pop(k, None)
+    dist_ctx.barrier()
+    if dist_ctx.rank == 0:
+        print(json.dumps(result))
+    dist_ctx.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -164,10 +164,11 @@ class KVPool:
             _check(load().kv_pool_set_timing_events(self.handle, None, None), "timing")
             self._events = None
             return
-        for ev in (start, stop):
-            if ev.cuda_event == 0:
-                ev.record()   # torch creates the event lazily
-        torch.cuda.synchronize()
+        fresh = [ev for ev in (start, stop) if ev.cuda_event == 0]
+        for ev in fresh:
+            ev.record()   # torch creates the event lazily, on first record
+        if fresh:
+            torch.cuda.synchronize()
         _check(load().kv_pool_set_timing_events(self.handle, ctypes.c_void_p(start.cuda_event),
                                                 ctypes.c_void_p(stop.cuda_event)), "timing")
         self._events = (start, stop)

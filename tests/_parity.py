@@ -143,5 +143,7 @@ def run_parity(w: Workload, seqs=None, part_blocks: int | None = None,
     rows = list(range(w.batch)) if seqs is None else list(seqs)
     got = out.cpu().numpy()[rows]
     max_abs, rel = assert_close(w, got, ref[rows], f"{w.name}/{w.size}")
+    print(f"PARITY {w.name}/{w.size} seqs={len(rows)} part_blocks={part_blocks} "
+          f"max_abs={max_abs:.3e} rel_l2={rel:.3e}")
     pool.destroy()
     return {"max_abs": max_abs, "rel_l2": rel}
