@@ -151,6 +151,33 @@ kv_status paged_decode_attention(kv_pool* pool, const void* q_dev, int32_t n_q_h
                                  void* stream);
 
 /*
+ * paged_decode_attention_noalloc -- paged_decode_attention for callers that
+ * cannot allocate device memory when they run decode, e.g. a serving runtime
+ * that gave all free memory to its KV pool at start-up and allows no later
+ * cudaMalloc, or a plugin interface with no workspace argument.  (The pages
+ * have no counterpart to this entry point.)
+ *   Same arguments and results as paged_decode_attention, without the
+ *   workspace: the split-K partials go to one static device array of
+ *   PAGED_DECODE_STATIC_SCRATCH_BYTES that this library holds on every GPU
+ *   that loads it, until the process exits.  The call itself allocates
+ *   nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *   Returns KV_ERR_INVALID_ARG when paged_decode_workspace_bytes() for these
+ *   sizes exceeds PAGED_DECODE_STATIC_SCRATCH_BYTES; use a larger partition
+ *   (kv_pool_set_partition_blocks) or the workspace entry point then.
+ *   The first call on a device looks up the array's device address (once,
+ *   with that device current); make that first call before any stream
+ *   capture.  All calls on a device share the array: calls that may overlap
+ *   on the GPU (different streams, no ordering between them) race on it.
+ */
+#define PAGED_DECODE_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+kv_status paged_decode_attention_noalloc(kv_pool* pool, const void* q_dev, int32_t n_q_heads,
+                                         const int32_t* block_tables_dev,
+                                         int32_t max_blocks_per_seq,
+                                         const int32_t* context_lens_dev, int32_t batch,
+                                         int32_t max_context_len, float scale,
+                                         int32_t sliding_window, float* out_dev, void* stream);
+
+/*
  * kv_pool_set_partition_blocks -- split-K partition size, in blocks (a
  * multiple of 4, 4..1024); 0 restores the automatic choice.  Tuning and tests
  * only: results are the same for every setting up to rounding.

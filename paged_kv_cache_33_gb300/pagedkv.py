@@ -65,6 +65,9 @@ def load() -> ctypes.CDLL:
             "paged_decode_attention": (c.c_int, [P, P, c.c_int32, P, c.c_int32, P, c.c_int32,
                                                  c.c_int32, c.c_float, c.c_int32, P, P,
                                                  c.c_size_t, P]),
+            "paged_decode_attention_noalloc": (c.c_int, [P, P, c.c_int32, P, c.c_int32, P,
+                                                         c.c_int32, c.c_int32, c.c_float,
+                                                         c.c_int32, P, P]),
             "kv_pool_set_partition_blocks": (c.c_int, [P, c.c_int32]),
             "kv_pool_set_timing_events": (c.c_int, [P, P, P]),
             "kv_pool_check_status": (c.c_int, [P, P]),
@@ -243,6 +246,23 @@ def paged_decode_attention(pool: KVPool, q: torch.Tensor, block_tables: torch.Te
         int(sliding_window), _dev(out, torch.float32, "out"), ws_ptr, ws_bytes, _stream(stream)),
         "paged_decode_attention")
     return out
+
+
+def paged_decode_attention_noalloc(pool: KVPool, q: torch.Tensor, block_tables: torch.Tensor,
+                                   context_lens: torch.Tensor, scale: float, sliding_window: int,
+                                   max_context_len: int, out: torch.Tensor, stream=None) -> None:
+    """Decode attention whose split-K scratch is the library's static device
+    array: nothing is allocated, so `out` ([B, Hq, D] fp32) and
+    `max_context_len` must come from the caller."""
+    B, Hq, _ = q.shape
+    if block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be [B, max_blocks_per_seq]")
+    _check(load().paged_decode_attention_noalloc(
+        pool.handle, _dev(q, torch.bfloat16, "q"), Hq,
+        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _dev(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
+        int(sliding_window), _dev(out, torch.float32, "out"), _stream(stream)),
+        "paged_decode_attention_noalloc")
 
 
 def kv_status_str(status: int) -> str:
