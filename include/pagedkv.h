@@ -140,8 +140,11 @@ size_t paged_decode_workspace_bytes(const kv_pool* pool, int32_t batch, int32_t 
  *   out_dev:             fp32 [batch][n_q_heads][head_dim], softmax(scale q K^T) V.
  *   workspace_dev:       at least paged_decode_workspace_bytes(...) bytes,
  *                        16-byte aligned; contents need no initialisation.
- * The split-K decode kernel and its reduce run on `stream` in order.  Calls
- * that share a workspace must not overlap in time.
+ * Work is split evenly over a persistent grid (stream-K over the list of
+ * (sequence, KV head, block) units); a (sequence, KV head) pair cut between
+ * warps leaves partial results that a reduce kernel merges.  On `stream`:
+ * the decode kernel, then the reduce kernel as its programmatic dependent.
+ * Calls that share a workspace must not overlap in time.
  */
 kv_status paged_decode_attention(kv_pool* pool, const void* q_dev, int32_t n_q_heads,
                                  const int32_t* block_tables_dev, int32_t max_blocks_per_seq,
@@ -149,6 +152,28 @@ kv_status paged_decode_attention(kv_pool* pool, const void* q_dev, int32_t n_q_h
                                  int32_t max_context_len, float scale, int32_t sliding_window,
                                  float* out_dev, void* workspace_dev, size_t workspace_bytes,
                                  void* stream);
+
+/*
+ * paged_decode_step -- one decode step of a layer: paged_kv_write of the
+ * step's new tokens, then paged_decode_attention over the pool that now holds
+ * them ("The Decode Phase": the new token's K/V go into the last block, then
+ * the query attends over every cached token including it).
+ *   Arguments: those of paged_kv_write (k_dev, v_dev, slot_mapping_dev,
+ *   num_tokens), then those of paged_decode_attention, with the same meaning,
+ *   layout and checks; context_lens must already count the new tokens.
+ *   Results are those of the two calls made one after the other.  The decode
+ *   kernel is launched as a programmatic dependent of the write kernel: it
+ *   reads its sequence table while the write runs and waits for the write to
+ *   complete before it reads the pool.  batch == 0 performs the write alone.
+ */
+kv_status paged_decode_step(kv_pool* pool, const void* k_dev, const void* v_dev,
+                            const int64_t* slot_mapping_dev, int64_t num_tokens,
+                            const void* q_dev, int32_t n_q_heads,
+                            const int32_t* block_tables_dev, int32_t max_blocks_per_seq,
+                            const int32_t* context_lens_dev, int32_t batch,
+                            int32_t max_context_len, float scale, int32_t sliding_window,
+                            float* out_dev, void* workspace_dev, size_t workspace_bytes,
+                            void* stream);
 
 /*
  * paged_decode_attention_noalloc -- paged_decode_attention for callers that
@@ -178,16 +203,21 @@ kv_status paged_decode_attention_noalloc(kv_pool* pool, const void* q_dev, int32
                                          int32_t sliding_window, float* out_dev, void* stream);
 
 /*
- * kv_pool_set_partition_blocks -- split-K partition size, in blocks (a
- * multiple of 4, 4..1024); 0 restores the automatic choice.  Tuning and tests
+ * kv_pool_set_partition_blocks -- split-K granularity: aim for about this
+ * many blocks per warp (a multiple of 4, 4..1024) for the longest possible
+ * call, using fewer warps than the full persistent grid when that needs
+ * fewer; 0 restores the automatic choice (the full grid).  Tuning and tests
  * only: results are the same for every setting up to rounding.
  */
 kv_status kv_pool_set_partition_blocks(kv_pool* pool, int32_t blocks_per_partition);
 
 /*
  * kv_pool_set_timing_events -- instrumentation: when both are non-NULL, each
- * paged_decode_attention records `start_event` just before its split-K decode
- * kernel and `stop_event` just after it (before the reduce), on its stream.
+ * paged_decode_attention / paged_decode_step records `start_event` just
+ * before each decode kernel launch and `stop_event` just after it, on its
+ * stream, so that the pair brackets the decode kernel alone.  While they are
+ * set, paged_decode_step launches its decode kernel after the write has
+ * completed instead of overlapping its start with it.
  * The events (cudaEvent_t) stay owned by the caller; NULL, NULL turns it off.
  */
 kv_status kv_pool_set_timing_events(kv_pool* pool, void* start_event, void* stop_event);

@@ -77,23 +77,29 @@ DecodePlan plan_decode(const kv_pool* pool, int32_t batch, int32_t n_q_heads,
   DecodePlan plan{};
   int32_t max_nblk = blocks_for(max_context_len);
   if (sliding_window > 0) max_nblk = std::min(max_nblk, (sliding_window - 1) / 16 + 2);
-  int32_t pb = pool->partition_blocks;
-  if (pb <= 0) {
-    // Enough partitions to give every SM several CTAs over the whole grid,
-    // assuming the average sequence is about half the longest one.
-    const int64_t total_blocks = static_cast<int64_t>(batch) * pool->n_kv_heads *
-                                 std::max<int64_t>(1, max_nblk / 2);
-    const int64_t target_ctas = static_cast<int64_t>(std::max(pool->sm_count, 1)) * 8;
-    int64_t want = (total_blocks + target_ctas - 1) / target_ctas;
-    want = std::max<int64_t>(16, std::min<int64_t>(want, 128));
-    pb = static_cast<int32_t>((want + 3) / 4 * 4);
+  plan.batch = std::min(batch, kMaxDecodeBatch);
+  const int nw = decode_warps_per_cta(pool);
+  // A persistent grid: every SM holds as many CTAs as fit at once.
+  const int64_t max_ctas = static_cast<int64_t>(std::max(pool->sm_count, 1)) *
+                           decode_ctas_per_sm(pool);
+  const int64_t t_max = static_cast<int64_t>(plan.batch) * pool->n_kv_heads * std::max(max_nblk, 1);
+  int64_t ctas = max_ctas;
+  if (pool->partition_blocks > 0) {
+    // about `partition_blocks` units per warp for the longest possible launch
+    const int64_t workers = (t_max + pool->partition_blocks - 1) / pool->partition_blocks;
+    ctas = std::max<int64_t>(1, std::min<int64_t>(max_ctas, (workers + nw - 1) / nw));
   }
-  plan.part_blocks = pb;
-  plan.max_parts = std::max(1, (max_nblk + pb - 1) / pb);
-  if (plan.max_parts > 1) {
-    const size_t rows = static_cast<size_t>(batch) * n_q_heads * plan.max_parts;
-    plan.workspace_bytes = rows * pool->head_dim * sizeof(float) + rows * 2 * sizeof(float);
-  }
+  plan.ctas = static_cast<int32_t>(ctas);
+  plan.workers = static_cast<int32_t>(ctas * nw);
+  const int64_t g = n_q_heads / pool->n_kv_heads;
+  const int64_t pairs = static_cast<int64_t>(plan.batch) * pool->n_kv_heads;
+  const int64_t chunks = decode_dynamic_units(t_max) / decode_chunk_units() + 2;
+  const int64_t slots = plan.workers + chunks + pairs;
+  auto round256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  plan.part_o_bytes = round256(static_cast<size_t>(slots * g * pool->head_dim) * sizeof(float));
+  plan.part_ml_bytes = round256(static_cast<size_t>(slots * g * 2) * sizeof(float));
+  plan.meta_bytes = round256(static_cast<size_t>(pairs) * 2 * sizeof(int32_t) + 16);
+  plan.workspace_bytes = plan.part_o_bytes + plan.part_ml_bytes + plan.meta_bytes;
   return plan;
 }
 
@@ -235,17 +241,40 @@ size_t paged_decode_workspace_bytes(const kv_pool* p, int32_t batch, int32_t n_q
   return pkv::plan_decode(p, batch, n_q_heads, max_context_len, sliding_window).workspace_bytes;
 }
 
-kv_status paged_decode_attention(kv_pool* p, const void* q, int32_t n_q_heads,
-                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                 const int32_t* context_lens, int32_t batch,
-                                 int32_t max_context_len, float scale, int32_t sliding_window,
-                                 float* out, void* workspace, size_t workspace_bytes,
-                                 void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The new tokens a fused step writes before its attention.
+struct StepWrite {
+  const void* k;
+  const void* v;
+  const int64_t* slots;
+  int64_t num_tokens;
+};
+
+kv_status decode_call(kv_pool* p, const StepWrite* w, const void* q, int32_t n_q_heads,
+                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                      const int32_t* context_lens, int32_t batch, int32_t max_context_len,
+                      float scale, int32_t sliding_window, float* out, void* workspace,
+                      size_t workspace_bytes, void* stream) {
   if (!p || batch < 0 || n_q_heads <= 0) return KV_ERR_INVALID_ARG;
   if (n_q_heads % p->n_kv_heads != 0) return KV_ERR_INVALID_ARG;
   const int32_t g = n_q_heads / p->n_kv_heads;
   if (g > 8) return KV_ERR_UNSUPPORTED;
-  if (batch == 0) return KV_OK;
+  if (w) {
+    if (w->num_tokens < 0 || w->num_tokens > (int64_t(1) << 40)) return KV_ERR_INVALID_ARG;
+    if (w->num_tokens > 0 && (!w->k || !w->v || !w->slots || !aligned16(w->k) || !aligned16(w->v)))
+      return KV_ERR_INVALID_ARG;
+  }
+  if (batch == 0) {
+    if (!w || w->num_tokens == 0) return KV_OK;
+    DeviceGuard guard(p->device);
+    return pkv::launch_kv_write(p, w->k, w->v, w->slots, w->num_tokens,
+                                static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KV_OK
+               : KV_ERR_CUDA;
+  }
   if (!q || !block_tables || !context_lens || !out || !aligned16(q)) return KV_ERR_INVALID_ARG;
   if (max_blocks_per_seq <= 0 || max_context_len < 0 ||
       static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * 16)
@@ -253,42 +282,91 @@ kv_status paged_decode_attention(kv_pool* p, const void* q, int32_t n_q_heads,
   if (!std::isfinite(scale)) return KV_ERR_INVALID_ARG;
   if (batch > 65535 || p->n_kv_heads > 65535) return KV_ERR_UNSUPPORTED;
 
+  DeviceGuard guard(p->device);
   const pkv::DecodePlan plan = pkv::plan_decode(p, batch, n_q_heads, max_context_len, sliding_window);
-  if (plan.workspace_bytes > 0 &&
-      (!workspace || workspace_bytes < plan.workspace_bytes || !aligned16(workspace)))
+  if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned16(workspace))
     return KV_ERR_INVALID_ARG;
+  {
+    int32_t max_nblk = blocks_for(max_context_len);
+    if (sliding_window > 0) max_nblk = std::min(max_nblk, (sliding_window - 1) / 16 + 2);
+    if (static_cast<int64_t>(plan.batch) * p->n_kv_heads * std::max(max_nblk, 1) >= (int64_t(1) << 30))
+      return KV_ERR_UNSUPPORTED;  // unit indices are 32-bit
+  }
 
   pkv::DecodeParams d{};
-  d.q = q;
-  d.block_tables = block_tables;
-  d.context_lens = context_lens;
-  d.out = out;
-  const size_t rows = static_cast<size_t>(batch) * n_q_heads * plan.max_parts;
-  d.part_o = plan.workspace_bytes ? static_cast<float*>(workspace) : nullptr;
-  d.part_ml = plan.workspace_bytes ? d.part_o + rows * p->head_dim : nullptr;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  d.part_o = reinterpret_cast<float*>(ws);
+  d.part_ml = reinterpret_cast<float*>(ws + plan.part_o_bytes);
+  d.pair_meta = reinterpret_cast<int2*>(ws + plan.part_o_bytes + plan.part_ml_bytes);
+  d.ticket = reinterpret_cast<int32_t*>(ws + plan.part_o_bytes + plan.part_ml_bytes +
+                                        plan.meta_bytes - 16);
   d.err = p->err;
   d.k_scale = p->scales;
   d.v_scale = p->scales + p->n_kv_heads;
   d.num_blocks = p->num_blocks;
   d.mbs = max_blocks_per_seq;
-  d.batch = batch;
   d.n_q_heads = n_q_heads;
   d.n_kv_heads = p->n_kv_heads;
   d.group = g;
   d.max_ctx = max_context_len;
   d.window = sliding_window > 0 ? sliding_window : 0;
-  d.part_blocks = plan.part_blocks;
-  d.max_parts = plan.max_parts;
+  d.num_workers = plan.workers;
   d.scale_log2 = scale * 1.4426950408889634f;
   d.wait_limit_ns = kWaitLimitNs;
 
-  DeviceGuard guard(p->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (p->ev_start && cudaEventRecord(p->ev_start, s) != cudaSuccess) return KV_ERR_CUDA;
-  if (pkv::launch_decode(p, d, s) != cudaSuccess) return KV_ERR_CUDA;
-  if (p->ev_stop && cudaEventRecord(p->ev_stop, s) != cudaSuccess) return KV_ERR_CUDA;
-  if (plan.max_parts > 1 && pkv::launch_reduce(p, d, s) != cudaSuccess) return KV_ERR_CUDA;
+  const bool timed = p->ev_start != nullptr;
+  // batches beyond one launch's table run as consecutive launches
+  for (int32_t b0 = 0; b0 < batch; b0 += plan.batch) {
+    const int32_t nb = std::min(plan.batch, batch - b0);
+    d.q = static_cast<const uint16_t*>(q) + static_cast<int64_t>(b0) * n_q_heads * p->head_dim;
+    d.block_tables = block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq;
+    d.context_lens = context_lens + b0;
+    d.out = out + static_cast<int64_t>(b0) * n_q_heads * p->head_dim;
+    d.batch = nb;
+    // The fused step's write kernel clears the ticket and lets the first
+    // decode launch start while it runs; otherwise a memset clears it.
+    const bool fused = w != nullptr && b0 == 0;
+    if (fused) {
+      if (pkv::launch_kv_write(p, w->k, w->v, w->slots, w->num_tokens, s, d.ticket) != cudaSuccess)
+        return KV_ERR_CUDA;
+    } else if (cudaMemsetAsync(d.ticket, 0, sizeof(int32_t), s) != cudaSuccess) {
+      return KV_ERR_CUDA;
+    }
+    if (timed && cudaEventRecord(p->ev_start, s) != cudaSuccess) return KV_ERR_CUDA;
+    if (pkv::launch_decode(p, d, s, fused && !timed) != cudaSuccess) return KV_ERR_CUDA;
+    if (timed && cudaEventRecord(p->ev_stop, s) != cudaSuccess) return KV_ERR_CUDA;
+    if (pkv::launch_reduce(p, d, s) != cudaSuccess) return KV_ERR_CUDA;
+  }
   return KV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kv_status paged_decode_attention(kv_pool* p, const void* q, int32_t n_q_heads,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* context_lens, int32_t batch,
+                                 int32_t max_context_len, float scale, int32_t sliding_window,
+                                 float* out, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  return decode_call(p, nullptr, q, n_q_heads, block_tables, max_blocks_per_seq, context_lens,
+                     batch, max_context_len, scale, sliding_window, out, workspace,
+                     workspace_bytes, stream);
+}
+
+kv_status paged_decode_step(kv_pool* p, const void* k, const void* v,
+                            const int64_t* slot_mapping, int64_t num_tokens, const void* q,
+                            int32_t n_q_heads, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* context_lens,
+                            int32_t batch, int32_t max_context_len, float scale,
+                            int32_t sliding_window, float* out, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  const StepWrite w{k, v, slot_mapping, num_tokens};
+  return decode_call(p, &w, q, n_q_heads, block_tables, max_blocks_per_seq, context_lens, batch,
+                     max_context_len, scale, sliding_window, out, workspace, workspace_bytes,
+                     stream);
 }
 
 kv_status kv_pool_set_partition_blocks(kv_pool* p, int32_t blocks_per_partition) {

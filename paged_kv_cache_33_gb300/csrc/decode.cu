@@ -1,4 +1,4 @@
-// Split-K paged decode attention for sm_103a, and its reduce.
+// Stream-K paged decode attention for sm_103a, and its reduce.
 //
 // What it computes ("Optimizing KV Cache Memory Management in vLLM with
 // PagedAttention and Dynamic Block Allocation", section "PagedAttention:
@@ -9,32 +9,48 @@
 // where token t is found in physical block table[b][t / 16] at offset t % 16.
 //
 // How (GB300 design):
-//  * Grid (partition, KV head, sequence).  A partition is a run of
-//    `part_blocks` consecutive logical blocks; one CTA per (b, h, partition)
-//    reads each K/V block once for all g = Hq/Hkv query heads of the group.
-//  * Every warp walks its own share of the partition's blocks (block i goes to
-//    warp i mod NW) through a private ring of STAGES shared-memory stages.
-//    Lane 0 resolves the physical block from the table and issues one TMA
-//    tensor copy per (block, head) (two for bf16 with head_dim 128), landing
-//    the K tile and the V tile with the 128-byte swizzle so that every
-//    ldmatrix below is bank-conflict free.  Completion is an mbarrier with a
-//    transaction count; every wait is bounded in wall time.
-//  * Scores S^T[16 tokens x 8 heads] = K Q^T on the tensor cores
-//    (mma.sync m16n8k16, fp32 accumulate), the online softmax in the exp2
-//    domain with warp shuffles over the token rows, and O^T[D x 8 heads] +=
-//    V^T P^T again on the tensor cores.  P^T is formed from the score
-//    accumulator by movmatrix.  For bf16 KV, P is split into a bf16 high part
-//    and a bf16 remainder so the product keeps ~16 bits of P; for FP8 KV,
-//    K and V are widened exactly from E4M3 to f16 and P is f16.
-//  * Masking uses selects: scores of positions outside [lo, ctx) become -inf
-//    and their V rows are zeroed before the product, so stale or NaN slots
-//    of a partly filled block never reach the result.
-//  * The warps of a CTA merge their (max, sum, O) in shared memory; a
-//    sequence with one partition writes its output directly, otherwise the
-//    partition's unnormalised partial goes to the workspace and the reduce
-//    kernel combines the partitions.
+//  * Work is the list of units (b, h, k-th attended block of b), ordered by
+//    b, then h, then k; one unit is one K tile and one V tile, read once for
+//    the g = Hq/Hkv query heads of its KV head.  Every CTA first builds a
+//    table of the batch in shared memory (context lengths and the prefix of
+//    units per sequence), so any unit is located by a binary search.
+//  * A persistent grid splits the list into segments: each warp streams a
+//    static share of the first ~75% of the units, then takes chunks of the
+//    rest from an atomic ticket counter -- 16 units, then 8, then 4 towards
+//    the end.  SMs do not all stream at the same rate; the dynamic tail lets
+//    fast warps absorb the difference, so the grid finishes together.
+//  * Each warp streams its segments through a private ring of STAGES shared
+//    memory stages without draining between them: lane 0 resolves the next
+//    unit's physical block from the table (read one issue ahead; a bad id is
+//    recorded and the block masked), writes the unit's coordinates into the
+//    stage's info slot and issues one or two 4-D TMA tensor copies, landing
+//    K and V with the 128-byte swizzle so every ldmatrix is free of bank
+//    conflicts.  Completion is an mbarrier with a transaction count; every
+//    wait is bounded in wall time.  A stage with no unit carries a sentinel.
+//  * S^T[16 tokens x 8 heads] = K Q^T on the tensor cores (mma.sync m16n8k16,
+//    fp32 accumulate); the V fragments are then moved to registers and the
+//    stage refilled at once; online softmax in the exp2 domain with warp
+//    shuffles over the token rows; O^T[D x 8 heads] += V^T P^T on the tensor
+//    cores.  P^T comes from the score accumulator by movmatrix.  For bf16 KV,
+//    P is a bf16 high part plus a bf16 remainder (two products) so ~16 bits
+//    of P survive; for FP8 KV, K and V are widened exactly from E4M3 to f16
+//    and P is f16.
+//  * Masking uses selects: scores outside [lo, ctx) become -inf and the V
+//    rows of masked positions are zeroed before the product, so stale or NaN
+//    slots of a partly filled block never reach the result.
+//  * A (b, h) pair inside one segment is normalised and written by its warp.
+//    A pair cut between segments leaves one unnormalised partial per segment
+//    in slot (segment + pair index) -- unique, because segments and pairs are
+//    both contiguous ranges of the same list -- and the warp holding the
+//    pair's first unit records (first segment, number of segments).  The
+//    reduce kernel, launched as a programmatic dependent of the decode
+//    kernel so that its CTAs are already resident, merges them.
+//  * Sequences with nothing to attend to get zeros from the CTAs' opening
+//    pass, which also reports context lengths out of bounds.
 
 #include <math.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
@@ -44,75 +60,198 @@ namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr uint64_t kShortWaitNs = 200000;  // wait bound once some warp has timed out
+#ifndef PKV_DYN_PCT
+#define PKV_DYN_PCT 25
+#endif
+#ifndef PKV_CHUNK_MAX
+#define PKV_CHUNK_MAX 16
+#endif
+constexpr int kDynNum = PKV_DYN_PCT, kDynDen = 100;  // dynamic share of the units
+// The dynamic part is cut into three regions of decreasing chunk size:
+// 60% in chunks of kChunkMax units, 30% in chunks of kChunkMax/2, the rest
+// in chunks of kChunkMax/4.
+constexpr int kChunkMax = PKV_CHUNK_MAX;   // region r uses chunks of kChunkMax >> r units
+constexpr int kRegion0Pct = 60, kRegion1Pct = 30;
 
 struct SeqRange {
   int32_t lo, ctx, first_blk, nblk;
-  bool bad;
 };
 
-// Attended positions [lo, ctx) of sequence b and the blocks that hold them.
-__device__ __forceinline__ SeqRange seq_range(const DecodeParams& p, int b) {
-  int32_t ctx = p.context_lens[b];
-  const bool bad = ctx < 0 || ctx > p.max_ctx || ctx > p.mbs * kBlockSize;
-  if (bad) ctx = 0;
+// Attended positions [lo, ctx) of a sequence and the blocks that hold them.
+__device__ __forceinline__ SeqRange seq_from_ctx(int32_t ctx, int32_t window) {
   SeqRange r;
   r.ctx = ctx;
-  r.bad = bad;
-  r.lo = p.window > 0 ? max(0, ctx - p.window) : 0;
+  r.lo = window > 0 ? max(0, ctx - window) : 0;
   r.first_blk = r.lo / kBlockSize;
   r.nblk = ctx > r.lo ? (ctx - 1) / kBlockSize - r.first_blk + 1 : 0;
   return r;
 }
 
+// A context length is usable when 0 <= ctx <= both bounds; others count as 0.
+__device__ __forceinline__ bool ctx_ok(const DecodeParams& p, int32_t ctx) {
+  return ctx >= 0 && ctx <= p.max_ctx && ctx <= p.mbs * kBlockSize;
+}
+
 template <int D, bool FP8>
 struct Geometry {
   static constexpr int kElem = FP8 ? 1 : 2;
-  static constexpr int kRowBytes = 128;                  // one swizzled smem row
-  static constexpr int kBoxes = FP8 ? 1 : D / 64;        // TMA boxes per (block, head)
+  static constexpr int kRowBytes = 128;                         // one swizzled smem row
+  static constexpr int kBoxes = FP8 ? 1 : D / 64;               // TMA boxes per unit
   static constexpr int kBoxBytes = 2 * kBlockSize * kRowBytes;  // K rows, then V rows
   static constexpr int kStageBytes = kBoxes * kBoxBytes;
-  static constexpr int kSteps = D / 16;                  // mma k-steps (QK) = m-tiles (PV)
+  static constexpr int kSteps = D / 16;                         // k-steps (QK) = m-tiles (PV)
   static_assert(kStageBytes == 2 * kBlockSize * D * kElem, "stage holds one K and one V tile");
   static_assert(!FP8 || D == 128, "FP8 rows are one 128-byte swizzle row");
 };
 
-template <int D, bool FP8, int NW, int STAGES>
-constexpr int decode_smem_bytes() {
-  return NW * STAGES * Geometry<D, FP8>::kStageBytes + NW * STAGES * 8 + 1024;
-}
+// Coordinates of the unit held by one ring stage (u < 0: no unit).
+struct StageInfo {
+  int32_t u, b, h, k, seg_end, seg;
+};
 
 template <int D, bool FP8, int NW, int STAGES>
-__global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_constant__ CUtensorMap tmap,
-                                                               const DecodeParams p) {
+struct Smem {
+  static constexpr int kRing = NW * STAGES * Geometry<D, FP8>::kStageBytes;
+  static constexpr int kBars = kRing;                          // uint64 [NW][STAGES]
+  static constexpr int kInfo = kBars + NW * STAGES * 8;        // StageInfo [NW][STAGES]
+  static constexpr int kCtx = kInfo + NW * STAGES * 24;        // int32 [kMaxDecodeBatch]
+  static constexpr int kPre = kCtx + kMaxDecodeBatch * 4;      // int32 [kMaxDecodeBatch + 1]
+  static constexpr int kScan = kPre + (kMaxDecodeBatch + 1) * 4 + 4;  // int32 [NW]
+  static constexpr int kBytes = kScan + NW * 4 + 1024;         // + alignment slack
+};
+
+// Position of one unit: sequence b, KV head h, k-th attended block of b.
+struct Cursor {
+  int b, h, k;
+  SeqRange r;
+};
+
+// The segments of one launch.  Static shares are [floor(w Ts / Ps),
+// floor((w+1) Ts / Ps)) for w < Ps; then chunk region r starts at unit
+// Ts, start1, start2 with chunks of kChunkMax, /2, /4 units, their first chunks being
+// tickets 0, ticket1, ticket2.  Segment ids: shares 0..Ps-1, then Ps + ticket.
+struct Split {
+  int T, Ts, Ps, Nc;
+  int start1, start2;      // first units of chunk regions 1 and 2 (region 0 starts at Ts)
+  int ticket1, ticket2;    // first tickets of regions 1 and 2
+
+  __device__ void init(int total, int P) {
+    T = total;
+    const int Td = T >= 8 * P ? static_cast<int>(static_cast<int64_t>(T) * kDynNum / kDynDen) : 0;
+    Ts = T - Td;
+    Ps = min(P, Ts);
+    const int r0 = Td * kRegion0Pct / 100 / kChunkMax * kChunkMax;
+    const int r1 = Td * kRegion1Pct / 100 / (kChunkMax >> 1) * (kChunkMax >> 1);
+    start1 = Ts + r0;
+    start2 = start1 + r1;
+    ticket1 = r0 / kChunkMax;
+    ticket2 = ticket1 + r1 / (kChunkMax >> 1);
+    Nc = ticket2 + (T - start2 + (kChunkMax >> 2) - 1) / (kChunkMax >> 2);
+  }
+  __device__ int seg_of(int u) const {
+    if (u < Ts) return static_cast<int>((static_cast<int64_t>(u + 1) * Ps - 1) / Ts);
+    if (u < start1) return Ps + (u - Ts) / kChunkMax;
+    if (u < start2) return Ps + ticket1 + (u - start1) / (kChunkMax >> 1);
+    return Ps + ticket2 + (u - start2) / (kChunkMax >> 2);
+  }
+  // [first, end) units of dynamic chunk `t` (t < Nc)
+  __device__ void chunk(int t, int& first, int& end) const {
+    if (t < ticket1) {
+      first = Ts + t * kChunkMax;
+      end = min(start1, first + kChunkMax);
+    } else if (t < ticket2) {
+      first = start1 + (t - ticket1) * (kChunkMax >> 1);
+      end = min(start2, first + (kChunkMax >> 1));
+    } else {
+      first = start2 + (t - ticket2) * (kChunkMax >> 2);
+      end = min(T, first + (kChunkMax >> 2));
+    }
+  }
+};
+
+template <int D, bool FP8, int NW, int STAGES>
+__global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                                  const DecodeParams p) {
   using G = Geometry<D, FP8>;
+  using S = Smem<D, FP8, NW, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment of the stage buffers keeps the 128-byte swizzle
   // pattern equal to (row mod 8).
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-
+  int32_t* s_ctx = reinterpret_cast<int32_t*>(smem + S::kCtx);
+  int32_t* s_pre = reinterpret_cast<int32_t*>(smem + S::kPre);
+  int32_t* s_scan = reinterpret_cast<int32_t*>(smem + S::kScan);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int part = blockIdx.x;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
-  const SeqRange r = seq_range(p, b);
-  if (r.bad && part == 0 && threadIdx.x == 0) atomicOr(p.err, kErrBadContext);
-  const int nparts = (r.nblk + p.part_blocks - 1) / p.part_blocks;
-  if (part >= max(nparts, 1)) return;  // uniform over the CTA
+  const int worker = blockIdx.x * NW + warp;
+  // the reduce kernel may be scheduled now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  const int g = p.group;
-  const int64_t row0 = static_cast<int64_t>(b) * p.n_q_heads + static_cast<int64_t>(h) * g;
-  if (r.nblk == 0) {  // nothing to attend to: zeros
-    for (int i = threadIdx.x; i < g * D; i += NW * 32) p.out[row0 * D + i] = 0.f;
-    return;
+  // ---- the batch table: usable context lengths and units before each sequence
+  {
+    constexpr int kThreads = NW * 32;
+    constexpr int kPer = kMaxDecodeBatch / kThreads + 1;
+    const int per = (p.batch + kThreads - 1) / kThreads;  // consecutive sequences per thread
+    const int b0 = threadIdx.x * per;
+    int32_t local[kPer];
+    int32_t sum = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      local[i] = 0;
+      const int b = b0 + i;
+      if (i < per && b < p.batch) {
+        int32_t ctx = p.context_lens[b];
+        if (!ctx_ok(p, ctx)) {
+          if (blockIdx.x == 0) atomicOr(p.err, kErrBadContext);
+          ctx = 0;
+        }
+        s_ctx[b] = ctx;
+        local[i] = seq_from_ctx(ctx, p.window).nblk * p.n_kv_heads;
+        sum += local[i];
+      }
+    }
+    // exclusive scan of the per-thread sums over the CTA
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_scan[warp] = incl;
+    __syncthreads();
+    int base = incl - sum;
+    for (int w = 0; w < warp; ++w) base += s_scan[w];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int b = b0 + i;
+      if (i < per && b < p.batch) s_pre[b] = base;
+      base += local[i];
+    }
+    if (threadIdx.x == kThreads - 1) s_pre[p.batch] = base;
+    __syncthreads();
+    // zero the outputs of sequences with nothing to attend to (CTA-strided)
+    for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+      if (s_pre[b + 1] == s_pre[b]) {
+        float* o = p.out + static_cast<int64_t>(b) * p.n_q_heads * D;
+        for (int x = threadIdx.x; x < p.n_q_heads * D; x += kThreads) o[x] = 0.f;
+      }
+    }
   }
-  const int blk_begin = r.first_blk + part * p.part_blocks;
-  const int blk_end = min(blk_begin + p.part_blocks, r.first_blk + r.nblk);
-  const int my_first = blk_begin + warp;
-  const int my_n = my_first < blk_end ? (blk_end - my_first + NW - 1) / NW : 0;
+
+  // Launched after the KV write of the same step as its programmatic
+  // dependent, this kernel has built its table while the write ran; the pool
+  // and the ticket counter are read only after the write has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("fence.proxy.async;" ::: "memory");
+
+  // ---- the split of this call's units into segments
+  Split sp;
+  sp.init(s_pre[p.batch], p.num_workers);
+  if (sp.T == 0) return;
 
   uint8_t* ring = smem + warp * STAGES * G::kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * STAGES * G::kStageBytes) + warp * STAGES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBars) + warp * STAGES;
+  StageInfo* info = reinterpret_cast<StageInfo*>(smem + S::kInfo) + warp * STAGES;
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) mbar_init(smem_addr(&bars[s]), 1);
@@ -120,79 +259,110 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
   }
   __syncwarp();
 
-  const int32_t* table = p.block_tables + static_cast<int64_t>(b) * p.mbs;
-
-  // Lane 0: stage logical block (my_first + it * NW) into ring slot it % STAGES.
-  auto issue = [&](int it) {
-    const int lb = my_first + it * NW;
-    int phys = table[lb];
-    if (phys < 0 || phys >= p.num_blocks) {
-      atomicOr(p.err, kErrBadBlock);
-      phys = 0;  // a valid address; every position of this block is masked below
+  // Cursor of unit u (u < T): binary search of the batch table.
+  auto locate = [&](int u) {
+    int lo = 0, hi = p.batch - 1;  // largest b with s_pre[b] <= u
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_pre[mid] <= u) lo = mid; else hi = mid - 1;
     }
-    const int s = it % STAGES;
+    Cursor c;
+    c.b = lo;
+    c.r = seq_from_ctx(s_ctx[lo], p.window);
+    const int off = u - s_pre[lo];
+    c.h = off / c.r.nblk;
+    c.k = off - c.h * c.r.nblk;
+    return c;
+  };
+  auto table_entry = [&](const Cursor& c) {
+    return p.block_tables[static_cast<int64_t>(c.b) * p.mbs + c.r.first_blk + c.k];
+  };
+
+  // ---- issue side (lane 0): the next unit to stage, in segment order
+  Cursor ic{};
+  int iu = 0, iu_end = 0, iseg = 0;
+  bool idone = false;
+  int next_phys = 0;
+  uint32_t bad_stages = 0, tma_stages = 0;
+  auto next_segment = [&]() {
+    const int t = atomicAdd(p.ticket, 1);
+    if (t >= sp.Nc) {
+      idone = true;
+      return;
+    }
+    sp.chunk(t, iu, iu_end);
+    iseg = sp.Ps + t;
+    ic = locate(iu);
+    next_phys = table_entry(ic);
+  };
+  auto issue = [&](int s) {
     const uint32_t bar = smem_addr(&bars[s]);
+    if (idone) {  // sentinel: no unit, the phase completes on the arrival alone
+      info[s].u = -1;
+      tma_stages &= ~(1u << s);
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+      return;
+    }
+    int phys = next_phys;
+    const bool bad = phys < 0 || phys >= p.num_blocks;
+    if (bad) {
+      atomicOr(p.err, kErrBadBlock);
+      phys = 0;  // a valid address; every position of this block is masked
+    }
+    bad_stages = (bad_stages & ~(1u << s)) | (static_cast<uint32_t>(bad) << s);
+    tma_stages |= 1u << s;
+    info[s] = StageInfo{iu, ic.b, ic.h, ic.k, iu_end, iseg};
     const uint32_t dst = smem_addr(ring + s * G::kStageBytes);
     mbar_arrive_expect_tx(bar, G::kStageBytes);
 #pragma unroll
     for (int bx = 0; bx < G::kBoxes; ++bx)
-      tma_load_4d(dst + bx * G::kBoxBytes, &tmap, bar, bx * 64, 0, 0, phys * p.n_kv_heads + h);
+      tma_load_4d(dst + bx * G::kBoxBytes, &tmap, bar, bx * 64, 0, 0, phys * p.n_kv_heads + ic.h);
+    // step to the next unit: within the segment, or the next chunk
+    if (++iu < iu_end) {
+      if (++ic.k == ic.r.nblk) {
+        ic.k = 0;
+        if (++ic.h == p.n_kv_heads) {
+          ic.h = 0;
+          do {
+            ++ic.b;
+            ic.r = seq_from_ctx(s_ctx[ic.b], p.window);
+          } while (ic.r.nblk == 0);
+        }
+      }
+      next_phys = table_entry(ic);
+    } else {
+      next_segment();
+    }
   };
   if (lane == 0) {
-    const int pre = min(STAGES, my_n);
-    for (int it = 0; it < pre; ++it) issue(it);
+    if (worker < sp.Ps) {
+      iu = static_cast<int>(static_cast<int64_t>(sp.Ts) * worker / sp.Ps);
+      iu_end = static_cast<int>(static_cast<int64_t>(sp.Ts) * (worker + 1) / sp.Ps);
+      iseg = worker;
+      ic = locate(iu);
+      next_phys = table_entry(ic);
+    } else {
+      next_segment();
+    }
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) issue(s);
   }
 
-  // ---- query fragments: B operand of S^T = K Q^T (k = head_dim, n = query head)
-  const int n = lane >> 2;  // query head of the group this lane feeds (n < 8)
+  // ---- compute side
+  const int n = lane >> 2;  // query head (within the group) this lane feeds, and token row
   const int j = lane & 3;
+  const int g = p.group;
+  const int trow_k = (lane & 7) + (((lane >> 3) & 1) << 3);  // ldmatrix row for K / FP8 V
+  const int swz = lane & 7;                                    // swizzle phase of that row
+
   uint32_t qf[G::kSteps][2];
   float score_scale = p.scale_log2;
-  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) + row0 * D;
-  if constexpr (!FP8) {
-    const uint32_t* qr = reinterpret_cast<const uint32_t*>(qg + n * D);
-#pragma unroll
-    for (int ks = 0; ks < G::kSteps; ++ks) {
-      qf[ks][0] = n < g ? qr[(ks * 16 + 2 * j) >> 1] : 0u;
-      qf[ks][1] = n < g ? qr[(ks * 16 + 8 + 2 * j) >> 1] : 0u;
-    }
-  } else {
-    // f16 operands: bring the group's queries into (-1, 1) by an exact power
-    // of two and fold that power back into the score scale.
-    float amax = 0.f;
-    for (int i = lane; i < g * D; i += 32) amax = fmaxf(amax, fabsf(__bfloat162float(qg[i])));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-    int e = 0;
-    if (amax > 0.f) frexpf(amax, &e);
-    const float qs = ldexpf(1.f, -e);
-    score_scale = p.scale_log2 * p.k_scale[h] * ldexpf(1.f, e);
-    // k-slot order matching the widened E4M3 fragments: slots 2j, 2j+1 hold
-    // d = 16c + 4j + {0, 1}; slots 2j+8, 2j+9 hold d = 16c + 4j + {2, 3}.
-#pragma unroll
-    for (int c = 0; c < G::kSteps; ++c) {
-      float v4[4] = {0.f, 0.f, 0.f, 0.f};
-      if (n < g) {
-#pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) v4[e4] = __bfloat162float(qg[n * D + 16 * c + 4 * j + e4]) * qs;
-      }
-      qf[c][0] = pack_f16x2(v4[0], v4[1]);
-      qf[c][1] = pack_f16x2(v4[2], v4[3]);
-    }
-  }
-
-  // ---- running state for query heads 2j and 2j+1
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   float acc[G::kSteps][4];
-#pragma unroll
-  for (int i = 0; i < G::kSteps; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-
-  const int trow_k = (lane & 7) + (((lane >> 3) & 1) << 3);  // ldmatrix row for the K operand
-  const int swz = lane & 7;                                    // 128B-swizzle phase of that row
+  int prev_u = -2;
   bool timed_out = false;
   int it = 0;
-  for (; it < my_n; ++it) {
+  for (;; ++it) {
     const int s = it % STAGES;
     const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (it / STAGES) & 1, p.wait_limit_ns,
                                       p.err, kErrTimeout, kShortWaitNs);
@@ -200,9 +370,54 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
       timed_out = true;
       break;
     }
-    const int lb = my_first + it * NW;
-    const int phys = table[lb];
-    const bool blk_ok = phys >= 0 && phys < p.num_blocks;
+    const StageInfo si = info[s];
+    if (si.u < 0) break;
+    const SeqRange r = seq_from_ctx(s_ctx[si.b], p.window);
+    const int64_t row0 = static_cast<int64_t>(si.b) * p.n_q_heads + static_cast<int64_t>(si.h) * g;
+    if (si.u != prev_u + 1 || si.k == 0) {
+      // ---- a new piece of a (b, h) pair: its query fragments, a fresh state
+      const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) + row0 * D;
+      if constexpr (!FP8) {
+        const uint32_t* qr = reinterpret_cast<const uint32_t*>(qg + n * D);
+#pragma unroll
+        for (int ks = 0; ks < G::kSteps; ++ks) {
+          qf[ks][0] = n < g ? qr[(ks * 16 + 2 * j) >> 1] : 0u;
+          qf[ks][1] = n < g ? qr[(ks * 16 + 8 + 2 * j) >> 1] : 0u;
+        }
+      } else {
+        // f16 operands: bring the group's queries into (-1, 1) by an exact
+        // power of two and fold that power back into the score scale.
+        float amax = 0.f;
+        for (int i = lane; i < g * D; i += 32) amax = fmaxf(amax, fabsf(__bfloat162float(qg[i])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+        int e = 0;
+        if (amax > 0.f) frexpf(amax, &e);
+        const float qs = ldexpf(1.f, -e);
+        score_scale = p.scale_log2 * p.k_scale[si.h] * ldexpf(1.f, e);
+        // k-slot order matching the widened E4M3 fragments: slots 2j, 2j+1
+        // hold d = 16c + 4j + {0, 1}; slots 2j+8, 2j+9 hold d = 16c + 4j + {2, 3}.
+#pragma unroll
+        for (int c = 0; c < G::kSteps; ++c) {
+          float v4[4] = {0.f, 0.f, 0.f, 0.f};
+          if (n < g) {
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4)
+              v4[e4] = __bfloat162float(qg[n * D + 16 * c + 4 * j + e4]) * qs;
+          }
+          qf[c][0] = pack_f16x2(v4[0], v4[1]);
+          qf[c][1] = pack_f16x2(v4[2], v4[3]);
+        }
+      }
+      m_run[0] = m_run[1] = -INFINITY;
+      l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+      for (int i = 0; i < G::kSteps; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    }
+    prev_u = si.u;
+
+    const int lb = r.first_blk + si.k;
+    const bool blk_ok = ((__shfl_sync(kFull, bad_stages, 0) >> s) & 1u) == 0;
     const int t0 = lb * kBlockSize;
     const bool full = blk_ok && t0 >= r.lo && t0 + kBlockSize <= r.ctx;
     auto tok_ok = [&](int tr) {
@@ -238,6 +453,33 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         mma_f16(sb, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
                 e4m3x2_to_f16x2(r3 >> 16), qf[cp + 1][0], qf[cp + 1][1]);
       }
+    }
+
+    // ---- V fragments to registers; then the stage is refilled at once, so
+    //      both ring stages are in flight while the softmax and V^T P^T run
+    uint32_t vf[G::kSteps][4];
+    if constexpr (!FP8) {
+      const int trow_v = kBlockSize + (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+      for (int mt = 0; mt < G::kSteps; ++mt) {
+        const int chunk = ((mt & 3) << 1) + ((lane >> 3) & 1);
+        const uint32_t addr = st + (mt >> 2) * G::kBoxBytes + trow_v * G::kRowBytes +
+                              ((chunk ^ swz) << 4);
+        ldsm_x4_trans(addr, vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
+      }
+    } else {
+#pragma unroll
+      for (int cp = 0; cp < G::kSteps; cp += 2) {
+        const int chunk = cp + (lane >> 4);
+        const uint32_t addr = st + (kBlockSize + trow_k) * G::kRowBytes + ((chunk ^ swz) << 4);
+        // V[token n or n+8][16 codes of chunk cp or cp+1]
+        ldsm_x4(addr, vf[cp >> 1][0], vf[cp >> 1][1], vf[cp >> 1][2], vf[cp >> 1][3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      fence_proxy_async_smem();  // this stage's reads happen before the next copy lands
+      issue(s);
     }
 
     // ---- online softmax (log2 domain); this lane holds tokens n, n+8 of heads 2j, 2j+1
@@ -283,18 +525,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         mlo = (tok_ok(2 * j) ? 0x0000ffffu : 0u) | (tok_ok(2 * j + 1) ? 0xffff0000u : 0u);
         mhi = (tok_ok(2 * j + 8) ? 0x0000ffffu : 0u) | (tok_ok(2 * j + 9) ? 0xffff0000u : 0u);
       }
-      const int trow_v = kBlockSize + (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
       for (int mt = 0; mt < G::kSteps; ++mt) {
-        const int chunk = ((mt & 3) << 1) + ((lane >> 3) & 1);
-        const uint32_t addr = st + (mt >> 2) * G::kBoxBytes + trow_v * G::kRowBytes +
-                              ((chunk ^ swz) << 4);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_trans(addr, a0, a1, a2, a3);
-        a0 &= mlo;
-        a1 &= mlo;
-        a2 &= mhi;
-        a3 &= mhi;
+        const uint32_t a0 = vf[mt][0] & mlo, a1 = vf[mt][1] & mlo;
+        const uint32_t a2 = vf[mt][2] & mhi, a3 = vf[mt][3] & mhi;
         mma_bf16(acc[mt], a0, a1, a2, a3, bh0, bh1);
         mma_bf16(acc[mt], a0, a1, a2, a3, bl0, bl1);
       }
@@ -303,10 +537,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
       const uint32_t b1 = movmatrix_trans(pack_f16x2(p2, p3));
 #pragma unroll
       for (int cp = 0; cp < G::kSteps; cp += 2) {
-        const int chunk = cp + (lane >> 4);
-        const uint32_t addr = st + (kBlockSize + trow_k) * G::kRowBytes + ((chunk ^ swz) << 4);
-        uint32_t r0, r1, r2, r3;  // V[token n or n+8][16 codes of chunk cp or cp+1]
-        ldsm_x4(addr, r0, r1, r2, r3);
+        uint32_t r0 = vf[cp >> 1][0], r1 = vf[cp >> 1][1], r2 = vf[cp >> 1][2], r3 = vf[cp >> 1][3];
         if (!v0) r0 = r2 = 0u;
         if (!v1) r1 = r3 = 0u;
         mma_f16(acc[cp], movmatrix_trans(e4m3x2_to_f16x2(r0)),
@@ -318,144 +549,254 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
       }
     }
 
-    __syncwarp();
-    if (lane == 0 && it + STAGES < my_n) {
-      fence_proxy_async_smem();  // this stage's reads happen before the next copy lands
-      issue(it + STAGES);
+    // ---- end of this piece of pair (b, h): write it out
+    if (si.k == r.nblk - 1 || si.u + 1 == si.seg_end) {
+      float l0 = l_run[0], l1 = l_run[1];
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(kFull, l0, o);
+        l1 += __shfl_xor_sync(kFull, l1, o);
+      }
+      const int pair = si.b * p.n_kv_heads + si.h;
+      const int pair_start = si.u - si.k;
+      const int first_seg = sp.seg_of(pair_start);
+      const int cnt = sp.seg_of(pair_start + r.nblk - 1) - first_seg + 1;
+      const bool whole = cnt == 1;
+      const float vsc = FP8 ? p.v_scale[si.h] : 1.f;
+      const int h0 = 2 * j, h1 = 2 * j + 1;  // query heads of this lane's columns
+      const float f0 = whole ? (l0 > 0.f ? vsc / l0 : 0.f) : vsc;
+      const float f1 = whole ? (l1 > 0.f ? vsc / l1 : 0.f) : vsc;
+      float* dst = whole ? p.out + row0 * D
+                         : p.part_o + (static_cast<int64_t>(si.seg) + pair) * g * D;
+#pragma unroll
+      for (int i = 0; i < G::kSteps; ++i) {
+        int da, db;  // head_dim rows of accumulator entries {0,1} and {2,3}
+        if constexpr (!FP8) {
+          da = 16 * i + n;
+          db = da + 8;
+        } else {
+          da = 16 * i + 4 * (n >> 1) + (n & 1);
+          db = da + 2;
+        }
+        if (h0 < g) {
+          dst[h0 * D + da] = acc[i][0] * f0;
+          dst[h0 * D + db] = acc[i][2] * f0;
+        }
+        if (h1 < g) {
+          dst[h1 * D + da] = acc[i][1] * f1;
+          dst[h1 * D + db] = acc[i][3] * f1;
+        }
+      }
+      if (!whole && n == 0) {
+        float* ml = p.part_ml + (static_cast<int64_t>(si.seg) + pair) * g * 2;
+        if (h0 < g) {
+          ml[2 * h0] = m_run[0];
+          ml[2 * h0 + 1] = l0;
+        }
+        if (h1 < g) {
+          ml[2 * h1] = m_run[1];
+          ml[2 * h1 + 1] = l1;
+        }
+      }
+      if (lane == 0 && si.seg == first_seg) p.pair_meta[pair] = make_int2(first_seg, cnt);
     }
   }
 
-  if (timed_out) {
-    if (lane == 0) {
-      atomicOr(p.err, kErrTimeout);
-      const int issued = min(my_n, it + STAGES);
-      for (int k = it; k < issued; ++k)
+  if (timed_out && lane == 0) {
+    // leave no copy in flight: wait (bounded) for every stage holding one
+    atomicOr(p.err, kErrTimeout);
+    for (int k = it; k < it + STAGES; ++k)
+      if ((tma_stages >> (k % STAGES)) & 1u)
         mbar_wait_bounded(smem_addr(&bars[k % STAGES]), (k / STAGES) & 1, p.wait_limit_ns, p.err,
                           kErrTimeout, kShortWaitNs);
-    }
-    __syncwarp();
-  }
-
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    l_run[0] += __shfl_xor_sync(kFull, l_run[0], o);
-    l_run[1] += __shfl_xor_sync(kFull, l_run[1], o);
-  }
-
-  // ---- merge the warps of this CTA in shared memory (the rings are idle now)
-  __syncthreads();
-  float* mbuf = reinterpret_cast<float*>(smem);  // [NW][8 max | 8 sum]
-  float* obuf = mbuf + NW * 16;                   // [NW][8 heads][D]
-  if (lane < 4) {
-    mbuf[warp * 16 + 2 * lane] = m_run[0];
-    mbuf[warp * 16 + 2 * lane + 1] = m_run[1];
-    mbuf[warp * 16 + 8 + 2 * lane] = l_run[0];
-    mbuf[warp * 16 + 8 + 2 * lane + 1] = l_run[1];
-  }
-  float* ow = obuf + warp * 8 * D;
-#pragma unroll
-  for (int i = 0; i < G::kSteps; ++i) {
-    int da, db;  // head_dim rows of accumulator entries {0,1} and {2,3}
-    if constexpr (!FP8) {
-      da = 16 * i + n;
-      db = da + 8;
-    } else {
-      da = 16 * i + 4 * (n >> 1) + (n & 1);
-      db = da + 2;
-    }
-    ow[(2 * j) * D + da] = acc[i][0];
-    ow[(2 * j + 1) * D + da] = acc[i][1];
-    ow[(2 * j) * D + db] = acc[i][2];
-    ow[(2 * j + 1) * D + db] = acc[i][3];
-  }
-  __syncthreads();
-
-  const bool single = nparts == 1;
-  const float vsc = FP8 ? p.v_scale[h] : 1.f;
-  for (int idx = threadIdx.x; idx < g * D; idx += NW * 32) {
-    const int hd = idx / D;
-    const int d = idx - hd * D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, mbuf[w * 16 + hd]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float f = fast_exp2(mbuf[w * 16 + hd] - M);
-        L += f * mbuf[w * 16 + 8 + hd];
-        O += f * obuf[(w * 8 + hd) * D + d];
-      }
-    }
-    O *= vsc;
-    if (single) {
-      p.out[(row0 + hd) * D + d] = L > 0.f ? O / L : 0.f;
-    } else {
-      const int64_t pi = (row0 + hd) * p.max_parts + part;
-      p.part_o[pi * D + d] = O;
-      if (d == 0) {
-        p.part_ml[2 * pi] = M;
-        p.part_ml[2 * pi + 1] = L;
-      }
-    }
   }
 }
 
-// Combine the partitions of one (sequence, query head):
-//   out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
+// Merge the partials of pairs cut between segments:
+//   out = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k,  M = max_k m_k.
+// One CTA per (sequence, KV head) pair; thread = (k-slice, query head, 4
+// columns).  Each k-slice folds every KS-th partial with a running maximum,
+// then slice 0 combines the slices in shared memory.  Launched as a
+// programmatic dependent of the decode kernel: everything before
+// griddepcontrol.wait reads only inputs of the call.
 template <int D>
-__global__ void __launch_bounds__(D) paged_decode_reduce_kernel(const DecodeParams p) {
-  const int hq = blockIdx.x;
-  const int b = blockIdx.y;
-  const SeqRange r = seq_range(p, b);
-  const int np = (r.nblk + p.part_blocks - 1) / p.part_blocks;
-  if (np <= 1) return;  // the decode kernel wrote this row itself
-  const int64_t base = (static_cast<int64_t>(b) * p.n_q_heads + hq) * p.max_parts;
-  const float* ml = p.part_ml + 2 * base;
-  float M = -INFINITY;
-  for (int i = 0; i < np; ++i) M = fmaxf(M, ml[2 * i]);
-  float L = 0.f, O = 0.f;
-  const int d = threadIdx.x;
-  if (M != -INFINITY) {
-    for (int i = 0; i < np; ++i) {
-      const float f = fast_exp2(ml[2 * i] - M);
-      L += f * ml[2 * i + 1];
-      O += f * p.part_o[(base + i) * D + d];
+__global__ void __launch_bounds__(512) paged_decode_reduce_kernel(const DecodeParams p) {
+  constexpr int kGroups = D / 4;  // float4 column groups per head
+  __shared__ float4 s_o[512];
+  __shared__ float2 s_ml[512];
+  const int pair = blockIdx.x;
+  const int b = pair / p.n_kv_heads;
+  const int h = pair - b * p.n_kv_heads;
+  const int g = p.group;
+  const int lanes = g * kGroups;  // threads of one k-slice
+  const int KS = blockDim.x / lanes;
+  const int ks = threadIdx.x / lanes;
+  const int idx = threadIdx.x - ks * lanes;
+  const int hd = idx / kGroups;
+  const int c4 = idx - hd * kGroups;
+  int32_t ctx = p.context_lens[b];
+  if (!ctx_ok(p, ctx)) ctx = 0;
+  const SeqRange r = seq_from_ctx(ctx, p.window);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (r.nblk == 0) return;  // empty sequences were zeroed by the decode kernel
+  const int2 meta = p.pair_meta[pair];
+  const int cnt = meta.y;
+  if (cnt <= 1) return;  // finished by the one warp that held it
+  const int64_t slot0 = static_cast<int64_t>(meta.x) + pair;
+  float M = -INFINITY, L = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = ks; k0 < cnt; k0 += 4 * KS) {
+    float2 ml[4];
+    float4 o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int k = k0 + i * KS;
+      const int kk = k < cnt ? k : k0;
+      ml[i] = *reinterpret_cast<const float2*>(&p.part_ml[((slot0 + kk) * g + hd) * 2]);
+      o[i] = *reinterpret_cast<const float4*>(&p.part_o[((slot0 + kk) * g + hd) * D + 4 * c4]);
+      if (k >= cnt) ml[i] = make_float2(-INFINITY, 0.f);
+    }
+    float mb = M;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mb = fmaxf(mb, ml[i].x);
+    if (mb == -INFINITY) continue;
+    const float a = fast_exp2(M - mb);  // rescale what was folded so far
+    L *= a;
+    O.x *= a;
+    O.y *= a;
+    O.z *= a;
+    O.w *= a;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float f = fast_exp2(ml[i].x - mb);
+      L += f * ml[i].y;
+      O.x += f * o[i].x;
+      O.y += f * o[i].y;
+      O.z += f * o[i].z;
+      O.w += f * o[i].w;
+    }
+    M = mb;
+  }
+  s_o[threadIdx.x] = O;
+  s_ml[threadIdx.x] = make_float2(M, L);
+  __syncthreads();
+  if (ks != 0) return;
+  float Mt = -INFINITY;
+  for (int q = 0; q < KS; ++q) Mt = fmaxf(Mt, s_ml[q * lanes + idx].x);
+  float Lt = 0.f;
+  float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (Mt != -INFINITY) {
+    for (int q = 0; q < KS; ++q) {
+      const float2 ml = s_ml[q * lanes + idx];
+      const float4 o = s_o[q * lanes + idx];
+      const float f = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - Mt);
+      Lt += f * ml.y;
+      Ot.x += f * o.x;
+      Ot.y += f * o.y;
+      Ot.z += f * o.z;
+      Ot.w += f * o.w;
     }
   }
-  p.out[(static_cast<int64_t>(b) * p.n_q_heads + hq) * D + d] = L > 0.f ? O / L : 0.f;
+  const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+  float4* dst = reinterpret_cast<float4*>(
+      p.out + (static_cast<int64_t>(b) * p.n_q_heads + static_cast<int64_t>(h) * g + hd) * D) + c4;
+  *dst = make_float4(Ot.x * inv, Ot.y * inv, Ot.z * inv, Ot.w * inv);
 }
 
 template <int D, bool FP8, int NW, int STAGES>
-cudaError_t launch_variant(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream) {
-  constexpr int smem = decode_smem_bytes<D, FP8, NW, STAGES>();
-  auto kernel = paged_decode_kernel<D, FP8, NW, STAGES>;
-  static bool attr_set = false;  // per instantiation; setting it again is harmless
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
+struct Variant {
+  static constexpr int kSmem = Smem<D, FP8, NW, STAGES>::kBytes;
+  static constexpr int kWarps = NW;
+
+  // Opt in to the dynamic shared memory once; report resident CTAs per SM.
+  static int ctas_per_sm() {
+    static int ctas = -1;
+    if (ctas < 0) {
+      auto kernel = paged_decode_kernel<D, FP8, NW, STAGES>;
+      int n = 0;
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+              cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, NW * 32, kSmem) !=
+              cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+      }
+      ctas = n > 0 ? n : 1;
+    }
+    return ctas;
   }
-  dim3 grid(p.max_parts, p.n_kv_heads, p.batch);
-  kernel<<<grid, NW * 32, smem, stream>>>(pool->tmap, p);
-  return cudaGetLastError();
-}
+
+  static cudaError_t launch(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream,
+                            bool dependent) {
+    ctas_per_sm();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.num_workers + NW - 1) / NW);
+    cfg.blockDim = dim3(NW * 32);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, FP8, NW, STAGES>, pool->tmap, p);
+  }
+};
+
+// Warps per CTA and ring stages per warp of each variant.
+#ifndef PKV_BF16_WARPS
+#define PKV_BF16_WARPS 4
+#endif
+#ifndef PKV_BF16_STAGES
+#define PKV_BF16_STAGES 2
+#endif
+#ifndef PKV_FP8_WARPS
+#define PKV_FP8_WARPS 4
+#endif
+#ifndef PKV_FP8_STAGES
+#define PKV_FP8_STAGES 4
+#endif
+
+using Bf16D128 = Variant<128, false, PKV_BF16_WARPS, PKV_BF16_STAGES>;
+using Bf16D64 = Variant<64, false, 4, 4>;
+using Fp8D128 = Variant<128, true, PKV_FP8_WARPS, PKV_FP8_STAGES>;
 
 }  // namespace
 
-cudaError_t launch_decode(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream) {
-  if (pool->dtype == KV_FP8_E4M3) return launch_variant<128, true, 4, 4>(pool, p, stream);
-  if (pool->head_dim == 128) return launch_variant<128, false, 4, 3>(pool, p, stream);
-  return launch_variant<64, false, 4, 4>(pool, p, stream);
+int decode_warps_per_cta(const kv_pool* pool) {
+  if (pool->dtype == KV_FP8_E4M3) return Fp8D128::kWarps;
+  return pool->head_dim == 128 ? Bf16D128::kWarps : Bf16D64::kWarps;
+}
+
+int decode_ctas_per_sm(const kv_pool* pool) {
+  if (pool->dtype == KV_FP8_E4M3) return Fp8D128::ctas_per_sm();
+  return pool->head_dim == 128 ? Bf16D128::ctas_per_sm() : Bf16D64::ctas_per_sm();
+}
+
+int decode_chunk_units() { return kChunkMax >> 2; }
+int64_t decode_dynamic_units(int64_t total) { return total * kDynNum / kDynDen; }
+
+cudaError_t launch_decode(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream,
+                          bool dependent) {
+  if (pool->dtype == KV_FP8_E4M3) return Fp8D128::launch(pool, p, stream, dependent);
+  if (pool->head_dim == 128) return Bf16D128::launch(pool, p, stream, dependent);
+  return Bf16D64::launch(pool, p, stream, dependent);
 }
 
 cudaError_t launch_reduce(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream) {
-  dim3 grid(p.n_q_heads, p.batch);
-  if (pool->head_dim == 128)
-    paged_decode_reduce_kernel<128><<<grid, 128, 0, stream>>>(p);
-  else
-    paged_decode_reduce_kernel<64><<<grid, 64, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.batch) * p.n_kv_heads);
+  const int lanes = p.group * pool->head_dim / 4;  // threads per k-slice
+  cfg.blockDim = dim3(lanes * std::max(1, std::min(4, 512 / lanes)));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (pool->head_dim == 128) return cudaLaunchKernelEx(&cfg, paged_decode_reduce_kernel<128>, p);
+  return cudaLaunchKernelEx(&cfg, paged_decode_reduce_kernel<64>, p);
 }
 
 }  // namespace pkv

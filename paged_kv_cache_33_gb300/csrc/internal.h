@@ -24,39 +24,69 @@ struct kv_pool {
 
 namespace pkv {
 
-// Arguments of the split-K decode and its reduce, shared by all variants.
+// Sequences per decode launch: every CTA keeps a table of the batch in shared
+// memory.  Larger batches are split into several launches by the host.
+constexpr int kMaxDecodeBatch = 512;
+
+// Arguments of the stream-K decode, shared by all variants.
+//
+// The work of one call is the sequence of "units" (sequence b, KV head h,
+// k-th attended block of b), ordered by b, then h, then k, cut into
+// segments: `num_workers` static shares of its first part, then fixed-size
+// chunks of the rest handed out through `ticket`.  A (b, h) pair inside one
+// segment is finished by the warp that holds it; a pair cut between segments
+// leaves one partial per segment in slot (segment + pair index), merged by
+// the reduce kernel.
 struct DecodeParams {
   const void* q;                // bf16 [B][Hq][D]
   const int32_t* block_tables;  // [B][mbs]
   const int32_t* context_lens;  // [B]
   float* out;                   // [B][Hq][D]
-  float* part_o;                // [B][Hq][max_parts][D]  unnormalised partial outputs
-  float* part_ml;               // [B][Hq][max_parts][2]  (running max in log2 units, sum)
+  float* part_o;                // [slots][g][D]  unnormalised partial outputs
+  float* part_ml;               // [slots][g][2]  (max in log2 units, sum)
+  int2* pair_meta;              // [B*Hkv]  (first segment, number of segments) per pair
+  int32_t* ticket;              // next dynamic chunk; zero at launch
   uint32_t* err;
   const float* k_scale;         // fp8: [Hkv]
   const float* v_scale;
   int64_t num_blocks;
   int32_t mbs, batch, n_q_heads, n_kv_heads, group;
-  int32_t max_ctx, window, part_blocks, max_parts;
+  int32_t max_ctx, window, num_workers;
   float scale_log2;             // softmax scale * log2(e)
   uint64_t wait_limit_ns;
 };
 
-// Geometry of the split-K launch for one call.
+// Geometry of one call.
 struct DecodePlan {
-  int32_t part_blocks;   // blocks per partition
-  int32_t max_parts;     // partitions of the longest sequence
+  int32_t ctas;          // persistent CTAs of the decode kernel
+  int32_t workers;       // warps sharing the work (ctas * warps per CTA)
+  int32_t batch;         // sequences per launch (<= kMaxDecodeBatch)
+  size_t part_o_bytes, part_ml_bytes, meta_bytes;
   size_t workspace_bytes;
 };
 
 DecodePlan plan_decode(const kv_pool* pool, int32_t batch, int32_t n_q_heads,
                        int32_t max_context_len, int32_t sliding_window);
 
+// Warps per CTA and resident CTAs per SM of the decode variant the pool uses.
+int decode_warps_per_cta(const kv_pool* pool);
+int decode_ctas_per_sm(const kv_pool* pool);
+// Units per dynamic chunk, and the dynamic part of a call with `total` units.
+int decode_chunk_units();
+int64_t decode_dynamic_units(int64_t total);
+
+// The KV write; with `zero_word` it also clears that int (the decode's ticket
+// counter) and lets a programmatic dependent launch early.
 cudaError_t launch_kv_write(const kv_pool* pool, const void* k, const void* v,
-                            const int64_t* slots, int64_t num_tokens, cudaStream_t stream);
+                            const int64_t* slots, int64_t num_tokens, cudaStream_t stream,
+                            int32_t* zero_word = nullptr);
 
-cudaError_t launch_decode(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream);
+// The decode kernel; `dependent`: launch as a programmatic dependent of the
+// kernel before it on the stream (the KV write of the same step).
+cudaError_t launch_decode(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream,
+                          bool dependent);
 
+// The merge of cut pairs, launched as a programmatic dependent of the decode.
 cudaError_t launch_reduce(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream);
 
 }  // namespace pkv

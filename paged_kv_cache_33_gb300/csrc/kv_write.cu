@@ -11,6 +11,8 @@
 // 16 bytes of destination; consecutive threads cover one destination row, so
 // every store is a full, coalesced 16-byte vector.
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -22,8 +24,12 @@ template <int D>
 __global__ void __launch_bounds__(256) kv_write_bf16_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
     int64_t num_tokens, int hkv, int64_t num_slots, uint4* __restrict__ pool,
-    uint32_t* __restrict__ err) {
+    uint32_t* __restrict__ err, int32_t* __restrict__ zero_word) {
   constexpr int kChunks = D / 8;  // 16-byte chunks per row
+  // a decode launched as this kernel's programmatic dependent may start now;
+  // it waits for this grid to complete before it reads the pool
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (zero_word && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t total = num_tokens * hkv * 2 * kChunks;
   if (i >= total) return;
@@ -53,8 +59,10 @@ template <int D>
 __global__ void __launch_bounds__(256) kv_write_fp8_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
     int64_t num_tokens, int hkv, int64_t num_slots, const float* __restrict__ scales,
-    uint4* __restrict__ pool, uint32_t* __restrict__ err) {
+    uint4* __restrict__ pool, uint32_t* __restrict__ err, int32_t* __restrict__ zero_word) {
   constexpr int kChunks = D / 16;  // 16-code chunks per row
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (zero_word && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t total = num_tokens * hkv * 2 * kChunks;
   if (i >= total) return;
@@ -98,27 +106,28 @@ __global__ void __launch_bounds__(256) kv_write_fp8_kernel(
 }  // namespace
 
 cudaError_t launch_kv_write(const kv_pool* pool, const void* k, const void* v,
-                            const int64_t* slots, int64_t num_tokens, cudaStream_t stream) {
+                            const int64_t* slots, int64_t num_tokens, cudaStream_t stream,
+                            int32_t* zero_word) {
   const int hkv = pool->n_kv_heads;
   const int64_t num_slots = pool->num_blocks * pool->block_size;
   const int threads = 256;
   if (pool->dtype == KV_BF16) {
     const int64_t total = num_tokens * hkv * 2 * (pool->head_dim / 8);
-    const int64_t blocks = (total + threads - 1) / threads;
+    const int64_t blocks = std::max<int64_t>(1, (total + threads - 1) / threads);
     if (pool->head_dim == 128)
       kv_write_bf16_kernel<128><<<blocks, threads, 0, stream>>>(
           static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, hkv,
-          num_slots, static_cast<uint4*>(pool->base), pool->err);
+          num_slots, static_cast<uint4*>(pool->base), pool->err, zero_word);
     else
       kv_write_bf16_kernel<64><<<blocks, threads, 0, stream>>>(
           static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, hkv,
-          num_slots, static_cast<uint4*>(pool->base), pool->err);
+          num_slots, static_cast<uint4*>(pool->base), pool->err, zero_word);
   } else {
     const int64_t total = num_tokens * hkv * 2 * (pool->head_dim / 16);
-    const int64_t blocks = (total + threads - 1) / threads;
+    const int64_t blocks = std::max<int64_t>(1, (total + threads - 1) / threads);
     kv_write_fp8_kernel<128><<<blocks, threads, 0, stream>>>(
         static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, hkv,
-        num_slots, pool->scales, static_cast<uint4*>(pool->base), pool->err);
+        num_slots, pool->scales, static_cast<uint4*>(pool->base), pool->err, zero_word);
   }
   return cudaGetLastError();
 }

@@ -65,6 +65,9 @@ def load() -> ctypes.CDLL:
             "paged_decode_attention": (c.c_int, [P, P, c.c_int32, P, c.c_int32, P, c.c_int32,
                                                  c.c_int32, c.c_float, c.c_int32, P, P,
                                                  c.c_size_t, P]),
+            "paged_decode_step": (c.c_int, [P, P, P, P, c.c_int64, P, c.c_int32, P, c.c_int32,
+                                            P, c.c_int32, c.c_int32, c.c_float, c.c_int32, P,
+                                            P, c.c_size_t, P]),
             "paged_decode_attention_noalloc": (c.c_int, [P, P, c.c_int32, P, c.c_int32, P,
                                                          c.c_int32, c.c_int32, c.c_float,
                                                          c.c_int32, P, P]),
@@ -245,6 +248,41 @@ def paged_decode_attention(pool: KVPool, q: torch.Tensor, block_tables: torch.Te
         _dev(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
         int(sliding_window), _dev(out, torch.float32, "out"), ws_ptr, ws_bytes, _stream(stream)),
         "paged_decode_attention")
+    return out
+
+
+def paged_decode_step(pool: KVPool, k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                      q: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                      scale: float, sliding_window: int = 0, max_context_len: int | None = None,
+                      out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """One decode step: write k, v ([T, Hkv, D] bf16) to `slot_mapping`, then
+    attend q [B, Hq, D] over the pool; context_lens already count the new
+    tokens.  Returns out [B, Hq, D] fp32."""
+    T = slot_mapping.shape[0]
+    shape = (T, pool.n_kv_heads, pool.head_dim)
+    if tuple(k.shape) != shape or tuple(v.shape) != shape:
+        raise ValueError(f"k and v must be {shape}")
+    B, Hq, D = q.shape
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if B else 0
+    if out is None:
+        out = torch.empty(B, Hq, D, dtype=torch.float32, device=q.device)
+    need = paged_decode_workspace_bytes(pool, B, Hq, max_context_len, sliding_window)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be [B, max_blocks_per_seq]")
+    _check(load().paged_decode_step(
+        pool.handle, _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
+        _dev(slot_mapping, torch.int64, "slot_mapping"), T,
+        _dev(q, torch.bfloat16, "q"), Hq,
+        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _dev(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
+        int(sliding_window), _dev(out, torch.float32, "out"), ws_ptr, ws_bytes, _stream(stream)),
+        "paged_decode_step")
     return out
 
 

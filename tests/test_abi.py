@@ -21,7 +21,7 @@ def declared_functions() -> list[str]:
 def test_header_declares_the_abi():
     names = declared_functions()
     for n in ("kv_pool_create", "paged_kv_write", "paged_decode_attention",
-              "kv_pool_check_status", "kv_status_str"):
+              "paged_decode_step", "kv_pool_check_status", "kv_status_str"):
         assert n in names
 
 
@@ -61,6 +61,8 @@ def test_null_handles_are_rejected():
     assert L.paged_kv_write(None, None, None, None, 1, None) == 1
     assert L.paged_decode_attention(None, None, 8, None, 4, None, 1, 64, 1.0, 0, None, None, 0,
                                     None) == 1
+    assert L.paged_decode_step(None, None, None, None, 1, None, 8, None, 4, None, 1, 64, 1.0, 0,
+                               None, None, 0, None) == 1
     assert L.paged_decode_workspace_bytes(None, 1, 8, 64, 0) == 0
     assert L.kv_pool_check_status(None, None) == 1
     assert L.kv_pool_set_partition_blocks(None, 8) == 1
