@@ -93,8 +93,8 @@ DecodePlan plan_decode(const kv_pool* pool, int32_t batch, int32_t n_q_heads,
   plan.workers = static_cast<int32_t>(ctas * nw);
   const int64_t g = n_q_heads / pool->n_kv_heads;
   const int64_t pairs = static_cast<int64_t>(plan.batch) * pool->n_kv_heads;
-  const int64_t chunks = decode_dynamic_units(t_max) / decode_chunk_units() + 2;
-  const int64_t slots = plan.workers + chunks + pairs;
+  // partial slot of (segment s, pair p) is s + p: segments + pairs slots
+  const int64_t slots = plan.workers + decode_max_chunks(t_max) + pairs;
   auto round256 = [](size_t x) { return (x + 255) / 256 * 256; };
   plan.part_o_bytes = round256(static_cast<size_t>(slots * g * pool->head_dim) * sizeof(float));
   plan.part_ml_bytes = round256(static_cast<size_t>(slots * g * 2) * sizeof(float));

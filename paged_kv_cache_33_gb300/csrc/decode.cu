@@ -773,8 +773,17 @@ int decode_ctas_per_sm(const kv_pool* pool) {
   return pool->head_dim == 128 ? Bf16D128::ctas_per_sm() : Bf16D64::ctas_per_sm();
 }
 
-int decode_chunk_units() { return kChunkMax >> 2; }
-int64_t decode_dynamic_units(int64_t total) { return total * kDynNum / kDynDen; }
+// Upper bound of Split::Nc over every launch of at most `max_units` units:
+// each region's chunk count grows with the dynamic part, and the last region
+// also takes what the rounding of the first two left over.
+int64_t decode_max_chunks(int64_t max_units) {
+  const int64_t td = max_units * kDynNum / kDynDen;
+  const int64_t c0 = kChunkMax, c1 = kChunkMax >> 1, c2 = kChunkMax >> 2;
+  const int64_t r0 = td * kRegion0Pct / 100 / c0 * c0;
+  const int64_t r1 = td * kRegion1Pct / 100 / c1 * c1;
+  const int64_t rest = td * (100 - kRegion0Pct - kRegion1Pct) / 100 + c0 + c1;
+  return r0 / c0 + r1 / c1 + (rest + c2 - 1) / c2 + 1;
+}
 
 cudaError_t launch_decode(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream,
                           bool dependent) {

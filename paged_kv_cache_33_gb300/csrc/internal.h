@@ -71,9 +71,8 @@ DecodePlan plan_decode(const kv_pool* pool, int32_t batch, int32_t n_q_heads,
 // Warps per CTA and resident CTAs per SM of the decode variant the pool uses.
 int decode_warps_per_cta(const kv_pool* pool);
 int decode_ctas_per_sm(const kv_pool* pool);
-// Units per dynamic chunk, and the dynamic part of a call with `total` units.
-int decode_chunk_units();
-int64_t decode_dynamic_units(int64_t total);
+// Most dynamic chunks a launch of at most `max_units` units can hand out.
+int64_t decode_max_chunks(int64_t max_units);
 
 // The KV write; with `zero_word` it also clears that int (the decode's ticket
 // counter) and lets a programmatic dependent launch early.
