@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
         "oracle_pool_bytes": (c.c_uint64, [P]),
         "oracle_pool_set_scales": (c.c_int, [P, P, P]),
         "oracle_kv_write": (c.c_int, [P, P, P, P, c.c_int64]),
+        "oracle_pool_copy_blocks": (c.c_int, [P, P, c.c_int64]),
         "oracle_paged_decode": (c.c_int, [P, P, c.c_int32, P, c.c_int32, P, c.c_int32,
                                           c.c_double, c.c_int32, P, c.c_int32, P]),
         "oracle_sha256": (None, [P, c.c_uint64, P]),
@@ -84,6 +85,8 @@ def lib() -> ctypes.CDLL:
                                          c.c_int32, P]),
         "oracle_alloc_append": (c.c_int, [P, c.c_int64, P, c.c_int64]),
         "oracle_alloc_free": (c.c_int, [P, c.c_int64]),
+        "oracle_alloc_fork": (c.c_int, [P, c.c_int64, c.c_int64]),
+        "oracle_alloc_copies": (c.c_int64, [P, P, c.c_int64, c.c_int32]),
         "oracle_alloc_preempt_newest": (c.c_int, [P, P]),
         "oracle_alloc_table": (c.c_int, [P, c.c_int64, P, c.c_int64, P]),
         "oracle_alloc_num_tokens": (c.c_int64, [P, c.c_int64]),
@@ -182,6 +185,13 @@ class Pool:
         if rc != OK:
             raise ValueError(f"oracle_kv_write: {rc}")
 
+    def copy_blocks(self, pairs) -> None:
+        """Copy block src to block dst for each (src, dst) row of `pairs`, in order."""
+        pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+        rc = lib().oracle_pool_copy_blocks(self._h, _ptr(pr), pr.shape[0])
+        if rc != OK:
+            raise ValueError(f"oracle_pool_copy_blocks: {rc}")
+
     def decode(self, q, block_tables, context_lens, scale: float, window: int = 0,
                seqs=None) -> np.ndarray:
         """fp64 paged decode attention; returns float32 [B, Hq, D] (rows outside `seqs` zero)."""
@@ -242,6 +252,16 @@ class Allocator:
 
     def free(self, req_id: int) -> int:
         return lib().oracle_alloc_free(self._h, int(req_id))
+
+    def fork(self, parent: int, child: int) -> int:
+        return lib().oracle_alloc_fork(self._h, int(parent), int(child))
+
+    def copies(self, take: bool = True) -> list[tuple[int, int]]:
+        """Pending copy-on-write pairs (src, dst), oldest first (cleared when take)."""
+        n = lib().oracle_alloc_copies(self._h, None, 0, 0)
+        out = np.zeros((max(n, 1), 2), np.int32)
+        lib().oracle_alloc_copies(self._h, _ptr(out), n, 1 if take else 0)
+        return [(int(a), int(b)) for a, b in out[:n]]
 
     def preempt_newest(self) -> tuple[int, int]:
         rid = ctypes.c_int64(-1)

@@ -30,6 +30,14 @@
 //  * "Why the KV cache is a pool of 16-token blocks", section "When memory
 //    runs out": with no free block, the newest running request is preempted
 //    and all of its blocks are freed.
+//  * "Optimizing KV Cache Memory Management in vLLM with PagedAttention and
+//    Dynamic Block Allocation", sections "Copy-on-Write (CoW) for Parallel
+//    Sampling and Prefix Caching" and "Simulating vLLM's Block Manager in
+//    Python": a fork maps the child's logical blocks to the parent's physical
+//    blocks and raises their reference counts; a sequence about to write a
+//    token into a block whose count is above one gets a new block, the old
+//    block's contents are copied into it on the device, the old block loses a
+//    reference and the table entry is switched to the new block.
 //
 // Readings where the pages leave details open: the hash input of block i is
 // parent_hash (32 bytes, all zero for block 0) || the block's token ids as
@@ -77,6 +85,7 @@ struct oracle_alloc {
   int32_t head = -1, tail = -1, nfree = 0;
   std::map<Hash, int32_t> hash_to_block;
   std::map<int64_t, Request> reqs;
+  std::vector<std::pair<int32_t, int32_t>> copies;  // pending copy-on-write (src, dst)
   uint64_t admit_counter = 0;
   int64_t queries = 0, hits = 0, evictions = 0, preemptions = 0;
 };
@@ -238,8 +247,18 @@ extern "C" int oracle_alloc_append(oracle_alloc* a, int64_t req_id, const int32_
   if (it == a->reqs.end() || n < 0) return 1;
   Request& r = it->second;
   const int32_t bs = a->bs;
-  const int64_t need = blocks_for(r.num_tokens + n, bs) - blocks_for(r.num_tokens, bs);
+  // The first new token lands in a partly filled last block shared with
+  // another request: that block must be copied before it is written.
+  const bool cow = n > 0 && r.num_tokens % bs != 0 && a->blocks[r.blocks.back()].ref_cnt > 1;
+  const int64_t need = blocks_for(r.num_tokens + n, bs) - blocks_for(r.num_tokens, bs) + (cow ? 1 : 0);
   if (a->nfree < need) return 2;
+  if (cow) {
+    const int32_t old_id = r.blocks.back();
+    const int32_t new_id = pop_free(a);
+    a->copies.emplace_back(old_id, new_id);
+    a->blocks[old_id].ref_cnt--;  // still >= 1: the other sharers keep it
+    r.blocks.back() = new_id;
+  }
   if (!tokens) r.content_known = false;  // content unknown from here on: no more hashes
   for (int64_t i = 0; i < n; ++i) {
     // The sequence reached a block boundary: it needs a new block.
@@ -259,6 +278,27 @@ extern "C" int oracle_alloc_append(oracle_alloc* a, int64_t req_id, const int32_
     }
   }
   return 0;
+}
+
+extern "C" int oracle_alloc_fork(oracle_alloc* a, int64_t parent, int64_t child) {
+  auto it = a->reqs.find(parent);
+  if (it == a->reqs.end() || a->reqs.count(child)) return 1;
+  Request r = it->second;  // same tokens, hashes, salt and extra keys
+  for (int32_t id : r.blocks) touch(a, id);
+  r.admit_order = ++a->admit_counter;
+  a->reqs.emplace(child, std::move(r));
+  return 0;
+}
+
+extern "C" int64_t oracle_alloc_copies(oracle_alloc* a, int32_t* pairs, int64_t cap,
+                                       int32_t take) {
+  const int64_t n = static_cast<int64_t>(a->copies.size());
+  for (int64_t i = 0; i < n && i < cap; ++i) {
+    pairs[2 * i] = a->copies[i].first;
+    pairs[2 * i + 1] = a->copies[i].second;
+  }
+  if (take) a->copies.clear();
+  return n;
 }
 
 extern "C" int oracle_alloc_free(oracle_alloc* a, int64_t req_id) {

@@ -145,6 +145,28 @@ extern "C" int oracle_pool_set_scales(oracle_pool* p, const float* k_scale, cons
   return 0;
 }
 
+// ------------------------------------------------------------ block copy --
+// Copy-on-write copies a whole physical block ("Optimizing KV Cache Memory
+// Management in vLLM with PagedAttention and Dynamic Block Allocation",
+// section "Copy-on-Write (CoW) for Parallel Sampling and Prefix Caching"):
+// every element (kv, off, h, d) of block src is copied to block dst.
+
+extern "C" int oracle_pool_copy_blocks(oracle_pool* p, const int32_t* pairs, int64_t n) {
+  for (int64_t i = 0; i < 2 * n; ++i)
+    if (pairs[i] < 0 || pairs[i] >= p->nb) return 1;
+  const size_t eb = elem_bytes(p);
+  for (int64_t i = 0; i < n; ++i) {
+    const int32_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+    for (int kv = 0; kv < 2; ++kv)
+      for (int off = 0; off < p->bs; ++off)
+        for (int h = 0; h < p->hkv; ++h)
+          for (int d = 0; d < p->d; ++d)
+            std::memcpy(&p->data[pool_index(p, dst, kv, off, h, d) * eb],
+                        &p->data[pool_index(p, src, kv, off, h, d) * eb], eb);
+  }
+  return 0;
+}
+
 // ------------------------------------------------------------- KV write --
 // Token t with slot s goes to physical block s / BS at offset s mod BS; a
 // negative slot marks a padded token and is skipped.

@@ -42,6 +42,11 @@ void*    oracle_pool_data(oracle_pool* p);
 uint64_t oracle_pool_bytes(const oracle_pool* p);
 int      oracle_pool_set_scales(oracle_pool* p, const float* k_scale, const float* v_scale);
 
+/* Copy every K and V row of block pairs[2i] into block pairs[2i+1] (both
+ * must be in [0, num_blocks)); pairs are applied in order.  1 on a bad id
+ * (nothing copied). */
+int oracle_pool_copy_blocks(oracle_pool* p, const int32_t* pairs, int64_t n);
+
 /* k, v: [T, Hkv, D] bf16 bits; slot < 0 = padded token (skipped). */
 int oracle_kv_write(oracle_pool* p, const uint16_t* k, const uint16_t* v,
                     const int64_t* slot_mapping, int64_t num_tokens);
@@ -68,8 +73,19 @@ int     oracle_alloc_admit(oracle_alloc* a, int64_t req_id, const int32_t* token
                            int64_t num_tokens, const uint8_t* salt, int32_t salt_len,
                            const uint8_t* extra, int32_t extra_len,
                            int64_t* cached_tokens);
-/* Grow a request by n tokens (tokens may be NULL). All-or-nothing. */
+/* Grow a request by n tokens (tokens may be NULL). All-or-nothing.  When the
+ * first new token falls into a partly filled last block that other requests
+ * share (ref_cnt > 1), that block is copied on write first: a fresh block
+ * replaces it in this request's table, the pair (old, new) joins the pending
+ * copies, and the old block loses one reference. */
 int     oracle_alloc_append(oracle_alloc* a, int64_t req_id, const int32_t* tokens, int64_t n);
+/* Fork: `child` shares every block of `parent` (one more reference each) and
+ * takes its token count, token ids, hashes, salt and extra keys; it counts as
+ * the newest admission.  1 if parent is unknown or child exists. */
+int     oracle_alloc_fork(oracle_alloc* a, int64_t parent, int64_t child);
+/* Pending copy-on-write pairs (src, dst), oldest first, into pairs[2*cap];
+ * returns their number; take != 0 clears the list. */
+int64_t oracle_alloc_copies(oracle_alloc* a, int32_t* pairs, int64_t cap, int32_t take);
 int     oracle_alloc_free(oracle_alloc* a, int64_t req_id);
 int     oracle_alloc_preempt_newest(oracle_alloc* a, int64_t* req_id);
 int     oracle_alloc_table(const oracle_alloc* a, int64_t req_id, int32_t* out,

@@ -273,3 +273,114 @@ def test_churned_tables_reach_the_requested_occupancy():
     assert abs(used / w.num_blocks - 0.95) < 0.01
     # the churn scatters the ids: far from the identity layout
     assert np.mean(np.diff(w.block_tables[0][: -(-int(w.context_lens[0]) // 16)]) == 1) < 0.9
+
+
+# ------------------------------------------------------ fork / copy-on-write --
+
+def test_cow_walkthrough_from_the_pages():
+    ex = json.load(open(os.path.join(GOLDEN, "cow_walkthrough.json")))
+    a = oracle.Allocator(ex["pool_blocks"], ex["block_size"])
+    for ev in ex["events"]:
+        if ev["op"] == "admit":
+            assert a.admit(ev["seq"], num_tokens=ev["tokens"])[0] == 0
+        elif ev["op"] == "fork":
+            assert a.fork(ev["parent"], ev["child"]) == 0
+        else:
+            assert a.append(ev["seq"], n=ev["n"]) == 0
+        for seq, table in ev["table"].items():
+            assert a.table(int(seq)) == table, ev
+        assert a.num_free() == ev["free"], ev
+        for blk, ref in ev["ref_cnt"].items():
+            assert a.block(int(blk))[0] == ref, ev
+        assert [list(p) for p in a.copies()] == ev["copies"], ev
+        for seq, n in ev.get("num_tokens", {}).items():
+            assert a.num_tokens(int(seq)) == n
+
+
+def test_fork_of_a_full_last_block_needs_no_copy():
+    a = oracle.Allocator(8, 4)
+    assert a.admit(1, num_tokens=8)[0] == 0
+    assert a.fork(1, 2) == 0
+    assert a.append(2, n=1) == 0            # position 8 opens a new block
+    assert a.table(2) == [0, 1, 2] and a.table(1) == [0, 1]
+    assert a.copies() == []
+    assert a.fork(1, 2) == 1 and a.fork(9, 3) == 1   # child exists / unknown parent
+
+
+def test_copy_on_write_counts_its_block_against_capacity():
+    a = oracle.Allocator(3, 4)
+    assert a.admit(1, num_tokens=6)[0] == 0             # blocks 0, 1 (1 partly full)
+    assert a.fork(1, 2) == 0
+    assert a.append(2, n=3) == oracle.OOM               # copy + new block: 2 needed, 1 free
+    assert a.table(2) == [0, 1] and a.copies() == []    # all-or-nothing
+    assert a.append(2, n=2) == 0                        # copy only
+    assert a.table(2) == [0, 2] and a.copies() == [(1, 2)]
+
+
+def test_every_request_reads_back_only_its_own_tokens():
+    """Brute force over a token-per-slot store: admitted tokens are written
+    from the first uncached position, pending copies are applied before each
+    append's writes, and after every step each live request's table must
+    yield exactly its own token history.  A missed copy-on-write lets one
+    sharer overwrite another's block; a wrong or reversed copy pair brings in
+    the wrong contents; a wrong prefix hit maps foreign tokens."""
+    rng = np.random.default_rng(7)
+    bs = 4
+    a = oracle.Allocator(48, bs)
+    store = np.full(48 * bs, -1, dtype=np.int64)
+    hist: dict[int, list[int]] = {}
+
+    def write(rid, first):
+        t = a.table(rid)
+        for p in range(first, len(hist[rid])):
+            store[t[p // bs] * bs + p % bs] = hist[rid][p]
+
+    def apply_copies():
+        for src, dst in a.copies():
+            store[dst * bs:(dst + 1) * bs] = store[src * bs:(src + 1) * bs]
+
+    next_id = 0
+    forks = cows = 0
+    for step in range(3000):
+        op = int(rng.integers(0, 10))
+        live = list(hist)
+        if op <= 2 or not live:
+            toks = rng.integers(0, 3, int(rng.integers(1, 14))).tolist()
+            rc, cached = a.admit(next_id, tokens=toks)
+            if rc == 0:
+                hist[next_id] = list(toks)
+                write(next_id, cached)
+            next_id += 1
+        elif op <= 4:
+            parent = live[int(rng.integers(0, len(live)))]
+            assert a.fork(parent, next_id) == 0
+            hist[next_id] = list(hist[parent])
+            next_id += 1
+            forks += 1
+        elif op <= 7:
+            rid = live[int(rng.integers(0, len(live)))]
+            toks = rng.integers(0, 3, int(rng.integers(1, 6))).tolist()
+            before = len(hist[rid])
+            if a.append(rid, tokens=toks) == 0:
+                pend = a.copies(take=False)
+                cows += len(pend)
+                apply_copies()
+                hist[rid] += toks
+                write(rid, before)
+            else:
+                assert a.copies(take=False) == []
+        elif op == 8:
+            rid = live[int(rng.integers(0, len(live)))]
+            assert a.free(rid) == 0
+            del hist[rid]
+        else:
+            rc, rid = a.preempt_newest()
+            if rc == 0:
+                del hist[rid]
+        for rid, h in hist.items():
+            t = a.table(rid)
+            got = [int(store[t[p // bs] * bs + p % bs]) for p in range(len(h))]
+            assert got == h, (step, rid)
+        if step % 100 == 0:
+            _check_invariants(a, {r: len(h) for r, h in hist.items()}, bs)
+    assert forks > 100 and cows > 15

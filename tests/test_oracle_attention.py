@@ -262,3 +262,21 @@ def test_write_skips_padded_slots_and_rejects_out_of_range():
     assert arr.sum(dtype=np.int64) == 2 * int(_bits(k[1, 0]).sum(dtype=np.int64))
     with pytest.raises(ValueError):
         pool.write(k, k, np.array([0, 1, 32]))
+
+
+def test_block_copy_moves_whole_blocks_in_order():
+    import torch
+    p = oracle.Pool(6, 16, 2, 64, "bf16")
+    g = torch.Generator().manual_seed(3)
+    k = torch.randn(6 * 16, 2, 64, generator=g).to(torch.bfloat16)
+    v = torch.randn(6 * 16, 2, 64, generator=g).to(torch.bfloat16)
+    p.write(k, v, np.arange(6 * 16))
+    before = p.array().copy()
+    p.copy_blocks([(1, 4), (4, 5)])         # in order: block 5 receives block 1's rows
+    after = p.array()
+    assert np.array_equal(after[4], before[1]) and np.array_equal(after[5], before[1])
+    for b in (0, 1, 2, 3):
+        assert np.array_equal(after[b], before[b])
+    with pytest.raises(ValueError):
+        p.copy_blocks([(0, 6)])
+    assert np.array_equal(p.array(), after)
