@@ -1,6 +1,6 @@
 """Build libpagedkv.so (CUDA for sm_103a) in-tree with nvcc.
 
-Each .cu file compiles to an object in parallel, then one link step makes the
+Each source (.cu kernels and C ABI, .cpp host code) compiles to an object in parallel, then one link step makes the
 shared library next to this file.  No torch extension machinery: the library
 exports a plain C ABI (include/pagedkv.h).
 """
@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libpagedkv.so")
-SOURCES = ["api.cu", "kv_write.cu", "decode.cu", "decode_noalloc.cu"]
+SOURCES = ["api.cu", "kv_write.cu", "decode.cu", "decode_noalloc.cu", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                 "--expt-relaxed-constexpr", "-Xptxas", "-v"]
@@ -31,7 +31,8 @@ def nvcc() -> str:
 
 def _deps() -> list[str]:
     hdrs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    hdrs.append(os.path.join(os.path.dirname(HERE), "include", "pagedkv.h"))
+    inc = os.path.join(os.path.dirname(HERE), "include")
+    hdrs += [os.path.join(inc, f) for f in os.listdir(inc) if f.endswith(".h")]
     return hdrs
 
 
@@ -47,7 +48,7 @@ def start_objects(verbose: bool = False) -> list[tuple[str, subprocess.Popen]]:
     os.makedirs(BUILD_DIR, exist_ok=True)
     procs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc(), *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
         procs.append((obj, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
     return procs

@@ -12,6 +12,8 @@ import ctypes
 import os
 import threading
 
+import numpy as np
+
 import torch
 
 from . import build as _build
@@ -75,6 +77,26 @@ def load() -> ctypes.CDLL:
             "kv_pool_set_timing_events": (c.c_int, [P, P, P]),
             "kv_pool_check_status": (c.c_int, [P, P]),
             "kv_status_str": (c.c_char_p, [c.c_int]),
+            "kv_bm_create": (c.c_int, [c.c_int64, c.c_int32, c.POINTER(P)]),
+            "kv_bm_destroy": (c.c_int, [P]),
+            "kv_bm_admit": (c.c_int, [P, c.c_int64, P, c.c_int64, P, c.c_int32, P, c.c_int32,
+                                      P]),
+            "kv_bm_append": (c.c_int, [P, c.c_int64, P, c.c_int64]),
+            "kv_bm_fork": (c.c_int, [P, c.c_int64, c.c_int64]),
+            "kv_bm_free": (c.c_int, [P, c.c_int64]),
+            "kv_bm_preempt_newest": (c.c_int, [P, P]),
+            "kv_bm_take_copies": (c.c_int64, [P, P, c.c_int64]),
+            "kv_bm_pending_copies": (c.c_int64, [P, P, c.c_int64]),
+            "kv_bm_block_table": (c.c_int, [P, c.c_int64, P, c.c_int64, P]),
+            "kv_bm_slot_mapping": (c.c_int, [P, c.c_int64, c.c_int64, c.c_int64, P]),
+            "kv_bm_decode_inputs": (c.c_int, [P, P, c.c_int32, c.c_int32, P, P, P]),
+            "kv_bm_num_tokens": (c.c_int64, [P, c.c_int64]),
+            "kv_bm_num_free": (c.c_int64, [P]),
+            "kv_bm_free_queue": (c.c_int64, [P, P, c.c_int64]),
+            "kv_bm_block_info": (c.c_int, [P, c.c_int32, P, P, P]),
+            "kv_bm_lookup": (c.c_int32, [P, P]),
+            "kv_bm_map_entries": (c.c_int64, [P, P, P, c.c_int64]),
+            "kv_bm_get_stats": (c.c_int, [P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -301,6 +323,136 @@ def paged_decode_attention_noalloc(pool: KVPool, q: torch.Tensor, block_tables: 
         _dev(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
         int(sliding_window), _dev(out, torch.float32, "out"), _stream(stream)),
         "paged_decode_attention_noalloc")
+
+
+# ------------------------------------------------------------ block manager --
+
+def _np_ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+class BlockManager:
+    """Host block manager of one pool (include/kv_block_manager.h).
+
+    Return codes are the C ABI's: 0 ok, 1 bad argument / unknown request,
+    2 not enough free blocks (nothing changed)."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16):
+        L = load()
+        h = ctypes.c_void_p()
+        _check(L.kv_bm_create(int(num_blocks), int(block_size), ctypes.byref(h)), "kv_bm_create")
+        self.handle, self.num_blocks, self.block_size = h, int(num_blocks), int(block_size)
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h and _lib is not None:
+            _lib.kv_bm_destroy(h)
+
+    def admit(self, req_id: int, num_tokens: int | None = None, tokens=None,
+              salt: bytes = b"", extra: bytes = b"") -> tuple[int, int]:
+        """Returns (status, cached_tokens)."""
+        toks = None if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32)
+        n = int(num_tokens if toks is None else toks.shape[0])
+        sb = np.frombuffer(salt, np.uint8) if salt else None
+        eb = np.frombuffer(extra, np.uint8) if extra else None
+        cached = ctypes.c_int64(0)
+        rc = load().kv_bm_admit(self.handle, int(req_id), _np_ptr(toks), n, _np_ptr(sb),
+                                len(salt), _np_ptr(eb), len(extra), ctypes.byref(cached))
+        return int(rc), cached.value
+
+    def append(self, req_id: int, n: int | None = None, tokens=None) -> int:
+        toks = None if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32)
+        cnt = int(n if toks is None else toks.shape[0])
+        return int(load().kv_bm_append(self.handle, int(req_id), _np_ptr(toks), cnt))
+
+    def fork(self, parent: int, child: int) -> int:
+        return int(load().kv_bm_fork(self.handle, int(parent), int(child)))
+
+    def free(self, req_id: int) -> int:
+        return int(load().kv_bm_free(self.handle, int(req_id)))
+
+    def preempt_newest(self) -> tuple[int, int]:
+        rid = ctypes.c_int64(-1)
+        rc = load().kv_bm_preempt_newest(self.handle, ctypes.byref(rid))
+        return int(rc), rid.value
+
+    def copies(self, take: bool = True) -> list[tuple[int, int]]:
+        """Pending copy-on-write pairs (src, dst), oldest first (cleared when take)."""
+        L = load()
+        n = L.kv_bm_pending_copies(self.handle, None, 0)
+        out = np.zeros((max(n, 1), 2), np.int32)
+        if take:
+            n = L.kv_bm_take_copies(self.handle, _np_ptr(out), n)
+        else:
+            L.kv_bm_pending_copies(self.handle, _np_ptr(out), n)
+        return [(int(a), int(b)) for a, b in out[:n]]
+
+    def table(self, req_id: int) -> list[int]:
+        n = ctypes.c_int64(0)
+        L = load()
+        if L.kv_bm_block_table(self.handle, int(req_id), None, 0, ctypes.byref(n)) != KV_OK:
+            raise KeyError(req_id)
+        out = np.zeros(max(n.value, 1), dtype=np.int32)
+        L.kv_bm_block_table(self.handle, int(req_id), _np_ptr(out), n.value, ctypes.byref(n))
+        return out[: n.value].tolist()
+
+    def slot_mapping(self, req_id: int, first_pos: int, n: int) -> np.ndarray:
+        out = np.zeros(max(int(n), 1), dtype=np.int64)
+        _check(load().kv_bm_slot_mapping(self.handle, int(req_id), int(first_pos), int(n),
+                                         _np_ptr(out)), "kv_bm_slot_mapping")
+        return out[: int(n)]
+
+    def decode_inputs(self, req_ids, max_blocks_per_seq: int):
+        """(block_tables [B, mbs] int32, context_lens [B] int32, slot_mapping [B] int64)."""
+        ids = np.ascontiguousarray(req_ids, dtype=np.int64)
+        B = ids.shape[0]
+        tables = np.zeros((max(B, 1), int(max_blocks_per_seq)), np.int32)
+        lens = np.zeros(max(B, 1), np.int32)
+        slots = np.zeros(max(B, 1), np.int64)
+        _check(load().kv_bm_decode_inputs(self.handle, _np_ptr(ids), B, int(max_blocks_per_seq),
+                                          _np_ptr(tables), _np_ptr(lens), _np_ptr(slots)),
+               "kv_bm_decode_inputs")
+        return tables[:B], lens[:B], slots[:B]
+
+    def num_tokens(self, req_id: int) -> int:
+        return int(load().kv_bm_num_tokens(self.handle, int(req_id)))
+
+    def num_free(self) -> int:
+        return int(load().kv_bm_num_free(self.handle))
+
+    def free_queue(self) -> list[int]:
+        L = load()
+        n = L.kv_bm_free_queue(self.handle, None, 0)
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        L.kv_bm_free_queue(self.handle, _np_ptr(out), n)
+        return out[:n].tolist()
+
+    def block(self, block_id: int) -> tuple[int, bytes | None]:
+        """(ref_cnt, hash or None)."""
+        ref, has = ctypes.c_int32(0), ctypes.c_int32(0)
+        h = np.zeros(32, np.uint8)
+        if load().kv_bm_block_info(self.handle, int(block_id), ctypes.byref(ref),
+                                   ctypes.byref(has), _np_ptr(h)) != KV_OK:
+            raise IndexError(block_id)
+        return ref.value, (h.tobytes() if has.value else None)
+
+    def lookup(self, h: bytes) -> int:
+        buf = np.frombuffer(bytes(h), np.uint8)
+        return int(load().kv_bm_lookup(self.handle, _np_ptr(buf)))
+
+    def map_entries(self) -> dict[bytes, int]:
+        L = load()
+        n = L.kv_bm_map_entries(self.handle, None, None, 0)
+        hs = np.zeros((max(n, 1), 32), np.uint8)
+        ids = np.zeros(max(n, 1), np.int32)
+        L.kv_bm_map_entries(self.handle, _np_ptr(hs), _np_ptr(ids), n)
+        return {hs[i].tobytes(): int(ids[i]) for i in range(n)}
+
+    def stats(self) -> dict[str, int]:
+        out = np.zeros(6, np.int64)
+        _check(load().kv_bm_get_stats(self.handle, _np_ptr(out)), "kv_bm_get_stats")
+        return dict(zip(["queries", "hits", "evictions", "preemptions", "running",
+                         "cow_copies"], out.tolist()))
 
 
 def kv_status_str(status: int) -> str:

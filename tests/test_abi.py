@@ -9,19 +9,26 @@ import pytest
 
 from paged_kv_cache_33_gb300 import pagedkv
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
-                      "include", "pagedkv.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
 
 
 def declared_functions() -> list[str]:
-    text = open(HEADER).read()
-    return re.findall(r"^(?:kv_status|size_t|const char\*)\s+(\w+)\(", text, re.M)
+    """Every function declared in include/*.h (return type at line start)."""
+    names = []
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            text = open(os.path.join(INCLUDE, h)).read()
+            names += re.findall(r"^(?:kv_status|size_t|int64_t|int32_t|const char\*)\s+(\w+)\(",
+                                text, re.M)
+    return names
 
 
 def test_header_declares_the_abi():
     names = declared_functions()
     for n in ("kv_pool_create", "paged_kv_write", "paged_decode_attention",
-              "paged_decode_step", "kv_pool_check_status", "kv_status_str"):
+              "paged_decode_step", "kv_pool_check_status", "kv_status_str",
+              "kv_bm_create", "kv_bm_admit", "kv_bm_append", "kv_bm_fork",
+              "kv_bm_take_copies", "kv_bm_decode_inputs"):
         assert n in names
 
 
