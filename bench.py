@@ -44,6 +44,9 @@ DESCRIPTIONS = {
            "ctx log-uniform [256,8192], 64-block shared prefix (ref_cnt 128)",
     "sw": "sliding-window layer decode: batch 32, 32 q / 8 KV heads, head_dim 128, "
           "window 4096, ctx U[4096,32768], only window blocks mapped",
+    "fp8": "FP8-E4M3 KV decode: batch 256, 32 q / 8 KV heads, head_dim 128, ctx U[1,16384], "
+           "per-KV-head scales, block tables from the host block manager after 10k seeded "
+           "alloc/free steps at 95% occupancy",
 }
 
 
@@ -52,7 +55,7 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="8b", choices=["tiny", "8b", "70b", "sw"])
+    ap.add_argument("--config", default="8b", choices=["tiny", "8b", "70b", "sw", "fp8"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--part-blocks", type=int, default=0, help="split-K partition size (0 = auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -168,6 +171,9 @@ class Step:
 
         self.torch, self.pk, self.w = torch, pagedkv, w
         self.pool = pagedkv.KVPool(w.num_blocks, w.block_size, w.n_kv_heads, w.head_dim, w.dtype)
+        if w.dtype == "fp8":
+            self.pool.set_scales(torch.from_numpy(w.k_scale).to(device),
+                                 torch.from_numpy(w.v_scale).to(device))
         if part_blocks:
             self.pool.set_partition_blocks(part_blocks)
         setup, (k_new, v_new, s_new) = w.fill_plan(device=device)
@@ -395,8 +401,9 @@ def run_reference(args) -> None:
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    import oracle
     from paged_kv_cache_33_gb300 import workloads as W
-    w = W.make(args.config, "full")
+    w = W.make(args.config, "full", make_allocator=oracle.Allocator)
     per_step_budget = min(6.0, 150.0 / max(1, args.steps + args.warmup))
     sampler = OracleSampler(w)
     for _ in range(args.warmup):
@@ -440,7 +447,8 @@ def main(argv=None) -> None:
     torch.cuda.set_device(dist_ctx.local_rank)
     device = torch.device("cuda", dist_ctx.local_rank)
     pagedkv.load()
-    w = W.make(args.config, "full")
+    # the fp8 workload's tables come from the library's own block manager
+    w = W.make(args.config, "full", make_allocator=pagedkv.BlockManager)
     step = Step(w, device, args.part_blocks)
     sampler = ClockSampler(dist_ctx.local_rank)
     dev = timed_device(step, args.steps, args.warmup, dist_ctx, sampler)

@@ -118,6 +118,24 @@ kv_status paged_kv_write(kv_pool* pool, const void* k_dev, const void* v_dev,
                          const int64_t* slot_mapping_dev, int64_t num_tokens, void* stream);
 
 /*
+ * paged_kv_copy_blocks -- copy whole physical blocks inside the pool, for
+ * copy-on-write ("Optimizing KV Cache Memory Management in vLLM with
+ * PagedAttention and Dynamic Block Allocation", "Copy-on-Write (CoW) for
+ * Parallel Sampling and Prefix Caching": the shared block's K/V states are
+ * copied device to device into the writer's new block).
+ *   pairs:      HOST int32 [num_pairs][2] of (src, dst) block ids, e.g. from
+ *               kv_bm_take_copies; every id in [0, num_blocks), else
+ *               KV_ERR_INVALID_ARG before any work.  src == dst is a no-op.
+ * The result is that of applying the pairs one after another (chains, a
+ * block written twice, a block read after it is written all behave so): the
+ * host cuts the list into waves without conflicts, one kernel per wave, the
+ * pairs passed in the launch parameters.  `pairs` may be reused when the
+ * call returns.  Asynchronous on `stream`.
+ */
+kv_status paged_kv_copy_blocks(kv_pool* pool, const int32_t* pairs, int64_t num_pairs,
+                               void* stream);
+
+/*
  * paged_decode_workspace_bytes -- bytes of device scratch that
  * paged_decode_attention needs for these sizes (split-K partial results).
  * Depends on the pool's partition setting; 0 for invalid arguments.

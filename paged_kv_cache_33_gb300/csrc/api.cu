@@ -235,6 +235,17 @@ kv_status paged_kv_write(kv_pool* p, const void* k, const void* v, const int64_t
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
+kv_status paged_kv_copy_blocks(kv_pool* p, const int32_t* pairs, int64_t num_pairs,
+                               void* stream) {
+  if (!p || num_pairs < 0 || (num_pairs > 0 && !pairs)) return KV_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < 2 * num_pairs; ++i)
+    if (pairs[i] < 0 || pairs[i] >= p->num_blocks) return KV_ERR_INVALID_ARG;
+  if (num_pairs == 0) return KV_OK;
+  DeviceGuard guard(p->device);
+  const cudaError_t e = pkv::launch_copy_blocks(p, pairs, num_pairs, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
 size_t paged_decode_workspace_bytes(const kv_pool* p, int32_t batch, int32_t n_q_heads,
                                     int32_t max_context_len, int32_t sliding_window) {
   if (!p || batch < 0 || n_q_heads <= 0 || max_context_len < 0) return 0;

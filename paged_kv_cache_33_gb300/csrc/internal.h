@@ -85,6 +85,14 @@ cudaError_t launch_kv_write(const kv_pool* pool, const void* k, const void* v,
 cudaError_t launch_decode(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream,
                           bool dependent);
 
+// Bytes of one physical block ([Hkv][2][16][D] elements).
+int64_t block_bytes(const kv_pool* pool);
+
+// Whole-block copies of host-validated (src, dst) pairs, with the result of
+// applying them in order.
+cudaError_t launch_copy_blocks(const kv_pool* pool, const int32_t* pairs, int64_t n,
+                               cudaStream_t stream);
+
 // The merge of cut pairs, launched as a programmatic dependent of the decode.
 cudaError_t launch_reduce(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream);
 

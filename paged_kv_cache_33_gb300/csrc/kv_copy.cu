@@ -1,0 +1,99 @@
+// Batched whole-block copy inside one pool, for copy-on-write.
+//
+// "Optimizing KV Cache Memory Management in vLLM with PagedAttention and
+// Dynamic Block Allocation", section "Copy-on-Write (CoW) for Parallel
+// Sampling and Prefix Caching": before a sequence writes into a block it
+// shares, the block's K/V states are copied device to device into a fresh
+// block that the sequence then owns.
+//
+// A physical block is one contiguous run of the pool ([Hkv][2][16][D]), so a
+// copy is a flat move of block_bytes.  The (src, dst) pairs come from the
+// host block manager; the host cuts them into waves in which no block is
+// both read and written, so every wave runs fully parallel and the result is
+// that of applying the pairs one after another.  Each wave's pairs travel in
+// the kernel's parameter space (no device staging buffer, no extra copy).
+// HBM-bound: 2 * block_bytes per pair (read + write), 16-byte vector accesses,
+// four loads in flight per thread before the stores.
+
+#include <algorithm>
+#include <unordered_set>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;                       // 16-byte chunks per thread
+constexpr int kChunksPerCta = kCopyThreads * kCopyUnroll;
+constexpr int kMaxWave = 2048;                       // pairs per launch (16 KB of parameters)
+
+struct CopyWave {
+  int2 pairs[kMaxWave];  // (src, dst) block ids, validated on the host
+};
+
+__global__ void __launch_bounds__(kCopyThreads) kv_copy_blocks_kernel(
+    const __grid_constant__ CopyWave wave, int slices, int64_t chunks_per_block,
+    uint4* __restrict__ pool) {
+  const int pair = blockIdx.x / slices;
+  const int slice = blockIdx.x - pair * slices;
+  const int2 pr = wave.pairs[pair];
+  const uint4* src = pool + static_cast<int64_t>(pr.x) * chunks_per_block;
+  uint4* dst = pool + static_cast<int64_t>(pr.y) * chunks_per_block;
+  const int64_t base = static_cast<int64_t>(slice) * kChunksPerCta + threadIdx.x;
+  uint4 v[kCopyUnroll];
+#pragma unroll
+  for (int u = 0; u < kCopyUnroll; ++u) {
+    const int64_t c = base + u * kCopyThreads;
+    if (c < chunks_per_block) v[u] = src[c];
+  }
+#pragma unroll
+  for (int u = 0; u < kCopyUnroll; ++u) {
+    const int64_t c = base + u * kCopyThreads;
+    if (c < chunks_per_block) dst[c] = v[u];
+  }
+}
+
+}  // namespace
+
+int64_t block_bytes(const kv_pool* pool) {
+  const int64_t elem = pool->dtype == KV_BF16 ? 2 : 1;
+  return static_cast<int64_t>(pool->n_kv_heads) * 2 * pool->block_size * pool->head_dim * elem;
+}
+
+cudaError_t launch_copy_blocks(const kv_pool* pool, const int32_t* pairs, int64_t n,
+                               cudaStream_t stream) {
+  const int64_t chunks = block_bytes(pool) / 16;
+  const int slices = static_cast<int>((chunks + kChunksPerCta - 1) / kChunksPerCta);
+  CopyWave wave;
+  int count = 0;
+  // blocks read / written by the pairs of the current wave
+  std::unordered_set<int32_t> reads, writes;
+  auto flush = [&]() -> cudaError_t {
+    if (count == 0) return cudaSuccess;
+    kv_copy_blocks_kernel<<<count * slices, kCopyThreads, 0, stream>>>(
+        wave, slices, chunks, static_cast<uint4*>(pool->base));
+    count = 0;
+    reads.clear();
+    writes.clear();
+    return cudaGetLastError();
+  };
+  for (int64_t i = 0; i < n; ++i) {
+    const int32_t s = pairs[2 * i], d = pairs[2 * i + 1];
+    if (s == d) continue;
+    // A pair that reads a block this wave writes, or writes a block this
+    // wave reads or writes, must see the wave's result: start a new wave.
+    if (count == kMaxWave || writes.count(s) || writes.count(d) || reads.count(d)) {
+      const cudaError_t e = flush();
+      if (e != cudaSuccess) return e;
+    }
+    wave.pairs[count++] = make_int2(s, d);
+    reads.insert(s);
+    writes.insert(d);
+  }
+  return flush();
+}
+
+}  // namespace pkv

@@ -62,6 +62,7 @@ def load() -> ctypes.CDLL:
             "kv_pool_info": (c.c_int, [P, c.POINTER(_Desc)]),
             "kv_pool_set_scales": (c.c_int, [P, P, P, P]),
             "paged_kv_write": (c.c_int, [P, P, P, P, c.c_int64, P]),
+            "paged_kv_copy_blocks": (c.c_int, [P, P, c.c_int64, P]),
             "paged_decode_workspace_bytes": (c.c_size_t, [P, c.c_int32, c.c_int32, c.c_int32,
                                                           c.c_int32]),
             "paged_decode_attention": (c.c_int, [P, P, c.c_int32, P, c.c_int32, P, c.c_int32,
@@ -236,6 +237,14 @@ def paged_kv_write(pool: KVPool, k: torch.Tensor, v: torch.Tensor, slot_mapping:
                                  _dev(v, torch.bfloat16, "v"),
                                  _dev(slot_mapping, torch.int64, "slot_mapping"), T,
                                  _stream(stream)), "paged_kv_write")
+
+
+def paged_kv_copy_blocks(pool: KVPool, pairs, stream=None) -> None:
+    """Copy whole blocks src -> dst for each (src, dst) row of `pairs` (host
+    data, e.g. BlockManager.copies()), with in-order semantics."""
+    pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+    _check(load().paged_kv_copy_blocks(pool.handle, _np_ptr(pr), pr.shape[0], _stream(stream)),
+           "paged_kv_copy_blocks")
 
 
 def paged_decode_workspace_bytes(pool: KVPool, batch: int, n_q_heads: int, max_context_len: int,
