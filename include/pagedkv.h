@@ -37,7 +37,11 @@
  *    [num_blocks][n_kv_heads][2 (K, V)][block_size][head_dim], head_dim
  *    contiguous, so the K tile and the V tile of one (block, KV head) are one
  *    contiguous run (8 KB for bf16, head_dim 128).  The base is 256-byte
- *    aligned; every row is 16-byte aligned.
+ *    aligned; every row is 16-byte aligned.  FP8 pools store each V tile
+ *    transposed instead ([head_dim][block_size] codes: one 16-byte row per
+ *    dimension), with token t of the block at code position
+ *    4 * ((t % 8) / 2) + t % 2 + 2 * (t / 8) of every row; kv_pool_desc's
+ *    v_layout says which.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -74,11 +78,14 @@ typedef struct {
   uint64_t bytes;         /* total pool bytes                                        */
   int32_t device;         /* CUDA device ordinal the pool lives on                   */
   float* scales_dev;      /* fp8: device float[2 * Hkv], K scales then V scales      */
+  int32_t v_layout;       /* 0: V tiles as K ([block_size][D]); 1: transposed (FP8)  */
 } kv_pool_desc;
 
 /*
  * kv_pool_create -- allocate one layer's block pool on the current device.
- *   num_blocks > 0, block_size == 16, n_kv_heads >= 1, head_dim in {64, 128}
+ *   num_blocks > 0, block_size 16 or 32 (the pages' default and the larger
+ *   size "Optimizing KV Cache ...", "Trade-offs of Block Size Tuning",
+ *   recommends for very long contexts), n_kv_heads >= 1, head_dim in {64, 128}
  *   (FP8: head_dim 128).  The pool owns its memory (cudaMalloc here, cudaFree
  *   in kv_pool_destroy); its contents start undefined.  FP8 scales start at
  *   1.0.  Returns KV_ERR_INVALID_ARG / KV_ERR_UNSUPPORTED for bad shapes,

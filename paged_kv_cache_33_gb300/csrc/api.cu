@@ -54,8 +54,10 @@ bool encode_pool_map(kv_pool* p) {
                         static_cast<cuuint64_t>(p->num_blocks) * p->n_kv_heads};
   cuuint64_t strides[3] = {p->head_dim * esz, p->block_size * p->head_dim * esz,
                            2 * p->block_size * p->head_dim * esz};
+  // bf16: 64 columns of the K rows and the V rows per box; FP8: the K rows
+  // (the transposed V tile is fetched by a plain bulk copy)
   cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(p->block_size),
-                       2, 1};
+                       p->dtype == KV_BF16 ? 2u : 1u, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = encode(&p->tmap,
                       p->dtype == KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -66,7 +68,16 @@ bool encode_pool_map(kv_pool* p) {
   return r == CUDA_SUCCESS;
 }
 
-int32_t blocks_for(int64_t tokens) { return static_cast<int32_t>((tokens + 15) / 16); }
+int32_t blocks_for(int64_t tokens, int32_t bs) { return static_cast<int32_t>((tokens + bs - 1) / bs); }
+
+// Most units one (sequence, KV head) pair can have in a launch.
+int64_t max_units_per_pair(const kv_pool* p, int32_t max_context_len, int32_t sliding_window) {
+  const int32_t bs = p->block_size;
+  int64_t nblk = blocks_for(max_context_len, bs);
+  if (sliding_window > 0) nblk = std::min<int64_t>(nblk, (sliding_window - 1) / bs + 2);
+  const int bpu = pkv::decode_blocks_per_unit(p);
+  return std::max<int64_t>(1, (nblk + bpu - 1) / bpu);
+}
 
 }  // namespace
 
@@ -75,14 +86,13 @@ namespace pkv {
 DecodePlan plan_decode(const kv_pool* pool, int32_t batch, int32_t n_q_heads,
                        int32_t max_context_len, int32_t sliding_window) {
   DecodePlan plan{};
-  int32_t max_nblk = blocks_for(max_context_len);
-  if (sliding_window > 0) max_nblk = std::min(max_nblk, (sliding_window - 1) / 16 + 2);
   plan.batch = std::min(batch, kMaxDecodeBatch);
   const int nw = decode_warps_per_cta(pool);
   // A persistent grid: every SM holds as many CTAs as fit at once.
   const int64_t max_ctas = static_cast<int64_t>(std::max(pool->sm_count, 1)) *
                            decode_ctas_per_sm(pool);
-  const int64_t t_max = static_cast<int64_t>(plan.batch) * pool->n_kv_heads * std::max(max_nblk, 1);
+  const int64_t t_max = static_cast<int64_t>(plan.batch) * pool->n_kv_heads *
+                        max_units_per_pair(pool, max_context_len, sliding_window);
   int64_t ctas = max_ctas;
   if (pool->partition_blocks > 0) {
     // about `partition_blocks` units per warp for the longest possible launch
@@ -129,7 +139,7 @@ kv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_he
   if (num_blocks <= 0 || n_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
     return KV_ERR_INVALID_ARG;
   if (dtype != KV_BF16 && dtype != KV_FP8_E4M3) return KV_ERR_INVALID_ARG;
-  if (block_size != 16) return KV_ERR_UNSUPPORTED;
+  if (block_size != 16 && block_size != 32) return KV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return KV_ERR_UNSUPPORTED;
   if (dtype == KV_FP8_E4M3 && head_dim != 128) return KV_ERR_UNSUPPORTED;
   if (num_blocks * n_kv_heads >= (int64_t(1) << 31)) return KV_ERR_UNSUPPORTED;
@@ -206,6 +216,7 @@ kv_status kv_pool_info(const kv_pool* p, kv_pool_desc* out) {
   out->bytes = p->bytes;
   out->device = p->device;
   out->scales_dev = p->scales;
+  out->v_layout = p->dtype == KV_FP8_E4M3 ? 1 : 0;
   return KV_OK;
 }
 
@@ -288,7 +299,7 @@ kv_status decode_call(kv_pool* p, const StepWrite* w, const void* q, int32_t n_q
   }
   if (!q || !block_tables || !context_lens || !out || !aligned16(q)) return KV_ERR_INVALID_ARG;
   if (max_blocks_per_seq <= 0 || max_context_len < 0 ||
-      static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * 16)
+      static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * p->block_size)
     return KV_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return KV_ERR_INVALID_ARG;
   if (batch > 65535 || p->n_kv_heads > 65535) return KV_ERR_UNSUPPORTED;
@@ -297,12 +308,9 @@ kv_status decode_call(kv_pool* p, const StepWrite* w, const void* q, int32_t n_q
   const pkv::DecodePlan plan = pkv::plan_decode(p, batch, n_q_heads, max_context_len, sliding_window);
   if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned16(workspace))
     return KV_ERR_INVALID_ARG;
-  {
-    int32_t max_nblk = blocks_for(max_context_len);
-    if (sliding_window > 0) max_nblk = std::min(max_nblk, (sliding_window - 1) / 16 + 2);
-    if (static_cast<int64_t>(plan.batch) * p->n_kv_heads * std::max(max_nblk, 1) >= (int64_t(1) << 30))
-      return KV_ERR_UNSUPPORTED;  // unit indices are 32-bit
-  }
+  if (static_cast<int64_t>(plan.batch) * p->n_kv_heads *
+          max_units_per_pair(p, max_context_len, sliding_window) >= (int64_t(1) << 30))
+    return KV_ERR_UNSUPPORTED;  // unit indices are 32-bit
 
   pkv::DecodeParams d{};
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -312,6 +320,7 @@ kv_status decode_call(kv_pool* p, const StepWrite* w, const void* q, int32_t n_q
   d.ticket = reinterpret_cast<int32_t*>(ws + plan.part_o_bytes + plan.part_ml_bytes +
                                         plan.meta_bytes - 16);
   d.err = p->err;
+  d.pool = static_cast<const uint8_t*>(p->base);
   d.k_scale = p->scales;
   d.v_scale = p->scales + p->n_kv_heads;
   d.num_blocks = p->num_blocks;

@@ -7,10 +7,11 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
+#include <string.h>
 
 namespace pkv {
 
-constexpr int kBlockSize = 16;  // tokens per physical block
+
 
 // Bits of the pool's device error word.
 enum : uint32_t {
@@ -91,6 +92,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Non-tensor bulk copy global -> shared of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned); completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // ------------------------------------------------- warp matrix operations --
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -135,6 +146,19 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D += A * B, m16n8k32 with E4M3 operands, fp32 accumulate.  Each A/B
+// register holds four codes of consecutive k (lowest byte first); a0/a1 are
+// rows g/g+8 at k 4t..4t+3, a2/a3 the same rows at k 16+4t..; b0/b1 are
+// column g at k 4t.. and 16+4t.. (g = lane / 4, t = lane % 4).
+__device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // ------------------------------------------------------------- numerics --
 
 // 2^x on the special-function unit (the PTX ex2.approx instruction).
@@ -156,6 +180,35 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ __half2 u32_as_half2(uint32_t v) {
+  __half2 h;
+  memcpy(&h, &v, sizeof h);
+  return h;
+}
+
+// a - b on two f16 lanes held as raw bits.
+__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
+  const __half2 d = __hsub2(u32_as_half2(a), u32_as_half2(b));
+  uint32_t v;
+  memcpy(&v, &d, sizeof v);
+  return v;
+}
+
+// Two f16 values (low half first) to two E4M3 codes (low byte first),
+// round to nearest even, saturating to +-448.
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t two_halves) {
+  __half2_raw h;
+  h.x = static_cast<unsigned short>(two_halves & 0xFFFFu);
+  h.y = static_cast<unsigned short>(two_halves >> 16);
+  return static_cast<uint32_t>(__nv_cvt_halfraw2_to_fp8x2(h, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Two floats to two E4M3 codes (first in the low byte), RNE, saturating.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  return static_cast<uint32_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
 
 // Two E4M3 codes (low byte first) to two exact f16 values (low half first).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {

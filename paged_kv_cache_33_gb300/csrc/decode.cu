@@ -33,8 +33,11 @@
 //    shuffles over the token rows; O^T[D x 8 heads] += V^T P^T on the tensor
 //    cores.  P^T comes from the score accumulator by movmatrix.  For bf16 KV,
 //    P is a bf16 high part plus a bf16 remainder (two products) so ~16 bits
-//    of P survive; for FP8 KV, K and V are widened exactly from E4M3 to f16
-//    and P is f16.
+//    of P survive.  For FP8 KV the codes go to the tensor cores untouched
+//    (mma.sync m16n8k32 on E4M3): the query and P are each split into an
+//    E4M3 high code and the E4M3 code of the remainder (~8 bits together),
+//    and the V tile is stored transposed in the pool so that its rows are
+//    the A operand of V^T P^T with no conversion or transpose on the SM.
 //  * Masking uses selects: scores outside [lo, ctx) become -inf and the V
 //    rows of masked positions are zeroed before the product, so stale or NaN
 //    slots of a partly filled block never reach the result.
@@ -74,34 +77,57 @@ constexpr int kChunkMax = PKV_CHUNK_MAX;   // region r uses chunks of kChunkMax 
 constexpr int kRegion0Pct = 60, kRegion1Pct = 30;
 
 struct SeqRange {
-  int32_t lo, ctx, first_blk, nblk;
+  int32_t lo, ctx, first_blk, nblk, nunit;
 };
 
-// Attended positions [lo, ctx) of a sequence and the blocks that hold them.
+// Attended positions [lo, ctx) of a sequence, the blocks of BS tokens that
+// hold them, and the units (runs of BPU consecutive blocks) that cover them.
+template <int BS, int BPU>
 __device__ __forceinline__ SeqRange seq_from_ctx(int32_t ctx, int32_t window) {
   SeqRange r;
   r.ctx = ctx;
   r.lo = window > 0 ? max(0, ctx - window) : 0;
-  r.first_blk = r.lo / kBlockSize;
-  r.nblk = ctx > r.lo ? (ctx - 1) / kBlockSize - r.first_blk + 1 : 0;
+  r.first_blk = r.lo / BS;
+  r.nblk = ctx > r.lo ? (ctx - 1) / BS - r.first_blk + 1 : 0;
+  r.nunit = (r.nblk + BPU - 1) / BPU;
   return r;
 }
 
 // A context length is usable when 0 <= ctx <= both bounds; others count as 0.
+template <int BS>
 __device__ __forceinline__ bool ctx_ok(const DecodeParams& p, int32_t ctx) {
-  return ctx >= 0 && ctx <= p.max_ctx && ctx <= p.mbs * kBlockSize;
+  return ctx >= 0 && ctx <= p.max_ctx && static_cast<int64_t>(ctx) <= static_cast<int64_t>(p.mbs) * BS;
 }
 
-template <int D, bool FP8>
+// Shared-memory image of one unit: BPU blocks of BS tokens, each as
+// bf16: D/64 boxes of [K rows | V rows] x 64 columns (128-byte swizzled rows);
+// FP8: one box of K rows (128 codes, swizzled), then the transposed V tile
+//      as BS/16 sub-tiles of [D][16] codes, fetched by a plain bulk copy.
+// The compute side walks the unit in sub-tiles of 16 tokens.
+template <int D, bool FP8, int BS, int BPU>
 struct Geometry {
   static constexpr int kElem = FP8 ? 1 : 2;
   static constexpr int kRowBytes = 128;                         // one swizzled smem row
-  static constexpr int kBoxes = FP8 ? 1 : D / 64;               // TMA boxes per unit
-  static constexpr int kBoxBytes = 2 * kBlockSize * kRowBytes;  // K rows, then V rows
-  static constexpr int kStageBytes = kBoxes * kBoxBytes;
+  static constexpr int kBoxes = FP8 ? 1 : D / 64;               // TMA boxes per block
+  static constexpr int kBoxBytes = (FP8 ? 1 : 2) * BS * kRowBytes;
+  static constexpr int kVtBytes = FP8 ? D * BS : 0;             // transposed V tile
+  static constexpr int kBlockBytes = kBoxes * kBoxBytes + kVtBytes;
+  static constexpr int kStageBytes = BPU * kBlockBytes;
+  static constexpr int kSubPerBlock = BS / 16;
+  static constexpr int kSub = BPU * kSubPerBlock;               // 16-token sub-tiles per unit
   static constexpr int kSteps = D / 16;                         // k-steps (QK) = m-tiles (PV)
-  static_assert(kStageBytes == 2 * kBlockSize * D * kElem, "stage holds one K and one V tile");
+  static_assert(kBlockBytes == 2 * BS * D * kElem, "a block is one K and one V tile");
   static_assert(!FP8 || D == 128, "FP8 rows are one 128-byte swizzle row");
+  static_assert(kBoxBytes % 1024 == 0, "boxes keep the 1024-byte swizzle alignment");
+  // byte offsets inside a stage of sub-tile `sub`: K row 0 of box 0, and
+  // (bf16) V row 0 of box 0 or (FP8) the [D][16] transposed V sub-tile
+  __device__ static constexpr int k_off(int sub) {
+    return (sub / kSubPerBlock) * kBlockBytes + (sub % kSubPerBlock) * 16 * kRowBytes;
+  }
+  __device__ static constexpr int v_off(int sub) {
+    return FP8 ? (sub / kSubPerBlock) * kBlockBytes + kBoxBytes + (sub % kSubPerBlock) * 16 * D
+               : k_off(sub) + BS * kRowBytes;
+  }
 };
 
 // Coordinates of the unit held by one ring stage (u < 0: no unit).
@@ -109,9 +135,9 @@ struct StageInfo {
   int32_t u, b, h, k, seg_end, seg;
 };
 
-template <int D, bool FP8, int NW, int STAGES>
+template <int D, bool FP8, int BS, int BPU, int NW, int STAGES>
 struct Smem {
-  static constexpr int kRing = NW * STAGES * Geometry<D, FP8>::kStageBytes;
+  static constexpr int kRing = NW * STAGES * Geometry<D, FP8, BS, BPU>::kStageBytes;
   static constexpr int kBars = kRing;                          // uint64 [NW][STAGES]
   static constexpr int kInfo = kBars + NW * STAGES * 8;        // StageInfo [NW][STAGES]
   static constexpr int kCtx = kInfo + NW * STAGES * 24;        // int32 [kMaxDecodeBatch]
@@ -169,11 +195,11 @@ struct Split {
   }
 };
 
-template <int D, bool FP8, int NW, int STAGES>
-__global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const __grid_constant__ CUtensorMap tmap,
-                                                                  const DecodeParams p) {
-  using G = Geometry<D, FP8>;
-  using S = Smem<D, FP8, NW, STAGES>;
+template <int D, bool FP8, int BS, int BPU, int NW, int STAGES>
+__global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kernel(
+    const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
+  using G = Geometry<D, FP8, BS, BPU>;
+  using S = Smem<D, FP8, BS, BPU, NW, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment of the stage buffers keeps the 128-byte swizzle
   // pattern equal to (row mod 8).
@@ -201,12 +227,12 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const __grid_c
       const int b = b0 + i;
       if (i < per && b < p.batch) {
         int32_t ctx = p.context_lens[b];
-        if (!ctx_ok(p, ctx)) {
+        if (!ctx_ok<BS>(p, ctx)) {
           if (blockIdx.x == 0) atomicOr(p.err, kErrBadContext);
           ctx = 0;
         }
         s_ctx[b] = ctx;
-        local[i] = seq_from_ctx(ctx, p.window).nblk * p.n_kv_heads;
+        local[i] = seq_from_ctx<BS, BPU>(ctx, p.window).nunit * p.n_kv_heads;
         sum += local[i];
       }
     }
@@ -268,22 +294,28 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const __grid_c
     }
     Cursor c;
     c.b = lo;
-    c.r = seq_from_ctx(s_ctx[lo], p.window);
+    c.r = seq_from_ctx<BS, BPU>(s_ctx[lo], p.window);
     const int off = u - s_pre[lo];
-    c.h = off / c.r.nblk;
-    c.k = off - c.h * c.r.nblk;
+    c.h = off / c.r.nunit;
+    c.k = off - c.h * c.r.nunit;
     return c;
   };
-  auto table_entry = [&](const Cursor& c) {
-    return p.block_tables[static_cast<int64_t>(c.b) * p.mbs + c.r.first_blk + c.k];
+  // Table entries of the unit's blocks (-1 past the sequence's last block).
+  auto table_entries = [&](const Cursor& c, int (&phys)[BPU]) {
+    const int32_t* row = p.block_tables + static_cast<int64_t>(c.b) * p.mbs + c.r.first_blk;
+#pragma unroll
+    for (int i = 0; i < BPU; ++i) {
+      const int kb = c.k * BPU + i;
+      phys[i] = kb < c.r.nblk ? row[kb] : -1;
+    }
   };
 
   // ---- issue side (lane 0): the next unit to stage, in segment order
   Cursor ic{};
   int iu = 0, iu_end = 0, iseg = 0;
   bool idone = false;
-  int next_phys = 0;
-  uint32_t bad_stages = 0, tma_stages = 0;
+  int next_phys[BPU];
+  uint32_t bad_stages = 0, tma_stages = 0;  // bad: bit s * BPU + i for block i of stage s
   auto next_segment = [&]() {
     const int t = atomicAdd(p.ticket, 1);
     if (t >= sp.Nc) {
@@ -293,7 +325,7 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const __grid_c
     sp.chunk(t, iu, iu_end);
     iseg = sp.Ps + t;
     ic = locate(iu);
-    next_phys = table_entry(ic);
+    table_entries(ic, next_phys);
   };
   auto issue = [&](int s) {
     const uint32_t bar = smem_addr(&bars[s]);
@@ -303,33 +335,54 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const __grid_c
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
       return;
     }
-    int phys = next_phys;
-    const bool bad = phys < 0 || phys >= p.num_blocks;
-    if (bad) {
-      atomicOr(p.err, kErrBadBlock);
-      phys = 0;  // a valid address; every position of this block is masked
+    uint32_t bad = 0;
+    int nload = 0;
+    int phys[BPU];
+#pragma unroll
+    for (int i = 0; i < BPU; ++i) {
+      phys[i] = next_phys[i];
+      if (ic.k * BPU + i >= ic.r.nblk) {
+        phys[i] = -2;  // past the sequence: nothing to load
+        continue;
+      }
+      if (phys[i] < 0 || phys[i] >= p.num_blocks) {
+        atomicOr(p.err, kErrBadBlock);
+        bad |= 1u << i;
+        phys[i] = 0;  // a valid address; every position of this block is masked
+      }
+      ++nload;
     }
-    bad_stages = (bad_stages & ~(1u << s)) | (static_cast<uint32_t>(bad) << s);
+    const uint32_t smask = ((1u << BPU) - 1u) << (s * BPU);
+    bad_stages = (bad_stages & ~smask) | (bad << (s * BPU));
     tma_stages |= 1u << s;
     info[s] = StageInfo{iu, ic.b, ic.h, ic.k, iu_end, iseg};
     const uint32_t dst = smem_addr(ring + s * G::kStageBytes);
-    mbar_arrive_expect_tx(bar, G::kStageBytes);
+    mbar_arrive_expect_tx(bar, nload * G::kBlockBytes);
 #pragma unroll
-    for (int bx = 0; bx < G::kBoxes; ++bx)
-      tma_load_4d(dst + bx * G::kBoxBytes, &tmap, bar, bx * 64, 0, 0, phys * p.n_kv_heads + ic.h);
+    for (int i = 0; i < BPU; ++i) {
+      if (phys[i] == -2) continue;
+      const int tile = phys[i] * p.n_kv_heads + ic.h;
+      const uint32_t bdst = dst + i * G::kBlockBytes;
+#pragma unroll
+      for (int bx = 0; bx < G::kBoxes; ++bx)
+        tma_load_4d(bdst + bx * G::kBoxBytes, &tmap, bar, bx * 64, 0, 0, tile);
+      if constexpr (FP8)
+        bulk_load(bdst + G::kBoxBytes, p.pool + (static_cast<int64_t>(tile) * 2 + 1) * G::kVtBytes,
+                  G::kVtBytes, bar);
+    }
     // step to the next unit: within the segment, or the next chunk
     if (++iu < iu_end) {
-      if (++ic.k == ic.r.nblk) {
+      if (++ic.k == ic.r.nunit) {
         ic.k = 0;
         if (++ic.h == p.n_kv_heads) {
           ic.h = 0;
           do {
             ++ic.b;
-            ic.r = seq_from_ctx(s_ctx[ic.b], p.window);
-          } while (ic.r.nblk == 0);
+            ic.r = seq_from_ctx<BS, BPU>(s_ctx[ic.b], p.window);
+          } while (ic.r.nunit == 0);
         }
       }
-      next_phys = table_entry(ic);
+      table_entries(ic, next_phys);
     } else {
       next_segment();
     }
@@ -340,7 +393,7 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const __grid_c
       iu_end = static_cast<int>(static_cast<int64_t>(sp.Ts) * (worker + 1) / sp.Ps);
       iseg = worker;
       ic = locate(iu);
-      next_phys = table_entry(ic);
+      table_entries(ic, next_phys);
     } else {
       next_segment();
     }
@@ -352,7 +405,7 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const __grid_c
   const int n = lane >> 2;  // query head (within the group) this lane feeds, and token row
   const int j = lane & 3;
   const int g = p.group;
-  const int trow_k = (lane & 7) + (((lane >> 3) & 1) << 3);  // ldmatrix row for K / FP8 V
+  const int trow_k = (lane & 7) + (((lane >> 3) & 1) << 3);  // ldmatrix row of K
   const int swz = lane & 7;                                    // swizzle phase of that row
 
   uint32_t qf[G::kSteps][2];
@@ -372,7 +425,7 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const __grid_c
     }
     const StageInfo si = info[s];
     if (si.u < 0) break;
-    const SeqRange r = seq_from_ctx(s_ctx[si.b], p.window);
+    const SeqRange r = seq_from_ctx<BS, BPU>(s_ctx[si.b], p.window);
     const int64_t row0 = static_cast<int64_t>(si.b) * p.n_q_heads + static_cast<int64_t>(si.h) * g;
     if (si.u != prev_u + 1 || si.k == 0) {
       // ---- a new piece of a (b, h) pair: its query fragments, a fresh state
@@ -385,28 +438,38 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const __grid_c
           qf[ks][1] = n < g ? qr[(ks * 16 + 8 + 2 * j) >> 1] : 0u;
         }
       } else {
-        // f16 operands: bring the group's queries into (-1, 1) by an exact
-        // power of two and fold that power back into the score scale.
+        // E4M3 operands: scale the group's queries by an exact power of two
+        // below 256, split each into a high code and the code of its
+        // remainder (~8 significant bits together), and fold the power back
+        // into the score scale.  qf[c] holds the high codes of k-step c
+        // (dims 32c + 4j.. and 32c + 16 + 4j..), qf[4 + c] the remainders.
         float amax = 0.f;
         for (int i = lane; i < g * D; i += 32) amax = fmaxf(amax, fabsf(__bfloat162float(qg[i])));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
         int e = 0;
         if (amax > 0.f) frexpf(amax, &e);
-        const float qs = ldexpf(1.f, -e);
-        score_scale = p.scale_log2 * p.k_scale[si.h] * ldexpf(1.f, e);
-        // k-slot order matching the widened E4M3 fragments: slots 2j, 2j+1
-        // hold d = 16c + 4j + {0, 1}; slots 2j+8, 2j+9 hold d = 16c + 4j + {2, 3}.
+        const float qs = ldexpf(1.f, 8 - e);  // amax * qs < 256
+        score_scale = p.scale_log2 * p.k_scale[si.h] * ldexpf(1.f, e - 8);
 #pragma unroll
-        for (int c = 0; c < G::kSteps; ++c) {
-          float v4[4] = {0.f, 0.f, 0.f, 0.f};
-          if (n < g) {
+        for (int c = 0; c < D / 32; ++c) {
 #pragma unroll
-            for (int e4 = 0; e4 < 4; ++e4)
-              v4[e4] = __bfloat162float(qg[n * D + 16 * c + 4 * j + e4]) * qs;
+          for (int half = 0; half < 2; ++half) {
+            float v4[4] = {0.f, 0.f, 0.f, 0.f};
+            if (n < g) {
+#pragma unroll
+              for (int e4 = 0; e4 < 4; ++e4)
+                v4[e4] = __bfloat162float(qg[n * D + 32 * c + 16 * half + 4 * j + e4]) * qs;
+            }
+            const uint32_t h01 = f32x2_to_e4m3x2(v4[0], v4[1]);
+            const uint32_t h23 = f32x2_to_e4m3x2(v4[2], v4[3]);
+            const __half2 b01 = u32_as_half2(e4m3x2_to_f16x2(h01));
+            const __half2 b23 = u32_as_half2(e4m3x2_to_f16x2(h23));
+            const uint32_t l01 = f32x2_to_e4m3x2(v4[0] - __low2float(b01), v4[1] - __high2float(b01));
+            const uint32_t l23 = f32x2_to_e4m3x2(v4[2] - __low2float(b23), v4[3] - __high2float(b23));
+            qf[c][half] = h01 | (h23 << 16);
+            qf[D / 32 + c][half] = l01 | (l23 << 16);
           }
-          qf[c][0] = pack_f16x2(v4[0], v4[1]);
-          qf[c][1] = pack_f16x2(v4[2], v4[3]);
         }
       }
       m_run[0] = m_run[1] = -INFINITY;
@@ -416,141 +479,166 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const __grid_c
     }
     prev_u = si.u;
 
-    const int lb = r.first_blk + si.k;
-    const bool blk_ok = ((__shfl_sync(kFull, bad_stages, 0) >> s) & 1u) == 0;
-    const int t0 = lb * kBlockSize;
-    const bool full = blk_ok && t0 >= r.lo && t0 + kBlockSize <= r.ctx;
-    auto tok_ok = [&](int tr) {
-      const int pos = t0 + tr;
-      return full || (blk_ok && pos >= r.lo && pos < r.ctx);
-    };
+    const uint32_t bad_blocks = __shfl_sync(kFull, bad_stages, 0) >> (s * BPU);
+    const int unit_t0 = (r.first_blk + si.k * BPU) * BS;  // first token of the unit
     const uint32_t st = smem_addr(ring + s * G::kStageBytes);
 
-    // ---- S^T = K Q^T : rows = 16 tokens, cols = 8 query heads
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-    if constexpr (!FP8) {
 #pragma unroll
-      for (int ks = 0; ks < G::kSteps; ++ks) {
-        const int chunk = ((ks & 3) << 1) + (lane >> 4);
-        const uint32_t addr = st + (ks >> 2) * G::kBoxBytes + trow_k * G::kRowBytes +
-                              ((chunk ^ swz) << 4);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(addr, a0, a1, a2, a3);
-        if (ks & 1)
-          mma_bf16(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-        else
-          mma_bf16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-      }
-    } else {
-#pragma unroll
-      for (int cp = 0; cp < G::kSteps; cp += 2) {
-        const int chunk = cp + (lane >> 4);
-        const uint32_t addr = st + trow_k * G::kRowBytes + ((chunk ^ swz) << 4);
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4(addr, r0, r1, r2, r3);
-        mma_f16(sa, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
-                e4m3x2_to_f16x2(r1 >> 16), qf[cp][0], qf[cp][1]);
-        mma_f16(sb, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
-                e4m3x2_to_f16x2(r3 >> 16), qf[cp + 1][0], qf[cp + 1][1]);
-      }
-    }
+    for (int sub = 0; sub < G::kSub; ++sub) {
+      const int t0 = unit_t0 + 16 * sub;
+      const bool blk_ok = ((bad_blocks >> (sub / G::kSubPerBlock)) & 1u) == 0;
+      // a sub-tile wholly outside [lo, ctx) (before the window, or past the
+      // sequence's end in its last unit) is skipped; the warp agrees on it
+      const bool live = t0 < r.ctx && t0 + 16 > r.lo;
+      const bool full = blk_ok && t0 >= r.lo && t0 + 16 <= r.ctx;
+      auto tok_ok = [&](int tr) {
+        const int pos = t0 + tr;
+        return full || (blk_ok && pos >= r.lo && pos < r.ctx);
+      };
+      const uint32_t sk = st + G::k_off(sub), sv = st + G::v_off(sub);
 
-    // ---- V fragments to registers; then the stage is refilled at once, so
-    //      both ring stages are in flight while the softmax and V^T P^T run
-    uint32_t vf[G::kSteps][4];
-    if constexpr (!FP8) {
-      const int trow_v = kBlockSize + (lane & 7) + ((lane >> 4) << 3);
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t vf[G::kSteps][4];
+      if (live) {
+        // ---- S^T = K Q^T : rows = 16 tokens, cols = 8 query heads
+        if constexpr (!FP8) {
 #pragma unroll
-      for (int mt = 0; mt < G::kSteps; ++mt) {
-        const int chunk = ((mt & 3) << 1) + ((lane >> 3) & 1);
-        const uint32_t addr = st + (mt >> 2) * G::kBoxBytes + trow_v * G::kRowBytes +
-                              ((chunk ^ swz) << 4);
-        ldsm_x4_trans(addr, vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
-      }
-    } else {
+          for (int ks = 0; ks < G::kSteps; ++ks) {
+            const int chunk = ((ks & 3) << 1) + (lane >> 4);
+            const uint32_t addr = sk + (ks >> 2) * G::kBoxBytes + trow_k * G::kRowBytes +
+                                  ((chunk ^ swz) << 4);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(addr, a0, a1, a2, a3);
+            if (ks & 1)
+              mma_bf16(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            else
+              mma_bf16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+          }
+        } else {
+          // K codes go to the tensor cores as they are: k-step c covers dims
+          // 32c..32c+31 (swizzled chunks 2c and 2c+1 of each K row)
 #pragma unroll
-      for (int cp = 0; cp < G::kSteps; cp += 2) {
-        const int chunk = cp + (lane >> 4);
-        const uint32_t addr = st + (kBlockSize + trow_k) * G::kRowBytes + ((chunk ^ swz) << 4);
-        // V[token n or n+8][16 codes of chunk cp or cp+1]
-        ldsm_x4(addr, vf[cp >> 1][0], vf[cp >> 1][1], vf[cp >> 1][2], vf[cp >> 1][3]);
+          for (int c = 0; c < D / 32; ++c) {
+            const int chunk = 2 * c + (lane >> 4);
+            const uint32_t addr = sk + trow_k * G::kRowBytes + ((chunk ^ swz) << 4);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(addr, a0, a1, a2, a3);
+            mma_e4m3(sa, a0, a1, a2, a3, qf[c][0], qf[c][1]);
+            mma_e4m3(sb, a0, a1, a2, a3, qf[D / 32 + c][0], qf[D / 32 + c][1]);
+          }
+        }
+        // ---- V fragments to registers
+        if constexpr (!FP8) {
+          const int trow_v = (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+          for (int mt = 0; mt < G::kSteps; ++mt) {
+            const int chunk = ((mt & 3) << 1) + ((lane >> 3) & 1);
+            const uint32_t addr = sv + (mt >> 2) * G::kBoxBytes + trow_v * G::kRowBytes +
+                                  ((chunk ^ swz) << 4);
+            ldsm_x4_trans(addr, vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
+          }
+        } else {
+          // transposed V: row d holds the 16 codes of dimension d; ldmatrix i
+          // takes dims 32i..32i+31, i.e. rows g and g+8 of m-tiles 2i and 2i+1
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i)
+            ldsm_x4(sv + (32 * i + lane) * 16, vf[i][0], vf[i][1], vf[i][2], vf[i][3]);
+        }
       }
-    }
-    __syncwarp();
-    if (lane == 0) {
-      fence_proxy_async_smem();  // this stage's reads happen before the next copy lands
-      issue(s);
-    }
+      // after the unit's last reads from the stage, refill it at once so the
+      // ring stays full while the softmax and V^T P^T run
+      if (sub == G::kSub - 1) {
+        __syncwarp();
+        if (lane == 0) {
+          fence_proxy_async_smem();  // this stage's reads happen before the next copy lands
+          issue(s);
+        }
+      }
+      if (!live) continue;
 
-    // ---- online softmax (log2 domain); this lane holds tokens n, n+8 of heads 2j, 2j+1
-    const bool v0 = tok_ok(n), v1 = tok_ok(n + 8);
-    const float s0 = v0 ? (sa[0] + sb[0]) * score_scale : -INFINITY;
-    const float s1 = v0 ? (sa[1] + sb[1]) * score_scale : -INFINITY;
-    const float s2 = v1 ? (sa[2] + sb[2]) * score_scale : -INFINITY;
-    const float s3 = v1 ? (sa[3] + sb[3]) * score_scale : -INFINITY;
-    float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+      // ---- online softmax (log2 domain); this lane holds tokens n, n+8 of heads 2j, 2j+1
+      const bool v0 = tok_ok(n), v1 = tok_ok(n + 8);
+      const float s0 = v0 ? (sa[0] + sb[0]) * score_scale : -INFINITY;
+      const float s1 = v0 ? (sa[1] + sb[1]) * score_scale : -INFINITY;
+      const float s2 = v1 ? (sa[2] + sb[2]) * score_scale : -INFINITY;
+      const float s3 = v1 ? (sa[3] + sb[3]) * score_scale : -INFINITY;
+      float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, o));
-      bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, o));
-    }
-    const float mn0 = fmaxf(m_run[0], bm0), mn1 = fmaxf(m_run[1], bm1);
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = fast_exp2(m_run[0] - mu0), al1 = fast_exp2(m_run[1] - mu1);
-    const float p0 = fast_exp2(s0 - mu0), p1 = fast_exp2(s1 - mu1);
-    const float p2 = fast_exp2(s2 - mu0), p3 = fast_exp2(s3 - mu1);
-    l_run[0] = l_run[0] * al0 + p0 + p2;
-    l_run[1] = l_run[1] * al1 + p1 + p3;
-    m_run[0] = mn0;
-    m_run[1] = mn1;
+      for (int o = 4; o < 32; o <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, o));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, o));
+      }
+      const float mn0 = fmaxf(m_run[0], bm0), mn1 = fmaxf(m_run[1], bm1);
+      const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float p0 = fast_exp2(s0 - mu0), p1 = fast_exp2(s1 - mu1);
+      const float p2 = fast_exp2(s2 - mu0), p3 = fast_exp2(s3 - mu1);
+      // rescale the running state only when some running maximum moved
+      if (__any_sync(kFull, mn0 != m_run[0] || mn1 != m_run[1])) {
+        const float al0 = fast_exp2(m_run[0] - mu0), al1 = fast_exp2(m_run[1] - mu1);
+        l_run[0] *= al0;
+        l_run[1] *= al1;
 #pragma unroll
-    for (int i = 0; i < G::kSteps; ++i) {
-      acc[i][0] *= al0;
-      acc[i][1] *= al1;
-      acc[i][2] *= al0;
-      acc[i][3] *= al1;
-    }
+        for (int i = 0; i < G::kSteps; ++i) {
+          acc[i][0] *= al0;
+          acc[i][1] *= al1;
+          acc[i][2] *= al0;
+          acc[i][3] *= al1;
+        }
+      }
+      l_run[0] += p0 + p2;
+      l_run[1] += p1 + p3;
+      m_run[0] = mn0;
+      m_run[1] = mn1;
 
-    // ---- O^T += V^T P^T : rows = head_dim, cols = 8 query heads, k = 16 tokens
-    if constexpr (!FP8) {
-      const uint32_t x01 = pack_bf16x2(p0, p1), x23 = pack_bf16x2(p2, p3);
-      const uint32_t y01 = pack_bf16x2(p0 - bf16_lo(x01), p1 - bf16_hi(x01));
-      const uint32_t y23 = pack_bf16x2(p2 - bf16_lo(x23), p3 - bf16_hi(x23));
-      const uint32_t bh0 = movmatrix_trans(x01), bh1 = movmatrix_trans(x23);
-      const uint32_t bl0 = movmatrix_trans(y01), bl1 = movmatrix_trans(y23);
-      // this lane's V^T fragment covers tokens 2j, 2j+1 (a0, a1) and 2j+8, 2j+9 (a2, a3)
-      uint32_t mlo = kFull, mhi = kFull;
-      if (!full) {
-        mlo = (tok_ok(2 * j) ? 0x0000ffffu : 0u) | (tok_ok(2 * j + 1) ? 0xffff0000u : 0u);
-        mhi = (tok_ok(2 * j + 8) ? 0x0000ffffu : 0u) | (tok_ok(2 * j + 9) ? 0xffff0000u : 0u);
-      }
+      // ---- O^T += V^T P^T : rows = head_dim, cols = 8 query heads, k = 16 tokens
+      if constexpr (!FP8) {
+        const uint32_t x01 = pack_bf16x2(p0, p1), x23 = pack_bf16x2(p2, p3);
+        const uint32_t y01 = pack_bf16x2(p0 - bf16_lo(x01), p1 - bf16_hi(x01));
+        const uint32_t y23 = pack_bf16x2(p2 - bf16_lo(x23), p3 - bf16_hi(x23));
+        const uint32_t bh0 = movmatrix_trans(x01), bh1 = movmatrix_trans(x23);
+        const uint32_t bl0 = movmatrix_trans(y01), bl1 = movmatrix_trans(y23);
+        // this lane's V^T fragment covers tokens 2j, 2j+1 (a0, a1) and 2j+8, 2j+9 (a2, a3)
+        uint32_t mlo = kFull, mhi = kFull;
+        if (!full) {
+          mlo = (tok_ok(2 * j) ? 0x0000ffffu : 0u) | (tok_ok(2 * j + 1) ? 0xffff0000u : 0u);
+          mhi = (tok_ok(2 * j + 8) ? 0x0000ffffu : 0u) | (tok_ok(2 * j + 9) ? 0xffff0000u : 0u);
+        }
 #pragma unroll
-      for (int mt = 0; mt < G::kSteps; ++mt) {
-        const uint32_t a0 = vf[mt][0] & mlo, a1 = vf[mt][1] & mlo;
-        const uint32_t a2 = vf[mt][2] & mhi, a3 = vf[mt][3] & mhi;
-        mma_bf16(acc[mt], a0, a1, a2, a3, bh0, bh1);
-        mma_bf16(acc[mt], a0, a1, a2, a3, bl0, bl1);
-      }
-    } else {
-      const uint32_t b0 = movmatrix_trans(pack_f16x2(p0, p1));
-      const uint32_t b1 = movmatrix_trans(pack_f16x2(p2, p3));
+        for (int mt = 0; mt < G::kSteps; ++mt) {
+          const uint32_t a0 = vf[mt][0] & mlo, a1 = vf[mt][1] & mlo;
+          const uint32_t a2 = vf[mt][2] & mhi, a3 = vf[mt][3] & mhi;
+          mma_bf16(acc[mt], a0, a1, a2, a3, bh0, bh1);
+          mma_bf16(acc[mt], a0, a1, a2, a3, bl0, bl1);
+        }
+      } else {
+        // P^T as E4M3 codes of 256 p: after the transpose this lane holds head
+        // n at tokens 2j, 2j+1 (tX) and 2j+8, 2j+9 (tY) -- the tokens the
+        // transposed V tile keeps at codes 4j..4j+3 of every row.  k 0..15 of
+        // the product take the high codes, k 16..31 the codes of the
+        // remainders against the same V codes, so P keeps ~8 bits.
+        const uint32_t tX = movmatrix_trans(pack_f16x2(p0 * 256.f, p1 * 256.f));
+        const uint32_t tY = movmatrix_trans(pack_f16x2(p2 * 256.f, p3 * 256.f));
+        const uint32_t hX = f16x2_to_e4m3x2(tX), hY = f16x2_to_e4m3x2(tY);
+        const uint32_t lX = f16x2_to_e4m3x2(hsub2_bits(tX, e4m3x2_to_f16x2(hX)));
+        const uint32_t lY = f16x2_to_e4m3x2(hsub2_bits(tY, e4m3x2_to_f16x2(hY)));
+        const uint32_t bhi = hX | (hY << 16), blo = lX | (lY << 16);
+        uint32_t vmask = kFull;
+        if (!full)
+          vmask = (tok_ok(2 * j) ? 0x000000ffu : 0u) | (tok_ok(2 * j + 1) ? 0x0000ff00u : 0u) |
+                  (tok_ok(2 * j + 8) ? 0x00ff0000u : 0u) | (tok_ok(2 * j + 9) ? 0xff000000u : 0u);
 #pragma unroll
-      for (int cp = 0; cp < G::kSteps; cp += 2) {
-        uint32_t r0 = vf[cp >> 1][0], r1 = vf[cp >> 1][1], r2 = vf[cp >> 1][2], r3 = vf[cp >> 1][3];
-        if (!v0) r0 = r2 = 0u;
-        if (!v1) r1 = r3 = 0u;
-        mma_f16(acc[cp], movmatrix_trans(e4m3x2_to_f16x2(r0)),
-                movmatrix_trans(e4m3x2_to_f16x2(r0 >> 16)), movmatrix_trans(e4m3x2_to_f16x2(r1)),
-                movmatrix_trans(e4m3x2_to_f16x2(r1 >> 16)), b0, b1);
-        mma_f16(acc[cp + 1], movmatrix_trans(e4m3x2_to_f16x2(r2)),
-                movmatrix_trans(e4m3x2_to_f16x2(r2 >> 16)), movmatrix_trans(e4m3x2_to_f16x2(r3)),
-                movmatrix_trans(e4m3x2_to_f16x2(r3 >> 16)), b0, b1);
+        for (int i = 0; i < D / 32; ++i) {
+          const uint32_t a0 = vf[i][0] & vmask, a1 = vf[i][1] & vmask;
+          const uint32_t c0 = vf[i][2] & vmask, c1 = vf[i][3] & vmask;
+          mma_e4m3(acc[2 * i], a0, a1, a0, a1, bhi, blo);
+          mma_e4m3(acc[2 * i + 1], c0, c1, c0, c1, bhi, blo);
+        }
       }
     }
 
     // ---- end of this piece of pair (b, h): write it out
-    if (si.k == r.nblk - 1 || si.u + 1 == si.seg_end) {
+    if (si.k == r.nunit - 1 || si.u + 1 == si.seg_end) {
       float l0 = l_run[0], l1 = l_run[1];
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
@@ -560,9 +648,9 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const __grid_c
       const int pair = si.b * p.n_kv_heads + si.h;
       const int pair_start = si.u - si.k;
       const int first_seg = sp.seg_of(pair_start);
-      const int cnt = sp.seg_of(pair_start + r.nblk - 1) - first_seg + 1;
+      const int cnt = sp.seg_of(pair_start + r.nunit - 1) - first_seg + 1;
       const bool whole = cnt == 1;
-      const float vsc = FP8 ? p.v_scale[si.h] : 1.f;
+      const float vsc = FP8 ? p.v_scale[si.h] * (1.f / 256.f) : 1.f;  // FP8: P was 256 p
       const int h0 = 2 * j, h1 = 2 * j + 1;  // query heads of this lane's columns
       const float f0 = whole ? (l0 > 0.f ? vsc / l0 : 0.f) : vsc;
       const float f1 = whole ? (l1 > 0.f ? vsc / l1 : 0.f) : vsc;
@@ -570,14 +658,7 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const __grid_c
                          : p.part_o + (static_cast<int64_t>(si.seg) + pair) * g * D;
 #pragma unroll
       for (int i = 0; i < G::kSteps; ++i) {
-        int da, db;  // head_dim rows of accumulator entries {0,1} and {2,3}
-        if constexpr (!FP8) {
-          da = 16 * i + n;
-          db = da + 8;
-        } else {
-          da = 16 * i + 4 * (n >> 1) + (n & 1);
-          db = da + 2;
-        }
+        const int da = 16 * i + n, db = da + 8;  // head_dim rows of entries {0,1}, {2,3}
         if (h0 < g) {
           dst[h0 * D + da] = acc[i][0] * f0;
           dst[h0 * D + db] = acc[i][2] * f0;
@@ -619,7 +700,7 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const __grid_c
 // then slice 0 combines the slices in shared memory.  Launched as a
 // programmatic dependent of the decode kernel: everything before
 // griddepcontrol.wait reads only inputs of the call.
-template <int D>
+template <int D, int BS>
 __global__ void __launch_bounds__(512) paged_decode_reduce_kernel(const DecodeParams p) {
   constexpr int kGroups = D / 4;  // float4 column groups per head
   __shared__ float4 s_o[512];
@@ -635,8 +716,8 @@ __global__ void __launch_bounds__(512) paged_decode_reduce_kernel(const DecodePa
   const int hd = idx / kGroups;
   const int c4 = idx - hd * kGroups;
   int32_t ctx = p.context_lens[b];
-  if (!ctx_ok(p, ctx)) ctx = 0;
-  const SeqRange r = seq_from_ctx(ctx, p.window);
+  if (!ctx_ok<BS>(p, ctx)) ctx = 0;
+  const SeqRange r = seq_from_ctx<BS, 1>(ctx, p.window);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (r.nblk == 0) return;  // empty sequences were zeroed by the decode kernel
   const int2 meta = p.pair_meta[pair];
@@ -703,16 +784,17 @@ __global__ void __launch_bounds__(512) paged_decode_reduce_kernel(const DecodePa
   *dst = make_float4(Ot.x * inv, Ot.y * inv, Ot.z * inv, Ot.w * inv);
 }
 
-template <int D, bool FP8, int NW, int STAGES>
+template <int D, bool FP8, int BS, int BPU, int NW, int STAGES>
 struct Variant {
-  static constexpr int kSmem = Smem<D, FP8, NW, STAGES>::kBytes;
+  static constexpr int kSmem = Smem<D, FP8, BS, BPU, NW, STAGES>::kBytes;
   static constexpr int kWarps = NW;
+  static constexpr int kBlocksPerUnit = BPU;
 
   // Opt in to the dynamic shared memory once; report resident CTAs per SM.
   static int ctas_per_sm() {
     static int ctas = -1;
     if (ctas < 0) {
-      auto kernel = paged_decode_kernel<D, FP8, NW, STAGES>;
+      auto kernel = paged_decode_kernel<D, FP8, BS, BPU, NW, STAGES>;
       int n = 0;
       if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
               cudaSuccess ||
@@ -739,7 +821,8 @@ struct Variant {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = dependent ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, FP8, NW, STAGES>, pool->tmap, p);
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, FP8, BS, BPU, NW, STAGES>, pool->tmap,
+                              p);
   }
 };
 
@@ -754,23 +837,50 @@ struct Variant {
 #define PKV_FP8_WARPS 4
 #endif
 #ifndef PKV_FP8_STAGES
-#define PKV_FP8_STAGES 4
+#define PKV_FP8_STAGES 2
+#endif
+#ifndef PKV_FP8_BPU
+#define PKV_FP8_BPU 2
+#endif
+#ifndef PKV_BS32_WARPS
+#define PKV_BS32_WARPS 2
 #endif
 
-using Bf16D128 = Variant<128, false, PKV_BF16_WARPS, PKV_BF16_STAGES>;
-using Bf16D64 = Variant<64, false, 4, 4>;
-using Fp8D128 = Variant<128, true, PKV_FP8_WARPS, PKV_FP8_STAGES>;
+// 16-token blocks: bf16 stages one block per unit; FP8 stages two, so a unit
+// carries 32 tokens (8 KB) and the per-unit work is spread over twice the
+// bytes.  32-token blocks: one block per unit (two 16-token sub-tiles).
+using Bf16D128 = Variant<128, false, 16, 1, PKV_BF16_WARPS, PKV_BF16_STAGES>;
+using Bf16D64 = Variant<64, false, 16, 1, 4, 4>;
+using Fp8D128 = Variant<128, true, 16, PKV_FP8_BPU, PKV_FP8_WARPS, PKV_FP8_STAGES>;
+using Bf16D128B32 = Variant<128, false, 32, 1, PKV_BS32_WARPS, 2>;
+using Bf16D64B32 = Variant<64, false, 32, 1, 4, 2>;
+using Fp8D128B32 = Variant<128, true, 32, 1, PKV_FP8_WARPS, 2>;
+
+// Call f with the variant type the pool uses.
+template <typename F>
+auto with_variant(const kv_pool* pool, F&& f) {
+  if (pool->block_size == 32) {
+    if (pool->dtype == KV_FP8_E4M3) return f(Fp8D128B32{});
+    if (pool->head_dim == 128) return f(Bf16D128B32{});
+    return f(Bf16D64B32{});
+  }
+  if (pool->dtype == KV_FP8_E4M3) return f(Fp8D128{});
+  if (pool->head_dim == 128) return f(Bf16D128{});
+  return f(Bf16D64{});
+}
 
 }  // namespace
 
 int decode_warps_per_cta(const kv_pool* pool) {
-  if (pool->dtype == KV_FP8_E4M3) return Fp8D128::kWarps;
-  return pool->head_dim == 128 ? Bf16D128::kWarps : Bf16D64::kWarps;
+  return with_variant(pool, [](auto v) { return decltype(v)::kWarps; });
 }
 
 int decode_ctas_per_sm(const kv_pool* pool) {
-  if (pool->dtype == KV_FP8_E4M3) return Fp8D128::ctas_per_sm();
-  return pool->head_dim == 128 ? Bf16D128::ctas_per_sm() : Bf16D64::ctas_per_sm();
+  return with_variant(pool, [](auto v) { return decltype(v)::ctas_per_sm(); });
+}
+
+int decode_blocks_per_unit(const kv_pool* pool) {
+  return with_variant(pool, [](auto v) { return decltype(v)::kBlocksPerUnit; });
 }
 
 // Upper bound of Split::Nc over every launch of at most `max_units` units:
@@ -787,9 +897,7 @@ int64_t decode_max_chunks(int64_t max_units) {
 
 cudaError_t launch_decode(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream,
                           bool dependent) {
-  if (pool->dtype == KV_FP8_E4M3) return Fp8D128::launch(pool, p, stream, dependent);
-  if (pool->head_dim == 128) return Bf16D128::launch(pool, p, stream, dependent);
-  return Bf16D64::launch(pool, p, stream, dependent);
+  return with_variant(pool, [&](auto v) { return decltype(v)::launch(pool, p, stream, dependent); });
 }
 
 cudaError_t launch_reduce(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream) {
@@ -804,8 +912,12 @@ cudaError_t launch_reduce(const kv_pool* pool, const DecodeParams& p, cudaStream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (pool->head_dim == 128) return cudaLaunchKernelEx(&cfg, paged_decode_reduce_kernel<128>, p);
-  return cudaLaunchKernelEx(&cfg, paged_decode_reduce_kernel<64>, p);
+  if (pool->block_size == 32) {
+    if (pool->head_dim == 128) return cudaLaunchKernelEx(&cfg, paged_decode_reduce_kernel<128, 32>, p);
+    return cudaLaunchKernelEx(&cfg, paged_decode_reduce_kernel<64, 32>, p);
+  }
+  if (pool->head_dim == 128) return cudaLaunchKernelEx(&cfg, paged_decode_reduce_kernel<128, 16>, p);
+  return cudaLaunchKernelEx(&cfg, paged_decode_reduce_kernel<64, 16>, p);
 }
 
 }  // namespace pkv

@@ -31,7 +31,7 @@ constexpr int kMaxDecodeBatch = 512;
 // Arguments of the stream-K decode, shared by all variants.
 //
 // The work of one call is the sequence of "units" (sequence b, KV head h,
-// k-th attended block of b), ordered by b, then h, then k, cut into
+// k-th run of BPU attended blocks of b), ordered by b, then h, then k, cut into
 // segments: `num_workers` static shares of its first part, then fixed-size
 // chunks of the rest handed out through `ticket`.  A (b, h) pair inside one
 // segment is finished by the warp that holds it; a pair cut between segments
@@ -39,6 +39,7 @@ constexpr int kMaxDecodeBatch = 512;
 // the reduce kernel.
 struct DecodeParams {
   const void* q;                // bf16 [B][Hq][D]
+  const uint8_t* pool;          // pool base (FP8: the transposed V tiles are bulk-copied)
   const int32_t* block_tables;  // [B][mbs]
   const int32_t* context_lens;  // [B]
   float* out;                   // [B][Hq][D]
@@ -68,9 +69,11 @@ struct DecodePlan {
 DecodePlan plan_decode(const kv_pool* pool, int32_t batch, int32_t n_q_heads,
                        int32_t max_context_len, int32_t sliding_window);
 
-// Warps per CTA and resident CTAs per SM of the decode variant the pool uses.
+// Warps per CTA, resident CTAs per SM, and pool blocks staged per work unit
+// of the decode variant the pool uses.
 int decode_warps_per_cta(const kv_pool* pool);
 int decode_ctas_per_sm(const kv_pool* pool);
+int decode_blocks_per_unit(const kv_pool* pool);
 // Most dynamic chunks a launch of at most `max_units` units can hand out.
 int64_t decode_max_chunks(int64_t max_units);
 

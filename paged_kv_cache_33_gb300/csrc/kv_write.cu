@@ -7,7 +7,8 @@
 // Slot s names physical block s / block_size and offset s mod block_size
 // (section "PagedAttention: Virtual Memory for LLMs").
 //
-// Pool layout: [num_blocks][Hkv][2][16][D], D contiguous.  One thread moves
+// Pool layout: [num_blocks][Hkv][2][block_size][D], D contiguous (FP8 pools
+// keep each V tile transposed, in [D][16] sub-tiles).  One thread moves
 // 16 bytes of destination; consecutive threads cover one destination row, so
 // every store is a full, coalesced 16-byte vector.
 
@@ -23,7 +24,7 @@ namespace {
 template <int D>
 __global__ void __launch_bounds__(256) kv_write_bf16_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
-    int64_t num_tokens, int hkv, int64_t num_slots, uint4* __restrict__ pool,
+    int64_t num_tokens, int hkv, int bs, int64_t num_slots, uint4* __restrict__ pool,
     uint32_t* __restrict__ err, int32_t* __restrict__ zero_word) {
   constexpr int kChunks = D / 8;  // 16-byte chunks per row
   // a decode launched as this kernel's programmatic dependent may start now;
@@ -45,20 +46,28 @@ __global__ void __launch_bounds__(256) kv_write_bf16_kernel(
     if (c == 0 && kv == 0 && h == 0) atomicOr(err, kErrBadSlot);
     return;
   }
-  const int64_t blk = s / kBlockSize;
-  const int off = static_cast<int>(s % kBlockSize);
+  const int64_t blk = s / bs;
+  const int off = static_cast<int>(s % bs);
   const uint4 val = (kv ? v : k)[(t * hkv + h) * kChunks + c];
-  const int64_t row = ((blk * hkv + h) * 2 + kv) * kBlockSize + off;
+  const int64_t row = ((blk * hkv + h) * 2 + kv) * bs + off;
   pool[row * kChunks + c] = val;
+}
+
+// Byte position of token `off` (0..15) inside a row of a transposed FP8 V
+// sub-tile: tokens 2t, 2t+1, 2t+8, 2t+9 sit at codes 4t..4t+3, the order in
+// which the decode kernel's probabilities arrive after their transpose.
+__device__ __forceinline__ int vt_slot(int off) {
+  return 4 * ((off & 7) >> 1) + (off & 1) + 2 * (off >> 3);
 }
 
 // FP8 pool: code = E4M3(float(x) / scale[h]) with round-to-nearest-even and
 // saturation to +-448 (the cvt.rn.satfinite conversion).  Thread i makes 16
-// codes (one 16-byte store) from 16 bf16 inputs.
+// codes from 16 bf16 inputs: one 16-byte store into a K row, or 16 byte
+// stores down one column of the transposed V tile ([D][16] codes).
 template <int D>
 __global__ void __launch_bounds__(256) kv_write_fp8_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
-    int64_t num_tokens, int hkv, int64_t num_slots, const float* __restrict__ scales,
+    int64_t num_tokens, int hkv, int bs, int64_t num_slots, const float* __restrict__ scales,
     uint4* __restrict__ pool, uint32_t* __restrict__ err, int32_t* __restrict__ zero_word) {
   constexpr int kChunks = D / 16;  // 16-code chunks per row
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -97,10 +106,19 @@ __global__ void __launch_bounds__(256) kv_write_fp8_kernel(
     }
     packed[q] = word;
   }
-  const int64_t blk = s / kBlockSize;
-  const int off = static_cast<int>(s % kBlockSize);
-  const int64_t row = ((blk * hkv + h) * 2 + kv) * kBlockSize + off;
-  pool[row * kChunks + c] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  const int64_t blk = s / bs;
+  const int off = static_cast<int>(s % bs);
+  const int64_t tile = (blk * hkv + h) * 2 + kv;  // K or V tile of (block, head)
+  if (kv == 0) {
+    pool[(tile * bs + off) * kChunks + c] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  } else {
+    // sub-tile off / 16 of the transposed V tile: [D][16] codes
+    uint8_t* vt = reinterpret_cast<uint8_t*>(pool) + tile * bs * D + (off >> 4) * 16 * D;
+    const int col = vt_slot(off & 15);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      vt[(16 * c + i) * 16 + col] = static_cast<uint8_t>(packed[i >> 2] >> (8 * (i & 3)));
+  }
 }
 
 }  // namespace
@@ -117,17 +135,17 @@ cudaError_t launch_kv_write(const kv_pool* pool, const void* k, const void* v,
     if (pool->head_dim == 128)
       kv_write_bf16_kernel<128><<<blocks, threads, 0, stream>>>(
           static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, hkv,
-          num_slots, static_cast<uint4*>(pool->base), pool->err, zero_word);
+          pool->block_size, num_slots, static_cast<uint4*>(pool->base), pool->err, zero_word);
     else
       kv_write_bf16_kernel<64><<<blocks, threads, 0, stream>>>(
           static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, hkv,
-          num_slots, static_cast<uint4*>(pool->base), pool->err, zero_word);
+          pool->block_size, num_slots, static_cast<uint4*>(pool->base), pool->err, zero_word);
   } else {
     const int64_t total = num_tokens * hkv * 2 * (pool->head_dim / 16);
     const int64_t blocks = std::max<int64_t>(1, (total + threads - 1) / threads);
     kv_write_fp8_kernel<128><<<blocks, threads, 0, stream>>>(
         static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, hkv,
-        num_slots, pool->scales, static_cast<uint4*>(pool->base), pool->err, zero_word);
+        pool->block_size, num_slots, pool->scales, static_cast<uint4*>(pool->base), pool->err, zero_word);
   }
   return cudaGetLastError();
 }

@@ -38,7 +38,8 @@ class _Desc(ctypes.Structure):
                 ("block_size", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("strides", ctypes.c_int64 * 5), ("bytes", ctypes.c_uint64),
-                ("device", ctypes.c_int32), ("scales_dev", ctypes.c_void_p)]
+                ("device", ctypes.c_int32), ("scales_dev", ctypes.c_void_p),
+                ("v_layout", ctypes.c_int32)]
 
 
 _lib = None
@@ -163,7 +164,7 @@ class KVPool:
         return {"base_dev": d.base_dev, "num_blocks": d.num_blocks, "block_size": d.block_size,
                 "n_kv_heads": d.n_kv_heads, "head_dim": d.head_dim, "dtype": d.dtype,
                 "strides": list(d.strides), "bytes": d.bytes, "device": d.device,
-                "scales_dev": d.scales_dev}
+                "scales_dev": d.scales_dev, "v_layout": d.v_layout}
 
     def view(self) -> torch.Tensor:
         """The pool memory as a torch tensor [NB, Hkv, 2, BS, D] (bf16 or uint8), no copy."""
@@ -177,6 +178,23 @@ class KVPool:
                                         "version": 3, "strides": None}
         t = torch.as_tensor(_Buf(), device=f"cuda:{i['device']}")
         return t.view(tdt) if tdt == torch.bfloat16 else t
+
+    def rows(self) -> torch.Tensor:
+        """Inspection: the pool as [NB, Hkv, 2, BS, D] with every V tile in
+        token-row order.  The raw view itself for row-major pools; a copy with
+        the transposed V tiles turned back for pools that store them so."""
+        raw = self.view()
+        if self.info()["v_layout"] == 0:
+            return raw
+        bs, d = self.block_size, self.head_dim
+        pos = torch.tensor([4 * ((t % 8) // 2) + t % 2 + 2 * (t // 8) for t in range(16)],
+                           device=raw.device)
+        # each V tile: bs/16 sub-tiles of [D][16] codes
+        vt = raw[:, :, 1].reshape(self.num_blocks, self.n_kv_heads, bs // 16, d, 16)
+        rows = vt[..., pos].transpose(3, 4)            # [NB, Hkv, sub, 16, D]
+        out = raw.clone()
+        out[:, :, 1] = rows.reshape(self.num_blocks, self.n_kv_heads, bs, d)
+        return out
 
     def set_scales(self, k_scale: torch.Tensor, v_scale: torch.Tensor, stream=None) -> None:
         _check(load().kv_pool_set_scales(self.handle, _dev(k_scale, torch.float32, "k_scale"),

@@ -33,11 +33,12 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-BLOCK_SIZE = 16
+BLOCK_SIZE = 16        # default tokens per block
+GROWTH_TOKENS = 16     # tokens a churn step appends to a running request
 CONFIGS = ("tiny", "8b", "70b", "sw", "fp8")
 
-DATA_SEED = {"tiny": 1000, "8b": 1001, "70b": 1002, "sw": 1003, "fp8": 1004}
-TABLE_SEED = {"tiny": 2000, "8b": 2001, "70b": 2002, "sw": 2003, "fp8": 2004}
+DATA_SEED = {"tiny": 1000, "8b": 1001, "70b": 1002, "sw": 1003, "fp8": 1004, "long": 1005}
+TABLE_SEED = {"tiny": 2000, "8b": 2001, "70b": 2002, "sw": 2003, "fp8": 2004, "long": 2005}
 
 
 @dataclass
@@ -192,66 +193,66 @@ def _cdiv(a: int, b: int) -> int:
     return -(-a // b)
 
 
-def _tiny(size: str) -> Workload:
+def _tiny(size: str, bs: int = BLOCK_SIZE) -> Workload:
     rng = np.random.default_rng(TABLE_SEED["tiny"])
     lens = np.array([5, 16, 33, 70], dtype=np.int32)
     nb = 64
     perm = rng.permutation(nb).astype(np.int32)
-    nblk = [_cdiv(int(c), BLOCK_SIZE) for c in lens]
+    nblk = [_cdiv(int(c), bs) for c in lens]
     tables = _tables_from_ids(nblk, perm, max(nblk))
-    return Workload("tiny", size, 4, 2, 1, 64, BLOCK_SIZE, nb, 0, "bf16", 1.0 / math.sqrt(64),
+    return Workload("tiny", size, 4, 2, 1, 64, bs, nb, 0, "bf16", 1.0 / math.sqrt(64),
                     lens, tables, (lens - 1).astype(np.int64), data_seed=DATA_SEED["tiny"])
 
 
-def _8b(size: str) -> Workload:
+def _8b(size: str, bs: int = BLOCK_SIZE) -> Workload:
     rng = np.random.default_rng(TABLE_SEED["8b"])
     B = 64 if size == "full" else 8
     lens = rng.integers(128, 4096, size=B, endpoint=True).astype(np.int32)
-    nblk = [_cdiv(int(c), BLOCK_SIZE) for c in lens]
+    nblk = [_cdiv(int(c), bs) for c in lens]
     needed = sum(nblk)
     nb = math.ceil(1.2 * needed)
     perm = rng.permutation(nb).astype(np.int32)
     tables = _tables_from_ids(nblk, perm, max(nblk))
-    return Workload("8b", size, B, 32, 8, 128, BLOCK_SIZE, nb, 0, "bf16", 1.0 / math.sqrt(128),
+    return Workload("8b", size, B, 32, 8, 128, bs, nb, 0, "bf16", 1.0 / math.sqrt(128),
                     lens, tables, (lens - 1).astype(np.int64), data_seed=DATA_SEED["8b"])
 
 
-def _70b(size: str) -> Workload:
+def _70b(size: str, bs: int = BLOCK_SIZE) -> Workload:
     rng = np.random.default_rng(TABLE_SEED["70b"])
     B = 128 if size == "full" else 12
     u = rng.uniform(math.log(256), math.log(8192), size=B)
     lens = np.clip(np.round(np.exp(u)), 256, 8192).astype(np.int32)
-    prefix_blocks = 64
-    private = [max(0, _cdiv(int(c), BLOCK_SIZE) - prefix_blocks) for c in lens]
+    prefix_blocks = 1024 // bs
+    private = [max(0, _cdiv(int(c), bs) - prefix_blocks) for c in lens]
     needed = prefix_blocks + sum(private)
     nb = math.ceil(1.2 * needed)
     perm = rng.permutation(nb).astype(np.int32)
     shared = perm[:prefix_blocks]
-    mbs = max(_cdiv(int(c), BLOCK_SIZE) for c in lens)
+    mbs = max(_cdiv(int(c), bs) for c in lens)
     tables = np.full((B, mbs), -1, dtype=np.int32)
     off = prefix_blocks
     for b, c in enumerate(lens):
-        n = _cdiv(int(c), BLOCK_SIZE)
+        n = _cdiv(int(c), bs)
         tables[b, :min(n, prefix_blocks)] = shared[:min(n, prefix_blocks)]
         if n > prefix_blocks:
             tables[b, prefix_blocks:n] = perm[off:off + n - prefix_blocks]
             off += n - prefix_blocks
     # Sequences that live inside the shared prefix write nothing this step:
     # their newest token is already part of the shared blocks.
-    new_pos = np.where(lens > prefix_blocks * BLOCK_SIZE, lens - 1, -1).astype(np.int64)
-    return Workload("70b", size, B, 64, 8, 128, BLOCK_SIZE, nb, 0, "bf16", 1.0 / math.sqrt(128),
-                    lens, tables, new_pos, shared_prefix_tokens=prefix_blocks * BLOCK_SIZE,
+    new_pos = np.where(lens > prefix_blocks * bs, lens - 1, -1).astype(np.int64)
+    return Workload("70b", size, B, 64, 8, 128, bs, nb, 0, "bf16", 1.0 / math.sqrt(128),
+                    lens, tables, new_pos, shared_prefix_tokens=prefix_blocks * bs,
                     prefix_blocks=shared.copy(), data_seed=DATA_SEED["70b"])
 
 
-def _sw(size: str) -> Workload:
+def _sw(size: str, bs: int = BLOCK_SIZE) -> Workload:
     rng = np.random.default_rng(TABLE_SEED["sw"])
     B = 32 if size == "full" else 4
     W = 4096
     lens = rng.integers(4096, 32768, size=B, endpoint=True).astype(np.int32)
-    mbs = _cdiv(32768, BLOCK_SIZE)
-    first = [(int(c) - W) // BLOCK_SIZE for c in lens]
-    last = [(int(c) - 1) // BLOCK_SIZE for c in lens]
+    mbs = _cdiv(32768, bs)
+    first = [(int(c) - W) // bs for c in lens]
+    last = [(int(c) - 1) // bs for c in lens]
     needed = sum(l - f + 1 for f, l in zip(first, last))
     nb = math.ceil(1.2 * needed)
     perm = rng.permutation(nb).astype(np.int32)
@@ -261,12 +262,12 @@ def _sw(size: str) -> Workload:
         n = last[b] - first[b] + 1
         tables[b, first[b]:last[b] + 1] = perm[off:off + n]
         off += n
-    return Workload("sw", size, B, 32, 8, 128, BLOCK_SIZE, nb, W, "bf16", 1.0 / math.sqrt(128),
+    return Workload("sw", size, B, 32, 8, 128, bs, nb, W, "bf16", 1.0 / math.sqrt(128),
                     lens, tables, (lens - 1).astype(np.int64), data_seed=DATA_SEED["sw"])
 
 
 def churn_tables(make_allocator, final_lens: np.ndarray, steps: int, occupancy: float,
-                 seed: int, max_len: int) -> tuple[int, np.ndarray, dict]:
+                 seed: int, max_len: int, bs: int = BLOCK_SIZE) -> tuple[int, np.ndarray, dict]:
     """Block tables for `final_lens` taken from an allocator after a seeded churn.
 
     The pool holds ceil(needed / occupancy) blocks.  Each churn step admits a
@@ -279,9 +280,9 @@ def churn_tables(make_allocator, final_lens: np.ndarray, steps: int, occupancy: 
     returns an object with admit/append/free/preempt_newest/table/num_free.
     """
     rng = np.random.default_rng(seed)
-    needed = int(sum(_cdiv(int(c), BLOCK_SIZE) for c in final_lens))
+    needed = int(sum(_cdiv(int(c), bs) for c in final_lens))
     nb = math.ceil(needed / occupancy)
-    alloc = make_allocator(nb, BLOCK_SIZE)
+    alloc = make_allocator(nb, bs)
     running: list[int] = []
     waiting: list[tuple[int, int]] = []   # (req_id, tokens), head first
     next_id = 0
@@ -320,13 +321,13 @@ def churn_tables(make_allocator, final_lens: np.ndarray, steps: int, occupancy: 
             stats["freed"] += 1
         if step % 4 == 3 and running:
             rid = running[int(rng.integers(0, len(running)))]
-            if alloc.append(rid, n=BLOCK_SIZE) == 0:
-                sizes[rid] += BLOCK_SIZE
+            if alloc.append(rid, n=GROWTH_TOKENS) == 0:
+                sizes[rid] += GROWTH_TOKENS
                 stats["grown"] += 1
     for i in rng.permutation(len(running)):
         alloc.free(running[i])
     base = 1 << 40
-    mbs = max(_cdiv(int(c), BLOCK_SIZE) for c in final_lens)
+    mbs = max(_cdiv(int(c), bs) for c in final_lens)
     tables = np.full((len(final_lens), mbs), -1, dtype=np.int32)
     for b, c in enumerate(final_lens):
         rc, _ = alloc.admit(base + b, num_tokens=int(c))
@@ -342,7 +343,7 @@ FP8_K_SCALE_BASE = 5.0   # per-KV-head scale = (base + step * h) / 448
 FP8_V_SCALE_BASE = 5.5
 
 
-def _fp8(size: str, make_allocator=None) -> Workload:
+def _fp8(size: str, make_allocator=None, bs: int = BLOCK_SIZE) -> Workload:
     rng = np.random.default_rng(TABLE_SEED["fp8"])
     B = 256 if size == "full" else 16
     max_len = 16384 if size == "full" else 4096
@@ -351,28 +352,48 @@ def _fp8(size: str, make_allocator=None) -> Workload:
     if make_allocator is None:
         raise ValueError("the fp8 workload needs a block allocator (make_allocator)")
     nb, tables, stats = churn_tables(make_allocator, lens, steps, 0.95,
-                                     int(rng.integers(0, 2**31)), max_len)
+                                     int(rng.integers(0, 2**31)), max_len, bs)
     hkv = 8
     # Fixed per-KV-head scales: N(0,1) data saturates only beyond ~5 sigma.
     k_scale = ((FP8_K_SCALE_BASE + 0.25 * np.arange(hkv)) / 448.0).astype(np.float32)
     v_scale = ((FP8_V_SCALE_BASE + 0.125 * np.arange(hkv)) / 448.0).astype(np.float32)
-    return Workload("fp8", size, B, 32, hkv, 128, BLOCK_SIZE, nb, 0, "fp8", 1.0 / math.sqrt(128),
+    return Workload("fp8", size, B, 32, hkv, 128, bs, nb, 0, "fp8", 1.0 / math.sqrt(128),
                     lens, tables, (lens - 1).astype(np.int64), k_scale=k_scale,
                     v_scale=v_scale, data_seed=DATA_SEED["fp8"], notes={"churn": stats})
 
 
-def make(name: str, size: str = "full", make_allocator=None) -> Workload:
-    """Build workload `name` ("tiny", "8b", "70b", "sw", "fp8") at size "full" or "small"."""
+def _long(size: str, bs: int = BLOCK_SIZE) -> Workload:
+    """8B-shaped decode over long contexts (the regime where the pages expect
+    32-token blocks to pay): batch 16, ctx U{32768..65536}."""
+    rng = np.random.default_rng(TABLE_SEED["long"])
+    B = 16 if size == "full" else 3
+    lo_len, hi_len = (32768, 65536) if size == "full" else (2048, 4096)
+    lens = rng.integers(lo_len, hi_len, size=B, endpoint=True).astype(np.int32)
+    nblk = [_cdiv(int(c), bs) for c in lens]
+    nb = math.ceil(1.2 * sum(nblk))
+    perm = rng.permutation(nb).astype(np.int32)
+    tables = _tables_from_ids(nblk, perm, max(nblk))
+    return Workload("long", size, B, 32, 8, 128, bs, nb, 0, "bf16", 1.0 / math.sqrt(128),
+                    lens, tables, (lens - 1).astype(np.int64), data_seed=DATA_SEED["long"])
+
+
+def make(name: str, size: str = "full", make_allocator=None, block_size: int = BLOCK_SIZE) -> Workload:
+    """Build workload `name` ("tiny", "8b", "70b", "sw", "fp8", "long") at size
+    "full" or "small", with pool blocks of `block_size` tokens (16 or 32)."""
     if size not in ("full", "small"):
         raise ValueError(size)
+    if block_size not in (16, 32):
+        raise ValueError(block_size)
     if name == "tiny":
-        return _tiny(size)
+        return _tiny(size, block_size)
     if name == "8b":
-        return _8b(size)
+        return _8b(size, block_size)
     if name == "70b":
-        return _70b(size)
+        return _70b(size, block_size)
     if name == "sw":
-        return _sw(size)
+        return _sw(size, block_size)
     if name == "fp8":
-        return _fp8(size, make_allocator)
+        return _fp8(size, make_allocator, block_size)
+    if name == "long":
+        return _long(size, block_size)
     raise ValueError(f"unknown workload {name!r}")

@@ -83,9 +83,12 @@ def compare_pools(pool: pagedkv.KVPool, opool: oracle.Pool, slots: np.ndarray,
     """Bit-exact comparison of the K/V rows at `slots` (GPU layout vs the pages' layout)."""
     if len(slots) > max_rows:
         slots = np.random.default_rng(0).choice(slots, max_rows, replace=False)
-    blk = torch.from_numpy(slots // 16)
-    off = torch.from_numpy(slots % 16)
-    v = pool.view()
+    bs = pool.block_size
+    assert opool.block_size == bs
+    assert len(slots) == 0 or (slots.min() >= 0 and slots.max() < pool.num_blocks * bs)
+    blk = torch.from_numpy(slots // bs)
+    off = torch.from_numpy(slots % bs)
+    v = pool.rows()
     g = v[blk.cuda(), :, :, off.cuda(), :]            # [n, Hkv, 2, D]
     g = g.permute(0, 2, 1, 3).contiguous().cpu()       # [n, 2, Hkv, D]
     if pool.dtype == "bf16":
@@ -93,7 +96,7 @@ def compare_pools(pool: pagedkv.KVPool, opool: oracle.Pool, slots: np.ndarray,
     else:
         g = g.numpy()
     arr = opool.array()                                # [NB, 2, BS, Hkv, D]
-    o = arr[slots // 16, :, slots % 16]                # [n, 2, Hkv, D]
+    o = arr[slots // bs, :, slots % bs]                # [n, 2, Hkv, D]
     bad = np.nonzero((g != o).reshape(len(slots), -1).any(axis=1))[0]
     assert bad.size == 0, f"{bad.size} rows differ, first slot {slots[bad[0]]}"
 
@@ -143,7 +146,7 @@ def run_parity(w: Workload, seqs=None, part_blocks: int | None = None,
     rows = list(range(w.batch)) if seqs is None else list(seqs)
     got = out.cpu().numpy()[rows]
     max_abs, rel = assert_close(w, got, ref[rows], f"{w.name}/{w.size}")
-    print(f"PARITY {w.name}/{w.size} seqs={len(rows)} part_blocks={part_blocks} "
+    print(f"PARITY {w.name}/{w.size} bs={w.block_size} seqs={len(rows)} part_blocks={part_blocks} "
           f"max_abs={max_abs:.3e} rel_l2={rel:.3e}")
     pool.destroy()
     return {"max_abs": max_abs, "rel_l2": rel}

@@ -51,7 +51,7 @@ def test_status_strings():
     ((10, 0, 8, 128, 0), 1),        # no block size
     ((10, 16, 0, 128, 0), 1),       # no heads
     ((10, 16, 8, 128, 7), 1),       # unknown dtype
-    ((10, 32, 8, 128, 0), 4),       # block size other than 16
+    ((10, 64, 8, 128, 0), 4),       # block size other than 16 or 32
     ((10, 16, 8, 96, 0), 4),        # head_dim not 64/128
     ((10, 16, 8, 64, 1), 4),        # FP8 needs head_dim 128
 ])

@@ -20,28 +20,32 @@ from _parity import (assert_close, compare_pools, decode_gpu, fill_both, make_gp
 pytestmark = pytest.mark.gpu
 
 
-def _workload(name, size):
-    return W.make(name, size, make_allocator=oracle.Allocator if name == "fp8" else None)
+def _workload(name, size, block_size=16):
+    return W.make(name, size, make_allocator=oracle.Allocator if name == "fp8" else None,
+                  block_size=block_size)
 
 
-def test_tiny_workload_exact_path():
-    w = W.make("tiny")
+@pytest.mark.parametrize("block_size", [16, 32])
+def test_tiny_workload_exact_path(block_size):
+    w = W.make("tiny", block_size=block_size)
     r = run_parity(w)
     assert r["max_abs"] < 1e-4
 
 
-@pytest.mark.parametrize("name", ["8b", "70b", "sw", "fp8"])
+@pytest.mark.parametrize("block_size", [16, 32])
+@pytest.mark.parametrize("name", ["8b", "70b", "sw", "fp8", "long"])
 @pytest.mark.parametrize("part_blocks", [None, 4, 12])
-def test_small_workloads(name, part_blocks):
+def test_small_workloads(name, part_blocks, block_size):
     # several partitions per sequence (forced small partitions exercise the reduce)
-    run_parity(_workload(name, "small"), part_blocks=part_blocks)
+    run_parity(_workload(name, "small", block_size), part_blocks=part_blocks)
 
 
-@pytest.mark.parametrize("name", ["8b", "70b", "sw", "fp8"])
-def test_full_workloads_sampled(name):
+@pytest.mark.parametrize("block_size", [16, 32])
+@pytest.mark.parametrize("name", ["8b", "70b", "sw", "fp8", "long"])
+def test_full_workloads_sampled(name, block_size):
     """Full-size workloads in the bench's launch configuration; the oracle
     computes a sample of sequences (the longest, the shortest, and random)."""
-    w = _workload(name, "full")
+    w = _workload(name, "full", block_size)
     lens = w.context_lens
     rng = np.random.default_rng(5)
     pick = {int(np.argmax(lens)), int(np.argmin(lens))}
@@ -49,11 +53,11 @@ def test_full_workloads_sampled(name):
     run_parity(w, seqs=sorted(pick), device_fill_rest=True)
 
 
-def _custom(lens, hq=8, hkv=2, d=128, window=0, dtype="bf16", extra_blocks=7, seed=0):
+def _custom(lens, hq=8, hkv=2, d=128, window=0, dtype="bf16", extra_blocks=7, seed=0, bs=16):
     """A workload with chosen context lengths and shuffled physical blocks."""
     rng = np.random.default_rng(seed)
     lens = np.asarray(lens, dtype=np.int32)
-    nblk = [max(1, -(-int(c) // 16)) for c in lens]
+    nblk = [max(1, -(-int(c) // bs)) for c in lens]
     nb = sum(nblk) + extra_blocks
     perm = rng.permutation(nb).astype(np.int32)
     mbs = max(nblk)
@@ -62,7 +66,7 @@ def _custom(lens, hq=8, hkv=2, d=128, window=0, dtype="bf16", extra_blocks=7, se
     for b, n in enumerate(nblk):
         tables[b, :n] = perm[off:off + n]
         off += n
-    w = W.Workload("custom", "small", len(lens), hq, hkv, d, 16, nb, window, dtype,
+    w = W.Workload("custom", "small", len(lens), hq, hkv, d, bs, nb, window, dtype,
                    1.0 / np.sqrt(d), lens, tables, np.where(lens > 0, lens - 1, -1).astype(np.int64),
                    data_seed=seed + 77)
     if dtype == "fp8":
@@ -71,28 +75,34 @@ def _custom(lens, hq=8, hkv=2, d=128, window=0, dtype="bf16", extra_blocks=7, se
     return w
 
 
+@pytest.mark.parametrize("bs", [16, 32])
 @pytest.mark.parametrize("hq,hkv,d", [(8, 8, 128), (4, 2, 128), (16, 4, 128), (16, 2, 128),
                                       (2, 1, 64), (8, 1, 64), (7, 7, 64), (24, 3, 128)])
-def test_head_grouping_and_head_dim(hq, hkv, d):
-    lens = [1, 15, 16, 17, 31, 32, 33, 200, 513]
-    run_parity(_custom(lens, hq, hkv, d, seed=hq + hkv + d))
+def test_head_grouping_and_head_dim(hq, hkv, d, bs):
+    lens = [1, 15, 16, 17, 31, 32, 33, 47, 48, 49, 200, 513]
+    run_parity(_custom(lens, hq, hkv, d, seed=hq + hkv + d, bs=bs))
 
 
-@pytest.mark.parametrize("window", [1, 15, 16, 17, 100, 512, 10_000])
-def test_sliding_window_edges(window):
-    lens = [1, 16, 17, 100, 101, 600, 1111]
-    w = _custom(lens, 16, 4, 128, window=window, seed=window)
+@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("window", [1, 15, 16, 17, 31, 33, 100, 512, 10_000])
+def test_sliding_window_edges(window, dtype, bs):
+    lens = [1, 16, 17, 32, 33, 100, 101, 600, 1111]
+    w = _custom(lens, 16, 4, 128, window=window, dtype=dtype, seed=window, bs=bs)
     # blocks wholly before the window are unmapped: the kernel must not read them
     for b, c in enumerate(w.context_lens):
         lo = max(0, int(c) - window)
-        w.block_tables[b, : lo // 16] = -1
+        w.block_tables[b, : lo // bs] = -1
     run_parity(w, part_blocks=4)
 
 
-def test_fp8_head_groups_and_partitions():
-    lens = [1, 5, 16, 47, 300, 2000]
+@pytest.mark.parametrize("bs", [16, 32])
+def test_fp8_head_groups_and_partitions(bs):
+    # 16-token blocks: FP8 units hold two blocks, so odd block counts leave a
+    # unit with one block; 32-token blocks: one block, two sub-tiles
+    lens = [1, 5, 16, 17, 31, 32, 33, 47, 300, 2000]
     for hq, hkv in [(8, 8), (16, 2), (32, 8)]:
-        run_parity(_custom(lens, hq, hkv, 128, dtype="fp8", seed=hq), part_blocks=8)
+        run_parity(_custom(lens, hq, hkv, 128, dtype="fp8", seed=hq, bs=bs), part_blocks=8)
 
 
 def test_empty_and_single_token_contexts():
@@ -151,12 +161,13 @@ def test_non_default_stream():
 
 # ----------------------------------------------------------------- KV write --
 
+@pytest.mark.parametrize("bs", [16, 32])
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("fp8", 128)])
-def test_write_bit_exact_with_padding_and_repeats(dtype, d):
+def test_write_bit_exact_with_padding_and_repeats(dtype, d, bs):
     torch.manual_seed(0)
     nb, hkv, T = 40, 4, 300
-    pool = pagedkv.KVPool(nb, 16, hkv, d, dtype)
-    opool = oracle.Pool(nb, 16, hkv, d, dtype)
+    pool = pagedkv.KVPool(nb, bs, hkv, d, dtype)
+    opool = oracle.Pool(nb, bs, hkv, d, dtype)
     if dtype == "fp8":
         ks = torch.tensor([0.01, 0.02, 0.003, 1.0])
         vs = torch.tensor([0.05, 0.001, 0.02, 0.5])
@@ -166,7 +177,7 @@ def test_write_bit_exact_with_padding_and_repeats(dtype, d):
     k = (torch.randn(T, hkv, d) * 4).bfloat16()
     v = torch.randn(T, hkv, d).bfloat16()
     k[0, 0, :4] = torch.tensor([1e6, -1e6, 1e-9, -0.0])    # saturation, underflow, signed zero
-    slots = torch.from_numpy(np.random.default_rng(1).permutation(nb * 16)[:T].astype(np.int64))
+    slots = torch.from_numpy(np.random.default_rng(1).permutation(nb * bs)[:T].astype(np.int64))
     slots[::7] = -1
     pagedkv.paged_kv_write(pool, k.cuda(), v.cuda(), slots.cuda())
     opool.write(k, v, slots.numpy())
@@ -175,8 +186,8 @@ def test_write_bit_exact_with_padding_and_repeats(dtype, d):
     s = slots.numpy()
     compare_pools(pool, opool, s[s >= 0])
     # a padded token's slot stays untouched (zero)
-    skipped = np.setdiff1d(np.arange(nb * 16), s[s >= 0])
-    vv = pool.view()[torch.from_numpy(skipped // 16).cuda(), :, :, torch.from_numpy(skipped % 16).cuda()]
+    skipped = np.setdiff1d(np.arange(nb * bs), s[s >= 0])
+    vv = pool.rows()[torch.from_numpy(skipped // bs).cuda(), :, :, torch.from_numpy(skipped % bs).cuda()]
     raw = vv.view(torch.int16) if dtype == "bf16" else vv
     assert int((raw != 0).sum()) == 0
 
