@@ -38,12 +38,14 @@ DESCRIPTIONS = {
     "tiny": "tiny paged decode: 4 seqs ctx {5,16,33,70}, 2 q / 1 KV heads, head_dim 64, "
             "64-block permuted pool, 4-token write",
     "8b": "Llama-3-8B-shaped layer decode: batch 64, 32 q / 8 KV heads, head_dim 128, "
-          "16-token blocks, ctx U[128,4096], pool 1.2x needed with shuffled ids, "
+          "ctx U[128,4096], pool 1.2x needed with shuffled ids, "
           "1-token KV write per seq before attention",
     "70b": "Llama-3-70B-shaped layer decode: batch 128, 64 q / 8 KV heads, head_dim 128, "
            "ctx log-uniform [256,8192], 64-block shared prefix (ref_cnt 128)",
     "sw": "sliding-window layer decode: batch 32, 32 q / 8 KV heads, head_dim 128, "
           "window 4096, ctx U[4096,32768], only window blocks mapped",
+    "long": "Llama-3-8B-shaped long-context decode: batch 16, 32 q / 8 KV heads, head_dim 128, "
+            "ctx U[32768,65536], pool 1.2x needed with shuffled ids",
     "fp8": "FP8-E4M3 KV decode: batch 256, 32 q / 8 KV heads, head_dim 128, ctx U[1,16384], "
            "per-KV-head scales, block tables from the host block manager after 10k seeded "
            "alloc/free steps at 95% occupancy",
@@ -55,7 +57,9 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="8b", choices=["tiny", "8b", "70b", "sw", "fp8"])
+    ap.add_argument("--config", default="8b", choices=["tiny", "8b", "70b", "sw", "fp8", "long"])
+    ap.add_argument("--block-size", type=int, default=16, choices=[16, 32],
+                    help="tokens per pool block")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--part-blocks", type=int, default=0, help="split-K partition size (0 = auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -403,7 +407,7 @@ def run_reference(args) -> None:
         return
     import oracle
     from paged_kv_cache_33_gb300 import workloads as W
-    w = W.make(args.config, "full", make_allocator=oracle.Allocator)
+    w = W.make(args.config, "full", make_allocator=oracle.Allocator, block_size=args.block_size)
     per_step_budget = min(6.0, 150.0 / max(1, args.steps + args.warmup))
     sampler = OracleSampler(w)
     for _ in range(args.warmup):
@@ -419,7 +423,8 @@ def run_reference(args) -> None:
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": DESCRIPTIONS[args.config], "name": args.config,
+            "config": {"workload": f"{DESCRIPTIONS[args.config]}, {w.block_size}-token blocks",
+                       "name": args.config,
                        "batch": w.batch, "parallelism": "none (host oracle)"},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": f"each step: sequences of the {args.config} workload in "
@@ -448,7 +453,8 @@ def main(argv=None) -> None:
     device = torch.device("cuda", dist_ctx.local_rank)
     pagedkv.load()
     # the fp8 workload's tables come from the library's own block manager
-    w = W.make(args.config, "full", make_allocator=pagedkv.BlockManager)
+    w = W.make(args.config, "full", make_allocator=pagedkv.BlockManager,
+               block_size=args.block_size)
     step = Step(w, device, args.part_blocks)
     sampler = ClockSampler(dist_ctx.local_rank)
     dev = timed_device(step, args.steps, args.warmup, dist_ctx, sampler)
@@ -474,7 +480,8 @@ def main(argv=None) -> None:
         "n_gpus": dist_ctx.world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": DESCRIPTIONS[args.config], "name": args.config,
+        "config": {"workload": f"{DESCRIPTIONS[args.config]}, {w.block_size}-token blocks",
+                   "name": args.config,
                    "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
                    "head_dim": w.head_dim, "block_size": w.block_size,
                    "num_blocks": w.num_blocks, "window": w.window,

@@ -54,10 +54,10 @@ bool encode_pool_map(kv_pool* p) {
                         static_cast<cuuint64_t>(p->num_blocks) * p->n_kv_heads};
   cuuint64_t strides[3] = {p->head_dim * esz, p->block_size * p->head_dim * esz,
                            2 * p->block_size * p->head_dim * esz};
-  // bf16: 64 columns of the K rows and the V rows per box; FP8: the K rows
-  // (the transposed V tile is fetched by a plain bulk copy)
+  // one box: 128 bytes of every K row and every V row of one (block, head)
+  // (FP8: the transposed V tile is read as block_size rows of 128 bytes)
   cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(p->block_size),
-                       p->dtype == KV_BF16 ? 2u : 1u, 1};
+                       2, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = encode(&p->tmap,
                       p->dtype == KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -320,7 +320,6 @@ kv_status decode_call(kv_pool* p, const StepWrite* w, const void* q, int32_t n_q
   d.ticket = reinterpret_cast<int32_t*>(ws + plan.part_o_bytes + plan.part_ml_bytes +
                                         plan.meta_bytes - 16);
   d.err = p->err;
-  d.pool = static_cast<const uint8_t*>(p->base);
   d.k_scale = p->scales;
   d.v_scale = p->scales + p->n_kv_heads;
   d.num_blocks = p->num_blocks;

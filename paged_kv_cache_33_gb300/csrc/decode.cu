@@ -99,19 +99,19 @@ __device__ __forceinline__ bool ctx_ok(const DecodeParams& p, int32_t ctx) {
   return ctx >= 0 && ctx <= p.max_ctx && static_cast<int64_t>(ctx) <= static_cast<int64_t>(p.mbs) * BS;
 }
 
-// Shared-memory image of one unit: BPU blocks of BS tokens, each as
-// bf16: D/64 boxes of [K rows | V rows] x 64 columns (128-byte swizzled rows);
-// FP8: one box of K rows (128 codes, swizzled), then the transposed V tile
-//      as BS/16 sub-tiles of [D][16] codes, fetched by a plain bulk copy.
+// Shared-memory image of one unit: BPU blocks of BS tokens, each as TMA
+// boxes of 128-byte rows with the 128-byte swizzle:
+// bf16: D/64 boxes of [K rows | V rows] x 64 columns;
+// FP8: one box of [K rows (128 codes) | the transposed V tile seen as BS
+//      rows of 128 bytes: BS/16 sub-tiles of [D][16] codes].
 // The compute side walks the unit in sub-tiles of 16 tokens.
 template <int D, bool FP8, int BS, int BPU>
 struct Geometry {
   static constexpr int kElem = FP8 ? 1 : 2;
   static constexpr int kRowBytes = 128;                         // one swizzled smem row
   static constexpr int kBoxes = FP8 ? 1 : D / 64;               // TMA boxes per block
-  static constexpr int kBoxBytes = (FP8 ? 1 : 2) * BS * kRowBytes;
-  static constexpr int kVtBytes = FP8 ? D * BS : 0;             // transposed V tile
-  static constexpr int kBlockBytes = kBoxes * kBoxBytes + kVtBytes;
+  static constexpr int kBoxBytes = 2 * BS * kRowBytes;
+  static constexpr int kBlockBytes = kBoxes * kBoxBytes;
   static constexpr int kStageBytes = BPU * kBlockBytes;
   static constexpr int kSubPerBlock = BS / 16;
   static constexpr int kSub = BPU * kSubPerBlock;               // 16-token sub-tiles per unit
@@ -120,12 +120,14 @@ struct Geometry {
   static_assert(!FP8 || D == 128, "FP8 rows are one 128-byte swizzle row");
   static_assert(kBoxBytes % 1024 == 0, "boxes keep the 1024-byte swizzle alignment");
   // byte offsets inside a stage of sub-tile `sub`: K row 0 of box 0, and
-  // (bf16) V row 0 of box 0 or (FP8) the [D][16] transposed V sub-tile
+  // (bf16) V row 0 of box 0 or (FP8) the first row of the transposed V
+  // sub-tile; all are multiples of 8 rows, so a row's swizzle phase is its
+  // row index from there, mod 8
   __device__ static constexpr int k_off(int sub) {
     return (sub / kSubPerBlock) * kBlockBytes + (sub % kSubPerBlock) * 16 * kRowBytes;
   }
   __device__ static constexpr int v_off(int sub) {
-    return FP8 ? (sub / kSubPerBlock) * kBlockBytes + kBoxBytes + (sub % kSubPerBlock) * 16 * D
+    return FP8 ? (sub / kSubPerBlock) * kBlockBytes + BS * kRowBytes + (sub % kSubPerBlock) * 16 * D
                : k_off(sub) + BS * kRowBytes;
   }
 };
@@ -366,9 +368,6 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
 #pragma unroll
       for (int bx = 0; bx < G::kBoxes; ++bx)
         tma_load_4d(bdst + bx * G::kBoxBytes, &tmap, bar, bx * 64, 0, 0, tile);
-      if constexpr (FP8)
-        bulk_load(bdst + G::kBoxBytes, p.pool + (static_cast<int64_t>(tile) * 2 + 1) * G::kVtBytes,
-                  G::kVtBytes, bar);
     }
     // step to the next unit: within the segment, or the next chunk
     if (++iu < iu_end) {
@@ -538,11 +537,15 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
             ldsm_x4_trans(addr, vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
           }
         } else {
-          // transposed V: row d holds the 16 codes of dimension d; ldmatrix i
-          // takes dims 32i..32i+31, i.e. rows g and g+8 of m-tiles 2i and 2i+1
+          // transposed V: dimension d's 16 codes are chunk d % 8 of smem row
+          // d / 8 (swizzled); ldmatrix i takes dims 32i..32i+31, i.e. rows g
+          // and g+8 of m-tiles 2i and 2i+1
 #pragma unroll
-          for (int i = 0; i < D / 32; ++i)
-            ldsm_x4(sv + (32 * i + lane) * 16, vf[i][0], vf[i][1], vf[i][2], vf[i][3]);
+          for (int i = 0; i < D / 32; ++i) {
+            const int row = 4 * i + (lane >> 3);
+            ldsm_x4(sv + row * G::kRowBytes + (((lane & 7) ^ (row & 7)) << 4), vf[i][0], vf[i][1],
+                    vf[i][2], vf[i][3]);
+          }
         }
       }
       // after the unit's last reads from the stage, refill it at once so the
@@ -849,7 +852,10 @@ struct Variant {
 // 16-token blocks: bf16 stages one block per unit; FP8 stages two, so a unit
 // carries 32 tokens (8 KB) and the per-unit work is spread over twice the
 // bytes.  32-token blocks: one block per unit (two 16-token sub-tiles).
-using Bf16D128 = Variant<128, false, 16, 1, PKV_BF16_WARPS, PKV_BF16_STAGES>;
+#ifndef PKV_BF16_BPU
+#define PKV_BF16_BPU 1
+#endif
+using Bf16D128 = Variant<128, false, 16, PKV_BF16_BPU, PKV_BF16_WARPS, PKV_BF16_STAGES>;
 using Bf16D64 = Variant<64, false, 16, 1, 4, 4>;
 using Fp8D128 = Variant<128, true, 16, PKV_FP8_BPU, PKV_FP8_WARPS, PKV_FP8_STAGES>;
 using Bf16D128B32 = Variant<128, false, 32, 1, PKV_BS32_WARPS, 2>;

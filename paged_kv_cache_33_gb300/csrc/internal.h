@@ -39,7 +39,6 @@ constexpr int kMaxDecodeBatch = 512;
 // the reduce kernel.
 struct DecodeParams {
   const void* q;                // bf16 [B][Hq][D]
-  const uint8_t* pool;          // pool base (FP8: the transposed V tiles are bulk-copied)
   const int32_t* block_tables;  // [B][mbs]
   const int32_t* context_lens;  // [B]
   float* out;                   // [B][Hq][D]
