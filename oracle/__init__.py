@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         "oracle_pool_copy_blocks": (c.c_int, [P, P, c.c_int64]),
         "oracle_paged_decode": (c.c_int, [P, P, c.c_int32, P, c.c_int32, P, c.c_int32,
                                           c.c_double, c.c_int32, P, c.c_int32, P]),
+        "oracle_paged_prefill": (c.c_int, [P, P, c.c_int32, P, P, c.c_int32, P, c.c_int32,
+                                           c.c_double, c.c_int32, P]),
         "oracle_sha256": (None, [P, c.c_uint64, P]),
         "oracle_alloc_create": (P, [c.c_int32, c.c_int32]),
         "oracle_alloc_destroy": (None, [P]),
@@ -207,6 +209,23 @@ class Pool:
                                        0 if sel is None else sel.shape[0], _ptr(out))
         if rc != OK:
             raise ValueError(f"oracle_paged_decode: {rc}")
+        return out
+
+    def prefill(self, q, cu_q_lens, block_tables, context_lens, scale: float,
+                window: int = 0) -> np.ndarray:
+        """fp64 paged prefill attention; q [T, Hq, D] bf16 -> float32 [T, Hq, D]."""
+        q = _u16(q)
+        T, Hq, D = q.shape
+        cu = np.ascontiguousarray(cu_q_lens, dtype=np.int32)
+        tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+        lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+        B = lens.shape[0]
+        assert cu.shape == (B + 1,) and cu[-1] == T and tables.shape[0] == B and D == self.head_dim
+        out = np.zeros((T, Hq, D), dtype=np.float32)
+        rc = lib().oracle_paged_prefill(self._h, _ptr(q), Hq, _ptr(cu), _ptr(tables), tables.shape[1],
+                                        _ptr(lens), B, float(scale), int(window), _ptr(out))
+        if rc != OK:
+            raise ValueError(f"oracle_paged_prefill: {rc}")
         return out
 
 

@@ -292,3 +292,67 @@ extern "C" int oracle_paged_decode(const oracle_pool* p, const uint16_t* q, int3
   }
   return 0;
 }
+
+// -------------------------------------------------------- paged prefill --
+// "Optimizing KV Cache Memory Management in vLLM with PagedAttention and
+// Dynamic Block Allocation", "The Prefill Phase": the prompt's key/value
+// states are computed in one parallel step and written into the physical
+// blocks; with prefix caching ("PagedAttention", "Walking through two
+// requests") only the uncached tail of the prompt is computed.  Each new
+// query token attends, causally, to every cached or new position up to its
+// own: token i of the q_len new tokens of sequence b sits at position
+// pos = ctx - q_len + i and attends to [lo, pos], lo = max(0, pos + 1 - W)
+// under a window W > 0, else 0 -- the decode rule applied with a context of
+// pos + 1.  fp64 throughout; outputs rounded to float.
+
+extern "C" int oracle_paged_prefill(const oracle_pool* p, const uint16_t* q, int32_t n_q_heads,
+                                    const int32_t* cu_q_lens, const int32_t* block_tables,
+                                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                    int32_t batch, double scale, int32_t window, float* out) {
+  if (n_q_heads <= 0 || n_q_heads % p->hkv != 0) return 1;
+  const int g = n_q_heads / p->hkv;
+  const int D = p->d;
+  std::vector<double> qd(D), kd(D), vd(D), o(D);
+  for (int b = 0; b < batch; ++b) {
+    const int64_t q0 = cu_q_lens[b], qn = cu_q_lens[b + 1] - cu_q_lens[b];
+    const int64_t ctx = context_lens[b];
+    if (qn < 0 || qn > ctx || ctx > static_cast<int64_t>(max_blocks_per_seq) * p->bs) return 1;
+    const int32_t* table = block_tables + static_cast<int64_t>(b) * max_blocks_per_seq;
+    for (int64_t i = 0; i < qn; ++i) {
+      const int64_t pos = ctx - qn + i;
+      const int64_t lo = window > 0 ? std::max<int64_t>(0, pos + 1 - window) : 0;
+      for (int hq = 0; hq < n_q_heads; ++hq) {
+        const int h = hq / g;
+        const uint16_t* qrow = q + ((q0 + i) * n_q_heads + hq) * D;
+        for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_to_double(qrow[d]);
+        // scores over [lo, pos], then softmax with the maximum subtracted
+        std::vector<double> s(pos - lo + 1);
+        for (int64_t t = lo; t <= pos; ++t) {
+          const int64_t blk = table[t / p->bs];
+          if (blk < 0 || blk >= p->nb) return 5;
+          const int off = static_cast<int>(t % p->bs);
+          double acc = 0.0;
+          for (int d = 0; d < D; ++d) acc += qd[d] * pool_value(p, blk, 0, off, h, d);
+          s[t - lo] = scale * acc;
+        }
+        double m = -INFINITY;
+        for (double x : s) m = std::max(m, x);
+        double l = 0.0;
+        for (double& x : s) {
+          x = std::exp(x - m);
+          l += x;
+        }
+        std::fill(o.begin(), o.end(), 0.0);
+        for (int64_t t = lo; t <= pos; ++t) {
+          const int64_t blk = table[t / p->bs];
+          const int off = static_cast<int>(t % p->bs);
+          const double wt = s[t - lo] / l;
+          for (int d = 0; d < D; ++d) o[d] += wt * pool_value(p, blk, 1, off, h, d);
+        }
+        float* orow = out + ((q0 + i) * n_q_heads + hq) * D;
+        for (int d = 0; d < D; ++d) orow[d] = static_cast<float>(o[d]);
+      }
+    }
+  }
+  return 0;
+}

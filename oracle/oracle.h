@@ -60,6 +60,16 @@ int oracle_paged_decode(const oracle_pool* p, const uint16_t* q, int32_t n_q_hea
                         double scale, int32_t window,
                         const int32_t* seqs, int32_t n_seqs, float* out);
 
+/* Paged prefill / extend attention: q is [T, Hq, D] bf16 bits with the new
+ * tokens of sequence b at rows cu_q_lens[b] .. cu_q_lens[b+1]-1 (the last
+ * positions of its context_lens[b] tokens, already written to the pool);
+ * each attends causally to positions [lo, pos] of its sequence.
+ * out: [T, Hq, D] float. */
+int oracle_paged_prefill(const oracle_pool* p, const uint16_t* q, int32_t n_q_heads,
+                         const int32_t* cu_q_lens, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* context_lens,
+                         int32_t batch, double scale, int32_t window, float* out);
+
 /* ---- SHA-256 (FIPS 180-4) ------------------------------------------------ */
 void oracle_sha256(const uint8_t* msg, uint64_t len, uint8_t digest[32]);
 
