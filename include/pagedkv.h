@@ -228,6 +228,38 @@ kv_status paged_decode_attention_noalloc(kv_pool* pool, const void* q_dev, int32
                                          int32_t sliding_window, float* out_dev, void* stream);
 
 /*
+ * paged_prefill_attention -- prefill / extend attention over the pool
+ * ("Optimizing KV Cache Memory Management in vLLM with PagedAttention and
+ * Dynamic Block Allocation", "The Prefill Phase": the prompt's states are
+ * computed in one parallel step; with prefix caching ("PagedAttention",
+ * "Walking through two requests") only the uncached tail is computed).
+ *   q_dev:             bf16 [T][n_q_heads][128]: the new tokens of all
+ *                      sequences, sequence b at rows cu_q_lens[b] ..
+ *                      cu_q_lens[b+1]-1; their K/V already written to the
+ *                      pool (paged_kv_write) at the last q_len positions.
+ *   cu_q_lens_dev:     int32 [batch + 1], cu_q_lens[0] = 0, non-decreasing.
+ *   block_tables_dev, max_blocks_per_seq, context_lens_dev: as for decode;
+ *                      context_lens counts the new tokens.
+ *   max_q_len:         host bound of cu_q_lens[b+1] - cu_q_lens[b] (sizes the grid).
+ *   max_context_len:   host bound of context_lens.
+ *   out_dev:           fp32 [T][n_q_heads][128]; token i of sequence b (at
+ *                      position pos = ctx - q_len + i) gets
+ *                      softmax(scale q K^T) V over positions [lo, pos], lo =
+ *                      max(0, pos + 1 - sliding_window) when the window is on.
+ * bf16 pools with head_dim 128 and a query group of at most 8 heads per KV
+ * head (KV_ERR_UNSUPPORTED otherwise).  Runs on the tcgen05 tensor cores
+ * (P rounded to bf16).  A sequence with q_len > context_len or a context
+ * above a bound sets KV_ERR_BAD_CONTEXT and is skipped.  Asynchronous on
+ * `stream`; no workspace.
+ */
+kv_status paged_prefill_attention(kv_pool* pool, const void* q_dev, int32_t n_q_heads,
+                                  const int32_t* cu_q_lens_dev, const int32_t* block_tables_dev,
+                                  int32_t max_blocks_per_seq, const int32_t* context_lens_dev,
+                                  int32_t batch, int32_t max_q_len, int32_t max_context_len,
+                                  float scale, int32_t sliding_window, float* out_dev,
+                                  void* stream);
+
+/*
  * kv_pool_set_partition_blocks -- split-K granularity: aim for about this
  * many blocks per warp (a multiple of 4, 4..1024) for the longest possible
  * call, using fewer warps than the full persistent grid when that needs

@@ -65,6 +65,14 @@ bool encode_pool_map(kv_pool* p) {
                       4, p->base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  if (p->dtype == KV_BF16) {
+    // the prefill gathers the K rows and the V rows of a block separately
+    cuuint32_t box_rows[4] = {64, static_cast<cuuint32_t>(p->block_size), 1, 1};
+    r = encode(&p->tmap_rows, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p->base, dims, strides, box_rows,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS;
 }
 
@@ -386,6 +394,55 @@ kv_status paged_decode_step(kv_pool* p, const void* k, const void* v,
   return decode_call(p, &w, q, n_q_heads, block_tables, max_blocks_per_seq, context_lens, batch,
                      max_context_len, scale, sliding_window, out, workspace, workspace_bytes,
                      stream);
+}
+
+kv_status paged_prefill_attention(kv_pool* p, const void* q, int32_t n_q_heads,
+                                  const int32_t* cu_q_lens, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                  int32_t batch, int32_t max_q_len, int32_t max_context_len,
+                                  float scale, int32_t sliding_window, float* out, void* stream) {
+  if (!p || batch < 0 || n_q_heads <= 0 || max_q_len < 0 || max_context_len < 0)
+    return KV_ERR_INVALID_ARG;
+  if (n_q_heads % p->n_kv_heads != 0) return KV_ERR_INVALID_ARG;
+  const int32_t g = n_q_heads / p->n_kv_heads;
+  if (g > 8 || p->dtype != KV_BF16 || p->head_dim != 128) return KV_ERR_UNSUPPORTED;
+  if (batch == 0 || max_q_len == 0) return KV_OK;
+  if (!q || !cu_q_lens || !block_tables || !context_lens || !out || !aligned16(q) || !aligned16(out))
+    return KV_ERR_INVALID_ARG;
+  if (max_blocks_per_seq <= 0 || max_q_len > max_context_len ||
+      static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * p->block_size)
+    return KV_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return KV_ERR_INVALID_ARG;
+  if (batch > 65535 || p->n_kv_heads > 65535) return KV_ERR_UNSUPPORTED;
+  int32_t gp = 1;
+  while (gp < g) gp <<= 1;
+  const int64_t tiles = (static_cast<int64_t>(max_q_len) * gp + 127) / 128;
+  if (tiles > (int64_t(1) << 31) - 1) return KV_ERR_UNSUPPORTED;
+  DeviceGuard guard(p->device);
+  pkv::PrefillParams d{};
+  d.q = q;
+  d.cu_q_lens = cu_q_lens;
+  d.block_tables = block_tables;
+  d.context_lens = context_lens;
+  d.out = out;
+  d.err = p->err;
+  d.num_blocks = p->num_blocks;
+  d.mbs = max_blocks_per_seq;
+  d.batch = batch;
+  d.n_q_heads = n_q_heads;
+  d.n_kv_heads = p->n_kv_heads;
+  d.group = g;
+  d.group_pow2 = gp;
+  d.max_ctx = max_context_len;
+  d.window = sliding_window > 0 ? sliding_window : 0;
+  d.scale_log2 = scale * 1.4426950408889634f;
+  d.wait_limit_ns = kWaitLimitNs;
+  const cudaError_t e = pkv::launch_prefill(p, d, max_q_len, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return KV_ERR_CUDA;
+  }
+  return KV_OK;
 }
 
 kv_status kv_pool_set_partition_blocks(kv_pool* p, int32_t blocks_per_partition) {

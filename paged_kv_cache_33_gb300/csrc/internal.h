@@ -18,6 +18,7 @@ struct kv_pool {
   float* scales = nullptr;     // device [2][Hkv]: K scales then V scales
   uint32_t* err = nullptr;     // device error word
   CUtensorMap tmap;            // pool viewed as [NB*Hkv][2][BS][D] for TMA
+  CUtensorMap tmap_rows;       // bf16 pools: the same view, boxes of one tile (K or V)
   int32_t partition_blocks = 0;  // 0 = automatic
   cudaEvent_t ev_start = nullptr, ev_stop = nullptr;  // optional timing hook
 };
@@ -94,6 +95,26 @@ int64_t block_bytes(const kv_pool* pool);
 // applying them in order.
 cudaError_t launch_copy_blocks(const kv_pool* pool, const int32_t* pairs, int64_t n,
                                cudaStream_t stream);
+
+// Arguments of the paged prefill (extend) attention.
+struct PrefillParams {
+  const void* q;                // bf16 [T][Hq][D], the new tokens of every sequence
+  const int32_t* cu_q_lens;     // [B + 1]
+  const int32_t* block_tables;  // [B][mbs]
+  const int32_t* context_lens;  // [B]
+  float* out;                   // [T][Hq][D]
+  uint32_t* err;
+  int64_t num_blocks;
+  int32_t mbs, batch, n_q_heads, n_kv_heads, group, group_pow2;
+  int32_t max_ctx, window;
+  float scale_log2;
+  uint64_t wait_limit_ns;
+};
+
+// Dynamic shared memory of the prefill kernel, and its launch.
+int prefill_smem_bytes();
+cudaError_t launch_prefill(const kv_pool* pool, const PrefillParams& p, int32_t max_q_len,
+                           cudaStream_t stream);
 
 // The merge of cut pairs, launched as a programmatic dependent of the decode.
 cudaError_t launch_reduce(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream);

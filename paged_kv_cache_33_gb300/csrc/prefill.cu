@@ -1,0 +1,379 @@
+// Paged prefill / extend attention on the 5th-generation tensor cores.
+//
+// What it computes ("Optimizing KV Cache Memory Management in vLLM with
+// PagedAttention and Dynamic Block Allocation", "The Prefill Phase"; prefix
+// caching from "PagedAttention", "Walking through two requests"): the q_len
+// new tokens of sequence b are the last positions of its context_lens[b]
+// tokens, their K/V already in the pool; token i at position
+// pos = ctx - q_len + i attends causally to [lo, pos] of the sequence, with
+// lo = max(0, pos + 1 - W) under a window W, else 0, resolving every key
+// through the block table.  GQA: query head hq reads KV head hq / g.
+//
+// How (GB300 design), one CTA per (128-row query tile, KV head, sequence):
+//  * Rows of the tile are (new token, query head of the group) pairs, the
+//    group padded to a power of two Gp: 128 / Gp tokens x Gp heads.  Q is
+//    staged once in shared memory (128-byte swizzled, K-major).
+//  * Keys run in tiles of 64 tokens (4 or 2 pool blocks).  A producer warp
+//    gathers each tile's K and V rows with one TMA box per block and column
+//    half into a 3-stage ring; blocks outside the attended range or with a
+//    bad id are left out and their rows masked.
+//  * One thread issues tcgen05.mma: S = Q K^T (128 x 64, fp32 in tensor
+//    memory, double-buffered so S of the next tile runs while the softmax of
+//    this one does), then O += P V (128 x 128, fp32 in tensor memory), with
+//    V read MN-major straight from its pool rows.
+//  * Four softmax warps own one row each per thread: tcgen05.ld the row of
+//    S, mask (causal, window, sequence end, missing blocks), online softmax
+//    in the exp2 domain with a lazy maximum (O in tensor memory is rescaled
+//    only when a row's maximum grows by more than 2^8), P to shared memory
+//    in bf16, and zeros into the V rows the product must not see (slots past
+//    the sequence's end, blocks not loaded).  The epilogue divides O by the
+//    row sum and stores the valid rows.
+//  * Every wait is bounded in wall time; on a timeout the CTA records
+//    KV_ERR_TIMEOUT, drains what it issued and frees its tensor memory.
+
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kRows = 128;           // query rows per tile (M)
+constexpr int kKv = 64;              // keys per tile (N of S, K of P V)
+constexpr int kStages = 3;           // K/V ring
+constexpr int kThreads = 192;        // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr float kLazy = 8.f;         // rescale O when a row maximum grows by more than this (log2)
+constexpr uint64_t kShortWaitNs = 200000;
+
+// Shared memory (offsets from a 1024-aligned base).
+constexpr int kQ = 0;                                 // 2 halves x [128][64] bf16
+constexpr int kK = kQ + 2 * kRows * 128;              // stages x 2 halves x [64][64]
+constexpr int kV = kK + kStages * 2 * kKv * 128;
+constexpr int kP = kV + kStages * 2 * kKv * 128;      // [128][64] bf16
+constexpr int kBars = kP + kRows * 128;
+// barriers: kv_full[3], kv_empty[3], s_full[2], q_full, p_full, o_done, mma_done
+constexpr int kNumBars = 2 * kStages + 2 + 4;
+constexpr int kTileMask = kBars + kNumBars * 8;       // uint32 [kStages]
+constexpr int kTmemSlot = kTileMask + kStages * 4;
+constexpr int kSmemBytes = kTmemSlot + 16 + 1024;     // + alignment slack
+constexpr uint32_t kTmemCols = 256;                   // S0 [0,64) S1 [64,128) O [128,256)
+
+__device__ __forceinline__ int swz128(int row, int chunk) {
+  return row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+template <int BS>
+__global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
+    const __grid_constant__ CUtensorMap tmap, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int Gp = p.group_pow2, g = p.group;
+  const int tok_per_tile = kRows / Gp;
+
+  // ---- this tile's queries and the keys they need (uniform over the CTA)
+  const int32_t q0 = p.cu_q_lens[b];
+  int32_t qn = p.cu_q_lens[b + 1] - q0;
+  const int32_t ctx = p.context_lens[b];
+  if (qn < 0 || qn > ctx || ctx > p.max_ctx || static_cast<int64_t>(ctx) > static_cast<int64_t>(p.mbs) * BS) {
+    if (qn != 0 && blockIdx.x == 0 && h == 0 && tid == 0) atomicOr(p.err, kErrBadContext);
+    return;
+  }
+  const int tok0 = blockIdx.x * tok_per_tile;
+  if (tok0 >= qn) return;
+  const int ntok = min(tok_per_tile, qn - tok0);
+  const int pos_first = ctx - qn + tok0, pos_last = pos_first + ntok - 1;
+  const int kv_begin = p.window > 0 ? max(0, pos_first + 1 - p.window) : 0;
+  const int kv_end = pos_last + 1;
+  const int jt0 = kv_begin / kKv;
+  const int n_tiles = (kv_end - 1) / kKv - jt0 + 1;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBars);
+  const uint32_t bar0 = smem_addr(bars);
+  auto kv_full = [&](int s) { return bar0 + 8u * s; };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto s_full = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
+  const uint32_t q_full = bar0 + 8u * (2 * kStages + 2);
+  const uint32_t p_full = q_full + 8, o_done = q_full + 16, mma_done = q_full + 24;
+  uint32_t* tile_mask = reinterpret_cast<uint32_t*>(smem + kTileMask);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+    }
+    mbar_init(s_full(0), 1);
+    mbar_init(s_full(1), 1);
+    mbar_init(q_full, kRows);
+    mbar_init(p_full, kRows);
+    mbar_init(o_done, 1);
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    return mbar_wait_bounded(bar, parity, p.wait_limit_ns, p.err, kErrTimeout, kShortWaitNs);
+  };
+
+  if (warp < 4) {
+    // =========================== softmax warps: one query row per thread
+    const int r = tid;
+    const int tq = r / Gp, jh = r - tq * Gp;
+    const bool row_ok = tq < ntok && jh < g;
+    const int pos = pos_first + tq;
+    const int lo = p.window > 0 ? max(0, pos + 1 - p.window) : 0;
+    const int hq = h * g + jh;
+    // Q row r -> shared memory (zeros for padding rows)
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const __nv_bfloat16*>(p.q) +
+          (static_cast<int64_t>(q0 + tok0 + tq) * p.n_q_heads + hq) * kD);
+#pragma unroll
+      for (int c = 0; c < kD / 8; ++c) {
+        const uint4 v = row_ok ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(smem + kQ + (c >> 3) * (kRows * 128) + swz128(r, c & 7)) = v;
+      }
+      fence_proxy_async_smem();
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(q_full) : "memory");
+    }
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int jt = 0; jt < n_tiles && ok; ++jt) {
+      const int s = jt % kStages, sb = jt & 1;
+      ok = wait(s_full(sb), (jt >> 1) & 1) && wait(kv_full(s), (jt / kStages) & 1);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t mask = tile_mask[s];
+      const int key0 = (jt0 + jt) * kKv;
+      float x[kKv];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t raw[32];
+        tmem_ld32(lane_base + sb * kKv + half * 32, raw);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = half * 32 + i;
+          const int t = key0 + c;
+          const bool valid = row_ok && t >= lo && t <= pos && ((mask >> (c / BS)) & 1u);
+          x[c] = valid ? __uint_as_float(raw[i]) * p.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, x[c]);
+        }
+      }
+      // O and the P buffer are free once the previous tile's product is done
+      if (jt > 0) {
+        ok = wait(o_done, (jt - 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+      }
+      const float m_new = fmaxf(m_run, mt);
+      // a row with nothing accumulated yet (O's row is zero) takes the new
+      // maximum; others keep theirs unless it grew by more than 2^kLazy
+      const bool rescale = m_run != -INFINITY && m_new > m_run + kLazy;
+      if (__any_sync(0xffffffffu, rescale)) {  // tensor-memory access is warp-wide
+        const float alpha = rescale ? fast_exp2(m_run - m_new) : 1.f;
+        l_run *= alpha;
+#pragma unroll
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + 2 * kKv + c0, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(lane_base + 2 * kKv + c0, o);
+        }
+      }
+      if (m_run == -INFINITY || rescale) m_run = m_new;
+      // P row (bf16, 128-byte swizzled) and its sum
+      const float mu = m_run == -INFINITY ? 0.f : m_run;
+#pragma unroll
+      for (int cc = 0; cc < kKv / 8; ++cc) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = fast_exp2(x[8 * cc + 2 * e] - mu);
+          const float b2 = fast_exp2(x[8 * cc + 2 * e + 1] - mu);
+          l_run += a + b2;
+          w[e] = pack_bf16x2(a, b2);
+        }
+        *reinterpret_cast<uint4*>(smem + kP + swz128(r, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      // V rows the product must not see: slots past the sequence's end and
+      // blocks that were not loaded (stale or never-written shared memory)
+      if (mask != (1u << (kKv / BS)) - 1u || key0 + kKv > ctx) {
+        for (int idx = tid; idx < kKv * 2 * 8; idx += kRows) {
+          const int key = idx >> 4, half = (idx >> 3) & 1, chunk = idx & 7;
+          if (key0 + key >= ctx || !((mask >> (key / BS)) & 1u))
+            *reinterpret_cast<uint4*>(smem + kV + s * (2 * kKv * 128) + half * (kKv * 128) +
+                                      key * 128 + chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(p_full) : "memory");
+    }
+    if (ok) ok = __all_sync(0xffffffffu, wait(o_done, (n_tiles - 1) & 1));
+    if (ok) {
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      float* dst = p.out + (static_cast<int64_t>(q0 + tok0 + tq) * p.n_q_heads + hq) * kD;
+#pragma unroll
+      for (int c0 = 0; c0 < kD; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + 2 * kKv + c0, o);
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + c0 + i) =
+                make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
+                            __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+        }
+      }
+    }
+  } else if (warp == 4) {
+    // =========================== producer: K and V rows of each key tile
+    if (lane == 0) {
+      int issued = 0;
+      for (int jt = 0; jt < n_tiles; ++jt) {
+        const int s = jt % kStages;
+        if (jt >= kStages && !wait(kv_empty(s), ((jt / kStages) - 1) & 1)) break;
+        const int key0 = (jt0 + jt) * kKv;
+        uint32_t mask = 0;
+        int phys[kKv / BS];
+#pragma unroll
+        for (int i = 0; i < kKv / BS; ++i) {
+          const int t0 = key0 + i * BS;
+          phys[i] = -1;
+          if (t0 + BS <= kv_begin || t0 >= kv_end) continue;
+          const int e = p.block_tables[static_cast<int64_t>(b) * p.mbs + t0 / BS];
+          if (e < 0 || e >= p.num_blocks) {
+            atomicOr(p.err, kErrBadBlock);
+            continue;
+          }
+          phys[i] = e;
+          mask |= 1u << i;
+        }
+        tile_mask[s] = mask;
+        const uint32_t bar = kv_full(s);
+        const int nblk = __popc(mask);
+        if (nblk == 0) {
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+        } else {
+          mbar_arrive_expect_tx(bar, nblk * 2 * 2 * BS * 128);
+          const uint32_t ks = smem_addr(smem + kK + s * (2 * kKv * 128));
+          const uint32_t vs = smem_addr(smem + kV + s * (2 * kKv * 128));
+#pragma unroll
+          for (int i = 0; i < kKv / BS; ++i) {
+            if (phys[i] < 0) continue;
+            const int tile = phys[i] * p.n_kv_heads + h;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const uint32_t off = half * (kKv * 128) + i * BS * 128;
+              tma_load_4d(ks + off, &tmap, bar, half * 64, 0, 0, tile);
+              tma_load_4d(vs + off, &tmap, bar, half * 64, 0, 1, tile);
+            }
+          }
+        }
+        ++issued;
+      }
+      // leave no copy in flight: wait (bounded) for the stages not yet consumed
+      for (int jt = max(0, issued - kStages); jt < issued; ++jt)
+        wait(kv_full(jt % kStages), (jt / kStages) & 1);
+    }
+    __syncwarp();
+  } else {
+    // =========================== MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = umma_idesc_bf16(kRows, kKv, false);
+      constexpr uint32_t idO = umma_idesc_bf16(kRows, kD, true);
+      const uint32_t qs = smem_addr(smem + kQ), ps = smem_addr(smem + kP);
+      bool ok = wait(q_full, 0);
+      if (ok) tc_fence_after();
+      auto issue_s = [&](int jt) {
+        const int s = jt % kStages;
+        const uint32_t ks = smem_addr(smem + kK + s * (2 * kKv * 128));
+#pragma unroll
+        for (int k = 0; k < kD / 16; ++k) {
+          const uint64_t a = umma_desc_sw128(qs + (k >> 2) * (kRows * 128) + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = umma_desc_sw128(ks + (k >> 2) * (kKv * 128) + (k & 3) * 32, 16, 1024);
+          umma_bf16(tmem + (jt & 1) * kKv, a, bd, idS, k > 0);
+        }
+        umma_commit(s_full(jt & 1));
+      };
+      auto issue_pv = [&](int jt) {
+        const int s = jt % kStages;
+        const uint32_t vs = smem_addr(smem + kV + s * (2 * kKv * 128));
+#pragma unroll
+        for (int k = 0; k < kKv / 16; ++k) {
+          const uint64_t a = umma_desc_sw128(ps + k * 32, 16, 1024);
+          const uint64_t bd = umma_desc_sw128(vs + k * 16 * 128, kKv * 128, 1024);
+          umma_bf16(tmem + 2 * kKv, a, bd, idO, (jt > 0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit(o_done);
+        umma_commit(kv_empty(s));
+      };
+      for (int jt = 0; ok && jt < n_tiles; ++jt) {
+        ok = wait(kv_full(jt % kStages), (jt / kStages) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(jt);
+        if (jt > 0) {
+          ok = wait(p_full, (jt - 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(jt - 1);
+        }
+      }
+      if (ok && wait(p_full, (n_tiles - 1) & 1)) {
+        tc_fence_after();
+        issue_pv(n_tiles - 1);
+      }
+      // every product issued has completed before the tensor memory is freed
+      umma_commit(mma_done);
+      wait(mma_done, 0);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int BS>
+int smem_opt_in() {
+  static int done = -1;
+  if (done < 0)
+    done = cudaFuncSetAttribute(paged_prefill_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemBytes) == cudaSuccess ? 1 : 0;
+  return done;
+}
+
+}  // namespace
+
+int prefill_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_prefill(const kv_pool* pool, const PrefillParams& p, int32_t max_q_len,
+                           cudaStream_t stream) {
+  const int tok_per_tile = kRows / p.group_pow2;
+  const dim3 grid((max_q_len + tok_per_tile - 1) / tok_per_tile, p.n_kv_heads, p.batch);
+  if (pool->block_size == 32) {
+    if (!smem_opt_in<32>()) return cudaErrorInvalidValue;
+    paged_prefill_kernel<32><<<grid, kThreads, kSmemBytes, stream>>>(pool->tmap_rows, p);
+  } else {
+    if (!smem_opt_in<16>()) return cudaErrorInvalidValue;
+    paged_prefill_kernel<16><<<grid, kThreads, kSmemBytes, stream>>>(pool->tmap_rows, p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -72,6 +72,9 @@ def load() -> ctypes.CDLL:
             "paged_decode_step": (c.c_int, [P, P, P, P, c.c_int64, P, c.c_int32, P, c.c_int32,
                                             P, c.c_int32, c.c_int32, c.c_float, c.c_int32, P,
                                             P, c.c_size_t, P]),
+            "paged_prefill_attention": (c.c_int, [P, P, c.c_int32, P, P, c.c_int32, P,
+                                                  c.c_int32, c.c_int32, c.c_int32, c.c_float,
+                                                  c.c_int32, P, P]),
             "paged_decode_attention_noalloc": (c.c_int, [P, P, c.c_int32, P, c.c_int32, P,
                                                          c.c_int32, c.c_int32, c.c_float,
                                                          c.c_int32, P, P]),
@@ -332,6 +335,33 @@ def paged_decode_step(pool: KVPool, k: torch.Tensor, v: torch.Tensor, slot_mappi
         _dev(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
         int(sliding_window), _dev(out, torch.float32, "out"), ws_ptr, ws_bytes, _stream(stream)),
         "paged_decode_step")
+    return out
+
+
+def paged_prefill_attention(pool: KVPool, q: torch.Tensor, cu_q_lens: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                            sliding_window: int = 0, max_q_len: int | None = None,
+                            max_context_len: int | None = None, out: torch.Tensor | None = None,
+                            stream=None) -> torch.Tensor:
+    """Prefill / extend attention: q [T, Hq, D] bf16 (the new tokens of every
+    sequence, split by cu_q_lens [B + 1] int32) -> out [T, Hq, D] fp32.  The
+    host bounds are read from the tensors (a synchronisation) when omitted."""
+    T, Hq, D = q.shape
+    B = context_lens.shape[0]
+    if max_q_len is None:
+        max_q_len = int((cu_q_lens[1:] - cu_q_lens[:-1]).max().item()) if B else 0
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if B else 0
+    if out is None:
+        out = torch.empty(T, Hq, D, dtype=torch.float32, device=q.device)
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or cu_q_lens.shape[0] != B + 1:
+        raise ValueError("block_tables must be [B, max_blocks_per_seq] and cu_q_lens [B + 1]")
+    _check(load().paged_prefill_attention(
+        pool.handle, _dev(q, torch.bfloat16, "q"), Hq, _dev(cu_q_lens, torch.int32, "cu_q_lens"),
+        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _dev(context_lens, torch.int32, "context_lens"), B, int(max_q_len),
+        int(max_context_len), float(scale), int(sliding_window), _dev(out, torch.float32, "out"),
+        _stream(stream)), "paged_prefill_attention")
     return out
 
 

@@ -1,0 +1,169 @@
+"""GPU parity of paged prefill (extend) attention on tcgen05 against the fp64
+oracle.
+
+Tolerance: the kernel rounds the softmax weights P to bf16 (8 significant
+bits, relative rounding error <= 2^-9) before the P V product, accumulating
+in fp32; every output is a convex combination of V rows, so its error is at
+most ~2^-9 * max|V| plus fp32 rounding.  With N(0,1) data (max|V| ~ 5) that
+gives max |err| <= 1e-2; the errors are independent over the attended
+tokens, so the relative L2 error stays near 2^-9 / sqrt(3) ~ 1.1e-3: the bar
+is 3e-3.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_33_gb300 import pagedkv
+
+from _parity import compare_pools, errors, poison
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 1e-2
+REL_L2 = 3e-3
+
+
+def _build(ctx_lens, q_lens, hq, hkv, bs=16, seed=0, extra_blocks=5):
+    """Pools (GPU poisoned, oracle) holding every context token; the queries
+    of the last q_len positions; shuffled tables."""
+    rng = np.random.default_rng(seed)
+    ctx_lens = np.asarray(ctx_lens, np.int32)
+    q_lens = np.asarray(q_lens, np.int32)
+    B = len(ctx_lens)
+    nblk = [max(1, -(-int(c) // bs)) for c in ctx_lens]
+    nb = sum(nblk) + extra_blocks
+    ids = rng.permutation(nb).astype(np.int32)
+    tables = np.full((B, max(nblk)), -1, np.int32)
+    at = 0
+    for b, n in enumerate(nblk):
+        tables[b, :n] = ids[at:at + n]
+        at += n
+    g = torch.Generator().manual_seed(seed + 1)
+    pool = pagedkv.KVPool(nb, bs, hkv, 128, "bf16")
+    poison(pool)
+    opool = oracle.Pool(nb, bs, hkv, 128, "bf16")
+    for b, c in enumerate(ctx_lens):
+        if c == 0:
+            continue
+        k = torch.randn(int(c), hkv, 128, generator=g).to(torch.bfloat16)
+        v = torch.randn(int(c), hkv, 128, generator=g).to(torch.bfloat16)
+        pos = np.arange(int(c))
+        slots = (tables[b, pos // bs].astype(np.int64) * bs + pos % bs)
+        pagedkv.paged_kv_write(pool, k.cuda(), v.cuda(), torch.from_numpy(slots).cuda())
+        opool.write(k, v, slots)
+    T = int(q_lens.sum())
+    q = torch.randn(T, hq, 128, generator=g).to(torch.bfloat16)
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    return pool, opool, q, cu, tables, ctx_lens
+
+
+def _run(pool, q, cu, tables, lens, scale, window=0):
+    return pagedkv.paged_prefill_attention(
+        pool, q.cuda(), torch.from_numpy(cu).cuda(), torch.from_numpy(tables).cuda(),
+        torch.from_numpy(lens).cuda(), scale, window,
+        max_q_len=int((cu[1:] - cu[:-1]).max()), max_context_len=int(lens.max()))
+
+
+def _check(out, ref, label):
+    got = out.cpu().numpy()
+    assert np.isfinite(got).all(), label
+    max_abs, rel = errors(got, ref)
+    print(f"PARITY prefill {label} max_abs={max_abs:.3e} rel_l2={rel:.3e}")
+    assert max_abs <= MAX_ABS and rel <= REL_L2, (label, max_abs, rel)
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (16, 2), (3, 1), (12, 2)])
+def test_prefill_matches_oracle(hq, hkv, bs):
+    # full prompts, cached prefixes with short and long tails, q_len 1 and 0
+    ctx = [1, 16, 17, 63, 64, 65, 200, 300, 129, 90]
+    ql = [1, 16, 5, 63, 1, 30, 200, 77, 0, 90]
+    pool, opool, q, cu, tables, lens = _build(ctx, ql, hq, hkv, bs=bs, seed=hq * 10 + hkv + bs)
+    out = _run(pool, q, cu, tables, lens, 128 ** -0.5)
+    torch.cuda.synchronize()
+    assert pool.check_status() == pagedkv.KV_OK
+    ref = opool.prefill(q, cu, tables, lens, 128 ** -0.5)
+    _check(out, ref, f"hq={hq} hkv={hkv} bs={bs}")
+    pool.destroy()
+
+
+@pytest.mark.parametrize("window", [1, 7, 64, 100, 5000])
+def test_prefill_sliding_window(window):
+    ctx = [50, 300, 700]
+    ql = [50, 120, 300]
+    pool, opool, q, cu, tables, lens = _build(ctx, ql, 16, 4, seed=window)
+    # blocks wholly before every window of the sequence are unmapped
+    for b, c in enumerate(lens):
+        first_pos = int(c) - int(ql[b])
+        lo = max(0, first_pos + 1 - window)
+        tables[b, : lo // 16] = -1
+    out = _run(pool, q, cu, tables, lens, 0.1, window)
+    torch.cuda.synchronize()
+    assert pool.check_status() == pagedkv.KV_OK
+    ref = opool.prefill(q, cu, tables, lens, 0.1, window)
+    _check(out, ref, f"window={window}")
+    pool.destroy()
+
+
+def test_prefill_long_prompt_many_tiles():
+    # several query tiles and many key tiles per (sequence, KV head)
+    pool, opool, q, cu, tables, lens = _build([2048, 1500], [300, 1500], 8, 2, seed=3)
+    out = _run(pool, q, cu, tables, lens, 128 ** -0.5)
+    torch.cuda.synchronize()
+    assert pool.check_status() == pagedkv.KV_OK
+    ref = opool.prefill(q, cu, tables, lens, 128 ** -0.5)
+    _check(out, ref, "long")
+    pool.destroy()
+
+
+def test_prefill_last_token_matches_decode():
+    pool, opool, q, cu, tables, lens = _build([77, 300], [20, 33], 8, 2, seed=11)
+    out = _run(pool, q, cu, tables, lens, 0.09)
+    last = q[torch.from_numpy(cu[1:] - 1).long()]
+    dec = pagedkv.paged_decode_attention(pool, last.cuda(), torch.from_numpy(tables).cuda(),
+                                         torch.from_numpy(lens).cuda(), 0.09,
+                                         max_context_len=int(lens.max()))
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()[cu[1:] - 1]
+    max_abs, _ = errors(got, dec.cpu().numpy())
+    assert max_abs <= MAX_ABS
+    pool.destroy()
+
+
+def test_prefill_bad_block_and_bad_context():
+    pool, opool, q, cu, tables, lens = _build([100, 100], [40, 40], 8, 2, seed=13)
+    bad = tables.copy()
+    bad[0, 2] = pool.num_blocks + 3
+    out = _run(pool, q, cu, bad, lens, 0.1)
+    torch.cuda.synchronize()
+    assert pool.check_status() == 5                        # KV_ERR_BAD_BLOCK_ID
+    ref = opool.prefill(q, cu, tables, lens, 0.1)
+    got = out.cpu().numpy()
+    assert np.isfinite(got).all()
+    r1 = slice(cu[1], cu[2])                                # the other sequence is unaffected
+    max_abs, _ = errors(got[r1], ref[r1])
+    assert max_abs <= MAX_ABS
+    # q_len above the context: reported, skipped
+    lens2 = lens.copy()
+    lens2[1] = 30
+    _run(pool, q, cu, tables, lens2, 0.1)
+    torch.cuda.synchronize()
+    assert pool.check_status() == 8                        # KV_ERR_BAD_CONTEXT
+    pool.destroy()
+
+
+def test_prefill_host_checks():
+    pool = pagedkv.KVPool(8, 16, 2, 128)
+    q = torch.zeros(4, 4, 128, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 4], dtype=torch.int32, device="cuda")
+    t = torch.zeros(1, 2, dtype=torch.int32, device="cuda")
+    c = torch.tensor([4], dtype=torch.int32, device="cuda")
+    with pytest.raises(pagedkv.KVError):
+        pagedkv.paged_prefill_attention(pool, q, cu, t, c, 0.1, max_q_len=4, max_context_len=64)
+    fp8 = pagedkv.KVPool(8, 16, 2, 128, "fp8")
+    with pytest.raises(pagedkv.KVError):
+        pagedkv.paged_prefill_attention(fp8, q, cu, t, c, 0.1, max_q_len=4, max_context_len=4)
+    pool.destroy()
+    fp8.destroy()
