@@ -62,6 +62,8 @@ def parse_args(argv=None):
                     help="tokens per pool block")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--part-blocks", type=int, default=0, help="split-K partition size (0 = auto)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the block-copy, prefill and host block-manager measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     return ap.parse_args(argv)
@@ -293,6 +295,99 @@ def timed_e2e(step: Step, steps: int, warmup: int, dist_ctx) -> dict:
     return {"elapsed_s": elapsed, "h2d": h2d, "d2h": d2h}
 
 
+# ----------------------------------------------------------------- extras --
+
+def _event_time(torch, fn, iters: int) -> float:
+    """Seconds per call of fn, CUDA events on the current stream, after warm-up."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / iters
+
+
+def measure_extras(step: Step, peaks: dict, device) -> dict:
+    """The other operations of the library, each against its own roofline:
+    copy-on-write block copies (HBM), prefill attention (tensor cores), and
+    the host block manager's per-step work.  Runs after the timed steps (the
+    block copies overwrite blocks of the bench pool)."""
+    import numpy as np
+    torch, pk, w = step.torch, step.pk, step.w
+    out = {}
+    # -- paged_kv_copy_blocks: disjoint random pairs over the whole pool
+    n = min(2048, w.num_blocks // 2)
+    pairs = np.random.default_rng(9).permutation(w.num_blocks)[:2 * n].astype(np.int32).reshape(n, 2)
+    elem = 2 if w.dtype == "bf16" else 1
+    blk_bytes = w.n_kv_heads * 2 * w.block_size * w.head_dim * elem
+    t = _event_time(torch, lambda: pk.paged_kv_copy_blocks(step.pool, pairs), 20)
+    gbs = 2 * blk_bytes * n / t / 1e9
+    out["paged_kv_copy_blocks"] = {
+        "pairs": n, "block_bytes": blk_bytes, "us_per_call": t * 1e6, "achieved": gbs,
+        "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
+        "bytes_per_pair": 2 * blk_bytes}
+    # -- paged_prefill_attention: 8B-shaped full prefill, 4 x 2048 tokens
+    B, ctx, hq, hkv = 4, 2048, 32, 8
+    nblk = ctx // 16
+    ppool = pk.KVPool(B * nblk, 16, hkv, 128, "bf16")
+    tables = torch.from_numpy(np.random.default_rng(3).permutation(B * nblk).astype(np.int32)
+                              .reshape(B, nblk)).to(device)
+    g = torch.Generator(device=device).manual_seed(5)
+    kk = torch.randn(B * ctx, hkv, 128, device=device, generator=g).to(torch.bfloat16)
+    pos = torch.arange(ctx, device=device)
+    slots = (tables[:, pos // 16].long() * 16 + pos % 16).reshape(-1)
+    pk.paged_kv_write(ppool, kk, kk, slots)
+    q = torch.randn(B * ctx, hq, 128, device=device, generator=g).to(torch.bfloat16)
+    cu = torch.arange(0, B * ctx + 1, ctx, dtype=torch.int32, device=device)
+    lens = torch.full((B,), ctx, dtype=torch.int32, device=device)
+    pout = torch.empty(B * ctx, hq, 128, device=device)
+    t = _event_time(torch, lambda: pk.paged_prefill_attention(
+        ppool, q, cu, tables, lens, 128 ** -0.5, 0, max_q_len=ctx, max_context_len=ctx,
+        out=pout), 20)
+    flops = 4.0 * 128 * hq * B * (ctx * (ctx + 1) // 2)   # QK and PV over the causal keys
+    tf = flops / t / 1e12
+    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
+    out["paged_prefill_attention"] = {
+        "workload": f"full causal prefill, {B} x {ctx} tokens, {hq} q / {hkv} KV heads, "
+                    "head_dim 128, 16-token blocks",
+        "us_per_call": t * 1e6, "achieved": tf, "unit": "TFLOP/s", "bound": "tensor",
+        "peak": bf16_peak, "frac": tf / bf16_peak, "flops_per_call": flops,
+        "peak_source": "MEASURED_PEAKS.json bf16_tflops (cuBLAS burst)"}
+    if ppool.check_status() != pk.KV_OK or step.pool.check_status() != pk.KV_OK:
+        raise RuntimeError("device error in the extra measurements")
+    ppool.destroy()
+    # -- host block manager: one decode step's inputs for the bench batch, and
+    #    admit / append / free churn
+    need = sum(-(-int(c) // w.block_size) for c in w.context_lens)
+    bm = pk.BlockManager(need + 64, w.block_size)
+    for b in range(w.batch):
+        if bm.admit(b, num_tokens=max(1, int(w.context_lens[b])))[0] != 0:
+            raise RuntimeError("host block manager: admission failed")
+    ids = np.arange(w.batch, dtype=np.int64)
+    t0 = time.perf_counter()
+    for _ in range(200):
+        bm.decode_inputs(ids, w.max_blocks_per_seq)
+    t_inputs = (time.perf_counter() - t0) / 200
+    t0 = time.perf_counter()
+    nops = 0
+    for i in range(2000):
+        rid = 10_000 + i
+        if bm.admit(rid, num_tokens=300)[0] == 0:
+            bm.append(rid, n=20)
+            bm.free(rid)
+            nops += 3
+    t_ops = time.perf_counter() - t0
+    out["host_block_manager"] = {
+        "decode_inputs_us": t_inputs * 1e6, "batch": w.batch,
+        "admit_append_free_ops_per_s": nops / t_ops if t_ops > 0 else None,
+        "note": "host CPU time through the ctypes binding (includes marshalling)"}
+    return out
+
+
 # ------------------------------------------------------------ distributed --
 
 class DistCtx:
@@ -470,8 +565,9 @@ def main(argv=None) -> None:
     peaks = measured_peaks()
     # algorithmic bytes of one decode launch: attended K/V (shared prefix once),
     # the queries, the outputs and the block-table entries read
+    bsz = w.block_size
     tables_read = 4 * w.n_kv_heads * sum(
-        (hi - 1) // 16 - lo // 16 + 1 for lo, hi in map(w.attended_range, range(w.batch)) if hi > lo)
+        (hi - 1) // bsz - lo // bsz + 1 for lo, hi in map(w.attended_range, range(w.batch)) if hi > lo)
     algo = unique + w.batch * w.n_q_heads * w.head_dim * (2 + 4) + tables_read
     achieved = algo / kernel_s / 1e9
     step_s = elapsed / args.steps
@@ -497,13 +593,16 @@ def main(argv=None) -> None:
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy)",
                      "algorithmic_bytes_per_launch": algo,
                      "kernel_ms": kernel_s * 1e3,
-                     "traffic": recorded_traffic(args.config)},
+                     "traffic": recorded_traffic(args.config if w.block_size == 16
+                                                 else f"{args.config}-bs{w.block_size}")},
         "e2e": {"value": e2e_bytes / e2e_elapsed / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "steps": e2e_steps},
         "clocks": clocks,
         "gpu_launches": step.launches * args.steps,
     }
+    if dist_ctx.rank == 0 and not args.no_extras:
+        result["extras"] = measure_extras(step, peaks, device)
     if dist_ctx.rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = oracle_sample(w, args.cpu_baseline_seconds)
     dist_ctx.barrier()

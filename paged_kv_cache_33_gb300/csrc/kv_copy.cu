@@ -16,7 +16,6 @@
 // four loads in flight per thread before the stores.
 
 #include <algorithm>
-#include <unordered_set>
 #include <vector>
 
 #include "common.cuh"
@@ -67,17 +66,31 @@ cudaError_t launch_copy_blocks(const kv_pool* pool, const int32_t* pairs, int64_
                                cudaStream_t stream) {
   const int64_t chunks = block_bytes(pool) / 16;
   const int slices = static_cast<int>((chunks + kChunksPerCta - 1) / kChunksPerCta);
-  CopyWave wave;
+  static thread_local CopyWave wave;
   int count = 0;
-  // blocks read / written by the pairs of the current wave
-  std::unordered_set<int32_t> reads, writes;
+  // Blocks read / written by the pairs of the current wave: a block is in
+  // the set when its stamp equals the wave's number (no clearing per wave).
+  static thread_local std::vector<uint32_t> read_stamp, write_stamp;
+  static thread_local uint32_t wave_id = 0;
+  if (read_stamp.size() < static_cast<size_t>(pool->num_blocks)) {
+    read_stamp.assign(pool->num_blocks, 0u);
+    write_stamp.assign(pool->num_blocks, 0u);
+    wave_id = 0;
+  }
+  auto next_wave = [&]() {
+    if (++wave_id == 0) {  // wrapped: forget every stamp
+      std::fill(read_stamp.begin(), read_stamp.end(), 0u);
+      std::fill(write_stamp.begin(), write_stamp.end(), 0u);
+      wave_id = 1;
+    }
+  };
+  next_wave();
   auto flush = [&]() -> cudaError_t {
     if (count == 0) return cudaSuccess;
     kv_copy_blocks_kernel<<<count * slices, kCopyThreads, 0, stream>>>(
         wave, slices, chunks, static_cast<uint4*>(pool->base));
     count = 0;
-    reads.clear();
-    writes.clear();
+    next_wave();
     return cudaGetLastError();
   };
   for (int64_t i = 0; i < n; ++i) {
@@ -85,13 +98,14 @@ cudaError_t launch_copy_blocks(const kv_pool* pool, const int32_t* pairs, int64_
     if (s == d) continue;
     // A pair that reads a block this wave writes, or writes a block this
     // wave reads or writes, must see the wave's result: start a new wave.
-    if (count == kMaxWave || writes.count(s) || writes.count(d) || reads.count(d)) {
+    if (count == kMaxWave || write_stamp[s] == wave_id || write_stamp[d] == wave_id ||
+        read_stamp[d] == wave_id) {
       const cudaError_t e = flush();
       if (e != cudaSuccess) return e;
     }
     wave.pairs[count++] = make_int2(s, d);
-    reads.insert(s);
-    writes.insert(d);
+    read_stamp[s] = wave_id;
+    write_stamp[d] = wave_id;
   }
   return flush();
 }
