@@ -262,22 +262,33 @@ def timed_device(step: Step, steps: int, warmup: int, dist_ctx, sampler) -> dict
 
 def timed_e2e(step: Step, steps: int, warmup: int, dist_ctx) -> dict:
     """Same steps through the public API with host inputs: every step copies q,
-    the new K/V, slots, block tables and context lengths from pinned memory
-    and reads the output back."""
+    the new K/V, slots, block tables and context lengths from pinned host
+    memory (laid out back to back in one pinned buffer, so one copy moves them
+    all) and reads the output back."""
     torch, w = step.torch, step.w
-    host = {
-        "q": step.q.cpu().pin_memory(), "k": step.k_new.cpu().pin_memory(),
-        "v": step.v_new.cpu().pin_memory(), "slots": step.slots.cpu().pin_memory(),
-        "tables": step.tables.cpu().pin_memory(), "lens": step.lens.cpu().pin_memory(),
-    }
-    dev = {k: torch.empty_like(v, device=step.q.device) for k, v in host.items()}
+    srcs = {"q": step.q, "k": step.k_new, "v": step.v_new, "slots": step.slots,
+            "tables": step.tables, "lens": step.lens}
+    offs, total = {}, 0
+    for name, t in srcs.items():
+        offs[name] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=step.q.device)
+
+    def view(buf, name):
+        t = srcs[name]
+        n = t.numel() * t.element_size()
+        return buf[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
+
+    for name, t in srcs.items():
+        view(host_buf, name).copy_(t.cpu())
+    dev = {name: view(dev_buf, name) for name in srcs}
     out_host = torch.empty(step.out.shape, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(t.numel() * t.element_size() for t in srcs.values())
     d2h = out_host.numel() * out_host.element_size()
 
     def one():
-        for k in host:
-            dev[k].copy_(host[k], non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
         step.run(q=dev["q"], tables=dev["tables"], lens=dev["lens"], k=dev["k"], v=dev["v"],
                  slots=dev["slots"])
         out_host.copy_(step.out, non_blocking=True)

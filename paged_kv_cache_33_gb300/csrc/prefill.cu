@@ -9,7 +9,7 @@
 // lo = max(0, pos + 1 - W) under a window W, else 0, resolving every key
 // through the block table.  GQA: query head hq reads KV head hq / g.
 //
-// How (GB300 design), one CTA per (128-row query tile, KV head, sequence):
+// How (GB300 design), one CTA per (two 128-row query tiles, KV head, sequence):
 //  * Rows of the tile are (new token, query head of the group) pairs, the
 //    group padded to a power of two Gp: 128 / Gp tokens x Gp heads.  Q is
 //    staged once in shared memory (128-byte swizzled, K-major).
@@ -21,7 +21,10 @@
 //    memory, double-buffered so S of the next tile runs while the softmax of
 //    this one does), then O += P V (128 x 128, fp32 in tensor memory), with
 //    V read MN-major straight from its pool rows.
-//  * Four softmax warps own one row each per thread: tcgen05.ld the row of
+//  * Two query tiles share every key tile: the tensor cores work on one
+//    tile's products while the softmax warps of the other run, which hides
+//    the latency chain of each (S ready -> softmax -> P -> product).
+//  * Four softmax warps per query tile own one row each per thread: tcgen05.ld the row of
 //    S, mask (causal, window, sequence end, missing blocks), online softmax
 //    in the exp2 domain with a lazy maximum (O in tensor memory is rescaled
 //    only when a row's maximum grows by more than 2^8), P to shared memory
@@ -41,24 +44,30 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kRows = 128;           // query rows per tile (M)
+constexpr int kTiles = 2;            // query tiles per CTA, in ping-pong over the same keys
 constexpr int kKv = 64;              // keys per tile (N of S, K of P V)
 constexpr int kStages = 3;           // K/V ring
-constexpr int kThreads = 192;        // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr int kSoftmax = kTiles * kRows;      // one softmax thread per query row
+constexpr int kThreads = kSoftmax + 64;       // + producer warp + MMA warp
+constexpr int kProducerWarp = kSoftmax / 32, kMmaWarp = kProducerWarp + 1;
 constexpr float kLazy = 8.f;         // rescale O when a row maximum grows by more than this (log2)
 constexpr uint64_t kShortWaitNs = 200000;
 
 // Shared memory (offsets from a 1024-aligned base).
-constexpr int kQ = 0;                                 // 2 halves x [128][64] bf16
-constexpr int kK = kQ + 2 * kRows * 128;              // stages x 2 halves x [64][64]
+constexpr int kQ = 0;                                 // tiles x 2 halves x [128][64] bf16
+constexpr int kQTile = 2 * kRows * 128;
+constexpr int kK = kQ + kTiles * kQTile;              // stages x 2 halves x [64][64]
 constexpr int kV = kK + kStages * 2 * kKv * 128;
-constexpr int kP = kV + kStages * 2 * kKv * 128;      // [128][64] bf16
-constexpr int kBars = kP + kRows * 128;
-// barriers: kv_full[3], kv_empty[3], s_full[2], q_full, p_full, o_done, mma_done
-constexpr int kNumBars = 2 * kStages + 2 + 4;
+constexpr int kP = kV + kStages * 2 * kKv * 128;      // tiles x [128][64] bf16
+constexpr int kBars = kP + kTiles * kRows * 128;
+// barriers: kv_full[3], kv_empty[3], then per tile s_full[2], p_full, o_done; q_full, mma_done
+constexpr int kNumBars = 2 * kStages + 4 * kTiles + 2;
 constexpr int kTileMask = kBars + kNumBars * 8;       // uint32 [kStages]
 constexpr int kTmemSlot = kTileMask + kStages * 4;
 constexpr int kSmemBytes = kTmemSlot + 16 + 1024;     // + alignment slack
-constexpr uint32_t kTmemCols = 256;                   // S0 [0,64) S1 [64,128) O [128,256)
+// tensor memory per query tile: S0 [0,64) S1 [64,128) O [128,256)
+constexpr uint32_t kTmemTile = 256;
+constexpr uint32_t kTmemCols = kTiles * kTmemTile;
 
 __device__ __forceinline__ int swz128(int row, int chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
@@ -72,32 +81,40 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.z, h = blockIdx.y;
   const int Gp = p.group_pow2, g = p.group;
-  const int tok_per_tile = kRows / Gp;
+  const int tpt = kRows / Gp;  // query tokens per tile
 
-  // ---- this tile's queries and the keys they need (uniform over the CTA)
+  // ---- the CTA's queries and the keys they need (uniform over the CTA)
   const int32_t q0 = p.cu_q_lens[b];
-  int32_t qn = p.cu_q_lens[b + 1] - q0;
+  const int32_t qn = p.cu_q_lens[b + 1] - q0;
   const int32_t ctx = p.context_lens[b];
   if (qn < 0 || qn > ctx || ctx > p.max_ctx || static_cast<int64_t>(ctx) > static_cast<int64_t>(p.mbs) * BS) {
     if (qn != 0 && blockIdx.x == 0 && h == 0 && tid == 0) atomicOr(p.err, kErrBadContext);
     return;
   }
-  const int tok0 = blockIdx.x * tok_per_tile;
+  const int tok0 = blockIdx.x * (kTiles * tpt);
   if (tok0 >= qn) return;
-  const int ntok = min(tok_per_tile, qn - tok0);
-  const int pos_first = ctx - qn + tok0, pos_last = pos_first + ntok - 1;
-  const int kv_begin = p.window > 0 ? max(0, pos_first + 1 - p.window) : 0;
-  const int kv_end = pos_last + 1;
+  const int pos_base = ctx - qn;  // position of new token 0
+  // tile t holds tokens tok0 + t * tpt .. (ntok[t] of them; tile 1 may be empty)
+  static_assert(kTiles == 2, "two query tiles in ping-pong");
+  const int kv_begin = p.window > 0 ? max(0, pos_base + tok0 + 1 - p.window) : 0;
   const int jt0 = kv_begin / kKv;
-  const int n_tiles = (kv_end - 1) / kKv - jt0 + 1;
+  const int ntok0 = min(tpt, qn - tok0), ntok1 = max(0, min(tpt, qn - tok0 - tpt));
+  const int last0 = pos_base + tok0 + ntok0 - 1;               // last position of tile 0
+  const int last1 = pos_base + tok0 + tpt + ntok1 - 1;         // (tile 1, when not empty)
+  const int n_kv0 = last0 / kKv - jt0 + 1;                     // key tiles of each query tile
+  const int n_kv1 = ntok1 > 0 ? last1 / kKv - jt0 + 1 : 0;
+  const int kv_end = (ntok1 > 0 ? last1 : last0) + 1;
+  const int n_tiles = max(n_kv0, n_kv1);                       // key tiles of the CTA
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBars);
   const uint32_t bar0 = smem_addr(bars);
   auto kv_full = [&](int s) { return bar0 + 8u * s; };
   auto kv_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
-  auto s_full = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
-  const uint32_t q_full = bar0 + 8u * (2 * kStages + 2);
-  const uint32_t p_full = q_full + 8, o_done = q_full + 16, mma_done = q_full + 24;
+  auto s_full = [&](int t, int i) { return bar0 + 8u * (2 * kStages + 4 * t + i); };
+  auto p_full = [&](int t) { return bar0 + 8u * (2 * kStages + 4 * t + 2); };
+  auto o_done = [&](int t) { return bar0 + 8u * (2 * kStages + 4 * t + 3); };
+  const uint32_t q_full = bar0 + 8u * (2 * kStages + 4 * kTiles);
+  const uint32_t mma_done = q_full + 8;
   uint32_t* tile_mask = reinterpret_cast<uint32_t*>(smem + kTileMask);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
 
@@ -106,15 +123,17 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 1);
     }
-    mbar_init(s_full(0), 1);
-    mbar_init(s_full(1), 1);
-    mbar_init(q_full, kRows);
-    mbar_init(p_full, kRows);
-    mbar_init(o_done, 1);
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(s_full(t, 0), 1);
+      mbar_init(s_full(t, 1), 1);
+      mbar_init(p_full(t), kRows);
+      mbar_init(o_done(t), 1);
+    }
+    mbar_init(q_full, kSoftmax);
     mbar_init(mma_done, 1);
     fence_mbar_init();
   }
-  if (warp == 5) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -123,33 +142,38 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     return mbar_wait_bounded(bar, parity, p.wait_limit_ns, p.err, kErrTimeout, kShortWaitNs);
   };
 
-  if (warp < 4) {
-    // =========================== softmax warps: one query row per thread
-    const int r = tid;
+  if (warp < kProducerWarp) {
+    // ====== softmax warps: warps 4t..4t+3 serve query tile t, one row per thread
+    const int t = warp >> 2;
+    const int r = tid & (kRows - 1);
     const int tq = r / Gp, jh = r - tq * Gp;
-    const bool row_ok = tq < ntok && jh < g;
-    const int pos = pos_first + tq;
+    const bool row_ok = tq < (t ? ntok1 : ntok0) && jh < g;
+    const int tok = tok0 + t * tpt + tq;
+    const int pos = pos_base + tok;
     const int lo = p.window > 0 ? max(0, pos + 1 - p.window) : 0;
     const int hq = h * g + jh;
-    // Q row r -> shared memory (zeros for padding rows)
+    // Q row r of tile t -> shared memory (zeros for padding rows)
     {
       const uint4* src = reinterpret_cast<const uint4*>(
           static_cast<const __nv_bfloat16*>(p.q) +
-          (static_cast<int64_t>(q0 + tok0 + tq) * p.n_q_heads + hq) * kD);
+          (static_cast<int64_t>(q0 + tok) * p.n_q_heads + hq) * kD);
+      uint8_t* qt = smem + kQ + t * kQTile;
 #pragma unroll
       for (int c = 0; c < kD / 8; ++c) {
         const uint4 v = row_ok ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(smem + kQ + (c >> 3) * (kRows * 128) + swz128(r, c & 7)) = v;
+        *reinterpret_cast<uint4*>(qt + (c >> 3) * (kRows * 128) + swz128(r, c & 7)) = v;
       }
       fence_proxy_async_smem();
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(q_full) : "memory");
     }
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+    const uint32_t lane_base = tmem + t * kTmemTile + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    uint8_t* pt = smem + kP + t * (kRows * 128);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int jt = 0; jt < n_tiles && ok; ++jt) {
+    const int nt = t ? n_kv1 : n_kv0;
+    for (int jt = 0; jt < nt && ok; ++jt) {
       const int s = jt % kStages, sb = jt & 1;
-      ok = wait(s_full(sb), (jt >> 1) & 1) && wait(kv_full(s), (jt / kStages) & 1);
+      ok = wait(s_full(t, sb), (jt >> 1) & 1) && wait(kv_full(s), (jt / kStages) & 1);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       const uint32_t mask = tile_mask[s];
@@ -163,15 +187,15 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int c = half * 32 + i;
-          const int t = key0 + c;
-          const bool valid = row_ok && t >= lo && t <= pos && ((mask >> (c / BS)) & 1u);
+          const int key = key0 + c;
+          const bool valid = row_ok && key >= lo && key <= pos && ((mask >> (c / BS)) & 1u);
           x[c] = valid ? __uint_as_float(raw[i]) * p.scale_log2 : -INFINITY;
           mt = fmaxf(mt, x[c]);
         }
       }
-      // O and the P buffer are free once the previous tile's product is done
+      // O and this tile's P buffer are free once its previous product is done
       if (jt > 0) {
-        ok = wait(o_done, (jt - 1) & 1);
+        ok = wait(o_done(t), (jt - 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
       }
@@ -204,12 +228,15 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
           l_run += a + b2;
           w[e] = pack_bf16x2(a, b2);
         }
-        *reinterpret_cast<uint4*>(smem + kP + swz128(r, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(pt + swz128(r, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      // V rows the product must not see: slots past the sequence's end and
-      // blocks that were not loaded (stale or never-written shared memory)
-      if (mask != (1u << (kKv / BS)) - 1u || key0 + kKv > ctx) {
-        for (int idx = tid; idx < kKv * 2 * 8; idx += kRows) {
+      // V rows the products must not see: slots past the sequence's end and
+      // blocks that were not loaded (stale or never-written shared memory).
+      // The first query tile that uses this key tile does it before handing
+      // its P over; the products of the other tile are issued after that.
+      const int zero_tile = jt < n_kv0 ? 0 : 1;
+      if (t == zero_tile && (mask != (1u << (kKv / BS)) - 1u || key0 + kKv > ctx)) {
+        for (int idx = r; idx < kKv * 2 * 8; idx += kRows) {
           const int key = idx >> 4, half = (idx >> 3) & 1, chunk = idx & 7;
           if (key0 + key >= ctx || !((mask >> (key / BS)) & 1u))
             *reinterpret_cast<uint4*>(smem + kV + s * (2 * kKv * 128) + half * (kKv * 128) +
@@ -218,13 +245,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(p_full) : "memory");
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(p_full(t)) : "memory");
     }
-    if (ok) ok = __all_sync(0xffffffffu, wait(o_done, (n_tiles - 1) & 1));
-    if (ok) {
+    if (ok && nt > 0) ok = __all_sync(0xffffffffu, wait(o_done(t), (nt - 1) & 1));
+    if (ok && nt > 0) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      float* dst = p.out + (static_cast<int64_t>(q0 + tok0 + tq) * p.n_q_heads + hq) * kD;
+      float* dst = p.out + (static_cast<int64_t>(q0 + tok) * p.n_q_heads + hq) * kD;
 #pragma unroll
       for (int c0 = 0; c0 < kD; c0 += 32) {
         uint32_t o[32];
@@ -238,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         }
       }
     }
-  } else if (warp == 4) {
+  } else if (warp == kProducerWarp) {
     // =========================== producer: K and V rows of each key tile
     if (lane == 0) {
       int issued = 0;
@@ -250,10 +277,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         int phys[kKv / BS];
 #pragma unroll
         for (int i = 0; i < kKv / BS; ++i) {
-          const int t0 = key0 + i * BS;
+          const int k0 = key0 + i * BS;
           phys[i] = -1;
-          if (t0 + BS <= kv_begin || t0 >= kv_end) continue;
-          const int e = p.block_tables[static_cast<int64_t>(b) * p.mbs + t0 / BS];
+          if (k0 + BS <= kv_begin || k0 >= kv_end) continue;
+          const int e = p.block_tables[static_cast<int64_t>(b) * p.mbs + k0 / BS];
           if (e < 0 || e >= p.num_blocks) {
             atomicOr(p.err, kErrBadBlock);
             continue;
@@ -290,52 +317,58 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     }
     __syncwarp();
   } else {
-    // =========================== MMA issuer
+    // =========================== MMA issuer: for every key tile, S of both
+    // query tiles, then the P V products of the previous key tile
     if (lane == 0) {
       constexpr uint32_t idS = umma_idesc_bf16(kRows, kKv, false);
       constexpr uint32_t idO = umma_idesc_bf16(kRows, kD, true);
       const uint32_t qs = smem_addr(smem + kQ), ps = smem_addr(smem + kP);
       bool ok = wait(q_full, 0);
       if (ok) tc_fence_after();
-      auto issue_s = [&](int jt) {
+      auto issue_s = [&](int t, int jt) {
         const int s = jt % kStages;
         const uint32_t ks = smem_addr(smem + kK + s * (2 * kKv * 128));
+        const uint32_t qt = qs + t * kQTile;
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k) {
-          const uint64_t a = umma_desc_sw128(qs + (k >> 2) * (kRows * 128) + (k & 3) * 32, 16, 1024);
+          const uint64_t a = umma_desc_sw128(qt + (k >> 2) * (kRows * 128) + (k & 3) * 32, 16, 1024);
           const uint64_t bd = umma_desc_sw128(ks + (k >> 2) * (kKv * 128) + (k & 3) * 32, 16, 1024);
-          umma_bf16(tmem + (jt & 1) * kKv, a, bd, idS, k > 0);
+          umma_bf16(tmem + t * kTmemTile + (jt & 1) * kKv, a, bd, idS, k > 0);
         }
-        umma_commit(s_full(jt & 1));
+        umma_commit(s_full(t, jt & 1));
       };
-      auto issue_pv = [&](int jt) {
+      auto issue_pv = [&](int t, int jt) {
         const int s = jt % kStages;
         const uint32_t vs = smem_addr(smem + kV + s * (2 * kKv * 128));
+        const uint32_t pt = ps + t * (kRows * 128);
 #pragma unroll
         for (int k = 0; k < kKv / 16; ++k) {
-          const uint64_t a = umma_desc_sw128(ps + k * 32, 16, 1024);
+          const uint64_t a = umma_desc_sw128(pt + k * 32, 16, 1024);
           const uint64_t bd = umma_desc_sw128(vs + k * 16 * 128, kKv * 128, 1024);
-          umma_bf16(tmem + 2 * kKv, a, bd, idO, (jt > 0 || k > 0) ? 1u : 0u);
+          umma_bf16(tmem + t * kTmemTile + 2 * kKv, a, bd, idO, (jt > 0 || k > 0) ? 1u : 0u);
         }
-        umma_commit(o_done);
-        umma_commit(kv_empty(s));
+        umma_commit(o_done(t));
+      };
+      // P V of key tile jt for every query tile that has it; then the stage is free
+      auto issue_pvs = [&](int jt) {
+        for (int t = 0; t < kTiles && ok; ++t) {
+          if (jt >= (t ? n_kv1 : n_kv0)) continue;
+          ok = wait(p_full(t), jt & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, jt);
+        }
+        if (ok) umma_commit(kv_empty(jt % kStages));
       };
       for (int jt = 0; ok && jt < n_tiles; ++jt) {
         ok = wait(kv_full(jt % kStages), (jt / kStages) & 1);
         if (!ok) break;
         tc_fence_after();
-        issue_s(jt);
-        if (jt > 0) {
-          ok = wait(p_full, (jt - 1) & 1);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(jt - 1);
-        }
+        for (int t = 0; t < kTiles; ++t)
+          if (jt < (t ? n_kv1 : n_kv0)) issue_s(t, jt);
+        if (jt > 0) issue_pvs(jt - 1);
       }
-      if (ok && wait(p_full, (n_tiles - 1) & 1)) {
-        tc_fence_after();
-        issue_pv(n_tiles - 1);
-      }
+      if (ok) issue_pvs(n_tiles - 1);
       // every product issued has completed before the tensor memory is freed
       umma_commit(mma_done);
       wait(mma_done, 0);
@@ -346,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int BS>
@@ -364,8 +397,8 @@ int prefill_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_prefill(const kv_pool* pool, const PrefillParams& p, int32_t max_q_len,
                            cudaStream_t stream) {
-  const int tok_per_tile = kRows / p.group_pow2;
-  const dim3 grid((max_q_len + tok_per_tile - 1) / tok_per_tile, p.n_kv_heads, p.batch);
+  const int tok_per_cta = kTiles * (kRows / p.group_pow2);
+  const dim3 grid((max_q_len + tok_per_cta - 1) / tok_per_cta, p.n_kv_heads, p.batch);
   if (pool->block_size == 32) {
     if (!smem_opt_in<32>()) return cudaErrorInvalidValue;
     paged_prefill_kernel<32><<<grid, kThreads, kSmemBytes, stream>>>(pool->tmap_rows, p);
