@@ -179,20 +179,19 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       const uint32_t mask = tile_mask[s];
       const int key0 = (jt0 + jt) * kKv;
       float x[kKv];
-      float mt = -INFINITY;
+      float mt4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      {
+        uint32_t raw[2][32];
+        tmem_ld32x2(lane_base + sb * kKv, lane_base + sb * kKv + 32, raw[0], raw[1]);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t raw[32];
-        tmem_ld32(lane_base + sb * kKv + half * 32, raw);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = half * 32 + i;
+        for (int c = 0; c < kKv; ++c) {
           const int key = key0 + c;
           const bool valid = row_ok && key >= lo && key <= pos && ((mask >> (c / BS)) & 1u);
-          x[c] = valid ? __uint_as_float(raw[i]) * p.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[c]);
+          x[c] = valid ? __uint_as_float(raw[c >> 5][c & 31]) * p.scale_log2 : -INFINITY;
+          mt4[c & 3] = fmaxf(mt4[c & 3], x[c]);
         }
       }
+      const float mt = fmaxf(fmaxf(mt4[0], mt4[1]), fmaxf(mt4[2], mt4[3]));
       // O and this tile's P buffer are free once its previous product is done
       if (jt > 0) {
         ok = wait(o_done(t), (jt - 1) & 1);
@@ -218,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       if (m_run == -INFINITY || rescale) m_run = m_new;
       // P row (bf16, 128-byte swizzled) and its sum
       const float mu = m_run == -INFINITY ? 0.f : m_run;
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int cc = 0; cc < kKv / 8; ++cc) {
         uint32_t w[4];
@@ -225,11 +225,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         for (int e = 0; e < 4; ++e) {
           const float a = fast_exp2(x[8 * cc + 2 * e] - mu);
           const float b2 = fast_exp2(x[8 * cc + 2 * e + 1] - mu);
-          l_run += a + b2;
+          l4[e] += a + b2;
           w[e] = pack_bf16x2(a, b2);
         }
         *reinterpret_cast<uint4*>(pt + swz128(r, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
+      l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
       // V rows the products must not see: slots past the sequence's end and
       // blocks that were not loaded (stale or never-written shared memory).
       // The first query tile that uses this key tile does it before handing
