@@ -178,20 +178,34 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       tc_fence_after();
       const uint32_t mask = tile_mask[s];
       const int key0 = (jt0 + jt) * kKv;
+      // raw scores; masked keys become -inf (the scale is applied in the exp)
       float x[kKv];
       float mt4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       {
         uint32_t raw[2][32];
         tmem_ld32x2(lane_base + sb * kKv, lane_base + sb * kKv + 32, raw[0], raw[1]);
+        // rows of this warp that see every key of the tile need no mask
+        const bool whole = row_ok && key0 >= lo && key0 + kKv - 1 <= pos &&
+                           mask == (1u << (kKv / BS)) - 1u;
+        if (__all_sync(0xffffffffu, whole)) {
 #pragma unroll
-        for (int c = 0; c < kKv; ++c) {
-          const int key = key0 + c;
-          const bool valid = row_ok && key >= lo && key <= pos && ((mask >> (c / BS)) & 1u);
-          x[c] = valid ? __uint_as_float(raw[c >> 5][c & 31]) * p.scale_log2 : -INFINITY;
-          mt4[c & 3] = fmaxf(mt4[c & 3], x[c]);
+          for (int c = 0; c < kKv; ++c) {
+            x[c] = __uint_as_float(raw[c >> 5][c & 31]);
+            mt4[c & 3] = fmaxf(mt4[c & 3], x[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kKv; ++c) {
+            const int key = key0 + c;
+            const bool valid = row_ok && key >= lo && key <= pos && ((mask >> (c / BS)) & 1u);
+            x[c] = valid ? __uint_as_float(raw[c >> 5][c & 31]) : -INFINITY;
+            mt4[c & 3] = fmaxf(mt4[c & 3], x[c]);
+          }
         }
       }
-      const float mt = fmaxf(fmaxf(mt4[0], mt4[1]), fmaxf(mt4[2], mt4[3]));
+      // row maximum in the exp2 domain (scale > 0)
+      const float mt_raw = fmaxf(fmaxf(mt4[0], mt4[1]), fmaxf(mt4[2], mt4[3]));
+      const float mt = mt_raw == -INFINITY ? -INFINITY : mt_raw * p.scale_log2;
       // O and this tile's P buffer are free once its previous product is done
       if (jt > 0) {
         ok = wait(o_done(t), (jt - 1) & 1);
@@ -217,14 +231,15 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       if (m_run == -INFINITY || rescale) m_run = m_new;
       // P row (bf16, 128-byte swizzled) and its sum
       const float mu = m_run == -INFINITY ? 0.f : m_run;
+      const float sc = p.scale_log2;
       float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int cc = 0; cc < kKv / 8; ++cc) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float a = fast_exp2(x[8 * cc + 2 * e] - mu);
-          const float b2 = fast_exp2(x[8 * cc + 2 * e + 1] - mu);
+          const float a = fast_exp2(fmaf(x[8 * cc + 2 * e], sc, -mu));
+          const float b2 = fast_exp2(fmaf(x[8 * cc + 2 * e + 1], sc, -mu));
           l4[e] += a + b2;
           w[e] = pack_bf16x2(a, b2);
         }
