@@ -258,6 +258,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 // ------------------------------------------------------------- numerics --
 
+// a * b + c on two fp32 lanes at once (the sm_100 packed-fp32 FMA).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(reinterpret_cast<const uint64_t&>(a)), "l"(reinterpret_cast<const uint64_t&>(b)),
+        "l"(reinterpret_cast<const uint64_t&>(c)));
+  return reinterpret_cast<const float2&>(d);
+}
+
+// a + b on two fp32 lanes at once.
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(reinterpret_cast<const uint64_t&>(a)), "l"(reinterpret_cast<const uint64_t&>(b)));
+  return reinterpret_cast<const float2&>(d);
+}
+
 // 2^x on the special-function unit (the PTX ex2.approx instruction).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

@@ -231,21 +231,21 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       if (m_run == -INFINITY || rescale) m_run = m_new;
       // P row (bf16, 128-byte swizzled) and its sum
       const float mu = m_run == -INFINITY ? 0.f : m_run;
-      const float sc = p.scale_log2;
-      float l4[4] = {0.f, 0.f, 0.f, 0.f};
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nmu2 = make_float2(-mu, -mu);
+      float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int cc = 0; cc < kKv / 8; ++cc) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float a = fast_exp2(fmaf(x[8 * cc + 2 * e], sc, -mu));
-          const float b2 = fast_exp2(fmaf(x[8 * cc + 2 * e + 1], sc, -mu));
-          l4[e] += a + b2;
-          w[e] = pack_bf16x2(a, b2);
+          const float2 arg = ffma2(make_float2(x[8 * cc + 2 * e], x[8 * cc + 2 * e + 1]), sc2, nmu2);
+          const float2 pe = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
+          l2[e & 1] = fadd2(l2[e & 1], pe);
+          w[e] = pack_bf16x2(pe.x, pe.y);
         }
         *reinterpret_cast<uint4*>(pt + swz128(r, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+      l_run += (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
       // V rows the products must not see: slots past the sequence's end and
       // blocks that were not loaded (stale or never-written shared memory).
       // The first query tile that uses this key tile does it before handing
