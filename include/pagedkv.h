@@ -280,6 +280,21 @@ kv_status kv_pool_set_partition_blocks(kv_pool* pool, int32_t blocks_per_partiti
 kv_status kv_pool_set_timing_events(kv_pool* pool, void* start_event, void* stop_event);
 
 /*
+ * kv_pool_set_wait_limit -- bound, in nanoseconds of wall time, of every wait
+ * the pool's kernels make on a copy or on another warp (default 1 s; 1e5 ..
+ * 1e10).  A wait that runs out records KV_ERR_TIMEOUT, the kernel drains
+ * what it issued and returns; nothing traps.
+ *
+ * kv_pool_set_test_stall -- test instrumentation for the timeout path: while
+ * enabled, the first copy of worker 0 in each decode launch expects 16 more
+ * bytes than it brings, so that warp's bounded wait runs out and the call
+ * reports KV_ERR_TIMEOUT (its outputs are then undefined).  No copy is left
+ * in flight and the context stays usable.  0 disables it (the default).
+ */
+kv_status kv_pool_set_wait_limit(kv_pool* pool, uint64_t limit_ns);
+kv_status kv_pool_set_test_stall(kv_pool* pool, int32_t enable);
+
+/*
  * kv_pool_check_status -- synchronise `stream`, read and clear the pool's
  * device error word.  Returns KV_OK, or the first recorded problem in the
  * order KV_ERR_TIMEOUT, KV_ERR_BAD_BLOCK_ID, KV_ERR_BAD_SLOT,

@@ -14,7 +14,6 @@
 
 namespace {
 
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s bound on any copy wait
 
 // Make the pool's device current for the duration of a call.
 struct DeviceGuard {
@@ -113,6 +112,7 @@ DecodePlan plan_decode(const kv_pool* pool, int32_t batch, int32_t n_q_heads,
   const int64_t pairs = static_cast<int64_t>(plan.batch) * pool->n_kv_heads;
   // partial slot of (segment s, pair p) is s + p: segments + pairs slots
   const int64_t slots = plan.workers + decode_max_chunks(t_max) + pairs;
+  plan.num_slots = slots;
   auto round256 = [](size_t x) { return (x + 255) / 256 * 256; };
   plan.part_o_bytes = round256(static_cast<size_t>(slots * g * pool->head_dim) * sizeof(float));
   plan.part_ml_bytes = round256(static_cast<size_t>(slots * g * 2) * sizeof(float));
@@ -338,8 +338,10 @@ kv_status decode_call(kv_pool* p, const StepWrite* w, const void* q, int32_t n_q
   d.max_ctx = max_context_len;
   d.window = sliding_window > 0 ? sliding_window : 0;
   d.num_workers = plan.workers;
+  d.num_slots = plan.num_slots;
+  d.stall_tx = p->stall_tx;
   d.scale_log2 = scale * 1.4426950408889634f;
-  d.wait_limit_ns = kWaitLimitNs;
+  d.wait_limit_ns = p->wait_limit_ns;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool timed = p->ev_start != nullptr;
@@ -436,7 +438,7 @@ kv_status paged_prefill_attention(kv_pool* p, const void* q, int32_t n_q_heads,
   d.max_ctx = max_context_len;
   d.window = sliding_window > 0 ? sliding_window : 0;
   d.scale_log2 = scale * 1.4426950408889634f;
-  d.wait_limit_ns = kWaitLimitNs;
+  d.wait_limit_ns = p->wait_limit_ns;
   const cudaError_t e = pkv::launch_prefill(p, d, max_q_len, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -458,6 +460,18 @@ kv_status kv_pool_set_timing_events(kv_pool* p, void* start_event, void* stop_ev
   if (!p || (!start_event) != (!stop_event)) return KV_ERR_INVALID_ARG;
   p->ev_start = static_cast<cudaEvent_t>(start_event);
   p->ev_stop = static_cast<cudaEvent_t>(stop_event);
+  return KV_OK;
+}
+
+kv_status kv_pool_set_wait_limit(kv_pool* p, uint64_t limit_ns) {
+  if (!p || limit_ns < 100000ull || limit_ns > 10000000000ull) return KV_ERR_INVALID_ARG;
+  p->wait_limit_ns = limit_ns;
+  return KV_OK;
+}
+
+kv_status kv_pool_set_test_stall(kv_pool* p, int32_t enable) {
+  if (!p) return KV_ERR_INVALID_ARG;
+  p->stall_tx = enable ? 16u : 0u;
   return KV_OK;
 }
 

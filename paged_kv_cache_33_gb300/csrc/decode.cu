@@ -318,6 +318,9 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
   bool idone = false;
   int next_phys[BPU];
   uint32_t bad_stages = 0, tma_stages = 0;  // bad: bit s * BPU + i for block i of stage s
+  // test hook: the first copy of worker 0 expects more bytes than it brings,
+  // so its (bounded) wait runs out
+  uint32_t stall = worker == 0 ? p.stall_tx : 0u;
   auto next_segment = [&]() {
     const int t = atomicAdd(p.ticket, 1);
     if (t >= sp.Nc) {
@@ -359,7 +362,8 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
     tma_stages |= 1u << s;
     info[s] = StageInfo{iu, ic.b, ic.h, ic.k, iu_end, iseg};
     const uint32_t dst = smem_addr(ring + s * G::kStageBytes);
-    mbar_arrive_expect_tx(bar, nload * G::kBlockBytes);
+    mbar_arrive_expect_tx(bar, nload * G::kBlockBytes + stall);
+    stall = 0;
 #pragma unroll
     for (int i = 0; i < BPU; ++i) {
       if (phys[i] == -2) continue;
@@ -727,6 +731,9 @@ __global__ void __launch_bounds__(512) paged_decode_reduce_kernel(const DecodePa
   const int cnt = meta.y;
   if (cnt <= 1) return;  // finished by the one warp that held it
   const int64_t slot0 = static_cast<int64_t>(meta.x) + pair;
+  // a pair whose record was never written (its first segment's warp gave up
+  // on a wait) can hold anything: stay inside the workspace
+  if (meta.x < 0 || slot0 + cnt > p.num_slots) return;
   float M = -INFINITY, L = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int k0 = ks; k0 < cnt; k0 += 4 * KS) {

@@ -20,6 +20,8 @@ struct kv_pool {
   CUtensorMap tmap;            // pool viewed as [NB*Hkv][2][BS][D] for TMA
   CUtensorMap tmap_rows;       // bf16 pools: the same view, boxes of one tile (K or V)
   int32_t partition_blocks = 0;  // 0 = automatic
+  uint64_t wait_limit_ns = 1000000000ull;  // bound of every wait in the kernels
+  uint32_t stall_tx = 0;       // test hook (kv_pool_set_test_stall)
   cudaEvent_t ev_start = nullptr, ev_stop = nullptr;  // optional timing hook
 };
 
@@ -53,8 +55,10 @@ struct DecodeParams {
   int64_t num_blocks;
   int32_t mbs, batch, n_q_heads, n_kv_heads, group;
   int32_t max_ctx, window, num_workers;
+  int64_t num_slots;            // partial slots in the workspace (bounds the reduce's reads)
   float scale_log2;             // softmax scale * log2(e)
   uint64_t wait_limit_ns;
+  uint32_t stall_tx;            // test hook: extra bytes expected by worker 0's first copy
 };
 
 // Geometry of one call.
@@ -64,6 +68,7 @@ struct DecodePlan {
   int32_t batch;         // sequences per launch (<= kMaxDecodeBatch)
   size_t part_o_bytes, part_ml_bytes, meta_bytes;
   size_t workspace_bytes;
+  int64_t num_slots;
 };
 
 DecodePlan plan_decode(const kv_pool* pool, int32_t batch, int32_t n_q_heads,

@@ -80,6 +80,8 @@ def load() -> ctypes.CDLL:
                                                          c.c_int32, P, P]),
             "kv_pool_set_partition_blocks": (c.c_int, [P, c.c_int32]),
             "kv_pool_set_timing_events": (c.c_int, [P, P, P]),
+            "kv_pool_set_wait_limit": (c.c_int, [P, c.c_uint64]),
+            "kv_pool_set_test_stall": (c.c_int, [P, c.c_int32]),
             "kv_pool_check_status": (c.c_int, [P, P]),
             "kv_status_str": (c.c_char_p, [c.c_int]),
             "kv_bm_create": (c.c_int, [c.c_int64, c.c_int32, c.POINTER(P)]),
@@ -222,6 +224,15 @@ class KVPool:
         _check(load().kv_pool_set_timing_events(self.handle, ctypes.c_void_p(start.cuda_event),
                                                 ctypes.c_void_p(stop.cuda_event)), "timing")
         self._events = (start, stop)
+
+    def set_wait_limit(self, limit_ns: int) -> None:
+        """Bound of every wait in this pool's kernels (ns of wall time)."""
+        _check(load().kv_pool_set_wait_limit(self.handle, int(limit_ns)), "kv_pool_set_wait_limit")
+
+    def set_test_stall(self, enable: bool) -> None:
+        """Test instrumentation: make one copy's wait run out in each decode."""
+        _check(load().kv_pool_set_test_stall(self.handle, 1 if enable else 0),
+               "kv_pool_set_test_stall")
 
     def check_status(self, stream=None) -> int:
         """Read and clear the device error word; returns the status code."""

@@ -73,6 +73,8 @@ def test_null_handles_are_rejected():
     assert L.paged_decode_workspace_bytes(None, 1, 8, 64, 0) == 0
     assert L.kv_pool_check_status(None, None) == 1
     assert L.kv_pool_set_partition_blocks(None, 8) == 1
+    assert L.kv_pool_set_wait_limit(None, 1000000) == 1
+    assert L.kv_pool_set_test_stall(None, 1) == 1
 
 
 def test_create_without_a_device_fails_cleanly():
