@@ -16,8 +16,7 @@
 //    units per sequence), so any unit is located by a binary search.
 //  * A persistent grid splits the list into segments: each warp streams a
 //    static share of the first ~75% of the units, then takes chunks of the
-//    rest from an atomic ticket counter -- 16 units, then 8, then 4 towards
-//    the end.  SMs do not all stream at the same rate; the dynamic tail lets
+//    rest from an atomic ticket counter, smaller and smaller towards the end.  SMs do not all stream at the same rate; the dynamic tail lets
 //    fast warps absorb the difference, so the grid finishes together.
 //  * Each warp streams its segments through a private ring of STAGES shared
 //    memory stages without draining between them: lane 0 resolves the next
@@ -66,15 +65,26 @@ constexpr uint64_t kShortWaitNs = 200000;  // wait bound once some warp has time
 #ifndef PKV_DYN_PCT
 #define PKV_DYN_PCT 25
 #endif
-#ifndef PKV_CHUNK_MAX
-#define PKV_CHUNK_MAX 16
+// The dynamic part is cut into four regions of decreasing chunk size: the
+// first three take kPlan.pct of it, the last region the rest.
+#ifndef PKV_C0
+#define PKV_C0 16
+#define PKV_C1 8
+#define PKV_C2 4
+#define PKV_C3 4
+#endif
+#ifndef PKV_P0
+#define PKV_P0 60
+#define PKV_P1 30
+#define PKV_P2 10
 #endif
 constexpr int kDynNum = PKV_DYN_PCT, kDynDen = 100;  // dynamic share of the units
-// The dynamic part is cut into three regions of decreasing chunk size:
-// 60% in chunks of kChunkMax units, 30% in chunks of kChunkMax/2, the rest
-// in chunks of kChunkMax/4.
-constexpr int kChunkMax = PKV_CHUNK_MAX;   // region r uses chunks of kChunkMax >> r units
-constexpr int kRegion0Pct = 60, kRegion1Pct = 30;
+struct ChunkPlan {
+  int c[4];    // units per chunk in each region
+  int pct[3];  // share of the dynamic units in regions 0..2
+};
+constexpr ChunkPlan kPlan = {{PKV_C0, PKV_C1, PKV_C2, PKV_C3}, {PKV_P0, PKV_P1, PKV_P2}};
+constexpr int kC0 = kPlan.c[0], kC1 = kPlan.c[1], kC2 = kPlan.c[2], kC3 = kPlan.c[3];
 
 struct SeqRange {
   int32_t lo, ctx, first_blk, nblk, nunit;
@@ -156,43 +166,50 @@ struct Cursor {
 
 // The segments of one launch.  Static shares are [floor(w Ts / Ps),
 // floor((w+1) Ts / Ps)) for w < Ps; then chunk region r starts at unit
-// Ts, start1, start2 with chunks of kChunkMax, /2, /4 units, their first chunks being
-// tickets 0, ticket1, ticket2.  Segment ids: shares 0..Ps-1, then Ps + ticket.
+// start[r] (start[0] = Ts) with chunks of kC<r> units, its first chunk being
+// ticket[r] (ticket[0] = 0).  Segment ids: shares 0..Ps-1, then Ps + ticket.
 struct Split {
   int T, Ts, Ps, Nc;
-  int start1, start2;      // first units of chunk regions 1 and 2 (region 0 starts at Ts)
-  int ticket1, ticket2;    // first tickets of regions 1 and 2
+  int start1, start2, start3;     // first units of chunk regions 1..3
+  int ticket1, ticket2, ticket3;  // first tickets of regions 1..3
 
   __device__ void init(int total, int P) {
     T = total;
     const int Td = T >= 8 * P ? static_cast<int>(static_cast<int64_t>(T) * kDynNum / kDynDen) : 0;
     Ts = T - Td;
     Ps = min(P, Ts);
-    const int r0 = Td * kRegion0Pct / 100 / kChunkMax * kChunkMax;
-    const int r1 = Td * kRegion1Pct / 100 / (kChunkMax >> 1) * (kChunkMax >> 1);
+    const int r0 = Td * kPlan.pct[0] / 100 / kC0 * kC0;
+    const int r1 = Td * kPlan.pct[1] / 100 / kC1 * kC1;
+    const int r2 = Td * kPlan.pct[2] / 100 / kC2 * kC2;
     start1 = Ts + r0;
     start2 = start1 + r1;
-    ticket1 = r0 / kChunkMax;
-    ticket2 = ticket1 + r1 / (kChunkMax >> 1);
-    Nc = ticket2 + (T - start2 + (kChunkMax >> 2) - 1) / (kChunkMax >> 2);
+    start3 = start2 + r2;
+    ticket1 = r0 / kC0;
+    ticket2 = ticket1 + r1 / kC1;
+    ticket3 = ticket2 + r2 / kC2;
+    Nc = ticket3 + (T - start3 + kC3 - 1) / kC3;
   }
   __device__ int seg_of(int u) const {
     if (u < Ts) return static_cast<int>((static_cast<int64_t>(u + 1) * Ps - 1) / Ts);
-    if (u < start1) return Ps + (u - Ts) / kChunkMax;
-    if (u < start2) return Ps + ticket1 + (u - start1) / (kChunkMax >> 1);
-    return Ps + ticket2 + (u - start2) / (kChunkMax >> 2);
+    if (u < start1) return Ps + (u - Ts) / kC0;
+    if (u < start2) return Ps + ticket1 + (u - start1) / kC1;
+    if (u < start3) return Ps + ticket2 + (u - start2) / kC2;
+    return Ps + ticket3 + (u - start3) / kC3;
   }
   // [first, end) units of dynamic chunk `t` (t < Nc)
   __device__ void chunk(int t, int& first, int& end) const {
     if (t < ticket1) {
-      first = Ts + t * kChunkMax;
-      end = min(start1, first + kChunkMax);
+      first = Ts + t * kC0;
+      end = min(start1, first + kC0);
     } else if (t < ticket2) {
-      first = start1 + (t - ticket1) * (kChunkMax >> 1);
-      end = min(start2, first + (kChunkMax >> 1));
+      first = start1 + (t - ticket1) * kC1;
+      end = min(start2, first + kC1);
+    } else if (t < ticket3) {
+      first = start2 + (t - ticket2) * kC2;
+      end = min(start3, first + kC2);
     } else {
-      first = start2 + (t - ticket2) * (kChunkMax >> 2);
-      end = min(T, first + (kChunkMax >> 2));
+      first = start3 + (t - ticket3) * kC3;
+      end = min(T, first + kC3);
     }
   }
 };
@@ -901,11 +918,11 @@ int decode_blocks_per_unit(const kv_pool* pool) {
 // also takes what the rounding of the first two left over.
 int64_t decode_max_chunks(int64_t max_units) {
   const int64_t td = max_units * kDynNum / kDynDen;
-  const int64_t c0 = kChunkMax, c1 = kChunkMax >> 1, c2 = kChunkMax >> 2;
-  const int64_t r0 = td * kRegion0Pct / 100 / c0 * c0;
-  const int64_t r1 = td * kRegion1Pct / 100 / c1 * c1;
-  const int64_t rest = td * (100 - kRegion0Pct - kRegion1Pct) / 100 + c0 + c1;
-  return r0 / c0 + r1 / c1 + (rest + c2 - 1) / c2 + 1;
+  const int64_t r0 = td * kPlan.pct[0] / 100 / kC0 * kC0;
+  const int64_t r1 = td * kPlan.pct[1] / 100 / kC1 * kC1;
+  const int64_t r2 = td * kPlan.pct[2] / 100 / kC2 * kC2;
+  const int64_t rest = td * (100 - kPlan.pct[0] - kPlan.pct[1] - kPlan.pct[2]) / 100 + kC0 + kC1 + kC2;
+  return r0 / kC0 + r1 / kC1 + r2 / kC2 + (rest + kC3 - 1) / kC3 + 1;
 }
 
 cudaError_t launch_decode(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream,
