@@ -76,8 +76,9 @@ def measured_peaks() -> dict:
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
 def kernel_source_sha() -> str:
@@ -361,13 +362,13 @@ def measure_extras(step: Step, peaks: dict, device) -> dict:
         out=pout), 20)
     flops = 4.0 * 128 * hq * B * (ctx * (ctx + 1) // 2)   # QK and PV over the causal keys
     tf = flops / t / 1e12
-    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
+    bf16_peak = peaks["bf16_tflops"]
     out["paged_prefill_attention"] = {
         "workload": f"full causal prefill, {B} x {ctx} tokens, {hq} q / {hkv} KV heads, "
                     "head_dim 128, 16-token blocks",
         "us_per_call": t * 1e6, "achieved": tf, "unit": "TFLOP/s", "bound": "tensor",
         "peak": bf16_peak, "frac": tf / bf16_peak, "flops_per_call": flops,
-        "peak_source": "MEASURED_PEAKS.json bf16_tflops (cuBLAS burst)"}
+        "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"}
     if ppool.check_status() != pk.KV_OK or step.pool.check_status() != pk.KV_OK:
         raise RuntimeError("device error in the extra measurements")
     ppool.destroy()
