@@ -79,7 +79,21 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.z, h = blockIdx.y;
+  // Heavy tiles first, in groups: the 1-D grid takes the (sequence, KV head)
+  // pairs four at a time and, inside a group, walks the query-tile index
+  // from the last (the most keys under the causal mask) down with the pairs
+  // fastest.  The block scheduler then starts every group's longest CTAs
+  // first, so short CTAs fill the end of the grid, while the CTAs running at
+  // once still share the K/V of only a few pairs in L2.
+  constexpr int kGroupPairs = 4;
+  const int pairs = p.n_kv_heads * p.batch;
+  const int nx = static_cast<int>(gridDim.x) / pairs;
+  const int grp = static_cast<int>(blockIdx.x) / (kGroupPairs * nx);
+  const int r = static_cast<int>(blockIdx.x) - grp * kGroupPairs * nx;
+  const int kc = min(kGroupPairs, pairs - grp * kGroupPairs);  // pairs in this group
+  const int qx = nx - 1 - r / kc;
+  const int hb = grp * kGroupPairs + r % kc;
+  const int b = hb / p.n_kv_heads, h = hb - b * p.n_kv_heads;
   const int Gp = p.group_pow2, g = p.group;
   const int tpt = kRows / Gp;  // query tokens per tile
 
@@ -88,10 +102,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   const int32_t qn = p.cu_q_lens[b + 1] - q0;
   const int32_t ctx = p.context_lens[b];
   if (qn < 0 || qn > ctx || ctx > p.max_ctx || static_cast<int64_t>(ctx) > static_cast<int64_t>(p.mbs) * BS) {
-    if (qn != 0 && blockIdx.x == 0 && h == 0 && tid == 0) atomicOr(p.err, kErrBadContext);
+    if (qn != 0 && qx == 0 && h == 0 && tid == 0) atomicOr(p.err, kErrBadContext);
     return;
   }
-  const int tok0 = blockIdx.x * (kTiles * tpt);
+  const int tok0 = qx * (kTiles * tpt);
   if (tok0 >= qn) return;
   const int pos_base = ctx - qn;  // position of new token 0
   // tile t holds tokens tok0 + t * tpt .. (ntok[t] of them; tile 1 may be empty)
@@ -414,7 +428,10 @@ int prefill_smem_bytes() { return kSmemBytes; }
 cudaError_t launch_prefill(const kv_pool* pool, const PrefillParams& p, int32_t max_q_len,
                            cudaStream_t stream) {
   const int tok_per_cta = kTiles * (kRows / p.group_pow2);
-  const dim3 grid((max_q_len + tok_per_cta - 1) / tok_per_cta, p.n_kv_heads, p.batch);
+  const int64_t ntiles = (max_q_len + tok_per_cta - 1) / tok_per_cta;
+  const int64_t ctas = ntiles * p.n_kv_heads * p.batch;
+  if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(ctas));
   if (pool->block_size == 32) {
     if (!smem_opt_in<32>()) return cudaErrorInvalidValue;
     paged_prefill_kernel<32><<<grid, kThreads, kSmemBytes, stream>>>(pool->tmap_rows, p);
