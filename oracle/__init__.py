@@ -1,7 +1,7 @@
 """Oracle for the paged KV cache decode path -- TEST INFRASTRUCTURE ONLY.
 
 A plain single-threaded C++ restatement (fp64 for the attention) of what the
-pages compute: the bf16 / FP8-E4M3 formats, the paged KV write, paged decode
+pages compute: the bf16 / FP8-E4M3 / FP4-E2M1 formats, the paged KV write, paged decode
 attention walking the block table, and the host block pool (LRU free queue,
 ref_cnt, touch, reverse-order free, chained SHA-256 hashes, lazy eviction,
 preemption).  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
@@ -69,6 +69,10 @@ def lib() -> ctypes.CDLL:
         "oracle_e4m3_to_double": (c.c_double, [c.c_uint8]),
         "oracle_e4m3_from_float": (c.c_uint8, [c.c_float]),
         "oracle_e4m3_quantize": (c.c_uint8, [c.c_uint16, c.c_float]),
+        "oracle_e2m1_to_double": (c.c_double, [c.c_uint8]),
+        "oracle_e2m1_from_float": (c.c_uint8, [c.c_float]),
+        "oracle_fp4_quantize_row": (None, [P, c.c_int32, c.c_float, P, P]),
+        "oracle_pool_block_scales": (P, [P]),
         "oracle_pool_create": (P, [c.c_int64, c.c_int32, c.c_int32, c.c_int32, c.c_int32]),
         "oracle_pool_destroy": (None, [P]),
         "oracle_pool_data": (P, [P]),
@@ -140,6 +144,24 @@ def e4m3_quantize(bf16_bits: int, scale: float) -> int:
     return int(lib().oracle_e4m3_quantize(int(bf16_bits), float(scale)))
 
 
+def e2m1_to_double(code: int) -> float:
+    return lib().oracle_e2m1_to_double(int(code))
+
+
+def e2m1_from_float(x: float) -> int:
+    return int(lib().oracle_e2m1_from_float(float(x)))
+
+
+def fp4_quantize_row(x, head_scale: float) -> tuple[np.ndarray, np.ndarray]:
+    """One row of bf16 values (length a multiple of 16) -> (E2M1 codes, E4M3 block scales)."""
+    x = _u16(x).reshape(-1)
+    n = x.shape[0]
+    codes = np.zeros(n, np.uint8)
+    scales = np.zeros(n // 16, np.uint8)
+    lib().oracle_fp4_quantize_row(_ptr(x), n, float(head_scale), _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
 # --------------------------------------------------------------------- pool --
 
 class Pool:
@@ -150,7 +172,7 @@ class Pool:
         self.num_blocks, self.block_size = int(num_blocks), int(block_size)
         self.n_kv_heads, self.head_dim = int(n_kv_heads), int(head_dim)
         self.dtype = dtype
-        code = {"bf16": 0, "fp8": 1}[dtype]
+        code = {"bf16": 0, "fp8": 1, "fp4": 2}[dtype]
         self._h = lib().oracle_pool_create(self.num_blocks, self.block_size, self.n_kv_heads,
                                            self.head_dim, code)
         if not self._h:
@@ -162,13 +184,22 @@ class Pool:
             _lib.oracle_pool_destroy(h)
 
     def array(self) -> np.ndarray:
-        """A numpy view of the pool: [NB, 2, BS, Hkv, D] of uint16 (bf16) or uint8 (e4m3)."""
+        """A numpy view of the pool: [NB, 2, BS, Hkv, D] of uint16 (bf16) or uint8
+        (an E4M3 code, or an E2M1 code in the low four bits, per element)."""
         n = lib().oracle_pool_bytes(self._h)
         buf = (ctypes.c_uint8 * n).from_address(lib().oracle_pool_data(self._h))
         a = np.frombuffer(buf, dtype=np.uint8)
         if self.dtype == "bf16":
             a = a.view(np.uint16)
         return a.reshape(self.num_blocks, 2, self.block_size, self.n_kv_heads, self.head_dim)
+
+    def block_scales(self) -> np.ndarray:
+        """FP4 pools: the E4M3 block scales, [NB, 2, BS, Hkv, D / 16] of uint8."""
+        assert self.dtype == "fp4"
+        n = self.num_blocks * 2 * self.block_size * self.n_kv_heads * (self.head_dim // 16)
+        buf = (ctypes.c_uint8 * n).from_address(lib().oracle_pool_block_scales(self._h))
+        return np.frombuffer(buf, dtype=np.uint8).reshape(
+            self.num_blocks, 2, self.block_size, self.n_kv_heads, self.head_dim // 16)
 
     def set_scales(self, k_scale, v_scale) -> None:
         ks = np.ascontiguousarray(k_scale, dtype=np.float32)

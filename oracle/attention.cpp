@@ -18,7 +18,10 @@
 //  * Number formats: bfloat16 is the upper 16 bits of an IEEE-754 binary32;
 //    FP8 E4M3 follows the OCP 8-bit floating point specification (1 sign,
 //    4 exponent bits with bias 7, 3 mantissa bits, no infinities, NaN is
-//    S.1111.111, largest finite magnitude 448, subnormal step 2^-9).
+//    S.1111.111, largest finite magnitude 448, subnormal step 2^-9).  FP4
+//    E2M1 is the element format of the OCP Microscaling (MX) specification
+//    (1 sign, 2 exponent bits with bias 1, 1 mantissa bit, no infinities or
+//    NaN; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6).
 //
 // Readings where the pages are silent (each one is listed in the design
 // notes): the query attends to positions [lo, ctx) with ctx counting the
@@ -26,6 +29,10 @@
 // query head hq uses KV head floor(hq / (Hq/Hkv)); a sequence with nothing to
 // attend to yields zeros; FP8 values carry one fp32 scale per KV head for K and
 // one for V, with value = code * scale and code = E4M3(float(x) / scale).
+// FP4 (the pages name it only as a format on its way to becoming standard)
+// takes NVIDIA's NVFP4 arrangement: every 16 consecutive head_dim elements of
+// a token's K or V row share one E4M3 block scale, on top of the per-KV-head
+// fp32 scale G; see oracle_fp4_quantize_row.
 
 #include "oracle.h"
 
@@ -97,12 +104,65 @@ extern "C" uint8_t oracle_e4m3_quantize(uint16_t bf16_bits, float scale) {
   return oracle_e4m3_from_float(q);
 }
 
+extern "C" double oracle_e2m1_to_double(uint8_t code) {
+  const int s = (code >> 3) & 1;
+  const int e = (code >> 1) & 0x3;
+  const int m = code & 0x1;
+  // normal: (1 + m/2) * 2^(e-1) = (2 + m) * 2^(e-2); subnormal (e = 0): m * 0.5.
+  double v = (e == 0) ? 0.5 * m : std::ldexp(static_cast<double>(2 + m), e - 2);
+  return s ? -v : v;
+}
+
+extern "C" uint8_t oracle_e2m1_from_float(float x) {
+  if (std::isnan(x)) return 0x0;  // the format has no NaN: a NaN input stores +0
+  const uint8_t sign = std::signbit(x) ? 0x8 : 0x0;
+  const double a = std::fabs(static_cast<double>(x));
+  if (a >= 6.0) return sign | 0x7;  // saturate (infinity included)
+  // The representable magnitudes are 0.5 * n for n = 0..4 (codes 0..3 and
+  // code 4 = 2.0) and then 3, 4, 6.  Below 2 the grid step is 0.5, from 2 to 4
+  // it is 1, from 4 to 6 it is 2; round to nearest, ties to the even code.
+  static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  int best = 0;
+  for (int c = 1; c < 8; ++c) {
+    const double dc = std::fabs(a - mag[c]), db = std::fabs(a - mag[best]);
+    if (dc < db || (dc == db && (c % 2) == 0 && (best % 2) != 0)) best = c;
+  }
+  return sign | static_cast<uint8_t>(best);
+}
+
+// One token's K or V row of n elements (n a multiple of 16) under the per-KV-
+// head scale G: for each group of 16 consecutive elements,
+//   amax  = max |x| over the group (NaN elements count as 0),
+//   sc    = E4M3(amax / (6 * G))            (binary32: t = 6 * G, then amax / t),
+//   S     = value(sc) * G                   (one binary32 product),
+//   code  = E2M1(x / S)                     (binary32 division), or +0 when S is 0,
+// so the stored value of x is e2m1(code) * e4m3(sc) * G.  6 is the largest
+// E2M1 magnitude: the group's largest element lands at the top of the grid.
+extern "C" void oracle_fp4_quantize_row(const uint16_t* x_bf16, int32_t n, float G,
+                                        uint8_t* codes, uint8_t* scales) {
+  for (int g0 = 0; g0 < n; g0 += 16) {
+    float x[16];
+    float amax = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t w = static_cast<uint32_t>(x_bf16[g0 + i]) << 16;
+      std::memcpy(&x[i], &w, sizeof(float));
+      if (!std::isnan(x[i])) amax = std::max(amax, std::fabs(x[i]));
+    }
+    const float t = 6.0f * G;
+    const uint8_t sc = oracle_e4m3_from_float(amax / t);
+    const float S = static_cast<float>(oracle_e4m3_to_double(sc)) * G;
+    scales[g0 / 16] = sc;
+    for (int i = 0; i < 16; ++i) codes[g0 + i] = (S == 0.0f) ? 0 : oracle_e2m1_from_float(x[i] / S);
+  }
+}
+
 // ------------------------------------------------------------------- pool --
 
 struct oracle_pool {
   int64_t nb;
   int32_t bs, hkv, d, dtype;
-  std::vector<uint8_t> data;
+  std::vector<uint8_t> data;          // bf16 bits, E4M3 codes or E2M1 codes (one per byte)
+  std::vector<uint8_t> block_scales;  // FP4: E4M3 scale of every 16 elements of a row
   std::vector<float> k_scale, v_scale;
 };
 
@@ -117,7 +177,8 @@ static inline uint64_t pool_index(const oracle_pool* p, int64_t blk, int kv, int
 extern "C" oracle_pool* oracle_pool_create(int64_t num_blocks, int32_t block_size,
                                            int32_t n_kv_heads, int32_t head_dim, int32_t dtype) {
   if (num_blocks <= 0 || block_size <= 0 || n_kv_heads <= 0 || head_dim <= 0) return nullptr;
-  if (dtype != 0 && dtype != 1) return nullptr;
+  if (dtype != 0 && dtype != 1 && dtype != 2) return nullptr;
+  if (dtype == 2 && head_dim % 16 != 0) return nullptr;
   oracle_pool* p = new oracle_pool;
   p->nb = num_blocks;
   p->bs = block_size;
@@ -127,6 +188,9 @@ extern "C" oracle_pool* oracle_pool_create(int64_t num_blocks, int32_t block_siz
   p->data.assign(static_cast<size_t>(num_blocks) * 2 * block_size * n_kv_heads * head_dim *
                      elem_bytes(p),
                  0);
+  if (dtype == 2)
+    p->block_scales.assign(static_cast<size_t>(num_blocks) * 2 * block_size * n_kv_heads *
+                               (head_dim / 16), 0);
   p->k_scale.assign(n_kv_heads, 1.0f);
   p->v_scale.assign(n_kv_heads, 1.0f);
   return p;
@@ -135,6 +199,15 @@ extern "C" oracle_pool* oracle_pool_create(int64_t num_blocks, int32_t block_siz
 extern "C" void oracle_pool_destroy(oracle_pool* p) { delete p; }
 extern "C" void* oracle_pool_data(oracle_pool* p) { return p->data.data(); }
 extern "C" uint64_t oracle_pool_bytes(const oracle_pool* p) { return p->data.size(); }
+extern "C" void* oracle_pool_block_scales(oracle_pool* p) {
+  return p->block_scales.empty() ? nullptr : p->block_scales.data();
+}
+
+// Block scale of row (blk, kv, off, h), elements 16 * j .. 16 * j + 15.
+static inline uint64_t scale_index(const oracle_pool* p, int64_t blk, int kv, int off, int h,
+                                   int j) {
+  return ((((static_cast<uint64_t>(blk) * 2 + kv) * p->bs + off) * p->hkv + h) * (p->d / 16)) + j;
+}
 
 extern "C" int oracle_pool_set_scales(oracle_pool* p, const float* k_scale, const float* v_scale) {
   for (int h = 0; h < p->hkv; ++h) {
@@ -163,6 +236,13 @@ extern "C" int oracle_pool_copy_blocks(oracle_pool* p, const int32_t* pairs, int
           for (int d = 0; d < p->d; ++d)
             std::memcpy(&p->data[pool_index(p, dst, kv, off, h, d) * eb],
                         &p->data[pool_index(p, src, kv, off, h, d) * eb], eb);
+    if (p->dtype == 2)
+      for (int kv = 0; kv < 2; ++kv)
+        for (int off = 0; off < p->bs; ++off)
+          for (int h = 0; h < p->hkv; ++h)
+            for (int j = 0; j < p->d / 16; ++j)
+              p->block_scales[scale_index(p, dst, kv, off, h, j)] =
+                  p->block_scales[scale_index(p, src, kv, off, h, j)];
   }
   return 0;
 }
@@ -184,6 +264,14 @@ extern "C" int oracle_kv_write(oracle_pool* p, const uint16_t* k, const uint16_t
       const uint16_t* src = (kv == 0 ? k : v) + static_cast<uint64_t>(t) * p->hkv * p->d;
       for (int h = 0; h < p->hkv; ++h) {
         const float sc = (kv == 0 ? p->k_scale : p->v_scale)[h];
+        if (p->dtype == 2) {
+          std::vector<uint8_t> codes(p->d), scales(p->d / 16);
+          oracle_fp4_quantize_row(src + h * p->d, p->d, sc, codes.data(), scales.data());
+          for (int d = 0; d < p->d; ++d) p->data[pool_index(p, blk, kv, off, h, d)] = codes[d];
+          for (int j = 0; j < p->d / 16; ++j)
+            p->block_scales[scale_index(p, blk, kv, off, h, j)] = scales[j];
+          continue;
+        }
         for (int d = 0; d < p->d; ++d) {
           const uint16_t x = src[h * p->d + d];
           const uint64_t idx = pool_index(p, blk, kv, off, h, d);
@@ -208,6 +296,9 @@ static inline double pool_value(const oracle_pool* p, int64_t blk, int kv, int o
     return oracle_bf16_to_double(x);
   }
   const double sc = static_cast<double>((kv == 0 ? p->k_scale : p->v_scale)[h]);
+  if (p->dtype == 2)
+    return oracle_e2m1_to_double(p->data[idx]) *
+           oracle_e4m3_to_double(p->block_scales[scale_index(p, blk, kv, off, h, d / 16)]) * sc;
   return oracle_e4m3_to_double(p->data[idx]) * sc;
 }
 

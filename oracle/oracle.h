@@ -2,7 +2,7 @@
  * Oracle for the paged KV cache decode path -- TEST INFRASTRUCTURE ONLY.
  *
  * A plain, slow, single-threaded CPU restatement of what the pages describe:
- *   - the bf16 and FP8-E4M3 number formats, from their definitions;
+ *   - the bf16, FP8-E4M3 and FP4-E2M1 number formats, from their definitions;
  *   - the paged KV write (each new token's K/V scattered to its slot);
  *   - paged decode attention, evaluated in fp64 by walking the block table;
  *   - the host block pool: LRU free queue, ref_cnt, touch, reverse-order
@@ -30,16 +30,24 @@ double  oracle_bf16_to_double(uint16_t bits);
 double  oracle_e4m3_to_double(uint8_t code);
 uint8_t oracle_e4m3_from_float(float x);                 /* RNE, saturate to +-448 */
 uint8_t oracle_e4m3_quantize(uint16_t bf16_bits, float scale); /* e4m3(float(x)/scale) */
+double  oracle_e2m1_to_double(uint8_t code);             /* low 4 bits: S.EE.M */
+uint8_t oracle_e2m1_from_float(float x);                 /* RNE, saturate to +-6, NaN -> +0 */
+/* FP4 row quantization (NVFP4 arrangement): E4M3 scale per 16 elements under
+ * the per-head fp32 scale G; codes[n] (one E2M1 code per byte), scales[n/16]. */
+void    oracle_fp4_quantize_row(const uint16_t* x_bf16, int32_t n, float G,
+                                uint8_t* codes, uint8_t* scales);
 
 /* ---- host KV pool in the pages' block shape ----------------------------- */
 /* element (blk, kv, off, h, d) lives at ((((blk*2+kv)*BS+off)*Hkv+h)*D+d)  */
+/* FP4 block scale (blk, kv, off, h, j) at ((((blk*2+kv)*BS+off)*Hkv+h)*(D/16)+j) */
 typedef struct oracle_pool oracle_pool;
 oracle_pool* oracle_pool_create(int64_t num_blocks, int32_t block_size,
                                 int32_t n_kv_heads, int32_t head_dim,
-                                int32_t dtype /* 0 bf16, 1 e4m3 */);
+                                int32_t dtype /* 0 bf16, 1 e4m3, 2 e2m1 + block scales */);
 void     oracle_pool_destroy(oracle_pool* p);
 void*    oracle_pool_data(oracle_pool* p);
 uint64_t oracle_pool_bytes(const oracle_pool* p);
+void*    oracle_pool_block_scales(oracle_pool* p);       /* FP4 only, else NULL */
 int      oracle_pool_set_scales(oracle_pool* p, const float* k_scale, const float* v_scale);
 
 /* Copy every K and V row of block pairs[2i] into block pairs[2i+1] (both
