@@ -49,6 +49,9 @@ DESCRIPTIONS = {
     "fp8": "FP8-E4M3 KV decode: batch 256, 32 q / 8 KV heads, head_dim 128, ctx U[1,16384], "
            "per-KV-head scales, block tables from the host block manager after 10k seeded "
            "alloc/free steps at 95% occupancy",
+    "fp4": "FP4-E2M1 KV decode (E4M3 scale per 16 elements, per-KV-head scales): batch 256, "
+           "32 q / 8 KV heads, head_dim 128, ctx U[1,16384], block tables from the host block "
+           "manager after 10k seeded alloc/free steps at 95% occupancy",
 }
 
 
@@ -57,7 +60,8 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="8b", choices=["tiny", "8b", "70b", "sw", "fp8", "long"])
+    ap.add_argument("--config", default="8b",
+                    choices=["tiny", "8b", "70b", "sw", "fp8", "fp4", "long"])
     ap.add_argument("--block-size", type=int, default=16, choices=[16, 32],
                     help="tokens per pool block")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -178,7 +182,7 @@ class Step:
 
         self.torch, self.pk, self.w = torch, pagedkv, w
         self.pool = pagedkv.KVPool(w.num_blocks, w.block_size, w.n_kv_heads, w.head_dim, w.dtype)
-        if w.dtype == "fp8":
+        if w.dtype in ("fp8", "fp4"):
             self.pool.set_scales(torch.from_numpy(w.k_scale).to(device),
                                  torch.from_numpy(w.v_scale).to(device))
         if part_blocks:
@@ -334,8 +338,7 @@ def measure_extras(step: Step, peaks: dict, device) -> dict:
     # -- paged_kv_copy_blocks: disjoint random pairs over the whole pool
     n = min(2048, w.num_blocks // 2)
     pairs = np.random.default_rng(9).permutation(w.num_blocks)[:2 * n].astype(np.int32).reshape(n, 2)
-    elem = 2 if w.dtype == "bf16" else 1
-    blk_bytes = w.n_kv_heads * 2 * w.block_size * w.head_dim * elem
+    blk_bytes = w.n_kv_heads * w.block_size * w.kv_bytes_per_token_head()
     t = _event_time(torch, lambda: pk.paged_kv_copy_blocks(step.pool, pairs), 20)
     gbs = 2 * blk_bytes * n / t / 1e9
     out["paged_kv_copy_blocks"] = {
@@ -463,10 +466,12 @@ class OracleSampler:
         self.w = w
         self.order = np.random.default_rng(0).permutation(w.batch)
         self.pool = oracle.Pool(w.num_blocks, w.block_size, w.n_kv_heads, w.head_dim, w.dtype)
+        if w.dtype in ("fp8", "fp4"):
+            self.pool.set_scales(w.k_scale, w.v_scale)
         self.q = w.query()
         self.filled: set[int] = set()
         self.decodes = 0
-        self.elem = 2 if w.dtype == "bf16" else 1
+        self.token_bytes = w.n_kv_heads * w.kv_bytes_per_token_head()
 
     def _fill(self, b: int) -> None:
         w = self.w
@@ -491,7 +496,7 @@ class OracleSampler:
             self.pool.decode(self.q, w.block_tables, w.context_lens, w.scale, w.window, seqs=[b])
             t += time.perf_counter() - t0
             lo, ctx = w.attended_range(b)
-            done += (ctx - lo) * w.n_kv_heads * 2 * w.head_dim * self.elem
+            done += (ctx - lo) * self.token_bytes
             self.decodes += 1
             n += 1
         return done, t, n

@@ -42,6 +42,23 @@
  *    dimension), with token t of the block at code position
  *    4 * ((t % 8) / 2) + t % 2 + 2 * (t / 8) of every row; kv_pool_desc's
  *    v_layout says which.
+ *  - FP4 pools (KV_FP4_E2M1, head_dim 128) hold E2M1 codes with one E4M3
+ *    scale per 16 consecutive elements of a token's K or V row, under the
+ *    per-KV-head fp32 scale (NVIDIA's NVFP4 arrangement; the pages name FP4
+ *    only as a format coming into use, "Optimizing KV Cache ...",
+ *    "Conclusion").  Each 16-token sub-tile of a (block, KV head) is one
+ *    2304-byte record, [num_blocks][n_kv_heads][block_size / 16][2304]:
+ *    bytes [0, 1024) K codes, [1024, 2048) V codes, [2048, 2176) K scales,
+ *    [2176, 2304) V scales, permuted inside each part into the order the
+ *    decode kernel's fragments consume (v_layout 2).  Byte offsets, for token
+ *    r of the sub-tile and element d (or 16-element group b):
+ *      K codes  (r / 8) * 512 + 16 * (4 * (r % 8) + (d % 8) / 2) + 2 * (d / 16)
+ *               + (d % 16) / 8, low nibble for even d;
+ *      V codes  1024 + 16 * (32 * (d / 64) + 4 * (d % 8) + (r % 8) / 2)
+ *               + 4 * ((d / 16) % 4) + r / 8 + 2 * ((d % 16) / 8), low
+ *               nibble for even r;
+ *      K scales 2048 + 8 * r + b;   V scales 2176 + 32 * ((r % 8) / 2) + 4 * b
+ *               + r % 2 + 2 * (r / 8).
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -65,7 +82,7 @@ typedef enum {
   KV_ERR_BAD_CONTEXT = 8    /* device: context_lens[b] < 0 or above a bound  */
 } kv_status;
 
-typedef enum { KV_BF16 = 0, KV_FP8_E4M3 = 1 } kv_dtype;
+typedef enum { KV_BF16 = 0, KV_FP8_E4M3 = 1, KV_FP4_E2M1 = 2 } kv_dtype;
 
 typedef struct kv_pool kv_pool; /* opaque */
 
@@ -78,7 +95,8 @@ typedef struct {
   uint64_t bytes;         /* total pool bytes                                        */
   int32_t device;         /* CUDA device ordinal the pool lives on                   */
   float* scales_dev;      /* fp8: device float[2 * Hkv], K scales then V scales      */
-  int32_t v_layout;       /* 0: V tiles as K ([block_size][D]); 1: transposed (FP8)  */
+  int32_t v_layout;       /* 0: V tiles as K ([block_size][D]); 1: transposed (FP8); */
+                          /* 2: FP4 sub-tile records (strides not meaningful)        */
 } kv_pool_desc;
 
 /*
@@ -86,7 +104,7 @@ typedef struct {
  *   num_blocks > 0, block_size 16 or 32 (the pages' default and the larger
  *   size "Optimizing KV Cache ...", "Trade-offs of Block Size Tuning",
  *   recommends for very long contexts), n_kv_heads >= 1, head_dim in {64, 128}
- *   (FP8: head_dim 128).  The pool owns its memory (cudaMalloc here, cudaFree
+ *   (FP8 and FP4: head_dim 128).  The pool owns its memory (cudaMalloc here, cudaFree
  *   in kv_pool_destroy); its contents start undefined.  FP8 scales start at
  *   1.0.  Returns KV_ERR_INVALID_ARG / KV_ERR_UNSUPPORTED for bad shapes,
  *   KV_ERR_OOM when the allocation fails, KV_ERR_CUDA when no device works.
@@ -101,11 +119,16 @@ kv_status kv_pool_destroy(kv_pool* pool);
 kv_status kv_pool_info(const kv_pool* pool, kv_pool_desc* out);
 
 /*
- * kv_pool_set_scales -- FP8 pools: copy per-KV-head scales (device float[Hkv]
- * each) into the pool, ordered on `stream`.  A stored FP8 code c of KV head h
- * stands for c * k_scale[h] (K) or c * v_scale[h] (V); the write quantises
- * x to E4M3(float(x) / scale) with round-to-nearest-even and saturation to
- * +-448.  Scales must be finite and > 0 (not checked on the device).
+ * kv_pool_set_scales -- FP8 and FP4 pools: copy per-KV-head scales (device
+ * float[Hkv] each) into the pool, ordered on `stream`.  A stored FP8 code c of
+ * KV head h stands for c * k_scale[h] (K) or c * v_scale[h] (V); the write
+ * quantises x to E4M3(float(x) / scale) with round-to-nearest-even and
+ * saturation to +-448.  FP4: with G the head's scale, each 16-element group
+ * of a row gets the E4M3 scale sc = E4M3(amax / (6 G)) (amax over the
+ * group's non-NaN |x|) and every element the code E2M1(x / S), S = value(sc)
+ * * G (+0 when S = 0; NaN stores +0; round to nearest even, saturation to
+ * +-6; each step one binary32 operation), standing for e2m1 * value(sc) * G.
+ * Scales must be finite and > 0 (not checked on the device).
  */
 kv_status kv_pool_set_scales(kv_pool* pool, const float* k_scale_dev, const float* v_scale_dev,
                              void* stream);
@@ -118,8 +141,9 @@ kv_status kv_pool_set_scales(kv_pool* pool, const float* k_scale_dev, const floa
  *   slot_mapping_dev:    int64 [num_tokens]; slot = physical_block * block_size
  *                        + offset; slot < 0 marks a padded token (skipped);
  *                        slot >= num_blocks * block_size sets KV_ERR_BAD_SLOT.
- * BF16 pools receive a bit copy; FP8 pools the quantised codes.  Two tokens
- * with the same slot in one call is undefined.  num_tokens == 0 is a no-op.
+ * BF16 pools receive a bit copy; FP8 and FP4 pools the quantised codes (see
+ * kv_pool_set_scales).  Two tokens with the same slot in one call is
+ * undefined.  num_tokens == 0 is a no-op.
  */
 kv_status paged_kv_write(kv_pool* pool, const void* k_dev, const void* v_dev,
                          const int64_t* slot_mapping_dev, int64_t num_tokens, void* stream);

@@ -45,6 +45,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // K+V pair: 64 bf16 columns (head_dim 128 takes two boxes) or 128 E4M3
 // columns, 16 token rows, both K and V; 128-byte swizzle in shared memory.
 bool encode_pool_map(kv_pool* p) {
+  if (p->dtype == KV_FP4_E2M1) return true;  // FP4 records are staged with plain bulk copies
   auto encode = tensor_map_encoder();
   if (!encode) return false;
   const uint64_t esz = p->dtype == KV_BF16 ? 2 : 1;
@@ -146,10 +147,10 @@ kv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_he
   *out = nullptr;
   if (num_blocks <= 0 || n_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
     return KV_ERR_INVALID_ARG;
-  if (dtype != KV_BF16 && dtype != KV_FP8_E4M3) return KV_ERR_INVALID_ARG;
+  if (dtype != KV_BF16 && dtype != KV_FP8_E4M3 && dtype != KV_FP4_E2M1) return KV_ERR_INVALID_ARG;
   if (block_size != 16 && block_size != 32) return KV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return KV_ERR_UNSUPPORTED;
-  if (dtype == KV_FP8_E4M3 && head_dim != 128) return KV_ERR_UNSUPPORTED;
+  if (dtype != KV_BF16 && head_dim != 128) return KV_ERR_UNSUPPORTED;
   if (num_blocks * n_kv_heads >= (int64_t(1) << 31)) return KV_ERR_UNSUPPORTED;
 
   kv_pool* p = new (std::nothrow) kv_pool;
@@ -159,8 +160,9 @@ kv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_he
   p->n_kv_heads = n_kv_heads;
   p->head_dim = head_dim;
   p->dtype = dtype;
-  const uint64_t esz = dtype == KV_BF16 ? 2 : 1;
-  p->bytes = static_cast<uint64_t>(num_blocks) * n_kv_heads * 2 * block_size * head_dim * esz;
+  std::memset(&p->tmap, 0, sizeof p->tmap);
+  std::memset(&p->tmap_rows, 0, sizeof p->tmap_rows);
+  p->bytes = static_cast<uint64_t>(num_blocks) * pkv::block_bytes(p);
   if (cudaGetDevice(&p->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) !=
           cudaSuccess) {
@@ -224,7 +226,9 @@ kv_status kv_pool_info(const kv_pool* p, kv_pool_desc* out) {
   out->bytes = p->bytes;
   out->device = p->device;
   out->scales_dev = p->scales;
-  out->v_layout = p->dtype == KV_FP8_E4M3 ? 1 : 0;
+  out->v_layout = p->dtype == KV_FP8_E4M3 ? 1 : p->dtype == KV_FP4_E2M1 ? 2 : 0;
+  if (p->dtype == KV_FP4_E2M1)
+    for (int i = 0; i < 5; ++i) out->strides[i] = 0;
   return KV_OK;
 }
 
@@ -328,6 +332,7 @@ kv_status decode_call(kv_pool* p, const StepWrite* w, const void* q, int32_t n_q
   d.ticket = reinterpret_cast<int32_t*>(ws + plan.part_o_bytes + plan.part_ml_bytes +
                                         plan.meta_bytes - 16);
   d.err = p->err;
+  d.pool = static_cast<const uint8_t*>(p->base);
   d.k_scale = p->scales;
   d.v_scale = p->scales + p->n_kv_heads;
   d.num_blocks = p->num_blocks;

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
 #include <string.h>
@@ -90,6 +91,30 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
+}
+
+// Untiled bulk copy global -> shared, completing on an mbarrier with its byte
+// count: both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
 }
 
 // ------------------------------------------------- warp matrix operations --
@@ -326,11 +351,57 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
       __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
 }
 
+// The two E2M1 codes of the low byte of w (low nibble first) as exact f16
+// values, times a pair of f16 scales; the products of an E2M1 value and an
+// E4M3 scale are exact in f16 (at most 5 significant bits, 2^-10 .. 2688).
+__device__ __forceinline__ uint32_t fp4x2_scaled(uint32_t w, __half2 scale) {
+  const __half2_raw r =
+      __nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>(w & 0xFFu), __NV_E2M1);
+  __half2 h;
+  memcpy(&h, &r, sizeof h);
+  const __half2 v = __hmul2(h, scale);
+  uint32_t out;
+  memcpy(&out, &v, sizeof out);
+  return out;
+}
+
 // Two E4M3 codes (low byte first) to two exact f16 values (low half first).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu),
                                              __NV_E4M3);
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// ----------------------------------------------------- FP4 pool records --
+// An FP4 pool (head_dim 128) stores each 16-token sub-tile of a (block, KV
+// head) as one 2304-byte record, laid out for the decode kernel's mma.sync
+// fragments (m16n8k16; lane = 4 n + j, n = lane / 4, j = lane % 4), so each
+// lane's operands are whole 16-byte vectors:
+//   [   0, 1024) K codes: token r, dims 2i, 2i+1 share a byte (low nibble =
+//                even dim).  Lane (n, j) reads 16 bytes for token n and 16
+//                for token n + 8 holding, for k-step ks, the dims 16 ks + 2j
+//                (+1) and 16 ks + 2j + 8 (+1) it feeds the QK product.
+//   [1024, 2048) V codes: tokens 2i, 2i+1 share a byte (low nibble = even
+//                token) at one dim; lane (n, j) reads 16 bytes for m-tiles
+//                0..3 and 16 for 4..7, each word holding its A-fragment bytes
+//                (tokens 2j / 2j+8 at dims 16 mt + n and 16 mt + n + 8).
+//   [2048, 2176) K block scales: token r, 8 E4M3 codes (dims 16 b .. 16 b + 15).
+//   [2176, 2304) V block scales: for each j, a word per m-tile b holding the
+//                codes of tokens 2j, 2j+1, 2j+8, 2j+9.
+constexpr int kFp4SubBytes = 2304;
+
+__host__ __device__ constexpr int fp4_k_code_offset(int r, int d) {
+  // d even; byte holds dims d (low nibble) and d + 1
+  return (r / 8) * 512 + 16 * (4 * (r % 8) + ((d % 16) % 8) / 2) + 2 * (d / 16) + (d % 16) / 8;
+}
+__host__ __device__ constexpr int fp4_v_code_offset(int r, int d) {
+  // byte holds tokens r & ~1 (low nibble) and r | 1 at dim d
+  return 1024 + 16 * ((d / 64) * 32 + 4 * (d % 8) + (r % 8) / 2) + 4 * ((d / 16) % 4) + r / 8 +
+         2 * ((d % 16) / 8);
+}
+__host__ __device__ constexpr int fp4_k_scale_offset(int r, int b) { return 2048 + 8 * r + b; }
+__host__ __device__ constexpr int fp4_v_scale_offset(int r, int b) {
+  return 2176 + 32 * ((r % 8) / 2) + 4 * b + r % 2 + 2 * (r / 8);
 }
 
 }  // namespace pkv

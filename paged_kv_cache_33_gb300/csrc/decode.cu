@@ -115,19 +115,25 @@ __device__ __forceinline__ bool ctx_ok(const DecodeParams& p, int32_t ctx) {
 // FP8: one box of [K rows (128 codes) | the transposed V tile seen as BS
 //      rows of 128 bytes: BS/16 sub-tiles of [D][16] codes].
 // The compute side walks the unit in sub-tiles of 16 tokens.
-template <int D, bool FP8, int BS, int BPU>
+// Element formats of the pool.
+constexpr int kBf16 = 0, kFp8 = 1, kFp4 = 2;
+
+template <int D, int KIND, int BS, int BPU>
 struct Geometry {
+  static constexpr bool FP8 = KIND == kFp8, FP4 = KIND == kFp4;
   static constexpr int kElem = FP8 ? 1 : 2;
   static constexpr int kRowBytes = 128;                         // one swizzled smem row
   static constexpr int kBoxes = FP8 ? 1 : D / 64;               // TMA boxes per block
   static constexpr int kBoxBytes = 2 * BS * kRowBytes;
-  static constexpr int kBlockBytes = kBoxes * kBoxBytes;
-  static constexpr int kStageBytes = BPU * kBlockBytes;
   static constexpr int kSubPerBlock = BS / 16;
+  // FP4: the block's BS/16 sub-tile records, one bulk copy
+  static constexpr int kBlockBytes = FP4 ? kSubPerBlock * kFp4SubBytes : kBoxes * kBoxBytes;
+  static constexpr int kStageBytes = BPU * kBlockBytes;
   static constexpr int kSub = BPU * kSubPerBlock;               // 16-token sub-tiles per unit
   static constexpr int kSteps = D / 16;                         // k-steps (QK) = m-tiles (PV)
-  static_assert(kBlockBytes == 2 * BS * D * kElem, "a block is one K and one V tile");
-  static_assert(!FP8 || D == 128, "FP8 rows are one 128-byte swizzle row");
+  static_assert(FP4 || kBlockBytes == 2 * BS * D * kElem, "a block is one K and one V tile");
+  static_assert(KIND == kBf16 || D == 128, "FP8 rows are one 128-byte swizzle row; FP4 records hold D = 128");
+  static_assert(kStageBytes % 16 == 0, "bulk copies land on 16-byte boundaries");
   static_assert(kBoxBytes % 1024 == 0, "boxes keep the 1024-byte swizzle alignment");
   // byte offsets inside a stage of sub-tile `sub`: K row 0 of box 0, and
   // (bf16) V row 0 of box 0 or (FP8) the first row of the transposed V
@@ -140,6 +146,10 @@ struct Geometry {
     return FP8 ? (sub / kSubPerBlock) * kBlockBytes + BS * kRowBytes + (sub % kSubPerBlock) * 16 * D
                : k_off(sub) + BS * kRowBytes;
   }
+  // FP4: the record of sub-tile `sub`
+  __device__ static constexpr int rec_off(int sub) {
+    return (sub / kSubPerBlock) * kBlockBytes + (sub % kSubPerBlock) * kFp4SubBytes;
+  }
 };
 
 // Coordinates of the unit held by one ring stage (u < 0: no unit).
@@ -147,9 +157,9 @@ struct StageInfo {
   int32_t u, b, h, k, seg_end, seg;
 };
 
-template <int D, bool FP8, int BS, int BPU, int NW, int STAGES>
+template <int D, int KIND, int BS, int BPU, int NW, int STAGES>
 struct Smem {
-  static constexpr int kRing = NW * STAGES * Geometry<D, FP8, BS, BPU>::kStageBytes;
+  static constexpr int kRing = NW * STAGES * Geometry<D, KIND, BS, BPU>::kStageBytes;
   static constexpr int kBars = kRing;                          // uint64 [NW][STAGES]
   static constexpr int kInfo = kBars + NW * STAGES * 8;        // StageInfo [NW][STAGES]
   static constexpr int kCtx = kInfo + NW * STAGES * 24;        // int32 [kMaxDecodeBatch]
@@ -214,11 +224,12 @@ struct Split {
   }
 };
 
-template <int D, bool FP8, int BS, int BPU, int NW, int STAGES>
+template <int D, int KIND, int BS, int BPU, int NW, int STAGES>
 __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kernel(
     const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
-  using G = Geometry<D, FP8, BS, BPU>;
-  using S = Smem<D, FP8, BS, BPU, NW, STAGES>;
+  using G = Geometry<D, KIND, BS, BPU>;
+  using S = Smem<D, KIND, BS, BPU, NW, STAGES>;
+  constexpr bool FP8 = G::FP8, FP4 = G::FP4;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment of the stage buffers keeps the 128-byte swizzle
   // pattern equal to (row mod 8).
@@ -386,9 +397,13 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
       if (phys[i] == -2) continue;
       const int tile = phys[i] * p.n_kv_heads + ic.h;
       const uint32_t bdst = dst + i * G::kBlockBytes;
+      if constexpr (FP4) {
+        bulk_load(bdst, p.pool + static_cast<int64_t>(tile) * G::kBlockBytes, G::kBlockBytes, bar);
+      } else {
 #pragma unroll
-      for (int bx = 0; bx < G::kBoxes; ++bx)
-        tma_load_4d(bdst + bx * G::kBoxBytes, &tmap, bar, bx * 64, 0, 0, tile);
+        for (int bx = 0; bx < G::kBoxes; ++bx)
+          tma_load_4d(bdst + bx * G::kBoxBytes, &tmap, bar, bx * 64, 0, 0, tile);
+      }
     }
     // step to the next unit: within the segment, or the next chunk
     if (++iu < iu_end) {
@@ -450,12 +465,33 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
     if (si.u != prev_u + 1 || si.k == 0) {
       // ---- a new piece of a (b, h) pair: its query fragments, a fresh state
       const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) + row0 * D;
-      if constexpr (!FP8) {
+      if constexpr (KIND == kBf16) {
         const uint32_t* qr = reinterpret_cast<const uint32_t*>(qg + n * D);
 #pragma unroll
         for (int ks = 0; ks < G::kSteps; ++ks) {
           qf[ks][0] = n < g ? qr[(ks * 16 + 2 * j) >> 1] : 0u;
           qf[ks][1] = n < g ? qr[(ks * 16 + 8 + 2 * j) >> 1] : 0u;
+        }
+      } else if constexpr (FP4) {
+        // f16 operands (the dequantised FP4 keys are exact in f16): scale the
+        // group's queries by a power of two that puts the largest below
+        // 2^15, which keeps every bf16 query exact, and fold it back into the
+        // score scale with the head's K scale.
+        float amax = 0.f;
+        for (int i = lane; i < g * D; i += 32) amax = fmaxf(amax, fabsf(__bfloat162float(qg[i])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+        int e = 0;
+        if (amax > 0.f) frexpf(amax, &e);
+        const float qs = ldexpf(1.f, 15 - e);  // amax * qs < 2^15
+        score_scale = p.scale_log2 * p.k_scale[si.h] * ldexpf(1.f, e - 15);
+        const uint32_t* qr = reinterpret_cast<const uint32_t*>(qg + n * D);
+#pragma unroll
+        for (int ks = 0; ks < G::kSteps; ++ks) {
+          const uint32_t w0 = n < g ? qr[(ks * 16 + 2 * j) >> 1] : 0u;
+          const uint32_t w1 = n < g ? qr[(ks * 16 + 8 + 2 * j) >> 1] : 0u;
+          qf[ks][0] = pack_f16x2(bf16_lo(w0) * qs, bf16_hi(w0) * qs);
+          qf[ks][1] = pack_f16x2(bf16_lo(w1) * qs, bf16_hi(w1) * qs);
         }
       } else {
         // E4M3 operands: scale the group's queries by an exact power of two
@@ -519,9 +555,41 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
 
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t vf[G::kSteps][4];
+      uint4 vq[4];  // FP4: this lane's V code words (m-tiles 0-3, 4-7) and V scale words
       if (live) {
         // ---- S^T = K Q^T : rows = 16 tokens, cols = 8 query heads
-        if constexpr (!FP8) {
+        if constexpr (FP4) {
+          // Dequantise the lane's K fragments exactly into f16: code value
+          // times its E4M3 block scale (a k-step's 16 dimensions are one
+          // scale group).  Tokens n and n + 8; the record puts each lane's
+          // bytes in one 16-byte vector per token.
+          const uint32_t rec = st + G::rec_off(sub);
+          const uint4 kc0 = lds128(rec + 16 * lane), kc1 = lds128(rec + 512 + 16 * lane);
+          const uint2 kq0 = lds64(rec + 2048 + 8 * n), kq1 = lds64(rec + 2048 + 64 + 8 * n);
+          const uint32_t kw0[4] = {kc0.x, kc0.y, kc0.z, kc0.w};
+          const uint32_t kw1[4] = {kc1.x, kc1.y, kc1.z, kc1.w};
+          const uint32_t kq[2][2] = {{kq0.x, kq0.y}, {kq1.x, kq1.y}};
+#pragma unroll
+          for (int ks = 0; ks < G::kSteps; ++ks) {
+            // scales of group ks for tokens n and n + 8, in both halves
+            const __half2 p0 = u32_as_half2(e4m3x2_to_f16x2(kq[0][ks >> 2] >> (16 * ((ks >> 1) & 1))));
+            const __half2 p1 = u32_as_half2(e4m3x2_to_f16x2(kq[1][ks >> 2] >> (16 * ((ks >> 1) & 1))));
+            const __half2 c0 = (ks & 1) ? __high2half2(p0) : __low2half2(p0);
+            const __half2 c1 = (ks & 1) ? __high2half2(p1) : __low2half2(p1);
+            const uint32_t w0 = kw0[ks >> 1] >> (16 * (ks & 1)), w1 = kw1[ks >> 1] >> (16 * (ks & 1));
+            const uint32_t a0 = fp4x2_scaled(w0, c0), a2 = fp4x2_scaled(w0 >> 8, c0);
+            const uint32_t a1 = fp4x2_scaled(w1, c1), a3 = fp4x2_scaled(w1 >> 8, c1);
+            if (ks & 1)
+              mma_f16(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            else
+              mma_f16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+          }
+          // V code and scale words, kept raw until the product
+          vq[0] = lds128(rec + 1024 + 16 * lane);
+          vq[1] = lds128(rec + 1536 + 16 * lane);
+          vq[2] = lds128(rec + 2176 + 32 * j);
+          vq[3] = lds128(rec + 2176 + 32 * j + 16);
+        } else if constexpr (!FP8) {
 #pragma unroll
           for (int ks = 0; ks < G::kSteps; ++ks) {
             const int chunk = ((ks & 3) << 1) + (lane >> 4);
@@ -548,7 +616,8 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
           }
         }
         // ---- V fragments to registers
-        if constexpr (!FP8) {
+        if constexpr (FP4) {
+        } else if constexpr (!FP8) {
           const int trow_v = (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
           for (int mt = 0; mt < G::kSteps; ++mt) {
@@ -616,7 +685,31 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
       m_run[1] = mn1;
 
       // ---- O^T += V^T P^T : rows = head_dim, cols = 8 query heads, k = 16 tokens
-      if constexpr (!FP8) {
+      if constexpr (FP4) {
+        // P in f16 (11 significant bits); V^T fragments dequantised exactly
+        // into f16 per m-tile: word mt of the codes holds tokens (2j, 2j+1)
+        // and (2j+8, 2j+9) at dims 16 mt + n and 16 mt + n + 8, word mt of
+        // the scales those four tokens' group-mt scales.
+        const uint32_t b0 = movmatrix_trans(pack_f16x2(p0, p1));
+        const uint32_t b1 = movmatrix_trans(pack_f16x2(p2, p3));
+        uint32_t mlo = kFull, mhi = kFull;
+        if (!full) {
+          mlo = (tok_ok(2 * j) ? 0x0000ffffu : 0u) | (tok_ok(2 * j + 1) ? 0xffff0000u : 0u);
+          mhi = (tok_ok(2 * j + 8) ? 0x0000ffffu : 0u) | (tok_ok(2 * j + 9) ? 0xffff0000u : 0u);
+        }
+        const uint32_t vw[8] = {vq[0].x, vq[0].y, vq[0].z, vq[0].w, vq[1].x, vq[1].y, vq[1].z, vq[1].w};
+        const uint32_t sw[8] = {vq[2].x, vq[2].y, vq[2].z, vq[2].w, vq[3].x, vq[3].y, vq[3].z, vq[3].w};
+#pragma unroll
+        for (int mt = 0; mt < G::kSteps; ++mt) {
+          const __half2 s01 = u32_as_half2(e4m3x2_to_f16x2(sw[mt]));
+          const __half2 s89 = u32_as_half2(e4m3x2_to_f16x2(sw[mt] >> 16));
+          const uint32_t a0 = fp4x2_scaled(vw[mt], s01) & mlo;
+          const uint32_t a2 = fp4x2_scaled(vw[mt] >> 8, s89) & mhi;
+          const uint32_t a1 = fp4x2_scaled(vw[mt] >> 16, s01) & mlo;
+          const uint32_t a3 = fp4x2_scaled(vw[mt] >> 24, s89) & mhi;
+          mma_f16(acc[mt], a0, a1, a2, a3, b0, b1);
+        }
+      } else if constexpr (!FP8) {
         const uint32_t x01 = pack_bf16x2(p0, p1), x23 = pack_bf16x2(p2, p3);
         const uint32_t y01 = pack_bf16x2(p0 - bf16_lo(x01), p1 - bf16_hi(x01));
         const uint32_t y23 = pack_bf16x2(p2 - bf16_lo(x23), p3 - bf16_hi(x23));
@@ -674,7 +767,8 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
       const int first_seg = sp.seg_of(pair_start);
       const int cnt = sp.seg_of(pair_start + r.nunit - 1) - first_seg + 1;
       const bool whole = cnt == 1;
-      const float vsc = FP8 ? p.v_scale[si.h] * (1.f / 256.f) : 1.f;  // FP8: P was 256 p
+      // FP8: P was 256 p; FP4: the head's V scale is not in the dequantised values
+      const float vsc = FP8 ? p.v_scale[si.h] * (1.f / 256.f) : FP4 ? p.v_scale[si.h] : 1.f;
       const int h0 = 2 * j, h1 = 2 * j + 1;  // query heads of this lane's columns
       const float f0 = whole ? (l0 > 0.f ? vsc / l0 : 0.f) : vsc;
       const float f1 = whole ? (l1 > 0.f ? vsc / l1 : 0.f) : vsc;
@@ -811,9 +905,9 @@ __global__ void __launch_bounds__(512) paged_decode_reduce_kernel(const DecodePa
   *dst = make_float4(Ot.x * inv, Ot.y * inv, Ot.z * inv, Ot.w * inv);
 }
 
-template <int D, bool FP8, int BS, int BPU, int NW, int STAGES>
+template <int D, int KIND, int BS, int BPU, int NW, int STAGES>
 struct Variant {
-  static constexpr int kSmem = Smem<D, FP8, BS, BPU, NW, STAGES>::kBytes;
+  static constexpr int kSmem = Smem<D, KIND, BS, BPU, NW, STAGES>::kBytes;
   static constexpr int kWarps = NW;
   static constexpr int kBlocksPerUnit = BPU;
 
@@ -821,7 +915,7 @@ struct Variant {
   static int ctas_per_sm() {
     static int ctas = -1;
     if (ctas < 0) {
-      auto kernel = paged_decode_kernel<D, FP8, BS, BPU, NW, STAGES>;
+      auto kernel = paged_decode_kernel<D, KIND, BS, BPU, NW, STAGES>;
       int n = 0;
       if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
               cudaSuccess ||
@@ -848,7 +942,7 @@ struct Variant {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = dependent ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, FP8, BS, BPU, NW, STAGES>, pool->tmap,
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, KIND, BS, BPU, NW, STAGES>, pool->tmap,
                               p);
   }
 };
@@ -879,21 +973,27 @@ struct Variant {
 #ifndef PKV_BF16_BPU
 #define PKV_BF16_BPU 1
 #endif
-using Bf16D128 = Variant<128, false, 16, PKV_BF16_BPU, PKV_BF16_WARPS, PKV_BF16_STAGES>;
-using Bf16D64 = Variant<64, false, 16, 1, 4, 4>;
-using Fp8D128 = Variant<128, true, 16, PKV_FP8_BPU, PKV_FP8_WARPS, PKV_FP8_STAGES>;
-using Bf16D128B32 = Variant<128, false, 32, 1, PKV_BS32_WARPS, 2>;
-using Bf16D64B32 = Variant<64, false, 32, 1, 4, 2>;
-using Fp8D128B32 = Variant<128, true, 32, 1, PKV_FP8_WARPS, 2>;
+using Bf16D128 = Variant<128, kBf16, 16, PKV_BF16_BPU, PKV_BF16_WARPS, PKV_BF16_STAGES>;
+using Bf16D64 = Variant<64, kBf16, 16, 1, 4, 4>;
+using Fp8D128 = Variant<128, kFp8, 16, PKV_FP8_BPU, PKV_FP8_WARPS, PKV_FP8_STAGES>;
+using Bf16D128B32 = Variant<128, kBf16, 32, 1, PKV_BS32_WARPS, 2>;
+using Bf16D64B32 = Variant<64, kBf16, 32, 1, 4, 2>;
+using Fp8D128B32 = Variant<128, kFp8, 32, 1, PKV_FP8_WARPS, 2>;
+// FP4 records are 2304 bytes per 16 tokens: units of three 16-token blocks
+// (one 32-token block) keep ~14 KB of ring per warp, as the other variants.
+using Fp4D128 = Variant<128, kFp4, 16, 3, 4, 2>;
+using Fp4D128B32 = Variant<128, kFp4, 32, 1, 4, 3>;
 
 // Call f with the variant type the pool uses.
 template <typename F>
 auto with_variant(const kv_pool* pool, F&& f) {
   if (pool->block_size == 32) {
+    if (pool->dtype == KV_FP4_E2M1) return f(Fp4D128B32{});
     if (pool->dtype == KV_FP8_E4M3) return f(Fp8D128B32{});
     if (pool->head_dim == 128) return f(Bf16D128B32{});
     return f(Bf16D64B32{});
   }
+  if (pool->dtype == KV_FP4_E2M1) return f(Fp4D128{});
   if (pool->dtype == KV_FP8_E4M3) return f(Fp8D128{});
   if (pool->head_dim == 128) return f(Bf16D128{});
   return f(Bf16D64{});

@@ -50,7 +50,8 @@ struct DecodeParams {
   int2* pair_meta;              // [B*Hkv]  (first segment, number of segments) per pair
   int32_t* ticket;              // next dynamic chunk; zero at launch
   uint32_t* err;
-  const float* k_scale;         // fp8: [Hkv]
+  const uint8_t* pool;          // pool base (FP4 records are staged with bulk copies)
+  const float* k_scale;         // fp8 / fp4: [Hkv]
   const float* v_scale;
   int64_t num_blocks;
   int32_t mbs, batch, n_q_heads, n_kv_heads, group;
@@ -93,7 +94,8 @@ cudaError_t launch_kv_write(const kv_pool* pool, const void* k, const void* v,
 cudaError_t launch_decode(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream,
                           bool dependent);
 
-// Bytes of one physical block ([Hkv][2][16][D] elements).
+// Bytes of one physical block ([Hkv][2][BS][D] elements, or the FP4 records
+// of its Hkv x BS/16 sub-tiles).
 int64_t block_bytes(const kv_pool* pool);
 
 // Whole-block copies of host-validated (src, dst) pairs, with the result of

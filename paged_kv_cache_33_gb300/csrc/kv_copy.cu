@@ -6,8 +6,8 @@
 // shares, the block's K/V states are copied device to device into a fresh
 // block that the sequence then owns.
 //
-// A physical block is one contiguous run of the pool ([Hkv][2][16][D]), so a
-// copy is a flat move of block_bytes.  The (src, dst) pairs come from the
+// A physical block is one contiguous run of the pool ([Hkv][2][BS][D], or
+// [Hkv][BS/16] FP4 records), so a copy is a flat move of block_bytes.  The (src, dst) pairs come from the
 // host block manager; the host cuts them into waves in which no block is
 // both read and written, so every wave runs fully parallel and the result is
 // that of applying the pairs one after another.  Each wave's pairs travel in
@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(kCopyThreads) kv_copy_blocks_kernel(
 }  // namespace
 
 int64_t block_bytes(const kv_pool* pool) {
+  if (pool->dtype == KV_FP4_E2M1)
+    return static_cast<int64_t>(pool->n_kv_heads) * (pool->block_size / 16) * kFp4SubBytes;
   const int64_t elem = pool->dtype == KV_BF16 ? 2 : 1;
   return static_cast<int64_t>(pool->n_kv_heads) * 2 * pool->block_size * pool->head_dim * elem;
 }

@@ -8,9 +8,10 @@
 // (section "PagedAttention: Virtual Memory for LLMs").
 //
 // Pool layout: [num_blocks][Hkv][2][block_size][D], D contiguous (FP8 pools
-// keep each V tile transposed, in [D][16] sub-tiles).  One thread moves
-// 16 bytes of destination; consecutive threads cover one destination row, so
-// every store is a full, coalesced 16-byte vector.
+// keep each V tile transposed, in [D][16] sub-tiles; FP4 pools hold one
+// packed record per 16-token sub-tile, see fp4_*_offset).  For bf16 and FP8
+// one thread moves 16 bytes of destination; consecutive threads cover one
+// destination row, so every store is a full, coalesced 16-byte vector.
 
 #include <algorithm>
 
@@ -121,6 +122,87 @@ __global__ void __launch_bounds__(256) kv_write_fp8_kernel(
   }
 }
 
+// E2M1 code of q (low four bits S.EE.M): round to nearest, ties to the even
+// code, saturating at +-6; NaN stores +0.  The representable magnitudes are
+// 0, 0.5, 1, 1.5, 2, 3, 4, 6: the code counts the decision points below |q|,
+// a tie going to the even neighbour (>= where the upper code is even).
+__device__ __forceinline__ uint32_t e2m1_code(float q) {
+  if (isnan(q)) return 0u;
+  const float a = fabsf(q);
+  const uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
+                     (a >= 3.5f) + (a > 5.0f);
+  return m | (signbit(q) ? 8u : 0u);
+}
+
+// FP4 pool: E2M1 codes with one E4M3 scale per 16 elements of a row, under the
+// per-KV-head fp32 scale G (NVIDIA's NVFP4 arrangement):
+//   sc = E4M3(amax / (6 G)), S = value(sc) * G, code = E2M1(x / S) (+0 if S = 0),
+// every step one binary32 operation rounded to nearest even.  One warp per
+// (token, KV head, K or V) row of 128 elements; lane l holds elements
+// 4l .. 4l+3, so the four lanes of a 16-element group agree on its maximum
+// with two shuffles.  The row goes to the decode layout of its 16-token
+// sub-tile record (fp4_*_offset): K codes as bytes of two consecutive
+// dimensions, V codes as bytes of two consecutive tokens, which a warp of
+// this kernel shares with its neighbour token, so V nibbles are merged into
+// their word with atomic AND / OR.
+__global__ void __launch_bounds__(256) kv_write_fp4_kernel(
+    const uint2* __restrict__ k, const uint2* __restrict__ v, const int64_t* __restrict__ slots,
+    int64_t num_tokens, int hkv, int bs, int64_t num_slots, const float* __restrict__ scales,
+    uint8_t* __restrict__ pool, uint32_t* __restrict__ err, int32_t* __restrict__ zero_word) {
+  constexpr int D = 128;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (zero_word && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (row >= num_tokens * hkv * 2) return;
+  const int kv = static_cast<int>(row & 1);
+  const int h = static_cast<int>((row >> 1) % hkv);
+  const int64_t t = (row >> 1) / hkv;
+  const int64_t s = slots[t];
+  if (s < 0) return;
+  if (s >= num_slots) {
+    if (lane == 0 && kv == 0 && h == 0) atomicOr(err, kErrBadSlot);
+    return;
+  }
+  const float G = scales[kv * hkv + h];
+  const uint2 raw = (kv ? v : k)[((t * hkv + h) * D) / 4 + lane];
+  const float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(x[i]));  // fmaxf drops a NaN operand
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const float r = __fdiv_rn(amax, __fmul_rn(6.0f, G));
+  const uint32_t sc = static_cast<uint32_t>(__nv_cvt_float_to_fp8(r, __NV_SATFINITE, __NV_E4M3));
+  const float S = __fmul_rn(__half2float(__ushort_as_half(
+                                static_cast<unsigned short>(e4m3x2_to_f16x2(sc) & 0xFFFFu))),
+                            G);
+  uint32_t code[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) code[i] = S == 0.f ? 0u : e2m1_code(__fdiv_rn(x[i], S));
+
+  const int64_t blk = s / bs;
+  const int off = static_cast<int>(s % bs);
+  uint8_t* rec = pool + ((blk * hkv + h) * (bs / 16) + off / 16) * kFp4SubBytes;
+  const int r16 = off & 15;  // token row inside the 16-token sub-tile
+  const int d0 = 4 * lane;
+  if (kv == 0) {
+    rec[fp4_k_code_offset(r16, d0)] = static_cast<uint8_t>(code[0] | (code[1] << 4));
+    rec[fp4_k_code_offset(r16, d0 + 2)] = static_cast<uint8_t>(code[2] | (code[3] << 4));
+    if ((lane & 3) == 0) rec[fp4_k_scale_offset(r16, d0 / 16)] = static_cast<uint8_t>(sc);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int o = fp4_v_code_offset(r16, d0 + i);  // byte of tokens (r16 & ~1, r16 | 1)
+      uint32_t* word = reinterpret_cast<uint32_t*>(rec + (o & ~3));
+      const int shift = 8 * (o & 3) + 4 * (r16 & 1);
+      atomicAnd(word, ~(0xFu << shift));
+      atomicOr(word, code[i] << shift);
+    }
+    if ((lane & 3) == 0) rec[fp4_v_scale_offset(r16, d0 / 16)] = static_cast<uint8_t>(sc);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_kv_write(const kv_pool* pool, const void* k, const void* v,
@@ -140,6 +222,13 @@ cudaError_t launch_kv_write(const kv_pool* pool, const void* k, const void* v,
       kv_write_bf16_kernel<64><<<blocks, threads, 0, stream>>>(
           static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, hkv,
           pool->block_size, num_slots, static_cast<uint4*>(pool->base), pool->err, zero_word);
+  } else if (pool->dtype == KV_FP4_E2M1) {
+    const int64_t total = num_tokens * hkv * 2 * 32;  // one warp per row
+    const int64_t blocks = std::max<int64_t>(1, (total + threads - 1) / threads);
+    kv_write_fp4_kernel<<<blocks, threads, 0, stream>>>(
+        static_cast<const uint2*>(k), static_cast<const uint2*>(v), slots, num_tokens, hkv,
+        pool->block_size, num_slots, pool->scales, static_cast<uint8_t*>(pool->base), pool->err,
+        zero_word);
   } else {
     const int64_t total = num_tokens * hkv * 2 * (pool->head_dim / 16);
     const int64_t blocks = std::max<int64_t>(1, (total + threads - 1) / threads);

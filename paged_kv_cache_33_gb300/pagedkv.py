@@ -22,7 +22,8 @@ KV_OK = 0
 STATUS = {0: "KV_OK", 1: "KV_ERR_INVALID_ARG", 2: "KV_ERR_OOM", 3: "KV_ERR_CUDA",
           4: "KV_ERR_UNSUPPORTED", 5: "KV_ERR_BAD_BLOCK_ID", 6: "KV_ERR_TIMEOUT",
           7: "KV_ERR_BAD_SLOT", 8: "KV_ERR_BAD_CONTEXT"}
-DTYPES = {"bf16": 0, "fp8": 1}
+DTYPES = {"bf16": 0, "fp8": 1, "fp4": 2}
+FP4_RECORD_BYTES = 2304  # one 16-token sub-tile of a (block, KV head) in an FP4 pool
 
 LIB_PATH = _build.LIB_PATH
 
@@ -172,10 +173,13 @@ class KVPool:
                 "scales_dev": d.scales_dev, "v_layout": d.v_layout}
 
     def view(self) -> torch.Tensor:
-        """The pool memory as a torch tensor [NB, Hkv, 2, BS, D] (bf16 or uint8), no copy."""
+        """The pool memory as a torch tensor, no copy: [NB, Hkv, 2, BS, D] (bf16 or
+        uint8), or for FP4 pools the raw records [NB, Hkv, BS/16, 2304] uint8."""
         i = self.info()
         tdt, typestr = (torch.bfloat16, "<V2") if self.dtype == "bf16" else (torch.uint8, "|u1")
         shape = (self.num_blocks, self.n_kv_heads, 2, self.block_size, self.head_dim)
+        if self.dtype == "fp4":
+            shape = (self.num_blocks, self.n_kv_heads, self.block_size // 16, FP4_RECORD_BYTES)
 
         class _Buf:
             __cuda_array_interface__ = {"shape": shape, "typestr": "|u1" if tdt == torch.uint8
@@ -187,7 +191,10 @@ class KVPool:
     def rows(self) -> torch.Tensor:
         """Inspection: the pool as [NB, Hkv, 2, BS, D] with every V tile in
         token-row order.  The raw view itself for row-major pools; a copy with
-        the transposed V tiles turned back for pools that store them so."""
+        the transposed V tiles turned back for pools that store them so; for
+        FP4 pools the E2M1 code of every element (see fp4_rows)."""
+        if self.dtype == "fp4":
+            return self.fp4_rows()[0]
         raw = self.view()
         if self.info()["v_layout"] == 0:
             return raw
@@ -200,6 +207,20 @@ class KVPool:
         out = raw.clone()
         out[:, :, 1] = rows.reshape(self.num_blocks, self.n_kv_heads, bs, d)
         return out
+
+    def fp4_rows(self) -> tuple[torch.Tensor, torch.Tensor]:
+        """Inspection of an FP4 pool: (codes [NB, Hkv, 2, BS, D], block scales
+        [NB, Hkv, 2, BS, D/16]) as uint8, gathered from the records with the
+        byte offsets include/pagedkv.h documents."""
+        assert self.dtype == "fp4" and self.head_dim == 128
+        rec = self.view()                                   # [NB, Hkv, S, 2304]
+        byte, shift, sbyte = _fp4_maps(rec.device)
+        NB, H, S = rec.shape[:3]
+        codes = (rec[..., byte] >> shift) & 0xF             # [NB, H, S, 2, 16, 128]
+        scales = rec[..., sbyte]                            # [NB, H, S, 2, 16, 8]
+        codes = codes.permute(0, 1, 3, 2, 4, 5).reshape(NB, H, 2, S * 16, 128)
+        scales = scales.permute(0, 1, 3, 2, 4, 5).reshape(NB, H, 2, S * 16, 8)
+        return codes, scales
 
     def set_scales(self, k_scale: torch.Tensor, v_scale: torch.Tensor, stream=None) -> None:
         _check(load().kv_pool_set_scales(self.handle, _dev(k_scale, torch.float32, "k_scale"),
@@ -237,6 +258,27 @@ class KVPool:
     def check_status(self, stream=None) -> int:
         """Read and clear the device error word; returns the status code."""
         return int(load().kv_pool_check_status(self.handle, _stream(stream)))
+
+
+def _fp4_maps(device):
+    """Byte index and nibble shift of every (K/V, token, dim) code of an FP4
+    record, and the byte of every (K/V, token, group) scale."""
+    byte = torch.zeros(2, 16, 128, dtype=torch.long)
+    shift = torch.zeros(2, 16, 128, dtype=torch.uint8)
+    sbyte = torch.zeros(2, 16, 8, dtype=torch.long)
+    for r in range(16):
+        for d in range(128):
+            e = d - d % 2
+            byte[0, r, d] = ((r // 8) * 512 + 16 * (4 * (r % 8) + (e % 8) // 2) + 2 * (e // 16)
+                             + (e % 16) // 8)
+            shift[0, r, d] = 4 * (d % 2)
+            byte[1, r, d] = (1024 + 16 * (32 * (d // 64) + 4 * (d % 8) + (r % 8) // 2)
+                             + 4 * ((d // 16) % 4) + r // 8 + 2 * ((d % 16) // 8))
+            shift[1, r, d] = 4 * (r % 2)
+        for b in range(8):
+            sbyte[0, r, b] = 2048 + 8 * r + b
+            sbyte[1, r, b] = 2176 + 32 * ((r % 8) // 2) + 4 * b + r % 2 + 2 * (r // 8)
+    return byte.to(device), shift.to(device), sbyte.to(device)
 
 
 # ----------------------------------------------------- C ABI named functions --

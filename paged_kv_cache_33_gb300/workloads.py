@@ -20,6 +20,8 @@ vLLM...", section "The Math of the KV Cache Bottleneck"):
   fp8   batch 256, 32/8 heads, e4m3 KV with per-KV-head scales,
         ctx ~ U{1..16384}; tables come from a block allocator after a seeded
         churn of 10,000 alloc/free steps at 95% occupancy
+  fp4   the fp8 workload's shape and table recipe (its own seeds) with an
+        FP4 pool: E2M1 codes, E4M3 scales per 16 elements, per-KV-head scales
 
 All numbers are N(0,1) draws from seeded torch generators; every sequence's
 K/V comes from its own seed so that a subset can be regenerated alone.
@@ -35,10 +37,12 @@ import torch
 
 BLOCK_SIZE = 16        # default tokens per block
 GROWTH_TOKENS = 16     # tokens a churn step appends to a running request
-CONFIGS = ("tiny", "8b", "70b", "sw", "fp8")
+CONFIGS = ("tiny", "8b", "70b", "sw", "fp8", "fp4")
 
-DATA_SEED = {"tiny": 1000, "8b": 1001, "70b": 1002, "sw": 1003, "fp8": 1004, "long": 1005}
-TABLE_SEED = {"tiny": 2000, "8b": 2001, "70b": 2002, "sw": 2003, "fp8": 2004, "long": 2005}
+DATA_SEED = {"tiny": 1000, "8b": 1001, "70b": 1002, "sw": 1003, "fp8": 1004, "long": 1005,
+             "fp4": 1006}
+TABLE_SEED = {"tiny": 2000, "8b": 2001, "70b": 2002, "sw": 2003, "fp8": 2004, "long": 2005,
+              "fp4": 2006}
 
 
 @dataclass
@@ -52,14 +56,14 @@ class Workload:
     block_size: int
     num_blocks: int
     window: int                 # <= 0: no sliding window
-    dtype: str                  # "bf16" or "fp8"
+    dtype: str                  # "bf16", "fp8" or "fp4"
     scale: float                # softmax scale
     context_lens: np.ndarray    # int32 [B]: tokens per sequence after this step's write
     block_tables: np.ndarray    # int32 [B, MBS]; -1 = no block mapped
     new_pos: np.ndarray         # int64 [B]: position written this step, -1 = none
     shared_prefix_tokens: int = 0
     prefix_blocks: np.ndarray | None = None   # int32: physical ids of the shared prefix
-    k_scale: np.ndarray | None = None   # fp32 [Hkv] (fp8 only)
+    k_scale: np.ndarray | None = None   # fp32 [Hkv] (fp8 and fp4 only)
     v_scale: np.ndarray | None = None
     data_seed: int = 0
     notes: dict = field(default_factory=dict)
@@ -94,14 +98,21 @@ class Workload:
         return int(sum(self.attended_range(b)[1] - self.attended_range(b)[0]
                        for b in range(self.batch)))
 
+    def kv_bytes_per_token_head(self) -> int:
+        """Stored K+V bytes of one token of one KV head: 2 bytes an element
+        (bf16), 1 (FP8), or half a byte plus one scale byte per 16 (FP4)."""
+        if self.dtype == "bf16":
+            return 2 * self.head_dim * 2
+        if self.dtype == "fp8":
+            return 2 * self.head_dim
+        return 2 * (self.head_dim // 2 + self.head_dim // 16)
+
     def kv_bytes_attended(self) -> int:
         """K+V bytes of the attended tokens (per layer), the roofline's unit of work."""
-        elem = 2 if self.dtype == "bf16" else 1
-        return self.attended_tokens() * self.n_kv_heads * 2 * self.head_dim * elem
+        return self.attended_tokens() * self.n_kv_heads * self.kv_bytes_per_token_head()
 
     def kv_bytes_unique(self) -> int:
         """K+V bytes of distinct attended tokens: the shared prefix counts once."""
-        elem = 2 if self.dtype == "bf16" else 1
         P = self.shared_prefix_tokens
         n = 0
         prefix_read = 0
@@ -113,7 +124,7 @@ class Workload:
                 n += max(0, ctx - max(lo, P))
             else:
                 n += ctx - lo
-        return (n + prefix_read) * self.n_kv_heads * 2 * self.head_dim * elem
+        return (n + prefix_read) * self.n_kv_heads * self.kv_bytes_per_token_head()
 
     # ---------------------------------------------------------------- data --
     def _gen(self, key: int, device) -> torch.Generator:
@@ -343,23 +354,26 @@ FP8_K_SCALE_BASE = 5.0   # per-KV-head scale = (base + step * h) / 448
 FP8_V_SCALE_BASE = 5.5
 
 
-def _fp8(size: str, make_allocator=None, bs: int = BLOCK_SIZE) -> Workload:
-    rng = np.random.default_rng(TABLE_SEED["fp8"])
+def _fp8(size: str, make_allocator=None, bs: int = BLOCK_SIZE, fmt: str = "fp8") -> Workload:
+    rng = np.random.default_rng(TABLE_SEED[fmt])
     B = 256 if size == "full" else 16
     max_len = 16384 if size == "full" else 4096
     steps = 10_000 if size == "full" else 2_000
     lens = rng.integers(1, max_len, size=B, endpoint=True).astype(np.int32)
     if make_allocator is None:
-        raise ValueError("the fp8 workload needs a block allocator (make_allocator)")
+        raise ValueError(f"the {fmt} workload needs a block allocator (make_allocator)")
     nb, tables, stats = churn_tables(make_allocator, lens, steps, 0.95,
                                      int(rng.integers(0, 2**31)), max_len, bs)
     hkv = 8
     # Fixed per-KV-head scales: N(0,1) data saturates only beyond ~5 sigma.
-    k_scale = ((FP8_K_SCALE_BASE + 0.25 * np.arange(hkv)) / 448.0).astype(np.float32)
-    v_scale = ((FP8_V_SCALE_BASE + 0.125 * np.arange(hkv)) / 448.0).astype(np.float32)
-    return Workload("fp8", size, B, 32, hkv, 128, bs, nb, 0, "fp8", 1.0 / math.sqrt(128),
+    # FP4: the head scale spans the E4M3 block scales' range once more (6 is
+    # the largest E2M1 magnitude), so a 16-element group's scale stays <= 448.
+    div = 448.0 if fmt == "fp8" else 6.0 * 448.0
+    k_scale = ((FP8_K_SCALE_BASE + 0.25 * np.arange(hkv)) / div).astype(np.float32)
+    v_scale = ((FP8_V_SCALE_BASE + 0.125 * np.arange(hkv)) / div).astype(np.float32)
+    return Workload(fmt, size, B, 32, hkv, 128, bs, nb, 0, fmt, 1.0 / math.sqrt(128),
                     lens, tables, (lens - 1).astype(np.int64), k_scale=k_scale,
-                    v_scale=v_scale, data_seed=DATA_SEED["fp8"], notes={"churn": stats})
+                    v_scale=v_scale, data_seed=DATA_SEED[fmt], notes={"churn": stats})
 
 
 def _long(size: str, bs: int = BLOCK_SIZE) -> Workload:
@@ -378,7 +392,7 @@ def _long(size: str, bs: int = BLOCK_SIZE) -> Workload:
 
 
 def make(name: str, size: str = "full", make_allocator=None, block_size: int = BLOCK_SIZE) -> Workload:
-    """Build workload `name` ("tiny", "8b", "70b", "sw", "fp8", "long") at size
+    """Build workload `name` ("tiny", "8b", "70b", "sw", "fp8", "fp4", "long") at size
     "full" or "small", with pool blocks of `block_size` tokens (16 or 32)."""
     if size not in ("full", "small"):
         raise ValueError(size)
@@ -392,8 +406,8 @@ def make(name: str, size: str = "full", make_allocator=None, block_size: int = B
         return _70b(size, block_size)
     if name == "sw":
         return _sw(size, block_size)
-    if name == "fp8":
-        return _fp8(size, make_allocator, block_size)
+    if name in ("fp8", "fp4"):
+        return _fp8(size, make_allocator, block_size, name)
     if name == "long":
         return _long(size, block_size)
     raise ValueError(f"unknown workload {name!r}")

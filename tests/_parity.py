@@ -17,6 +17,12 @@ from paged_kv_cache_33_gb300.workloads import Workload
 BF16_MAX_ABS = 2e-3   # acceptance for bf16 KV: max |err|
 BF16_REL_L2 = 1e-3    # and relative L2
 FP8_MAX_ABS = 3e-2    # acceptance for FP8 KV
+# FP4 KV: the keys and values are dequantised exactly (f16), the queries are
+# exact in f16 after a power-of-two scaling, scores accumulate in fp32; the
+# softmax weights enter the P V product as f16 (relative rounding <= 2^-11),
+# so against the oracle on the same codes the error is below the bf16 bar.
+FP4_MAX_ABS = BF16_MAX_ABS
+FP4_REL_L2 = BF16_REL_L2
 
 
 def poison(pool: pagedkv.KVPool) -> None:
@@ -24,6 +30,8 @@ def poison(pool: pagedkv.KVPool) -> None:
     v = pool.view()
     if pool.dtype == "bf16":
         v.view(torch.int16).fill_(0x7FC0)
+    elif pool.dtype == "fp4":
+        v.fill_(0xFF)          # codes -6 under NaN (0xFF) block scales
     else:
         v.fill_(0x7F)
 
@@ -32,14 +40,14 @@ def make_gpu_pool(w: Workload, poison_pool: bool = True) -> pagedkv.KVPool:
     pool = pagedkv.KVPool(w.num_blocks, w.block_size, w.n_kv_heads, w.head_dim, w.dtype)
     if poison_pool:
         poison(pool)
-    if w.dtype == "fp8":
+    if w.dtype in ("fp8", "fp4"):
         pool.set_scales(torch.from_numpy(w.k_scale).cuda(), torch.from_numpy(w.v_scale).cuda())
     return pool
 
 
 def make_oracle_pool(w: Workload) -> oracle.Pool:
     op = oracle.Pool(w.num_blocks, w.block_size, w.n_kv_heads, w.head_dim, w.dtype)
-    if w.dtype == "fp8":
+    if w.dtype in ("fp8", "fp4"):
         op.set_scales(w.k_scale, w.v_scale)
     return op
 
@@ -88,6 +96,14 @@ def compare_pools(pool: pagedkv.KVPool, opool: oracle.Pool, slots: np.ndarray,
     assert len(slots) == 0 or (slots.min() >= 0 and slots.max() < pool.num_blocks * bs)
     blk = torch.from_numpy(slots // bs)
     off = torch.from_numpy(slots % bs)
+    if pool.dtype == "fp4":
+        codes, scales = pool.fp4_rows()                # [NB, Hkv, 2, BS, D], [.., D/16]
+        for gpu, ora in ((codes, opool.array()), (scales, opool.block_scales())):
+            g = gpu[blk.cuda(), :, :, off.cuda(), :].permute(0, 2, 1, 3).cpu().numpy()
+            o = ora[slots // bs, :, slots % bs]
+            bad = np.nonzero((g != o).reshape(len(slots), -1).any(axis=1))[0]
+            assert bad.size == 0, f"{bad.size} FP4 rows differ, first slot {slots[bad[0]]}"
+        return
     v = pool.rows()
     g = v[blk.cuda(), :, :, off.cuda(), :]            # [n, Hkv, 2, D]
     g = g.permute(0, 2, 1, 3).contiguous().cpu()       # [n, 2, Hkv, D]
@@ -114,6 +130,8 @@ def assert_close(w: Workload, out: np.ndarray, ref: np.ndarray, label: str = "")
     max_abs, rel = errors(out, ref)
     if w.dtype == "bf16":
         assert max_abs <= BF16_MAX_ABS and rel <= BF16_REL_L2, (label, max_abs, rel)
+    elif w.dtype == "fp4":
+        assert max_abs <= FP4_MAX_ABS and rel <= FP4_REL_L2, (label, max_abs, rel)
     else:
         assert max_abs <= FP8_MAX_ABS, (label, max_abs, rel)
     return max_abs, rel

@@ -54,6 +54,7 @@ def test_status_strings():
     ((10, 64, 8, 128, 0), 4),       # block size other than 16 or 32
     ((10, 16, 8, 96, 0), 4),        # head_dim not 64/128
     ((10, 16, 8, 64, 1), 4),        # FP8 needs head_dim 128
+    ((10, 16, 8, 64, 2), 4),        # FP4 needs head_dim 128
 ])
 def test_create_rejects_bad_shapes_before_any_cuda_call(args, status):
     L = pagedkv.load()

@@ -24,7 +24,7 @@ def _filled_pair(nb, hkv, d, dtype, seed):
     """A GPU pool and an oracle pool holding the same random contents in every slot."""
     pool = pagedkv.KVPool(nb, 16, hkv, d, dtype)
     opool = oracle.Pool(nb, 16, hkv, d, dtype)
-    if dtype == "fp8":
+    if dtype in ("fp8", "fp4"):
         ks = (0.5 + np.arange(hkv)).astype(np.float32) / 448.0 * 4
         vs = (0.75 + np.arange(hkv)).astype(np.float32) / 448.0 * 4
         pool.set_scales(torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda())
@@ -39,7 +39,8 @@ def _filled_pair(nb, hkv, d, dtype, seed):
     return pool, opool
 
 
-@pytest.mark.parametrize("dtype,hkv,d", [("bf16", 8, 128), ("bf16", 2, 64), ("fp8", 4, 128)])
+@pytest.mark.parametrize("dtype,hkv,d", [("bf16", 8, 128), ("bf16", 2, 64), ("fp8", 4, 128),
+                                         ("fp4", 4, 128)])
 def test_copies_match_in_order_application(dtype, hkv, d):
     nb = 48
     pool, opool = _filled_pair(nb, hkv, d, dtype, seed=5)

@@ -1,7 +1,8 @@
 """GPU parity: the sm_103a kernels through the C ABI against the fp64 oracle.
 
-The KV write must be bit-exact (bf16 bit copy, FP8 codes); attention must be
-within max |err| <= 2e-3 and relative L2 <= 1e-3 for bf16 KV, max |err| <=
+The KV write must be bit-exact (bf16 bit copy, FP8 codes, FP4 codes and block
+scales); attention must be within max |err| <= 2e-3 and relative L2 <= 1e-3
+for bf16 and FP4 KV (against the oracle on the stored codes), max |err| <=
 3e-2 for FP8 KV.  The pool is poisoned with NaN codes before any write, so a
 read of a slot that was never written would surface as a non-finite output.
 """
@@ -14,14 +15,14 @@ import oracle
 from paged_kv_cache_33_gb300 import pagedkv
 from paged_kv_cache_33_gb300 import workloads as W
 
-from _parity import (assert_close, compare_pools, decode_gpu, fill_both, make_gpu_pool,
+from _parity import (assert_close, compare_pools, decode_gpu, fill_both, make_gpu_pool, poison,
                      make_oracle_pool, run_parity, written_slots)
 
 pytestmark = pytest.mark.gpu
 
 
 def _workload(name, size, block_size=16):
-    return W.make(name, size, make_allocator=oracle.Allocator if name == "fp8" else None,
+    return W.make(name, size, make_allocator=oracle.Allocator if name in ("fp8", "fp4") else None,
                   block_size=block_size)
 
 
@@ -33,7 +34,7 @@ def test_tiny_workload_exact_path(block_size):
 
 
 @pytest.mark.parametrize("block_size", [16, 32])
-@pytest.mark.parametrize("name", ["8b", "70b", "sw", "fp8", "long"])
+@pytest.mark.parametrize("name", ["8b", "70b", "sw", "fp8", "fp4", "long"])
 @pytest.mark.parametrize("part_blocks", [None, 4, 12])
 def test_small_workloads(name, part_blocks, block_size):
     # several partitions per sequence (forced small partitions exercise the reduce)
@@ -41,7 +42,7 @@ def test_small_workloads(name, part_blocks, block_size):
 
 
 @pytest.mark.parametrize("block_size", [16, 32])
-@pytest.mark.parametrize("name", ["8b", "70b", "sw", "fp8", "long"])
+@pytest.mark.parametrize("name", ["8b", "70b", "sw", "fp8", "fp4", "long"])
 def test_full_workloads_sampled(name, block_size):
     """Full-size workloads in the bench's launch configuration; the oracle
     computes a sample of sequences (the longest, the shortest, and random)."""
@@ -72,6 +73,9 @@ def _custom(lens, hq=8, hkv=2, d=128, window=0, dtype="bf16", extra_blocks=7, se
     if dtype == "fp8":
         w.k_scale = np.linspace(0.009, 0.013, hkv).astype(np.float32)
         w.v_scale = np.linspace(0.011, 0.015, hkv).astype(np.float32)
+    if dtype == "fp4":
+        w.k_scale = np.linspace(0.0015, 0.0022, hkv).astype(np.float32)
+        w.v_scale = np.linspace(0.0019, 0.0025, hkv).astype(np.float32)
     return w
 
 
@@ -84,7 +88,7 @@ def test_head_grouping_and_head_dim(hq, hkv, d, bs):
 
 
 @pytest.mark.parametrize("bs", [16, 32])
-@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "fp4"])
 @pytest.mark.parametrize("window", [1, 15, 16, 17, 31, 33, 100, 512, 10_000])
 def test_sliding_window_edges(window, dtype, bs):
     lens = [1, 16, 17, 32, 33, 100, 101, 600, 1111]
@@ -97,12 +101,13 @@ def test_sliding_window_edges(window, dtype, bs):
 
 
 @pytest.mark.parametrize("bs", [16, 32])
-def test_fp8_head_groups_and_partitions(bs):
-    # 16-token blocks: FP8 units hold two blocks, so odd block counts leave a
-    # unit with one block; 32-token blocks: one block, two sub-tiles
-    lens = [1, 5, 16, 17, 31, 32, 33, 47, 300, 2000]
-    for hq, hkv in [(8, 8), (16, 2), (32, 8)]:
-        run_parity(_custom(lens, hq, hkv, 128, dtype="fp8", seed=hq, bs=bs), part_blocks=8)
+@pytest.mark.parametrize("dtype", ["fp8", "fp4"])
+def test_quantised_head_groups_and_partitions(bs, dtype):
+    # 16-token blocks: FP8 units hold two blocks and FP4 units three, so block
+    # counts leave partial units; 32-token blocks: one block, two sub-tiles
+    lens = [1, 5, 16, 17, 31, 32, 33, 47, 48, 49, 300, 2000]
+    for hq, hkv in [(8, 8), (16, 2), (32, 8), (3, 1), (24, 3)]:
+        run_parity(_custom(lens, hq, hkv, 128, dtype=dtype, seed=hq, bs=bs), part_blocks=8)
 
 
 def test_empty_and_single_token_contexts():
@@ -162,13 +167,13 @@ def test_non_default_stream():
 # ----------------------------------------------------------------- KV write --
 
 @pytest.mark.parametrize("bs", [16, 32])
-@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("fp8", 128)])
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("fp8", 128), ("fp4", 128)])
 def test_write_bit_exact_with_padding_and_repeats(dtype, d, bs):
     torch.manual_seed(0)
     nb, hkv, T = 40, 4, 300
     pool = pagedkv.KVPool(nb, bs, hkv, d, dtype)
     opool = oracle.Pool(nb, bs, hkv, d, dtype)
-    if dtype == "fp8":
+    if dtype in ("fp8", "fp4"):
         ks = torch.tensor([0.01, 0.02, 0.003, 1.0])
         vs = torch.tensor([0.05, 0.001, 0.02, 0.5])
         pool.set_scales(ks.cuda(), vs.cuda())
@@ -190,6 +195,40 @@ def test_write_bit_exact_with_padding_and_repeats(dtype, d, bs):
     vv = pool.rows()[torch.from_numpy(skipped // bs).cuda(), :, :, torch.from_numpy(skipped % bs).cuda()]
     raw = vv.view(torch.int16) if dtype == "bf16" else vv
     assert int((raw != 0).sum()) == 0
+
+
+def test_fp4_write_special_values_and_one_token_calls():
+    """FP4: NaN, infinities, zero and tiny rows, and tokens written one call
+    at a time at every offset (the V bytes pair two tokens, so each call
+    merges its nibble next to the other token's), bit-exact against the oracle."""
+    torch.manual_seed(3)
+    nb, hkv, bs = 12, 2, 16
+    pool = pagedkv.KVPool(nb, bs, hkv, 128, "fp4")
+    poison(pool)
+    opool = oracle.Pool(nb, bs, hkv, 128, "fp4")
+    ks, vs = torch.tensor([0.004, 0.9]), torch.tensor([0.002, 0.03])
+    pool.set_scales(ks.cuda(), vs.cuda())
+    opool.set_scales(ks.numpy(), vs.numpy())
+    T = nb * bs
+    k = (torch.randn(T, hkv, 128) * 3).bfloat16()
+    v = torch.randn(T, hkv, 128).bfloat16()
+    k[0, 0, :5] = torch.tensor([float("nan"), float("inf"), -float("inf"), 0.0, -0.0])
+    v[1, 1, 16:32] = 0.0                                     # an all-zero group
+    v[2, 0, 32:48] = 1e-30                                   # a group whose scale underflows
+    k[3, 1, :] = 1e5                                         # saturated block scales
+    perm = np.random.default_rng(4).permutation(T)
+    # one call per token, in shuffled order (partners land before or after)
+    for t in perm[: T // 2]:
+        s1 = torch.tensor([int(t)], dtype=torch.int64)
+        pagedkv.paged_kv_write(pool, k[t:t + 1].cuda(), v[t:t + 1].cuda(), s1.cuda())
+        opool.write(k[t:t + 1], v[t:t + 1], s1.numpy())
+    # the rest in one call
+    rest = torch.from_numpy(perm[T // 2:].astype(np.int64))
+    pagedkv.paged_kv_write(pool, k[rest].cuda(), v[rest].cuda(), rest.cuda())
+    opool.write(k[rest], v[rest], rest.numpy())
+    torch.cuda.synchronize()
+    assert pool.check_status() == pagedkv.KV_OK
+    compare_pools(pool, opool, np.arange(T))
 
 
 def test_write_reports_a_slot_outside_the_pool():

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _workload(name, size):
-    return W.make(name, size, make_allocator=oracle.Allocator if name == "fp8" else None)
+    return W.make(name, size, make_allocator=oracle.Allocator if name in ("fp8", "fp4") else None)
 
 
 def _setup(w, pool, opool=None):
@@ -65,7 +65,7 @@ def _two_ways(w, hook=False):
     return out_f, out_s, fused, opool, written_slots(setup, (k, v, s))
 
 
-@pytest.mark.parametrize("name", ["tiny", "8b", "70b", "sw", "fp8"])
+@pytest.mark.parametrize("name", ["tiny", "8b", "70b", "sw", "fp8", "fp4"])
 def test_step_equals_write_then_attention(name):
     w = W.make("tiny") if name == "tiny" else _workload(name, "small")
     out_f, out_s, fused, opool, slots = _two_ways(w)
