@@ -351,18 +351,38 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
       __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
 }
 
-// The two E2M1 codes of the low byte of w (low nibble first) as exact f16
-// values, times a pair of f16 scales; the products of an E2M1 value and an
-// E4M3 scale are exact in f16 (at most 5 significant bits, 2^-10 .. 2688).
-__device__ __forceinline__ uint32_t fp4x2_scaled(uint32_t w, __half2 scale) {
-  const __half2_raw r =
-      __nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>(w & 0xFFu), __NV_E2M1);
-  __half2 h;
-  memcpy(&h, &r, sizeof h);
-  const __half2 v = __hmul2(h, scale);
-  uint32_t out;
-  memcpy(&out, &v, sizeof out);
-  return out;
+// The eight E2M1 codes of w as four f16x2 registers: r[i] holds the codes of
+// byte i (low nibble in the low half).  Exact.
+__device__ __forceinline__ void fp4x8_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
+  asm("{\n"
+      " .reg .b8 b0, b1, b2, b3;\n"
+      " mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+      " cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+      " cvt.rn.f16x2.e2m1x2 %3, b3;\n"
+      "}"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(w));
+}
+
+// The four E4M3 codes of w as two f16x2 registers: lo = bytes 0, 1 and
+// hi = bytes 2, 3 (lower byte in the low half).  Exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n"
+      " .reg .b16 h0, h1;\n"
+      " mov.b32 {h0, h1}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, h0;\n"
+      " cvt.rn.f16x2.e4m3x2 %1, h1;\n"
+      "}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t half2_as_u32(__half2 h) {
+  uint32_t v;
+  memcpy(&v, &h, sizeof v);
+  return v;
 }
 
 // Two E4M3 codes (low byte first) to two exact f16 values (low half first).

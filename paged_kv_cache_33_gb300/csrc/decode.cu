@@ -566,23 +566,37 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
           const uint32_t rec = st + G::rec_off(sub);
           const uint4 kc0 = lds128(rec + 16 * lane), kc1 = lds128(rec + 512 + 16 * lane);
           const uint2 kq0 = lds64(rec + 2048 + 8 * n), kq1 = lds64(rec + 2048 + 64 + 8 * n);
-          const uint32_t kw0[4] = {kc0.x, kc0.y, kc0.z, kc0.w};
-          const uint32_t kw1[4] = {kc1.x, kc1.y, kc1.z, kc1.w};
+          const uint32_t kw[2][4] = {{kc0.x, kc0.y, kc0.z, kc0.w}, {kc1.x, kc1.y, kc1.z, kc1.w}};
           const uint32_t kq[2][2] = {{kq0.x, kq0.y}, {kq1.x, kq1.y}};
+          // scale pairs (groups 2i, 2i+1) of tokens n and n + 8
+          uint32_t ksp[2][4];
 #pragma unroll
-          for (int ks = 0; ks < G::kSteps; ++ks) {
-            // scales of group ks for tokens n and n + 8, in both halves
-            const __half2 p0 = u32_as_half2(e4m3x2_to_f16x2(kq[0][ks >> 2] >> (16 * ((ks >> 1) & 1))));
-            const __half2 p1 = u32_as_half2(e4m3x2_to_f16x2(kq[1][ks >> 2] >> (16 * ((ks >> 1) & 1))));
-            const __half2 c0 = (ks & 1) ? __high2half2(p0) : __low2half2(p0);
-            const __half2 c1 = (ks & 1) ? __high2half2(p1) : __low2half2(p1);
-            const uint32_t w0 = kw0[ks >> 1] >> (16 * (ks & 1)), w1 = kw1[ks >> 1] >> (16 * (ks & 1));
-            const uint32_t a0 = fp4x2_scaled(w0, c0), a2 = fp4x2_scaled(w0 >> 8, c0);
-            const uint32_t a1 = fp4x2_scaled(w1, c1), a3 = fp4x2_scaled(w1 >> 8, c1);
-            if (ks & 1)
-              mma_f16(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-            else
-              mma_f16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+          for (int t = 0; t < 2; ++t) {
+            e4m3x4_to_f16x2(kq[t][0], ksp[t][0], ksp[t][1]);
+            e4m3x4_to_f16x2(kq[t][1], ksp[t][2], ksp[t][3]);
+          }
+#pragma unroll
+          for (int i = 0; i < G::kSteps / 2; ++i) {
+            // word i of a token's chunk: k-steps 2i and 2i+1, each the bytes
+            // of dims (2j, 2j+1) and (2j+8, 2j+9)
+            uint32_t c0[4], c1[4];
+            fp4x8_to_f16x2(kw[0][i], c0);
+            fp4x8_to_f16x2(kw[1][i], c1);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int ks = 2 * i + e;
+              const __half2 p0 = u32_as_half2(ksp[0][i]), p1 = u32_as_half2(ksp[1][i]);
+              const __half2 s0 = e ? __high2half2(p0) : __low2half2(p0);
+              const __half2 s1 = e ? __high2half2(p1) : __low2half2(p1);
+              const uint32_t a0 = half2_as_u32(__hmul2(u32_as_half2(c0[2 * e]), s0));
+              const uint32_t a2 = half2_as_u32(__hmul2(u32_as_half2(c0[2 * e + 1]), s0));
+              const uint32_t a1 = half2_as_u32(__hmul2(u32_as_half2(c1[2 * e]), s1));
+              const uint32_t a3 = half2_as_u32(__hmul2(u32_as_half2(c1[2 * e + 1]), s1));
+              if (ks & 1)
+                mma_f16(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+              else
+                mma_f16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            }
           }
           // V code and scale words, kept raw until the product
           vq[0] = lds128(rec + 1024 + 16 * lane);
@@ -686,28 +700,31 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
 
       // ---- O^T += V^T P^T : rows = head_dim, cols = 8 query heads, k = 16 tokens
       if constexpr (FP4) {
-        // P in f16 (11 significant bits); V^T fragments dequantised exactly
-        // into f16 per m-tile: word mt of the codes holds tokens (2j, 2j+1)
-        // and (2j+8, 2j+9) at dims 16 mt + n and 16 mt + n + 8, word mt of
-        // the scales those four tokens' group-mt scales.
-        const uint32_t b0 = movmatrix_trans(pack_f16x2(p0, p1));
-        const uint32_t b1 = movmatrix_trans(pack_f16x2(p2, p3));
-        uint32_t mlo = kFull, mhi = kFull;
-        if (!full) {
-          mlo = (tok_ok(2 * j) ? 0x0000ffffu : 0u) | (tok_ok(2 * j + 1) ? 0xffff0000u : 0u);
-          mhi = (tok_ok(2 * j + 8) ? 0x0000ffffu : 0u) | (tok_ok(2 * j + 9) ? 0xffff0000u : 0u);
-        }
+        // P in f16 (11 significant bits).  The A fragments are the V codes as
+        // exact f16 values; each token's E4M3 group scale of m-tile mt goes
+        // into its P entry instead (word mt of the lane's scale words holds
+        // tokens 2j, 2j+1, 2j+8, 2j+9: the tokens of b0 and b1), so a
+        // fragment costs two conversions of codes and none of scales.
+        // Masked tokens get a zero scale: stale slots contribute nothing.
+        const __half2 b0 = u32_as_half2(movmatrix_trans(pack_f16x2(p0, p1)));
+        const __half2 b1 = u32_as_half2(movmatrix_trans(pack_f16x2(p2, p3)));
         const uint32_t vw[8] = {vq[0].x, vq[0].y, vq[0].z, vq[0].w, vq[1].x, vq[1].y, vq[1].z, vq[1].w};
-        const uint32_t sw[8] = {vq[2].x, vq[2].y, vq[2].z, vq[2].w, vq[3].x, vq[3].y, vq[3].z, vq[3].w};
+        uint32_t sw[8] = {vq[2].x, vq[2].y, vq[2].z, vq[2].w, vq[3].x, vq[3].y, vq[3].z, vq[3].w};
+        if (!full) {
+          const uint32_t m = (tok_ok(2 * j) ? 0x000000ffu : 0u) | (tok_ok(2 * j + 1) ? 0x0000ff00u : 0u) |
+                             (tok_ok(2 * j + 8) ? 0x00ff0000u : 0u) | (tok_ok(2 * j + 9) ? 0xff000000u : 0u);
+#pragma unroll
+          for (int mt = 0; mt < G::kSteps; ++mt) sw[mt] &= m;
+        }
 #pragma unroll
         for (int mt = 0; mt < G::kSteps; ++mt) {
-          const __half2 s01 = u32_as_half2(e4m3x2_to_f16x2(sw[mt]));
-          const __half2 s89 = u32_as_half2(e4m3x2_to_f16x2(sw[mt] >> 16));
-          const uint32_t a0 = fp4x2_scaled(vw[mt], s01) & mlo;
-          const uint32_t a2 = fp4x2_scaled(vw[mt] >> 8, s89) & mhi;
-          const uint32_t a1 = fp4x2_scaled(vw[mt] >> 16, s01) & mlo;
-          const uint32_t a3 = fp4x2_scaled(vw[mt] >> 24, s89) & mhi;
-          mma_f16(acc[mt], a0, a1, a2, a3, b0, b1);
+          uint32_t slo, shi, a[4];
+          e4m3x4_to_f16x2(sw[mt], slo, shi);
+          fp4x8_to_f16x2(vw[mt], a);
+          const uint32_t bb0 = half2_as_u32(__hmul2(b0, u32_as_half2(slo)));
+          const uint32_t bb1 = half2_as_u32(__hmul2(b1, u32_as_half2(shi)));
+          // bytes 0..3: tokens (2j, 2j+1) / (2j+8, 2j+9) at dim n, then dim n + 8
+          mma_f16(acc[mt], a[0], a[2], a[1], a[3], bb0, bb1);
         }
       } else if constexpr (!FP8) {
         const uint32_t x01 = pack_bf16x2(p0, p1), x23 = pack_bf16x2(p2, p3);
@@ -981,7 +998,11 @@ using Bf16D64B32 = Variant<64, kBf16, 32, 1, 4, 2>;
 using Fp8D128B32 = Variant<128, kFp8, 32, 1, PKV_FP8_WARPS, 2>;
 // FP4 records are 2304 bytes per 16 tokens: units of three 16-token blocks
 // (one 32-token block) keep ~14 KB of ring per warp, as the other variants.
-using Fp4D128 = Variant<128, kFp4, 16, 3, 4, 2>;
+#ifndef PKV_FP4_BPU
+#define PKV_FP4_BPU 3
+#define PKV_FP4_STAGES 2
+#endif
+using Fp4D128 = Variant<128, kFp4, 16, PKV_FP4_BPU, 4, PKV_FP4_STAGES>;
 using Fp4D128B32 = Variant<128, kFp4, 32, 1, 4, 3>;
 
 // Call f with the variant type the pool uses.
