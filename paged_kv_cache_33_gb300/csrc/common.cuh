@@ -366,6 +366,22 @@ __device__ __forceinline__ void fp4x8_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
       : "r"(w));
 }
 
+// Two f16x2 registers to four E4M3 codes, round to nearest even, saturating
+// to +-448: a's halves into bytes 0, 1 and b's into bytes 2, 3 (low half in
+// the lower byte).
+__device__ __forceinline__ uint32_t f16x2x2_to_e4m3x4(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("{\n"
+      " .reg .b16 l, h;\n"
+      " cvt.rn.satfinite.e4m3x2.f16x2 l, %1;\n"
+      " cvt.rn.satfinite.e4m3x2.f16x2 h, %2;\n"
+      " mov.b32 %0, {l, h};\n"
+      "}"
+      : "=r"(d)
+      : "r"(a), "r"(b));
+  return d;
+}
+
 // The four E4M3 codes of w as two f16x2 registers: lo = bytes 0, 1 and
 // hi = bytes 2, 3 (lower byte in the low half).  Exact.
 __device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {

@@ -78,6 +78,15 @@ constexpr uint64_t kShortWaitNs = 200000;  // wait bound once some warp has time
 #define PKV_P1 30
 #define PKV_P2 10
 #endif
+#ifndef PKV_FP4_MINB
+#define PKV_FP4_MINB 3  // FP4 decode CTAs per SM the registers must allow
+#endif
+#ifndef PKV_RIF
+#define PKV_RIF 4
+#define PKV_RMB 1
+#endif
+// The reduce: threads per CTA and the CTAs per SM its registers must allow.
+constexpr int kReduceThreads = 512, kReduceCtas = PKV_RMB;
 constexpr int kDynNum = PKV_DYN_PCT, kDynDen = 100;  // dynamic share of the units
 struct ChunkPlan {
   int c[4];    // units per chunk in each region
@@ -225,7 +234,7 @@ struct Split {
 };
 
 template <int D, int KIND, int BS, int BPU, int NW, int STAGES>
-__global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kernel(
+__global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : (KIND == kFp4 ? PKV_FP4_MINB : 3))) paged_decode_kernel(
     const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
   using G = Geometry<D, KIND, BS, BPU>;
   using S = Smem<D, KIND, BS, BPU, NW, STAGES>;
@@ -733,17 +742,21 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
         const uint32_t bh0 = movmatrix_trans(x01), bh1 = movmatrix_trans(x23);
         const uint32_t bl0 = movmatrix_trans(y01), bl1 = movmatrix_trans(y23);
         // this lane's V^T fragment covers tokens 2j, 2j+1 (a0, a1) and 2j+8, 2j+9 (a2, a3)
-        uint32_t mlo = kFull, mhi = kFull;
         if (!full) {
-          mlo = (tok_ok(2 * j) ? 0x0000ffffu : 0u) | (tok_ok(2 * j + 1) ? 0xffff0000u : 0u);
-          mhi = (tok_ok(2 * j + 8) ? 0x0000ffffu : 0u) | (tok_ok(2 * j + 9) ? 0xffff0000u : 0u);
+          const uint32_t mlo = (tok_ok(2 * j) ? 0x0000ffffu : 0u) | (tok_ok(2 * j + 1) ? 0xffff0000u : 0u);
+          const uint32_t mhi = (tok_ok(2 * j + 8) ? 0x0000ffffu : 0u) | (tok_ok(2 * j + 9) ? 0xffff0000u : 0u);
+#pragma unroll
+          for (int mt = 0; mt < G::kSteps; ++mt) {
+            vf[mt][0] &= mlo;
+            vf[mt][1] &= mlo;
+            vf[mt][2] &= mhi;
+            vf[mt][3] &= mhi;
+          }
         }
 #pragma unroll
         for (int mt = 0; mt < G::kSteps; ++mt) {
-          const uint32_t a0 = vf[mt][0] & mlo, a1 = vf[mt][1] & mlo;
-          const uint32_t a2 = vf[mt][2] & mhi, a3 = vf[mt][3] & mhi;
-          mma_bf16(acc[mt], a0, a1, a2, a3, bh0, bh1);
-          mma_bf16(acc[mt], a0, a1, a2, a3, bl0, bl1);
+          mma_bf16(acc[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], bh0, bh1);
+          mma_bf16(acc[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], bl0, bl1);
         }
       } else {
         // P^T as E4M3 codes of 256 p: after the transpose this lane holds head
@@ -753,20 +766,22 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
         // remainders against the same V codes, so P keeps ~8 bits.
         const uint32_t tX = movmatrix_trans(pack_f16x2(p0 * 256.f, p1 * 256.f));
         const uint32_t tY = movmatrix_trans(pack_f16x2(p2 * 256.f, p3 * 256.f));
-        const uint32_t hX = f16x2_to_e4m3x2(tX), hY = f16x2_to_e4m3x2(tY);
-        const uint32_t lX = f16x2_to_e4m3x2(hsub2_bits(tX, e4m3x2_to_f16x2(hX)));
-        const uint32_t lY = f16x2_to_e4m3x2(hsub2_bits(tY, e4m3x2_to_f16x2(hY)));
-        const uint32_t bhi = hX | (hY << 16), blo = lX | (lY << 16);
-        uint32_t vmask = kFull;
-        if (!full)
-          vmask = (tok_ok(2 * j) ? 0x000000ffu : 0u) | (tok_ok(2 * j + 1) ? 0x0000ff00u : 0u) |
-                  (tok_ok(2 * j + 8) ? 0x00ff0000u : 0u) | (tok_ok(2 * j + 9) ? 0xff000000u : 0u);
+        const uint32_t bhi = f16x2x2_to_e4m3x4(tX, tY);
+        uint32_t dX, dY;
+        e4m3x4_to_f16x2(bhi, dX, dY);
+        const uint32_t blo = f16x2x2_to_e4m3x4(hsub2_bits(tX, dX), hsub2_bits(tY, dY));
+        if (!full) {
+          const uint32_t vmask = (tok_ok(2 * j) ? 0x000000ffu : 0u) | (tok_ok(2 * j + 1) ? 0x0000ff00u : 0u) |
+                                 (tok_ok(2 * j + 8) ? 0x00ff0000u : 0u) | (tok_ok(2 * j + 9) ? 0xff000000u : 0u);
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) vf[i][e] &= vmask;
+        }
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
-          const uint32_t a0 = vf[i][0] & vmask, a1 = vf[i][1] & vmask;
-          const uint32_t c0 = vf[i][2] & vmask, c1 = vf[i][3] & vmask;
-          mma_e4m3(acc[2 * i], a0, a1, a0, a1, bhi, blo);
-          mma_e4m3(acc[2 * i + 1], c0, c1, c0, c1, bhi, blo);
+          mma_e4m3(acc[2 * i], vf[i][0], vf[i][1], vf[i][0], vf[i][1], bhi, blo);
+          mma_e4m3(acc[2 * i + 1], vf[i][2], vf[i][3], vf[i][2], vf[i][3], bhi, blo);
         }
       }
     }
@@ -836,10 +851,12 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : 3)) paged_decode_kerne
 // programmatic dependent of the decode kernel: everything before
 // griddepcontrol.wait reads only inputs of the call.
 template <int D, int BS>
-__global__ void __launch_bounds__(512) paged_decode_reduce_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kReduceThreads, kReduceCtas) paged_decode_reduce_kernel(
+    const DecodeParams p) {
   constexpr int kGroups = D / 4;  // float4 column groups per head
-  __shared__ float4 s_o[512];
-  __shared__ float2 s_ml[512];
+  constexpr int kInFlight = PKV_RIF;  // partials loaded at once per thread
+  __shared__ float4 s_o[kReduceThreads];
+  __shared__ float2 s_ml[kReduceThreads];
   const int pair = blockIdx.x;
   const int b = pair / p.n_kv_heads;
   const int h = pair - b * p.n_kv_heads;
@@ -852,9 +869,8 @@ __global__ void __launch_bounds__(512) paged_decode_reduce_kernel(const DecodePa
   const int c4 = idx - hd * kGroups;
   int32_t ctx = p.context_lens[b];
   if (!ctx_ok<BS>(p, ctx)) ctx = 0;
-  const SeqRange r = seq_from_ctx<BS, 1>(ctx, p.window);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (r.nblk == 0) return;  // empty sequences were zeroed by the decode kernel
+  if (ctx == 0) return;  // nothing attended: zeroed by the decode kernel
   const int2 meta = p.pair_meta[pair];
   const int cnt = meta.y;
   if (cnt <= 1) return;  // finished by the one warp that held it
@@ -862,22 +878,26 @@ __global__ void __launch_bounds__(512) paged_decode_reduce_kernel(const DecodePa
   // a pair whose record was never written (its first segment's warp gave up
   // on a wait) can hold anything: stay inside the workspace
   if (meta.x < 0 || slot0 + cnt > p.num_slots) return;
+  // partial k of this thread's head: ml at pm + 2 g k, its columns at po + g D k
+  const float* pm = p.part_ml + (slot0 * g + hd) * 2;
+  const float* po = p.part_o + (slot0 * g + hd) * D + 4 * c4;
+  const int sm = 2 * g, so = g * D;
   float M = -INFINITY, L = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k0 = ks; k0 < cnt; k0 += 4 * KS) {
-    float2 ml[4];
-    float4 o[4];
+  for (int k0 = ks; k0 < cnt; k0 += kInFlight * KS) {
+    float2 ml[kInFlight];
+    float4 o[kInFlight];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kInFlight; ++i) {
       const int k = k0 + i * KS;
       const int kk = k < cnt ? k : k0;
-      ml[i] = *reinterpret_cast<const float2*>(&p.part_ml[((slot0 + kk) * g + hd) * 2]);
-      o[i] = *reinterpret_cast<const float4*>(&p.part_o[((slot0 + kk) * g + hd) * D + 4 * c4]);
-      if (k >= cnt) ml[i] = make_float2(-INFINITY, 0.f);
+      ml[i] = *reinterpret_cast<const float2*>(pm + kk * sm);
+      o[i] = *reinterpret_cast<const float4*>(po + kk * so);
+      if (k >= cnt) ml[i].x = -INFINITY;
     }
     float mb = M;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) mb = fmaxf(mb, ml[i].x);
+    for (int i = 0; i < kInFlight; ++i) mb = fmaxf(mb, ml[i].x);
     if (mb == -INFINITY) continue;
     const float a = fast_exp2(M - mb);  // rescale what was folded so far
     L *= a;
@@ -886,7 +906,7 @@ __global__ void __launch_bounds__(512) paged_decode_reduce_kernel(const DecodePa
     O.z *= a;
     O.w *= a;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kInFlight; ++i) {
       const float f = fast_exp2(ml[i].x - mb);
       L += f * ml[i].y;
       O.x += f * o[i].x;
@@ -1055,7 +1075,7 @@ cudaError_t launch_reduce(const kv_pool* pool, const DecodeParams& p, cudaStream
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.batch) * p.n_kv_heads);
   const int lanes = p.group * pool->head_dim / 4;  // threads per k-slice
-  cfg.blockDim = dim3(lanes * std::max(1, std::min(4, 512 / lanes)));
+  cfg.blockDim = dim3(lanes * std::max(1, std::min(4, kReduceThreads / lanes)));
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
