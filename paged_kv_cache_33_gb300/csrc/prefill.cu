@@ -220,18 +220,34 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       // row maximum in the exp2 domain (scale > 0)
       const float mt_raw = fmaxf(fmaxf(mt4[0], mt4[1]), fmaxf(mt4[2], mt4[3]));
       const float mt = mt_raw == -INFINITY ? -INFINITY : mt_raw * p.scale_log2;
+      // The new running maximum needs no tensor memory: a row with nothing
+      // accumulated yet (O's row is zero) takes it; others keep theirs unless
+      // it grew by more than 2^kLazy.  The exponentials are computed now,
+      // while the previous P V product of this tile may still run; only the
+      // rescale of O and the store of P wait for it.
+      const float m_new = fmaxf(m_run, mt);
+      const bool rescale = m_run != -INFINITY && m_new > m_run + kLazy;
+      const float m_old = m_run;
+      if (m_run == -INFINITY || rescale) m_run = m_new;
+      const float mu = m_run == -INFINITY ? 0.f : m_run;
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nmu2 = make_float2(-mu, -mu);
+      float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      uint32_t w[kKv / 2];  // the P row, bf16 pairs
+#pragma unroll
+      for (int e = 0; e < kKv / 2; ++e) {
+        const float2 arg = ffma2(make_float2(x[2 * e], x[2 * e + 1]), sc2, nmu2);
+        const float2 pe = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
+        l2[e & 1] = fadd2(l2[e & 1], pe);
+        w[e] = pack_bf16x2(pe.x, pe.y);
+      }
       // O and this tile's P buffer are free once its previous product is done
       if (jt > 0) {
         ok = wait(o_done(t), (jt - 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
       }
-      const float m_new = fmaxf(m_run, mt);
-      // a row with nothing accumulated yet (O's row is zero) takes the new
-      // maximum; others keep theirs unless it grew by more than 2^kLazy
-      const bool rescale = m_run != -INFINITY && m_new > m_run + kLazy;
       if (__any_sync(0xffffffffu, rescale)) {  // tensor-memory access is warp-wide
-        const float alpha = rescale ? fast_exp2(m_run - m_new) : 1.f;
+        const float alpha = rescale ? fast_exp2(m_old - m_new) : 1.f;
         l_run *= alpha;
 #pragma unroll
         for (int c0 = 0; c0 < kD; c0 += 32) {
@@ -242,23 +258,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
           tmem_st32(lane_base + 2 * kKv + c0, o);
         }
       }
-      if (m_run == -INFINITY || rescale) m_run = m_new;
       // P row (bf16, 128-byte swizzled) and its sum
-      const float mu = m_run == -INFINITY ? 0.f : m_run;
-      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nmu2 = make_float2(-mu, -mu);
-      float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int cc = 0; cc < kKv / 8; ++cc) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 arg = ffma2(make_float2(x[8 * cc + 2 * e], x[8 * cc + 2 * e + 1]), sc2, nmu2);
-          const float2 pe = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
-          l2[e & 1] = fadd2(l2[e & 1], pe);
-          w[e] = pack_bf16x2(pe.x, pe.y);
-        }
-        *reinterpret_cast<uint4*>(pt + swz128(r, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
+      for (int cc = 0; cc < kKv / 8; ++cc)
+        *reinterpret_cast<uint4*>(pt + swz128(r, cc)) =
+            make_uint4(w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
       l_run += (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
       // V rows the products must not see: slots past the sequence's end and
       // blocks that were not loaded (stale or never-written shared memory).
