@@ -15,21 +15,23 @@
 //    staged once in shared memory (128-byte swizzled, K-major).
 //  * Keys run in tiles of 64 tokens (4 or 2 pool blocks).  A producer warp
 //    gathers each tile's K and V rows with one TMA box per block and column
-//    half into a 3-stage ring; blocks outside the attended range or with a
+//    half into a 4-stage ring; blocks outside the attended range or with a
 //    bad id are left out and their rows masked.
 //  * One thread issues tcgen05.mma: S = Q K^T (128 x 64, fp32 in tensor
 //    memory, double-buffered so S of the next tile runs while the softmax of
-//    this one does), then O += P V (128 x 128, fp32 in tensor memory), with
-//    V read MN-major straight from its pool rows.
+//    this one does), then O += P V (128 x 128, fp32 in tensor memory), P
+//    from tensor memory and V read MN-major straight from its pool rows.
 //  * Two query tiles share every key tile: the tensor cores work on one
 //    tile's products while the softmax warps of the other run, which hides
 //    the latency chain of each (S ready -> softmax -> P -> product).
 //  * Four softmax warps per query tile own one row each per thread: tcgen05.ld the row of
 //    S, mask (causal, window, sequence end, missing blocks), online softmax
 //    in the exp2 domain with a lazy maximum (O in tensor memory is rescaled
-//    only when a row's maximum grows by more than 2^8), P to shared memory
-//    in bf16, and zeros into the V rows the product must not see (slots past
-//    the sequence's end, blocks not loaded).  The epilogue divides O by the
+//    only when a row's maximum grows by more than 2^8), P in bf16 back into
+//    the tensor-memory columns of its S (the P V product reads its A operand
+//    from there, so P never touches shared memory, whose bandwidth the
+//    products' operand reads already use up), and zeros into the V rows the
+//    product must not see (slots past the sequence's end, blocks not loaded).  The epilogue divides O by the
 //    row sum and stores the valid rows.
 //  * Every wait is bounded in wall time; on a timeout the CTA records
 //    KV_ERR_TIMEOUT, drains what it issued and frees its tensor memory.
@@ -46,7 +48,10 @@ constexpr int kD = 128;
 constexpr int kRows = 128;           // query rows per tile (M)
 constexpr int kTiles = 2;            // query tiles per CTA, in ping-pong over the same keys
 constexpr int kKv = 64;              // keys per tile (N of S, K of P V)
-constexpr int kStages = 3;           // K/V ring
+#ifndef PKV_PF_STAGES
+#define PKV_PF_STAGES 4
+#endif
+constexpr int kStages = PKV_PF_STAGES;  // K/V ring
 constexpr int kSoftmax = kTiles * kRows;      // one softmax thread per query row
 constexpr int kThreads = kSoftmax + 64;       // + producer warp + MMA warp
 constexpr int kProducerWarp = kSoftmax / 32, kMmaWarp = kProducerWarp + 1;
@@ -58,14 +63,14 @@ constexpr int kQ = 0;                                 // tiles x 2 halves x [128
 constexpr int kQTile = 2 * kRows * 128;
 constexpr int kK = kQ + kTiles * kQTile;              // stages x 2 halves x [64][64]
 constexpr int kV = kK + kStages * 2 * kKv * 128;
-constexpr int kP = kV + kStages * 2 * kKv * 128;      // tiles x [128][64] bf16
-constexpr int kBars = kP + kTiles * kRows * 128;
+constexpr int kBars = kV + kStages * 2 * kKv * 128;
 // barriers: kv_full[3], kv_empty[3], then per tile s_full[2], p_full, o_done; q_full, mma_done
 constexpr int kNumBars = 2 * kStages + 4 * kTiles + 2;
 constexpr int kTileMask = kBars + kNumBars * 8;       // uint32 [kStages]
 constexpr int kTmemSlot = kTileMask + kStages * 4;
 constexpr int kSmemBytes = kTmemSlot + 16 + 1024;     // + alignment slack
-// tensor memory per query tile: S0 [0,64) S1 [64,128) O [128,256)
+// tensor memory per query tile: S0 [0,64) S1 [64,128) O [128,256); the
+// softmax overwrites the first 32 columns of S_i with P (bf16 pairs)
 constexpr uint32_t kTmemTile = 256;
 constexpr uint32_t kTmemCols = kTiles * kTmemTile;
 
@@ -181,7 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(q_full) : "memory");
     }
     const uint32_t lane_base = tmem + t * kTmemTile + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    uint8_t* pt = smem + kP + t * (kRows * 128);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     const int nt = t ? n_kv1 : n_kv0;
@@ -222,9 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       const float mt = mt_raw == -INFINITY ? -INFINITY : mt_raw * p.scale_log2;
       // The new running maximum needs no tensor memory: a row with nothing
       // accumulated yet (O's row is zero) takes it; others keep theirs unless
-      // it grew by more than 2^kLazy.  The exponentials are computed now,
-      // while the previous P V product of this tile may still run; only the
-      // rescale of O and the store of P wait for it.
+      // it grew by more than 2^kLazy.  The exponentials and the store of P
+      // (into the other S buffer) proceed while the previous P V product of
+      // this tile may still run; the rescale of O waits for it.
       const float m_new = fmaxf(m_run, mt);
       const bool rescale = m_run != -INFINITY && m_new > m_run + kLazy;
       const float m_old = m_run;
@@ -240,7 +244,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         l2[e & 1] = fadd2(l2[e & 1], pe);
         w[e] = pack_bf16x2(pe.x, pe.y);
       }
-      // O and this tile's P buffer are free once its previous product is done
+      // P row (bf16 pairs) over the S columns just read: the product of key
+      // tile jt takes its A operand from there, and S of key tile jt + 2,
+      // the next writer of these columns, is issued after that product
+      tmem_st32(lane_base + sb * kKv, w);
+      // The previous product of this tile: O is stable once it is done.  The
+      // wait is taken every key tile, so the barrier's phases stay in step
+      // with jt (its parity then names exactly one product).
       if (jt > 0) {
         ok = wait(o_done(t), (jt - 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -258,11 +268,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
           tmem_st32(lane_base + 2 * kKv + c0, o);
         }
       }
-      // P row (bf16, 128-byte swizzled) and its sum
-#pragma unroll
-      for (int cc = 0; cc < kKv / 8; ++cc)
-        *reinterpret_cast<uint4*>(pt + swz128(r, cc)) =
-            make_uint4(w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
       l_run += (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
       // V rows the products must not see: slots past the sequence's end and
       // blocks that were not loaded (stale or never-written shared memory).
@@ -356,31 +361,35 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     if (lane == 0) {
       constexpr uint32_t idS = umma_idesc_bf16(kRows, kKv, false);
       constexpr uint32_t idO = umma_idesc_bf16(kRows, kD, true);
-      const uint32_t qs = smem_addr(smem + kQ), ps = smem_addr(smem + kP);
+      // Descriptors as 32-bit halves, computed once: a stage or k-step moves
+      // only the start address (16-byte units, low half).
+      const uint64_t q_desc = umma_desc_sw128(smem_addr(smem + kQ), 16, 1024);
+      const uint64_t k_desc = umma_desc_sw128(smem_addr(smem + kK), 16, 1024);
+      const uint64_t v_desc = umma_desc_sw128(smem_addr(smem + kV), kKv * 128, 1024);
+      const uint32_t q_lo = static_cast<uint32_t>(q_desc), q_hi = static_cast<uint32_t>(q_desc >> 32);
+      const uint32_t k_lo = static_cast<uint32_t>(k_desc), k_hi = static_cast<uint32_t>(k_desc >> 32);
+      const uint32_t v_lo = static_cast<uint32_t>(v_desc), v_hi = static_cast<uint32_t>(v_desc >> 32);
+      constexpr uint32_t kStageUnits = (2 * kKv * 128) >> 4;
       bool ok = wait(q_full, 0);
       if (ok) tc_fence_after();
       auto issue_s = [&](int t, int jt) {
-        const int s = jt % kStages;
-        const uint32_t ks = smem_addr(smem + kK + s * (2 * kKv * 128));
-        const uint32_t qt = qs + t * kQTile;
+        const uint32_t ka = k_lo + (jt % kStages) * kStageUnits;
+        const uint32_t qa = q_lo + t * (kQTile >> 4);
+        const uint32_t d = tmem + t * kTmemTile + (jt & 1) * kKv;
 #pragma unroll
-        for (int k = 0; k < kD / 16; ++k) {
-          const uint64_t a = umma_desc_sw128(qt + (k >> 2) * (kRows * 128) + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = umma_desc_sw128(ks + (k >> 2) * (kKv * 128) + (k & 3) * 32, 16, 1024);
-          umma_bf16(tmem + t * kTmemTile + (jt & 1) * kKv, a, bd, idS, k > 0);
-        }
+        for (int k = 0; k < kD / 16; ++k)
+          umma_bf16_w(d, qa + (((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4), q_hi,
+                      ka + (((k >> 2) * (kKv * 128) + (k & 3) * 32) >> 4), k_hi, idS, k > 0);
         umma_commit(s_full(t, jt & 1));
       };
       auto issue_pv = [&](int t, int jt) {
-        const int s = jt % kStages;
-        const uint32_t vs = smem_addr(smem + kV + s * (2 * kKv * 128));
-        const uint32_t pt = ps + t * (kRows * 128);
+        const uint32_t va = v_lo + (jt % kStages) * kStageUnits;
+        const uint32_t pt = tmem + t * kTmemTile + (jt & 1) * kKv;  // P in tensor memory
+        const uint32_t d = tmem + t * kTmemTile + 2 * kKv;
 #pragma unroll
-        for (int k = 0; k < kKv / 16; ++k) {
-          const uint64_t a = umma_desc_sw128(pt + k * 32, 16, 1024);
-          const uint64_t bd = umma_desc_sw128(vs + k * 16 * 128, kKv * 128, 1024);
-          umma_bf16(tmem + t * kTmemTile + 2 * kKv, a, bd, idO, (jt > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < kKv / 16; ++k)
+          umma_bf16_ta_w(d, pt + k * 8, va + ((k * 16 * 128) >> 4), v_hi, idO,
+                         (jt > 0 || k > 0) ? 1u : 0u);
         umma_commit(o_done(t));
       };
       // P V of key tile jt for every query tile that has it; then the stage is free
