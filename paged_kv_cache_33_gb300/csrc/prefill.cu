@@ -307,19 +307,35 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   } else if (warp == kProducerWarp) {
     // =========================== producer: K and V rows of each key tile
     if (lane == 0) {
+      // The block-table entries of a key tile are read one tile ahead, so
+      // their global-memory latency overlaps the wait for a free stage.
+      const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.mbs;
+      auto needed = [&](int jt, int i) {
+        const int k0 = (jt0 + jt) * kKv + i * BS;
+        return k0 + BS > kv_begin && k0 < kv_end;
+      };
+      int next[kKv / BS];
+      auto fetch = [&](int jt) {
+#pragma unroll
+        for (int i = 0; i < kKv / BS; ++i)
+          next[i] = needed(jt, i) ? trow[((jt0 + jt) * kKv + i * BS) / BS] : 0;
+      };
+      if (n_tiles > 0) fetch(0);
       int issued = 0;
       for (int jt = 0; jt < n_tiles; ++jt) {
         const int s = jt % kStages;
+        int cur[kKv / BS];
+#pragma unroll
+        for (int i = 0; i < kKv / BS; ++i) cur[i] = next[i];
+        if (jt + 1 < n_tiles) fetch(jt + 1);
         if (jt >= kStages && !wait(kv_empty(s), ((jt / kStages) - 1) & 1)) break;
-        const int key0 = (jt0 + jt) * kKv;
         uint32_t mask = 0;
         int phys[kKv / BS];
 #pragma unroll
         for (int i = 0; i < kKv / BS; ++i) {
-          const int k0 = key0 + i * BS;
           phys[i] = -1;
-          if (k0 + BS <= kv_begin || k0 >= kv_end) continue;
-          const int e = p.block_tables[static_cast<int64_t>(b) * p.mbs + k0 / BS];
+          if (!needed(jt, i)) continue;
+          const int e = cur[i];
           if (e < 0 || e >= p.num_blocks) {
             atomicOr(p.err, kErrBadBlock);
             continue;
