@@ -13,26 +13,31 @@
 //  * Rows of the tile are (new token, query head of the group) pairs, the
 //    group padded to a power of two Gp: 128 / Gp tokens x Gp heads.  Q is
 //    staged once in shared memory (128-byte swizzled, K-major).
-//  * Keys run in tiles of 64 tokens (4 or 2 pool blocks).  A producer warp
-//    gathers each tile's K and V rows with one TMA box per block and column
-//    half into a 4-stage ring; blocks outside the attended range or with a
-//    bad id are left out and their rows masked.
-//  * One thread issues tcgen05.mma: S = Q K^T (128 x 64, fp32 in tensor
-//    memory, double-buffered so S of the next tile runs while the softmax of
-//    this one does), then O += P V (128 x 128, fp32 in tensor memory), P
+//  * Keys run in tiles of 128 tokens (8 or 4 pool blocks).  Two producer
+//    warps gather each tile's K rows and V rows with one TMA box per block
+//    and column half, K into a 3-stage ring and V into a 2-stage ring: a K
+//    stage is refilled as soon as the S products of its tile are done, a V
+//    stage once its P V products are.  Blocks outside the attended range or
+//    with a bad id are left out and their rows masked.
+//  * One thread issues tcgen05.mma: S = Q K^T (128 x 128, fp32 in tensor
+//    memory), then O += P V (128 x 128, fp32 in tensor memory) with P read
 //    from tensor memory and V read MN-major straight from its pool rows.
-//  * Two query tiles share every key tile: the tensor cores work on one
-//    tile's products while the softmax warps of the other run, which hides
-//    the latency chain of each (S ready -> softmax -> P -> product).
-//  * Four softmax warps per query tile own one row each per thread: tcgen05.ld the row of
-//    S, mask (causal, window, sequence end, missing blocks), online softmax
-//    in the exp2 domain with a lazy maximum (O in tensor memory is rescaled
-//    only when a row's maximum grows by more than 2^8), P in bf16 back into
-//    the tensor-memory columns of its S (the P V product reads its A operand
-//    from there, so P never touches shared memory, whose bandwidth the
-//    products' operand reads already use up), and zeros into the V rows the
-//    product must not see (slots past the sequence's end, blocks not loaded).  The epilogue divides O by the
-//    row sum and stores the valid rows.
+//    128-key products run the tensor pipe at its full rate; 64-key ones
+//    reach two thirds of it.
+//  * Two query tiles share every key tile and alternate on the tensor pipe:
+//    the products of one tile run while the softmax warps of the other do.
+//    Each tile has one S buffer: S of the next key tile is issued once the
+//    P V product that reads P from it has completed (products with different
+//    accumulators are not ordered), so a finished S also means O is stable.
+//  * Four softmax warps per query tile own one row each per thread: one
+//    tensor-memory load of the row of S (128 columns), masking (causal, window, sequence end, missing blocks),
+//    online softmax in the exp2 domain with a lazy maximum (O in tensor
+//    memory is rescaled only when a row's maximum grows by more than 2^8),
+//    P in bf16 back over the first columns of S (P never touches shared
+//    memory, whose bandwidth the products' operand reads use), and zeros into
+//    the V rows the product must not see (slots past the sequence's end,
+//    blocks not loaded).  The epilogue divides O by the row sum and stores
+//    the valid rows.
 //  * Every wait is bounded in wall time; on a timeout the CTA records
 //    KV_ERR_TIMEOUT, drains what it issued and frees its tensor memory.
 
@@ -46,33 +51,58 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kRows = 128;           // query rows per tile (M)
-constexpr int kTiles = 2;            // query tiles per CTA, in ping-pong over the same keys
-constexpr int kKv = 64;              // keys per tile (N of S, K of P V)
-#ifndef PKV_PF_STAGES
-#define PKV_PF_STAGES 4
-#endif
-constexpr int kStages = PKV_PF_STAGES;  // K/V ring
+constexpr int kTiles = 2;            // query tiles per CTA, alternating over the same keys
+constexpr int kKv = 128;             // keys per key tile (N of S, K of P V)
+constexpr int kKStages = 3;          // K ring
+constexpr int kVStages = 2;          // V ring
 constexpr int kSoftmax = kTiles * kRows;      // one softmax thread per query row
-constexpr int kThreads = kSoftmax + 64;       // + producer warp + MMA warp
-constexpr int kProducerWarp = kSoftmax / 32, kMmaWarp = kProducerWarp + 1;
+constexpr int kThreads = kSoftmax + 96;       // + K producer, V producer, MMA warps
+constexpr int kKWarp = kSoftmax / 32, kVWarp = kKWarp + 1, kMmaWarp = kVWarp + 1;
 constexpr float kLazy = 8.f;         // rescale O when a row maximum grows by more than this (log2)
 constexpr uint64_t kShortWaitNs = 200000;
 
 // Shared memory (offsets from a 1024-aligned base).
 constexpr int kQ = 0;                                 // tiles x 2 halves x [128][64] bf16
 constexpr int kQTile = 2 * kRows * 128;
-constexpr int kK = kQ + kTiles * kQTile;              // stages x 2 halves x [64][64]
-constexpr int kV = kK + kStages * 2 * kKv * 128;
-constexpr int kBars = kV + kStages * 2 * kKv * 128;
-// barriers: kv_full[3], kv_empty[3], then per tile s_full[2], p_full, o_done; q_full, mma_done
-constexpr int kNumBars = 2 * kStages + 4 * kTiles + 2;
-constexpr int kTileMask = kBars + kNumBars * 8;       // uint32 [kStages]
-constexpr int kTmemSlot = kTileMask + kStages * 4;
+constexpr int kKvStage = 2 * kKv * 128;               // 2 column halves x [128 keys][64] bf16
+constexpr int kK = kQ + kTiles * kQTile;
+constexpr int kV = kK + kKStages * kKvStage;
+constexpr int kBars = kV + kVStages * kKvStage;
+// barriers: k_full[3], k_empty[3], v_full[2], v_empty[2], per tile s_full, p_full,
+// pv_done, o_final; q_full, mma_done
+constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 4 * kTiles + 2;
+constexpr int kTmemSlot = kBars + kNumBars * 8;
 constexpr int kSmemBytes = kTmemSlot + 16 + 1024;     // + alignment slack
-// tensor memory per query tile: S0 [0,64) S1 [64,128) O [128,256); the
-// softmax overwrites the first 32 columns of S_i with P (bf16 pairs)
+static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
+// tensor memory per query tile: S [0,128) (P over its first 64 columns), O [128,256)
+constexpr uint32_t kOCol = kKv;
 constexpr uint32_t kTmemTile = 256;
 constexpr uint32_t kTmemCols = kTiles * kTmemTile;
+
+// Exponentials off the MUFU pipe: of every 8 pairs of a P row, kPolyPairs
+// are evaluated as 2^x = 2^n * 2^f with n = round(x), f = x - n in [-1/2, 1/2]
+// and 2^f by a cubic fitted here to relative error 2.2e-4 (well under the
+// 2^-9 of the bf16 P it feeds), the power of two added to the exponent bits.
+#ifndef PKV_PF_POLY
+#define PKV_PF_POLY 0
+#endif
+constexpr int kPolyPairs = PKV_PF_POLY;
+
+__device__ __forceinline__ float2 exp2_poly2(float2 x0) {
+  constexpr float kRound = 12582912.f;  // 1.5 * 2^23: adding it rounds to an integer
+  const float2 x = make_float2(fmaxf(x0.x, -126.f), fmaxf(x0.y, -126.f));
+  const float2 r = fadd2(x, make_float2(kRound, kRound));
+  const float2 n = fadd2(r, make_float2(-kRound, -kRound));
+  const float2 f = fadd2(x, make_float2(-n.x, -n.y));
+  float2 q = ffma2(f, make_float2(0x1.b1170cp-5f, 0x1.b1170cp-5f), make_float2(0x1.efed54p-3f, 0x1.efed54p-3f));
+  q = ffma2(q, f, make_float2(0x1.631dcep-1f, 0x1.631dcep-1f));
+  q = ffma2(q, f, make_float2(0x1.fffb1ep-1f, 0x1.fffb1ep-1f));
+  // the low mantissa bits of r hold n: shifted into the exponent field;
+  // below 2^-126 (masked keys are -inf) the result is 0, as from MUFU
+  const float a = __int_as_float(__float_as_int(q.x) + (__float_as_int(r.x) << 23));
+  const float b = __int_as_float(__float_as_int(q.y) + (__float_as_int(r.y) << 23));
+  return make_float2(x0.x < -126.f ? 0.f : a, x0.y < -126.f ? 0.f : b);
+}
 
 __device__ __forceinline__ int swz128(int row, int chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
@@ -114,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   if (tok0 >= qn) return;
   const int pos_base = ctx - qn;  // position of new token 0
   // tile t holds tokens tok0 + t * tpt .. (ntok[t] of them; tile 1 may be empty)
-  static_assert(kTiles == 2, "two query tiles in ping-pong");
+  static_assert(kTiles == 2, "two query tiles alternating");
   const int kv_begin = p.window > 0 ? max(0, pos_base + tok0 + 1 - p.window) : 0;
   const int jt0 = kv_begin / kKv;
   const int ntok0 = min(tpt, qn - tok0), ntok1 = max(0, min(tpt, qn - tok0 - tpt));
@@ -127,26 +157,33 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBars);
   const uint32_t bar0 = smem_addr(bars);
-  auto kv_full = [&](int s) { return bar0 + 8u * s; };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
-  auto s_full = [&](int t, int i) { return bar0 + 8u * (2 * kStages + 4 * t + i); };
-  auto p_full = [&](int t) { return bar0 + 8u * (2 * kStages + 4 * t + 2); };
-  auto o_done = [&](int t) { return bar0 + 8u * (2 * kStages + 4 * t + 3); };
-  const uint32_t q_full = bar0 + 8u * (2 * kStages + 4 * kTiles);
+  auto k_full = [&](int s) { return bar0 + 8u * s; };
+  auto k_empty = [&](int s) { return bar0 + 8u * (kKStages + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (2 * kKStages + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (2 * kKStages + kVStages + s); };
+  constexpr int kTileBars = 2 * kKStages + 2 * kVStages;
+  auto s_full = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t); };
+  auto p_full = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t + 1); };
+  auto pv_done = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t + 2); };
+  auto o_final = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t + 3); };
+  const uint32_t q_full = bar0 + 8u * (kTileBars + 4 * kTiles);
   const uint32_t mma_done = q_full + 8;
-  uint32_t* tile_mask = reinterpret_cast<uint32_t*>(smem + kTileMask);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
     }
     for (int t = 0; t < kTiles; ++t) {
-      mbar_init(s_full(t, 0), 1);
-      mbar_init(s_full(t, 1), 1);
+      mbar_init(s_full(t), 1);
       mbar_init(p_full(t), kRows);
-      mbar_init(o_done(t), 1);
+      mbar_init(pv_done(t), 1);
+      mbar_init(o_final(t), 1);
     }
     mbar_init(q_full, kSoftmax);
     mbar_init(mma_done, 1);
@@ -161,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     return mbar_wait_bounded(bar, parity, p.wait_limit_ns, p.err, kErrTimeout, kShortWaitNs);
   };
 
-  if (warp < kProducerWarp) {
+  if (warp < kKWarp) {
     // ====== softmax warps: warps 4t..4t+3 serve query tile t, one row per thread
     const int t = warp >> 2;
     const int r = tid & (kRows - 1);
@@ -186,107 +223,115 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(q_full) : "memory");
     }
     const uint32_t lane_base = tmem + t * kTmemTile + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    constexpr uint32_t kAllBlocks = (1u << (kKv / BS)) - 1u;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     const int nt = t ? n_kv1 : n_kv0;
+    // Which blocks of a key tile hold keys: the same rule the producers use
+    // (inside [kv_begin, kv_end), a table entry inside the pool), from the
+    // table entries read one key tile ahead, so the softmax never waits for
+    // the V copy it does not read.
+    const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.mbs;
+    auto needed = [&](int jt, int i) {
+      const int k0 = (jt0 + jt) * kKv + i * BS;
+      return k0 + BS > kv_begin && k0 < kv_end;
+    };
+    int next[kKv / BS];
+    auto fetch = [&](int jt) {
+#pragma unroll
+      for (int i = 0; i < kKv / BS; ++i)
+        next[i] = needed(jt, i) ? trow[((jt0 + jt) * kKv + i * BS) / BS] : -1;
+    };
+    if (nt > 0) fetch(0);
     for (int jt = 0; jt < nt && ok; ++jt) {
-      const int s = jt % kStages, sb = jt & 1;
-      ok = wait(s_full(t, sb), (jt >> 1) & 1) && wait(kv_full(s), (jt / kStages) & 1);
+      uint32_t mask = 0;
+#pragma unroll
+      for (int i = 0; i < kKv / BS; ++i)
+        if (next[i] >= 0 && next[i] < p.num_blocks) mask |= 1u << i;
+      if (jt + 1 < nt) fetch(jt + 1);
+      const int sv = jt % kVStages;
+      ok = wait(s_full(t), jt & 1);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t mask = tile_mask[s];
       const int key0 = (jt0 + jt) * kKv;
-      // raw scores; masked keys become -inf (the scale is applied in the exp)
-      float x[kKv];
-      float mt4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      {
-        uint32_t raw[2][32];
-        tmem_ld32x2(lane_base + sb * kKv, lane_base + sb * kKv + 32, raw[0], raw[1]);
-        // rows of this warp that see every key of the tile need no mask
-        const bool whole = row_ok && key0 >= lo && key0 + kKv - 1 <= pos &&
-                           mask == (1u << (kKv / BS)) - 1u;
-        if (__all_sync(0xffffffffu, whole)) {
+      // the row of S: one tensor-memory load of all kKv columns
+      uint32_t x[kKv];
+      tmem_ld128(lane_base, x);
+      // rows of this warp that see every key of the tile need no mask;
+      // masked keys become -inf (the scale is applied in the exp)
+      if (!__all_sync(0xffffffffu, row_ok && key0 >= lo && key0 + kKv - 1 <= pos &&
+                                       mask == kAllBlocks)) {
 #pragma unroll
-          for (int c = 0; c < kKv; ++c) {
-            x[c] = __uint_as_float(raw[c >> 5][c & 31]);
-            mt4[c & 3] = fmaxf(mt4[c & 3], x[c]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kKv; ++c) {
-            const int key = key0 + c;
-            const bool valid = row_ok && key >= lo && key <= pos && ((mask >> (c / BS)) & 1u);
-            x[c] = valid ? __uint_as_float(raw[c >> 5][c & 31]) : -INFINITY;
-            mt4[c & 3] = fmaxf(mt4[c & 3], x[c]);
-          }
+        for (int c = 0; c < kKv; ++c) {
+          const int key = key0 + c;
+          const bool valid = row_ok && key >= lo && key <= pos && ((mask >> (c / BS)) & 1u);
+          if (!valid) x[c] = __float_as_uint(-INFINITY);
         }
       }
-      // row maximum in the exp2 domain (scale > 0)
+      float mt4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < kKv; ++c) mt4[c & 3] = fmaxf(mt4[c & 3], __uint_as_float(x[c]));
       const float mt_raw = fmaxf(fmaxf(mt4[0], mt4[1]), fmaxf(mt4[2], mt4[3]));
       const float mt = mt_raw == -INFINITY ? -INFINITY : mt_raw * p.scale_log2;
-      // The new running maximum needs no tensor memory: a row with nothing
-      // accumulated yet (O's row is zero) takes it; others keep theirs unless
-      // it grew by more than 2^kLazy.  The exponentials and the store of P
-      // (into the other S buffer) proceed while the previous P V product of
-      // this tile may still run; the rescale of O waits for it.
+      // A row with nothing accumulated yet (O's row is zero) takes the new
+      // maximum; others keep theirs unless it grew by more than 2^kLazy.
       const float m_new = fmaxf(m_run, mt);
       const bool rescale = m_run != -INFINITY && m_new > m_run + kLazy;
       const float m_old = m_run;
       if (m_run == -INFINITY || rescale) m_run = m_new;
       const float mu = m_run == -INFINITY ? 0.f : m_run;
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nmu2 = make_float2(-mu, -mu);
+      // the exponentials; P (bf16 pairs) over the first kKv/2 columns of S,
+      // one tensor-memory store
       float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      uint32_t w[kKv / 2];  // the P row, bf16 pairs
+      uint32_t w[kKv / 2];
 #pragma unroll
       for (int e = 0; e < kKv / 2; ++e) {
-        const float2 arg = ffma2(make_float2(x[2 * e], x[2 * e + 1]), sc2, nmu2);
-        const float2 pe = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
+        const float2 arg = ffma2(make_float2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])),
+                                 sc2, nmu2);
+        const float2 pe = (e % 8) < kPolyPairs ? exp2_poly2(arg)
+                                               : make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
         l2[e & 1] = fadd2(l2[e & 1], pe);
         w[e] = pack_bf16x2(pe.x, pe.y);
       }
-      // P row (bf16 pairs) over the S columns just read: the product of key
-      // tile jt takes its A operand from there, and S of key tile jt + 2,
-      // the next writer of these columns, is issued after that product
-      tmem_st32(lane_base + sb * kKv, w);
-      // The previous product of this tile: O is stable once it is done.  The
-      // wait is taken every key tile, so the barrier's phases stay in step
-      // with jt (its parity then names exactly one product).
-      if (jt > 0) {
-        ok = wait(o_done(t), (jt - 1) & 1);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-      }
+      tmem_st64(lane_base, w);
+      // O is stable: S of this key tile was issued only after the tile's
+      // previous P V product had completed
       if (__any_sync(0xffffffffu, rescale)) {  // tensor-memory access is warp-wide
         const float alpha = rescale ? fast_exp2(m_old - m_new) : 1.f;
         l_run *= alpha;
 #pragma unroll
         for (int c0 = 0; c0 < kD; c0 += 32) {
           uint32_t o[32];
-          tmem_ld32(lane_base + 2 * kKv + c0, o);
+          tmem_ld32(lane_base + kOCol + c0, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(lane_base + 2 * kKv + c0, o);
+          tmem_st32(lane_base + kOCol + c0, o);
         }
       }
       l_run += (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
       // V rows the products must not see: slots past the sequence's end and
       // blocks that were not loaded (stale or never-written shared memory).
       // The first query tile that uses this key tile does it before handing
-      // its P over; the products of the other tile are issued after that.
+      // its P over; the product of the other tile is issued after that.
       const int zero_tile = jt < n_kv0 ? 0 : 1;
-      if (t == zero_tile && (mask != (1u << (kKv / BS)) - 1u || key0 + kKv > ctx)) {
+      if (t == zero_tile && (mask != kAllBlocks || key0 + kKv > ctx)) {
+        // the V stage of this key tile cannot be refilled before this tile's
+        // P of it is consumed, so its phase is safe to wait on here
+        ok = wait(v_full(sv), (jt / kVStages) & 1);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         for (int idx = r; idx < kKv * 2 * 8; idx += kRows) {
           const int key = idx >> 4, half = (idx >> 3) & 1, chunk = idx & 7;
           if (key0 + key >= ctx || !((mask >> (key / BS)) & 1u))
-            *reinterpret_cast<uint4*>(smem + kV + s * (2 * kKv * 128) + half * (kKv * 128) +
-                                      key * 128 + chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(smem + kV + sv * kKvStage + half * (kKv * 128) + key * 128 +
+                                      chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(p_full(t)) : "memory");
     }
-    if (ok && nt > 0) ok = __all_sync(0xffffffffu, wait(o_done(t), (nt - 1) & 1));
+    if (ok && nt > 0) ok = __all_sync(0xffffffffu, wait(o_final(t), 0));
     if (ok && nt > 0) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -294,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
 #pragma unroll
       for (int c0 = 0; c0 < kD; c0 += 32) {
         uint32_t o[32];
-        tmem_ld32(lane_base + 2 * kKv + c0, o);
+        tmem_ld32(lane_base + kOCol + c0, o);
         if (row_ok) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
@@ -304,9 +349,16 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         }
       }
     }
-  } else if (warp == kProducerWarp) {
-    // =========================== producer: K and V rows of each key tile
+  } else if (warp == kKWarp || warp == kVWarp) {
+    // =========================== producers: the K rows (one warp) and the V
+    // rows (the other) of each key tile, each into its own ring
     if (lane == 0) {
+      const bool is_v = warp == kVWarp;
+      const int stages = is_v ? kVStages : kKStages;
+      const int rows = is_v ? 1 : 0;  // the pool's K / V index
+      uint8_t* ring = smem + (is_v ? kV : kK);
+      auto full = [&](int s) { return is_v ? v_full(s) : k_full(s); };
+      auto empty = [&](int s) { return is_v ? v_empty(s) : k_empty(s); };
       // The block-table entries of a key tile are read one tile ahead, so
       // their global-memory latency overlaps the wait for a free stage.
       const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.mbs;
@@ -323,12 +375,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       if (n_tiles > 0) fetch(0);
       int issued = 0;
       for (int jt = 0; jt < n_tiles; ++jt) {
-        const int s = jt % kStages;
+        const int s = jt % stages;
         int cur[kKv / BS];
 #pragma unroll
         for (int i = 0; i < kKv / BS; ++i) cur[i] = next[i];
         if (jt + 1 < n_tiles) fetch(jt + 1);
-        if (jt >= kStages && !wait(kv_empty(s), ((jt / kStages) - 1) & 1)) break;
+        if (jt >= stages && !wait(empty(s), ((jt / stages) - 1) & 1)) break;
         uint32_t mask = 0;
         int phys[kKv / BS];
 #pragma unroll
@@ -337,43 +389,40 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
           if (!needed(jt, i)) continue;
           const int e = cur[i];
           if (e < 0 || e >= p.num_blocks) {
-            atomicOr(p.err, kErrBadBlock);
+            if (!is_v) atomicOr(p.err, kErrBadBlock);
             continue;
           }
           phys[i] = e;
           mask |= 1u << i;
         }
-        tile_mask[s] = mask;
-        const uint32_t bar = kv_full(s);
+        const uint32_t bar = full(s);
         const int nblk = __popc(mask);
         if (nblk == 0) {
           asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
         } else {
-          mbar_arrive_expect_tx(bar, nblk * 2 * 2 * BS * 128);
-          const uint32_t ks = smem_addr(smem + kK + s * (2 * kKv * 128));
-          const uint32_t vs = smem_addr(smem + kV + s * (2 * kKv * 128));
+          mbar_arrive_expect_tx(bar, nblk * 2 * BS * 128);
+          const uint32_t st = smem_addr(ring + s * kKvStage);
 #pragma unroll
           for (int i = 0; i < kKv / BS; ++i) {
             if (phys[i] < 0) continue;
             const int tile = phys[i] * p.n_kv_heads + h;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const uint32_t off = half * (kKv * 128) + i * BS * 128;
-              tma_load_4d(ks + off, &tmap, bar, half * 64, 0, 0, tile);
-              tma_load_4d(vs + off, &tmap, bar, half * 64, 0, 1, tile);
-            }
+            for (int half = 0; half < 2; ++half)
+              tma_load_4d(st + half * (kKv * 128) + i * BS * 128, &tmap, bar, half * 64, 0, rows,
+                          tile);
           }
         }
         ++issued;
       }
       // leave no copy in flight: wait (bounded) for the stages not yet consumed
-      for (int jt = max(0, issued - kStages); jt < issued; ++jt)
-        wait(kv_full(jt % kStages), (jt / kStages) & 1);
+      for (int jt = max(0, issued - stages); jt < issued; ++jt)
+        wait(full(jt % stages), (jt / stages) & 1);
     }
     __syncwarp();
   } else {
-    // =========================== MMA issuer: for every key tile, S of both
-    // query tiles, then the P V products of the previous key tile
+    // =========================== MMA issuer.  Key tile jt: for each query
+    // tile, the P V product of key tile jt - 1 (which reads P from the S
+    // buffer), then S of key tile jt into that buffer.
     if (lane == 0) {
       constexpr uint32_t idS = umma_idesc_bf16(kRows, kKv, false);
       constexpr uint32_t idO = umma_idesc_bf16(kRows, kD, true);
@@ -385,49 +434,68 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       const uint32_t q_lo = static_cast<uint32_t>(q_desc), q_hi = static_cast<uint32_t>(q_desc >> 32);
       const uint32_t k_lo = static_cast<uint32_t>(k_desc), k_hi = static_cast<uint32_t>(k_desc >> 32);
       const uint32_t v_lo = static_cast<uint32_t>(v_desc), v_hi = static_cast<uint32_t>(v_desc >> 32);
-      constexpr uint32_t kStageUnits = (2 * kKv * 128) >> 4;
+      constexpr uint32_t kStageUnits = kKvStage >> 4;
       bool ok = wait(q_full, 0);
       if (ok) tc_fence_after();
       auto issue_s = [&](int t, int jt) {
-        const uint32_t ka = k_lo + (jt % kStages) * kStageUnits;
+        const uint32_t ka = k_lo + (jt % kKStages) * kStageUnits;
         const uint32_t qa = q_lo + t * (kQTile >> 4);
-        const uint32_t d = tmem + t * kTmemTile + (jt & 1) * kKv;
+        const uint32_t d = tmem + t * kTmemTile;
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k)
           umma_bf16_w(d, qa + (((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4), q_hi,
                       ka + (((k >> 2) * (kKv * 128) + (k & 3) * 32) >> 4), k_hi, idS, k > 0);
-        umma_commit(s_full(t, jt & 1));
+        umma_commit(s_full(t));
       };
       auto issue_pv = [&](int t, int jt) {
-        const uint32_t va = v_lo + (jt % kStages) * kStageUnits;
-        const uint32_t pt = tmem + t * kTmemTile + (jt & 1) * kKv;  // P in tensor memory
-        const uint32_t d = tmem + t * kTmemTile + 2 * kKv;
+        const uint32_t va = v_lo + (jt % kVStages) * kStageUnits;
+        const uint32_t pt = tmem + t * kTmemTile;  // P over the S columns
+        const uint32_t d = tmem + t * kTmemTile + kOCol;
 #pragma unroll
         for (int k = 0; k < kKv / 16; ++k)
           umma_bf16_ta_w(d, pt + k * 8, va + ((k * 16 * 128) >> 4), v_hi, idO,
                          (jt > 0 || k > 0) ? 1u : 0u);
-        umma_commit(o_done(t));
       };
-      // P V of key tile jt for every query tile that has it; then the stage is free
-      auto issue_pvs = [&](int jt) {
+      for (int jt = 0; ok && jt <= n_tiles; ++jt) {
+        bool v_ready = false, k_ready = false;
         for (int t = 0; t < kTiles && ok; ++t) {
-          if (jt >= (t ? n_kv1 : n_kv0)) continue;
-          ok = wait(p_full(t), jt & 1);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(t, jt);
+          const int nt = t ? n_kv1 : n_kv0;
+          if (jt > 0 && jt - 1 < nt) {
+            if (!v_ready) {
+              ok = wait(v_full((jt - 1) % kVStages), ((jt - 1) / kVStages) & 1);
+              if (!ok) break;
+              v_ready = true;
+            }
+            ok = wait(p_full(t), (jt - 1) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, jt - 1);
+            umma_commit(jt == nt ? o_final(t) : pv_done(t));
+          }
+          if (jt < nt) {
+            // tcgen05 products with different accumulators are not ordered:
+            // S of this key tile overwrites the P the previous product reads,
+            // and the softmax rescales O once this S is done, so that product
+            // must have completed first (the tensor pipe is busy with it
+            // meanwhile)
+            if (jt > 0) {
+              ok = wait(pv_done(t), (jt - 1) & 1);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            if (!k_ready) {
+              ok = wait(k_full(jt % kKStages), (jt / kKStages) & 1);
+              if (!ok) break;
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_s(t, jt);
+          }
         }
-        if (ok) umma_commit(kv_empty(jt % kStages));
-      };
-      for (int jt = 0; ok && jt < n_tiles; ++jt) {
-        ok = wait(kv_full(jt % kStages), (jt / kStages) & 1);
         if (!ok) break;
-        tc_fence_after();
-        for (int t = 0; t < kTiles; ++t)
-          if (jt < (t ? n_kv1 : n_kv0)) issue_s(t, jt);
-        if (jt > 0) issue_pvs(jt - 1);
+        if (k_ready) umma_commit(k_empty(jt % kKStages));  // free once these products are done
+        if (v_ready) umma_commit(v_empty((jt - 1) % kVStages));
       }
-      if (ok) issue_pvs(n_tiles - 1);
       // every product issued has completed before the tensor memory is freed
       umma_commit(mma_done);
       wait(mma_done, 0);

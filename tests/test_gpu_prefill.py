@@ -167,3 +167,38 @@ def test_prefill_host_checks():
         pagedkv.paged_prefill_attention(fp8, q, cu, t, c, 0.1, max_q_len=4, max_context_len=4)
     pool.destroy()
     fp8.destroy()
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+def test_prefill_rescales_on_every_key_tile(bs):
+    """Keys aligned with the queries and growing along the sequence push each
+    row's maximum up by more than the lazy-rescale threshold on nearly every
+    key tile, so O in tensor memory is rescaled again and again (and the
+    product that feeds it must have finished first)."""
+    hkv, hq, ctx, ql = 2, 8, 900, 700
+    nblk = -(-ctx // bs)
+    rng = np.random.default_rng(7)
+    tables = rng.permutation(nblk + 3)[:nblk].astype(np.int32).reshape(1, nblk)
+    pool = pagedkv.KVPool(nblk + 3, bs, hkv, 128, "bf16")
+    poison(pool)
+    opool = oracle.Pool(nblk + 3, bs, hkv, 128, "bf16")
+    g = torch.Generator().manual_seed(8)
+    direction = torch.randn(hkv, 128, generator=g)
+    direction = direction / direction.norm(dim=1, keepdim=True)
+    growth = torch.arange(ctx, dtype=torch.float32).view(ctx, 1, 1) * 0.02
+    k = (growth * direction.view(1, hkv, 128) + 0.1 * torch.randn(ctx, hkv, 128, generator=g)).bfloat16()
+    v = torch.randn(ctx, hkv, 128, generator=g).bfloat16()
+    pos = np.arange(ctx)
+    slots = tables[0, pos // bs].astype(np.int64) * bs + pos % bs
+    pagedkv.paged_kv_write(pool, k.cuda(), v.cuda(), torch.from_numpy(slots).cuda())
+    opool.write(k, v, slots)
+    q = (direction.repeat_interleave(hq // hkv, dim=0).view(1, hq, 128) * 3
+         + 0.1 * torch.randn(ql, hq, 128, generator=g)).bfloat16()
+    cu = np.array([0, ql], np.int32)
+    lens = np.array([ctx], np.int32)
+    out = _run(pool, q, cu, tables, lens, 1.0)
+    torch.cuda.synchronize()
+    assert pool.check_status() == pagedkv.KV_OK
+    ref = opool.prefill(q, cu, tables, lens, 1.0)
+    _check(out, ref, f"rescale bs={bs}")
+    pool.destroy()
