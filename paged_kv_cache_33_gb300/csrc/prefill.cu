@@ -79,31 +79,6 @@ constexpr uint32_t kOCol = kKv;
 constexpr uint32_t kTmemTile = 256;
 constexpr uint32_t kTmemCols = kTiles * kTmemTile;
 
-// Exponentials off the MUFU pipe: of every 8 pairs of a P row, kPolyPairs
-// are evaluated as 2^x = 2^n * 2^f with n = round(x), f = x - n in [-1/2, 1/2]
-// and 2^f by a cubic fitted here to relative error 2.2e-4 (well under the
-// 2^-9 of the bf16 P it feeds), the power of two added to the exponent bits.
-#ifndef PKV_PF_POLY
-#define PKV_PF_POLY 0
-#endif
-constexpr int kPolyPairs = PKV_PF_POLY;
-
-__device__ __forceinline__ float2 exp2_poly2(float2 x0) {
-  constexpr float kRound = 12582912.f;  // 1.5 * 2^23: adding it rounds to an integer
-  const float2 x = make_float2(fmaxf(x0.x, -126.f), fmaxf(x0.y, -126.f));
-  const float2 r = fadd2(x, make_float2(kRound, kRound));
-  const float2 n = fadd2(r, make_float2(-kRound, -kRound));
-  const float2 f = fadd2(x, make_float2(-n.x, -n.y));
-  float2 q = ffma2(f, make_float2(0x1.b1170cp-5f, 0x1.b1170cp-5f), make_float2(0x1.efed54p-3f, 0x1.efed54p-3f));
-  q = ffma2(q, f, make_float2(0x1.631dcep-1f, 0x1.631dcep-1f));
-  q = ffma2(q, f, make_float2(0x1.fffb1ep-1f, 0x1.fffb1ep-1f));
-  // the low mantissa bits of r hold n: shifted into the exponent field;
-  // below 2^-126 (masked keys are -inf) the result is 0, as from MUFU
-  const float a = __int_as_float(__float_as_int(q.x) + (__float_as_int(r.x) << 23));
-  const float b = __int_as_float(__float_as_int(q.y) + (__float_as_int(r.y) << 23));
-  return make_float2(x0.x < -126.f ? 0.f : a, x0.y < -126.f ? 0.f : b);
-}
-
 __device__ __forceinline__ int swz128(int row, int chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
 }
@@ -289,8 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       for (int e = 0; e < kKv / 2; ++e) {
         const float2 arg = ffma2(make_float2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])),
                                  sc2, nmu2);
-        const float2 pe = (e % 8) < kPolyPairs ? exp2_poly2(arg)
-                                               : make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
+        const float2 pe = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
         l2[e & 1] = fadd2(l2[e & 1], pe);
         w[e] = pack_bf16x2(pe.x, pe.y);
       }
