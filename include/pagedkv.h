@@ -186,7 +186,12 @@ size_t paged_decode_workspace_bytes(const kv_pool* pool, int32_t batch, int32_t 
  *   max_context_len:     host-side upper bound of context_lens (sizes the grid).
  *   scale:               softmax scale applied to q.k.
  *   sliding_window:      <= 0 disables the window.
- *   out_dev:             fp32 [batch][n_q_heads][head_dim], softmax(scale q K^T) V.
+ *   out_dev:             fp32 [batch][n_q_heads][head_dim], softmax(scale q K^T) V;
+ *                        16-byte aligned.  Device memory, or pinned host memory
+ *                        the device can address (cudaHostAlloc, or
+ *                        cudaHostRegister with cudaHostRegisterMapped, under
+ *                        unified addressing): the kernels then write the result
+ *                        into host memory directly, with no separate copy.
  *   workspace_dev:       at least paged_decode_workspace_bytes(...) bytes,
  *                        16-byte aligned; contents need no initialisation.
  * Work is split evenly over a persistent grid (stream-K over the list of

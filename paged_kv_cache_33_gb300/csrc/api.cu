@@ -309,7 +309,8 @@ kv_status decode_call(kv_pool* p, const StepWrite* w, const void* q, int32_t n_q
                ? KV_OK
                : KV_ERR_CUDA;
   }
-  if (!q || !block_tables || !context_lens || !out || !aligned16(q)) return KV_ERR_INVALID_ARG;
+  if (!q || !block_tables || !context_lens || !out || !aligned16(q) || !aligned16(out))
+    return KV_ERR_INVALID_ARG;
   if (max_blocks_per_seq <= 0 || max_context_len < 0 ||
       static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * p->block_size)
     return KV_ERR_INVALID_ARG;

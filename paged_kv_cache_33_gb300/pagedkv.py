@@ -133,6 +133,18 @@ def _dev(t: torch.Tensor, dtype: torch.dtype, name: str) -> ctypes.c_void_p:
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _out(t: torch.Tensor, name: str) -> ctypes.c_void_p:
+    """An fp32 result buffer: a CUDA tensor, or a pinned host tensor, which
+    the kernels write directly (mapped host memory; no device-to-host copy)."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda:
+        if not t.is_pinned():
+            raise TypeError(f"{name} must be a CUDA tensor or a pinned host tensor")
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise TypeError(f"{name} must be contiguous float32")
+        return ctypes.c_void_p(t.data_ptr())
+    return _dev(t, torch.float32, name)
+
+
 class KVPool:
     """One layer's block pool on the current CUDA device (owns its memory)."""
 
@@ -334,12 +346,16 @@ def paged_decode_attention(pool: KVPool, q: torch.Tensor, block_tables: torch.Te
     """Decode attention: q [B, Hq, D] bf16 -> out [B, Hq, D] fp32.
 
     `max_context_len` bounds context_lens (the host side sizes the launch with
-    it); when omitted it is read from context_lens, which synchronises."""
+    it); when omitted it is read from context_lens, which synchronises.  `out`
+    may be a pinned host tensor: the kernels then write the result into host
+    memory directly."""
     B, Hq, D = q.shape
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if B else 0
     if out is None:
         out = torch.empty(B, Hq, D, dtype=torch.float32, device=q.device)
+    if tuple(out.shape) != (B, Hq, D):
+        raise ValueError(f"out must be {(B, Hq, D)}")
     need = paged_decode_workspace_bytes(pool, B, Hq, max_context_len, sliding_window)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -351,7 +367,7 @@ def paged_decode_attention(pool: KVPool, q: torch.Tensor, block_tables: torch.Te
         pool.handle, _dev(q, torch.bfloat16, "q"), Hq,
         _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
         _dev(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
-        int(sliding_window), _dev(out, torch.float32, "out"), ws_ptr, ws_bytes, _stream(stream)),
+        int(sliding_window), _out(out, "out"), ws_ptr, ws_bytes, _stream(stream)),
         "paged_decode_attention")
     return out
 
@@ -363,7 +379,8 @@ def paged_decode_step(pool: KVPool, k: torch.Tensor, v: torch.Tensor, slot_mappi
                       stream=None) -> torch.Tensor:
     """One decode step: write k, v ([T, Hkv, D] bf16) to `slot_mapping`, then
     attend q [B, Hq, D] over the pool; context_lens already count the new
-    tokens.  Returns out [B, Hq, D] fp32."""
+    tokens.  Returns out [B, Hq, D] fp32 (a CUDA tensor, or the pinned host
+    tensor given as `out`, which the kernels write directly)."""
     T = slot_mapping.shape[0]
     shape = (T, pool.n_kv_heads, pool.head_dim)
     if tuple(k.shape) != shape or tuple(v.shape) != shape:
@@ -373,6 +390,8 @@ def paged_decode_step(pool: KVPool, k: torch.Tensor, v: torch.Tensor, slot_mappi
         max_context_len = int(context_lens.max().item()) if B else 0
     if out is None:
         out = torch.empty(B, Hq, D, dtype=torch.float32, device=q.device)
+    if tuple(out.shape) != (B, Hq, D):
+        raise ValueError(f"out must be {(B, Hq, D)}")
     need = paged_decode_workspace_bytes(pool, B, Hq, max_context_len, sliding_window)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -386,7 +405,7 @@ def paged_decode_step(pool: KVPool, k: torch.Tensor, v: torch.Tensor, slot_mappi
         _dev(q, torch.bfloat16, "q"), Hq,
         _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
         _dev(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
-        int(sliding_window), _dev(out, torch.float32, "out"), ws_ptr, ws_bytes, _stream(stream)),
+        int(sliding_window), _out(out, "out"), ws_ptr, ws_bytes, _stream(stream)),
         "paged_decode_step")
     return out
 

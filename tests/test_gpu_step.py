@@ -105,6 +105,39 @@ def test_repeated_steps_reuse_the_workspace():
     pool.destroy()
 
 
+@pytest.mark.parametrize("name", ["8b", "fp8"])
+def test_result_written_into_pinned_host_memory(name):
+    # the kernels write a pinned host `out` directly (mapped host memory): the
+    # same bits as a device result, for the fused step and the plain call
+    w = _workload(name, "small")
+    q, tables, lens = _inputs(w)
+    pool = make_gpu_pool(w)
+    _, (k, v, s) = _setup(w, pool)
+    k, v, s = k.cuda(), v.cuda(), s.cuda()
+    host = torch.full((w.batch, w.n_q_heads, w.head_dim), float("nan")).pin_memory()
+    dev = pagedkv.paged_decode_step(pool, k, v, s, q, tables, lens, w.scale, w.window,
+                                    max_context_len=w.max_context_len)
+    got = pagedkv.paged_decode_step(pool, k, v, s, q, tables, lens, w.scale, w.window,
+                                    max_context_len=w.max_context_len, out=host)
+    torch.cuda.synchronize()
+    assert got is host
+    assert torch.equal(host, dev.cpu())
+    host2 = torch.full_like(host, float("nan")).pin_memory()
+    pagedkv.paged_decode_attention(pool, q, tables, lens, w.scale, w.window,
+                                   max_context_len=w.max_context_len, out=host2)
+    torch.cuda.synchronize()
+    assert torch.equal(host2, dev.cpu())
+    assert pool.check_status() == pagedkv.KV_OK
+    with pytest.raises(TypeError):  # pageable host memory is not accepted
+        pagedkv.paged_decode_attention(pool, q, tables, lens, w.scale, w.window,
+                                       max_context_len=w.max_context_len,
+                                       out=torch.empty_like(host2))
+    with pytest.raises(ValueError):
+        pagedkv.paged_decode_attention(pool, q, tables, lens, w.scale, w.window,
+                                       max_context_len=w.max_context_len, out=host2[:1])
+    pool.destroy()
+
+
 def test_step_over_more_sequences_than_one_launch():
     # 600 sequences: two decode launches, the write fused into the first only
     rng = np.random.default_rng(3)
