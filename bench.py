@@ -346,36 +346,40 @@ def measure_extras(step: Step, peaks: dict, device) -> dict:
         "pairs": n, "block_bytes": blk_bytes, "us_per_call": t * 1e6, "achieved": gbs,
         "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
         "bytes_per_pair": 2 * blk_bytes}
-    # -- paged_prefill_attention: 8B-shaped full prefill, 4 x 2048 tokens
-    B, ctx, hq, hkv = 4, 2048, 32, 8
-    nblk = ctx // 16
-    ppool = pk.KVPool(B * nblk, 16, hkv, 128, "bf16")
-    tables = torch.from_numpy(np.random.default_rng(3).permutation(B * nblk).astype(np.int32)
-                              .reshape(B, nblk)).to(device)
-    g = torch.Generator(device=device).manual_seed(5)
-    kk = torch.randn(B * ctx, hkv, 128, device=device, generator=g).to(torch.bfloat16)
-    pos = torch.arange(ctx, device=device)
-    slots = (tables[:, pos // 16].long() * 16 + pos % 16).reshape(-1)
-    pk.paged_kv_write(ppool, kk, kk, slots)
-    q = torch.randn(B * ctx, hq, 128, device=device, generator=g).to(torch.bfloat16)
-    cu = torch.arange(0, B * ctx + 1, ctx, dtype=torch.int32, device=device)
-    lens = torch.full((B,), ctx, dtype=torch.int32, device=device)
-    pout = torch.empty(B * ctx, hq, 128, device=device)
-    t = _event_time(torch, lambda: pk.paged_prefill_attention(
-        ppool, q, cu, tables, lens, 128 ** -0.5, 0, max_q_len=ctx, max_context_len=ctx,
-        out=pout), 20)
-    flops = 4.0 * 128 * hq * B * (ctx * (ctx + 1) // 2)   # QK and PV over the causal keys
-    tf = flops / t / 1e12
+    # -- paged_prefill_attention: 8B-shaped full causal prefill, 4 x 2048 tokens
+    #    (short prompts: per-CTA set-up weighs more) and 4 x 8192 tokens
     bf16_peak = peaks["bf16_tflops"]
-    out["paged_prefill_attention"] = {
-        "workload": f"full causal prefill, {B} x {ctx} tokens, {hq} q / {hkv} KV heads, "
-                    "head_dim 128, 16-token blocks",
-        "us_per_call": t * 1e6, "achieved": tf, "unit": "TFLOP/s", "bound": "tensor",
-        "peak": bf16_peak, "frac": tf / bf16_peak, "flops_per_call": flops,
-        "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"}
-    if ppool.check_status() != pk.KV_OK or step.pool.check_status() != pk.KV_OK:
-        raise RuntimeError("device error in the extra measurements")
-    ppool.destroy()
+    for key, (B, ctx) in (("paged_prefill_attention", (4, 2048)),
+                          ("paged_prefill_attention_long", (4, 8192))):
+        hq, hkv = 32, 8
+        nblk = ctx // 16
+        ppool = pk.KVPool(B * nblk, 16, hkv, 128, "bf16")
+        tables = torch.from_numpy(np.random.default_rng(3).permutation(B * nblk).astype(np.int32)
+                                  .reshape(B, nblk)).to(device)
+        g = torch.Generator(device=device).manual_seed(5)
+        kk = torch.randn(B * ctx, hkv, 128, device=device, generator=g).to(torch.bfloat16)
+        pos = torch.arange(ctx, device=device)
+        slots = (tables[:, pos // 16].long() * 16 + pos % 16).reshape(-1)
+        pk.paged_kv_write(ppool, kk, kk, slots)
+        q = torch.randn(B * ctx, hq, 128, device=device, generator=g).to(torch.bfloat16)
+        cu = torch.arange(0, B * ctx + 1, ctx, dtype=torch.int32, device=device)
+        lens = torch.full((B,), ctx, dtype=torch.int32, device=device)
+        pout = torch.empty(B * ctx, hq, 128, device=device)
+        t = _event_time(torch, lambda: pk.paged_prefill_attention(
+            ppool, q, cu, tables, lens, 128 ** -0.5, 0, max_q_len=ctx, max_context_len=ctx,
+            out=pout), 20)
+        flops = 4.0 * 128 * hq * B * (ctx * (ctx + 1) // 2)   # QK and PV over the causal keys
+        tf = flops / t / 1e12
+        out[key] = {
+            "workload": f"full causal prefill, {B} x {ctx} tokens, {hq} q / {hkv} KV heads, "
+                        "head_dim 128, 16-token blocks",
+            "us_per_call": t * 1e6, "achieved": tf, "unit": "TFLOP/s", "bound": "tensor",
+            "peak": bf16_peak, "frac": tf / bf16_peak, "flops_per_call": flops,
+            "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"}
+        if ppool.check_status() != pk.KV_OK or step.pool.check_status() != pk.KV_OK:
+            raise RuntimeError("device error in the extra measurements")
+        ppool.destroy()
+        del kk, q, pout, tables, slots
     # -- host block manager: one decode step's inputs for the bench batch, and
     #    admit / append / free churn
     need = sum(-(-int(c) // w.block_size) for c in w.context_lens)
