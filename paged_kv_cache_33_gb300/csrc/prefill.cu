@@ -12,7 +12,8 @@
 // How (GB300 design), one CTA per (two 128-row query tiles, KV head, sequence):
 //  * Rows of the tile are (new token, query head of the group) pairs, the
 //    group padded to a power of two Gp: 128 / Gp tokens x Gp heads.  Q is
-//    staged once in shared memory (128-byte swizzled, K-major).
+//    staged once in shared memory (128-byte swizzled, K-major), read with
+//    whole rows per load instruction.
 //  * Keys run in tiles of 128 tokens (8 or 4 pool blocks).  Two producer
 //    warps gather each tile's K rows and V rows with one TMA box per block
 //    and column half, K into a 3-stage ring and V into a 2-stage ring: a K
@@ -37,7 +38,8 @@
 //    memory, whose bandwidth the products' operand reads use), and zeros into
 //    the V rows the product must not see (slots past the sequence's end,
 //    blocks not loaded).  The epilogue divides O by the row sum and stores
-//    the valid rows.
+//    the valid rows through a per-warp staging area in the tile's (then
+//    unused) Q buffer, so that every store instruction writes whole rows.
 //  * Every wait is bounded in wall time; on a timeout the CTA records
 //    KV_ERR_TIMEOUT, drains what it issued and frees its tensor memory.
 
@@ -105,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   const int hb = grp * kGroupPairs + r % kc;
   const int b = hb / p.n_kv_heads, h = hb - b * p.n_kv_heads;
   const int Gp = p.group_pow2, g = p.group;
+  const int log2_gp = __ffs(Gp) - 1;
   const int tpt = kRows / Gp;  // query tokens per tile
 
   // ---- the CTA's queries and the keys they need (uniform over the CTA)
@@ -183,16 +186,24 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     const int pos = pos_base + tok;
     const int lo = p.window > 0 ? max(0, pos + 1 - p.window) : 0;
     const int hq = h * g + jh;
-    // Q row r of tile t -> shared memory (zeros for padding rows)
+    // Q of both tiles -> shared memory (zeros for padding rows), coalesced:
+    // 16 threads per row, so one load instruction reads two whole 256-byte
+    // rows of q
     {
-      const uint4* src = reinterpret_cast<const uint4*>(
-          static_cast<const __nv_bfloat16*>(p.q) +
-          (static_cast<int64_t>(q0 + tok) * p.n_q_heads + hq) * kD);
-      uint8_t* qt = smem + kQ + t * kQTile;
+      const uint4* qg = static_cast<const uint4*>(p.q);
+      constexpr int kChunks = kD / 8;  // 16-byte chunks per row
 #pragma unroll
-      for (int c = 0; c < kD / 8; ++c) {
-        const uint4 v = row_ok ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(qt + (c >> 3) * (kRows * 128) + swz128(r, c & 7)) = v;
+      for (int it = 0; it < kTiles * kRows * kChunks / kSoftmax; ++it) {
+        const int idx = it * kSoftmax + tid;
+        const int row = idx / kChunks, ch = idx % kChunks;
+        const int tt = row / kRows, rr = row % kRows;
+        const int tq2 = rr >> log2_gp, jh2 = rr & (Gp - 1);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (tq2 < (tt ? ntok1 : ntok0) && jh2 < g)
+          v = qg[(static_cast<int64_t>(q0 + tok0 + tt * tpt + tq2) * p.n_q_heads + h * g + jh2) *
+                     kChunks + ch];
+        *reinterpret_cast<uint4*>(smem + kQ + tt * kQTile + (ch >> 3) * (kRows * 128) +
+                                  swz128(rr, ch & 7)) = v;
       }
       fence_proxy_async_smem();
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(q_full) : "memory");
@@ -309,18 +320,39 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     if (ok && nt > 0) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      float* dst = p.out + (static_cast<int64_t>(q0 + tok) * p.n_q_heads + hq) * kD;
+      // O / l -> out, coalesced: each warp stages its 32 rows, 64 columns at a
+      // time, in shared memory (the tile's Q buffer, free once the tile's last
+      // product is done; 16-byte chunk c of row r at slot c ^ (r & 15)), then
+      // stores two whole 256-byte row halves per instruction.
+      uint8_t* stg = smem + kQ + t * kQTile + (warp & 3) * (32 * 256);
 #pragma unroll
-      for (int c0 = 0; c0 < kD; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + kOCol + c0, o);
-        if (row_ok) {
+      for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(dst + c0 + i) =
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + kOCol + hh * 64 + c0, o);
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const int ch = (c0 + i) >> 2;
+            *reinterpret_cast<float4*>(stg + lane * 256 + ((ch ^ (lane & 15)) << 4)) =
                 make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
                             __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+          }
         }
+        __syncwarp();
+#pragma unroll 4
+        for (int rr = 0; rr < 32; rr += 2) {
+          const int row = rr + (lane >> 4), ch = lane & 15;
+          const int r_t = 32 * (warp & 3) + row;  // row of the tile
+          const int tq2 = r_t >> log2_gp, jh2 = r_t & (Gp - 1);
+          if (tq2 < (t ? ntok1 : ntok0) && jh2 < g) {
+            const float4 v = *reinterpret_cast<const float4*>(stg + row * 256 + ((ch ^ (row & 15)) << 4));
+            *reinterpret_cast<float4*>(
+                p.out + (static_cast<int64_t>(q0 + tok0 + t * tpt + tq2) * p.n_q_heads + h * g + jh2) * kD +
+                hh * 64 + ch * 4) = v;
+          }
+        }
+        __syncwarp();
       }
     }
   } else if (warp == kKWarp || warp == kVWarp) {
