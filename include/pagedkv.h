@@ -218,7 +218,11 @@ kv_status paged_decode_attention(kv_pool* pool, const void* q_dev, int32_t n_q_h
  *   Results are those of the two calls made one after the other.  The decode
  *   kernel is launched as a programmatic dependent of the write kernel: it
  *   reads its sequence table while the write runs and waits for the write to
- *   complete before it reads the pool.  batch == 0 performs the write alone.
+ *   complete before it reads the pool.  The write kernel is itself launched as
+ *   a programmatic dependent of the kernel before it on the stream: after the
+ *   previous step's reduce (which lets it start once the previous decode has
+ *   completed) it runs alongside that reduce, and it waits for the reduce to
+ *   complete before it exits.  batch == 0 performs the write alone.
  */
 kv_status paged_decode_step(kv_pool* pool, const void* k_dev, const void* v_dev,
                             const int64_t* slot_mapping_dev, int64_t num_tokens,

@@ -21,6 +21,17 @@
 namespace pkv {
 namespace {
 
+// In the fused decode step this kernel is launched as a programmatic dependent
+// of the previous step's reduce kernel, which lets it run once the previous
+// decode is complete (the reduce reads neither the pool nor the counters
+// cleared here).  Every thread then waits, before it exits, for that reduce to
+// complete, so the next decode -- this kernel's own dependent, which overwrites
+// the split-K partials -- starts only after the reduce has read them.  Outside
+// that chain the wait returns at once.
+struct WaitForPrerequisitesOnExit {
+  __device__ ~WaitForPrerequisitesOnExit() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+};
+
 // BF16 pool: bit copy.  Thread i handles chunk c of row (t, h, kv).
 template <int D>
 __global__ void __launch_bounds__(256) kv_write_bf16_kernel(
@@ -31,6 +42,7 @@ __global__ void __launch_bounds__(256) kv_write_bf16_kernel(
   // a decode launched as this kernel's programmatic dependent may start now;
   // it waits for this grid to complete before it reads the pool
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const WaitForPrerequisitesOnExit wait_on_exit;
   if (zero_word && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t total = num_tokens * hkv * 2 * kChunks;
@@ -72,6 +84,7 @@ __global__ void __launch_bounds__(256) kv_write_fp8_kernel(
     uint4* __restrict__ pool, uint32_t* __restrict__ err, int32_t* __restrict__ zero_word) {
   constexpr int kChunks = D / 16;  // 16-code chunks per row
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const WaitForPrerequisitesOnExit wait_on_exit;
   if (zero_word && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t total = num_tokens * hkv * 2 * kChunks;
@@ -151,6 +164,7 @@ __global__ void __launch_bounds__(256) kv_write_fp4_kernel(
     uint8_t* __restrict__ pool, uint32_t* __restrict__ err, int32_t* __restrict__ zero_word) {
   constexpr int D = 128;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const WaitForPrerequisitesOnExit wait_on_exit;
   if (zero_word && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0;
   const int lane = threadIdx.x & 31;
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -205,38 +219,62 @@ __global__ void __launch_bounds__(256) kv_write_fp4_kernel(
 
 }  // namespace
 
+// The fused step's write (the one that clears the decode's counters) is
+// launched as a programmatic dependent of whatever kernel precedes it on the
+// stream: after the previous step's reduce it overlaps that reduce (see the
+// kernels' exit wait); after anything else it starts as usual.
+template <typename Kernel, typename... Args>
+cudaError_t launch_write(Kernel kernel, int64_t blocks, cudaStream_t stream, bool dependent,
+                         Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_kv_write(const kv_pool* pool, const void* k, const void* v,
                             const int64_t* slots, int64_t num_tokens, cudaStream_t stream,
                             int32_t* zero_word) {
   const int hkv = pool->n_kv_heads;
   const int64_t num_slots = pool->num_blocks * pool->block_size;
   const int threads = 256;
+  const bool dependent = zero_word != nullptr;
   if (pool->dtype == KV_BF16) {
     const int64_t total = num_tokens * hkv * 2 * (pool->head_dim / 8);
     const int64_t blocks = std::max<int64_t>(1, (total + threads - 1) / threads);
     if (pool->head_dim == 128)
-      kv_write_bf16_kernel<128><<<blocks, threads, 0, stream>>>(
-          static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, hkv,
-          pool->block_size, num_slots, static_cast<uint4*>(pool->base), pool->err, zero_word);
-    else
-      kv_write_bf16_kernel<64><<<blocks, threads, 0, stream>>>(
-          static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, hkv,
-          pool->block_size, num_slots, static_cast<uint4*>(pool->base), pool->err, zero_word);
-  } else if (pool->dtype == KV_FP4_E2M1) {
+      return launch_write(kv_write_bf16_kernel<128>, blocks, stream, dependent,
+                          static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots,
+                          num_tokens, hkv, pool->block_size, num_slots,
+                          static_cast<uint4*>(pool->base), pool->err, zero_word);
+    return launch_write(kv_write_bf16_kernel<64>, blocks, stream, dependent,
+                        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots,
+                        num_tokens, hkv, pool->block_size, num_slots,
+                        static_cast<uint4*>(pool->base), pool->err, zero_word);
+  }
+  if (pool->dtype == KV_FP4_E2M1) {
     const int64_t total = num_tokens * hkv * 2 * 32;  // one warp per row
     const int64_t blocks = std::max<int64_t>(1, (total + threads - 1) / threads);
-    kv_write_fp4_kernel<<<blocks, threads, 0, stream>>>(
-        static_cast<const uint2*>(k), static_cast<const uint2*>(v), slots, num_tokens, hkv,
-        pool->block_size, num_slots, pool->scales, static_cast<uint8_t*>(pool->base), pool->err,
-        zero_word);
-  } else {
-    const int64_t total = num_tokens * hkv * 2 * (pool->head_dim / 16);
-    const int64_t blocks = std::max<int64_t>(1, (total + threads - 1) / threads);
-    kv_write_fp8_kernel<128><<<blocks, threads, 0, stream>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, hkv,
-        pool->block_size, num_slots, pool->scales, static_cast<uint4*>(pool->base), pool->err, zero_word);
+    return launch_write(kv_write_fp4_kernel, blocks, stream, dependent,
+                        static_cast<const uint2*>(k), static_cast<const uint2*>(v), slots,
+                        num_tokens, hkv, pool->block_size, num_slots,
+                        static_cast<const float*>(pool->scales), static_cast<uint8_t*>(pool->base),
+                        pool->err, zero_word);
   }
-  return cudaGetLastError();
+  const int64_t total = num_tokens * hkv * 2 * (pool->head_dim / 16);
+  const int64_t blocks = std::max<int64_t>(1, (total + threads - 1) / threads);
+  return launch_write(kv_write_fp8_kernel<128>, blocks, stream, dependent,
+                      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots,
+                      num_tokens, hkv, pool->block_size, num_slots,
+                      static_cast<const float*>(pool->scales), static_cast<uint4*>(pool->base),
+                      pool->err, zero_word);
 }
 
 }  // namespace pkv
