@@ -265,6 +265,39 @@ def timed_device(step: Step, steps: int, warmup: int, dist_ctx, sampler) -> dict
     return {"elapsed_s": elapsed, "wall_s": wall, "decode_kernel_s": kernel}
 
 
+def timed_cold(step: Step, iters: int) -> float:
+    """Seconds per step with L2 flushed before each one, outside the events
+    that time the step: a 256 MB buffer (about twice the L2) is written, then
+    a second one read, so the written lines are evicted (and written back)
+    before the step starts and L2 holds only clean lines.  The main figures
+    stream inputs larger than L2 back to back; this one also removes what a
+    step leaves in L2 for the next (the 70b workload's shared prefix, the
+    block tables, the queries) and the overlap between consecutive steps."""
+    torch = step.torch
+    n = 256 * 1024 * 1024
+    flush_w = torch.empty(n, dtype=torch.uint8, device=step.q.device)
+    flush_r = torch.ones(n // 4, dtype=torch.int32, device=step.q.device)
+
+    def flush():
+        flush_w.fill_(1)
+        flush_r.sum()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(iters)]
+    for _ in range(3):
+        flush()
+        step.run()
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush()
+        a.record()
+        step.run()
+        b.record()
+    torch.cuda.synchronize()
+    del flush_w, flush_r
+    return sum(a.elapsed_time(b) for a, b in ev) / 1e3 / iters
+
+
 def timed_e2e(step: Step, steps: int, warmup: int, dist_ctx) -> dict:
     """Same steps through the public API with host inputs and a host result:
     every step copies q, the new K/V, slots, block tables and context lengths
@@ -577,6 +610,7 @@ def main(argv=None) -> None:
     dev = timed_device(step, args.steps, args.warmup, dist_ctx, sampler)
     clocks = sampler.stop()
     e2e = timed_e2e(step, max(10, min(args.steps, 500)), min(args.warmup, 10), dist_ctx)
+    cold_s = dist_ctx.max(timed_cold(step, max(5, min(args.steps, 50))))
 
     kv_bytes = w.kv_bytes_attended()
     unique = w.kv_bytes_unique()
@@ -607,6 +641,10 @@ def main(argv=None) -> None:
                    "l2": f"inputs larger than L2: {unique / 1e6:.0f} MB of distinct K/V per "
                          f"step vs {L2_BYTES / 1e6:.0f} MB L2, no flush",
                    "parallelism": f"replicas x{dist_ctx.world} (no collective on the path)"},
+        "cold_l2": {"ms_per_step": cold_s * 1e3,
+                    "value": dist_ctx.world * kv_bytes / cold_s / 1e9, "unit": "GB/s",
+                    "note": "each step alone, L2 flushed (256 MB written, another 256 MB read) "
+                            "before it, outside its events"},
         "pct_of_hbm_peak": 100.0 * achieved / peaks["hbm_gbs"],
         "tokens_per_s_per_layer": dist_ctx.world * w.batch / step_s,
         "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel", "achieved": achieved,
