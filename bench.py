@@ -540,10 +540,28 @@ class OracleSampler:
         return done, t, n
 
 
+def host_info() -> dict:
+    """The host the CPU figures were taken on: logical CPUs and the CPU model
+    (the first model line of /proc/cpuinfo, when the kernel gives one)."""
+    import platform
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"logical_cpus": os.cpu_count(), "machine": platform.machine(), "model": model}
+
+
 def oracle_sample(w, budget_s: float) -> dict:
     """The cpu_baseline object: the oracle on ~budget_s of the workload."""
     done, t, n = OracleSampler(w).run(budget_s)
     return {"value": done / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "host": host_info(),
             "sample": f"{n} sequence decodes in seeded order ({n / w.batch:.2f} passes over the "
                       f"{w.batch} sequences, {done / 1e6:.1f} MB of K/V), single-threaded fp64 "
                       f"oracle, {t:.1f} s"}
@@ -577,6 +595,7 @@ def run_reference(args) -> None:
                        "name": args.config,
                        "batch": w.batch, "parallelism": "none (host oracle)"},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "host": host_info(),
                              "sample": f"each step: sequences of the {args.config} workload in "
                                        f"seeded order for ~{per_step_budget:.2f} s of "
                                        f"single-threaded fp64 oracle work ({tot_n} sequence "
