@@ -219,10 +219,10 @@ kv_status paged_decode_attention(kv_pool* pool, const void* q_dev, int32_t n_q_h
  *   kernel is launched as a programmatic dependent of the write kernel: it
  *   reads its sequence table while the write runs and waits for the write to
  *   complete before it reads the pool.  The write kernel is itself launched as
- *   a programmatic dependent of the kernel before it on the stream: after the
- *   previous step's reduce (which lets it start once the previous decode has
- *   completed) it runs alongside that reduce, and it waits for the reduce to
- *   complete before it exits.  batch == 0 performs the write alone.
+ *   a programmatic dependent of the kernel before it on the stream: it may be
+ *   scheduled while that kernel runs and waits for it to complete before it
+ *   reads or writes anything (so inputs produced by any earlier kernel are
+ *   safe).  batch == 0 performs the write alone.
  */
 kv_status paged_decode_step(kv_pool* pool, const void* k_dev, const void* v_dev,
                             const int64_t* slot_mapping_dev, int64_t num_tokens,

@@ -870,9 +870,9 @@ __global__ void __launch_bounds__(kReduceThreads, kReduceCtas) paged_decode_redu
   int32_t ctx = p.context_lens[b];
   if (!ctx_ok<BS>(p, ctx)) ctx = 0;
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // The decode is complete: the next step's KV write (a programmatic
-  // dependent of this kernel) may start; it waits for this grid before it
-  // exits, so the next decode cannot overwrite partials still being read.
+  // The decode is complete: the next kernel on the stream may be scheduled
+  // (the next step's KV write, a programmatic dependent, waits for this grid
+  // to complete before it reads or writes anything).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (ctx == 0) return;  // nothing attended: zeroed by the decode kernel
   const int2 meta = p.pair_meta[pair];

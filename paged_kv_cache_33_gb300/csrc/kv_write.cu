@@ -22,15 +22,15 @@ namespace pkv {
 namespace {
 
 // In the fused decode step this kernel is launched as a programmatic dependent
-// of the previous step's reduce kernel, which lets it run once the previous
-// decode is complete (the reduce reads neither the pool nor the counters
-// cleared here).  Every thread then waits, before it exits, for that reduce to
-// complete, so the next decode -- this kernel's own dependent, which overwrites
-// the split-K partials -- starts only after the reduce has read them.  Outside
-// that chain the wait returns at once.
-struct WaitForPrerequisitesOnExit {
-  __device__ ~WaitForPrerequisitesOnExit() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-};
+// of the kernel before it on the stream (the previous step's reduce, in a loop
+// of steps): it may be scheduled while that kernel runs, and waits for it to
+// complete -- and its results to be visible -- before it reads its inputs or
+// writes anything.  The early launch hides the launch latency; the wait keeps
+// every input (k, v, slots, produced by any earlier kernel) and the previous
+// decode's partials safe.  Outside such a launch the wait returns at once.
+__device__ __forceinline__ void wait_for_prerequisites() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 // BF16 pool: bit copy.  Thread i handles chunk c of row (t, h, kv).
 template <int D>
@@ -39,10 +39,11 @@ __global__ void __launch_bounds__(256) kv_write_bf16_kernel(
     int64_t num_tokens, int hkv, int bs, int64_t num_slots, uint4* __restrict__ pool,
     uint32_t* __restrict__ err, int32_t* __restrict__ zero_word) {
   constexpr int kChunks = D / 8;  // 16-byte chunks per row
-  // a decode launched as this kernel's programmatic dependent may start now;
-  // it waits for this grid to complete before it reads the pool
+  // Once the kernels before this one are complete, a decode launched as this
+  // kernel's programmatic dependent may start (it reads its inputs at once,
+  // and waits for this grid to complete before it reads the pool).
+  wait_for_prerequisites();
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const WaitForPrerequisitesOnExit wait_on_exit;
   if (zero_word && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t total = num_tokens * hkv * 2 * kChunks;
@@ -83,8 +84,8 @@ __global__ void __launch_bounds__(256) kv_write_fp8_kernel(
     int64_t num_tokens, int hkv, int bs, int64_t num_slots, const float* __restrict__ scales,
     uint4* __restrict__ pool, uint32_t* __restrict__ err, int32_t* __restrict__ zero_word) {
   constexpr int kChunks = D / 16;  // 16-code chunks per row
+  wait_for_prerequisites();
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const WaitForPrerequisitesOnExit wait_on_exit;
   if (zero_word && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t total = num_tokens * hkv * 2 * kChunks;
@@ -163,8 +164,8 @@ __global__ void __launch_bounds__(256) kv_write_fp4_kernel(
     int64_t num_tokens, int hkv, int bs, int64_t num_slots, const float* __restrict__ scales,
     uint8_t* __restrict__ pool, uint32_t* __restrict__ err, int32_t* __restrict__ zero_word) {
   constexpr int D = 128;
+  wait_for_prerequisites();
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const WaitForPrerequisitesOnExit wait_on_exit;
   if (zero_word && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0;
   const int lane = threadIdx.x & 31;
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -221,8 +222,7 @@ __global__ void __launch_bounds__(256) kv_write_fp4_kernel(
 
 // The fused step's write (the one that clears the decode's counters) is
 // launched as a programmatic dependent of whatever kernel precedes it on the
-// stream: after the previous step's reduce it overlaps that reduce (see the
-// kernels' exit wait); after anything else it starts as usual.
+// stream; the kernels wait for their prerequisites before they do anything.
 template <typename Kernel, typename... Args>
 cudaError_t launch_write(Kernel kernel, int64_t blocks, cudaStream_t stream, bool dependent,
                          Args... args) {
