@@ -92,12 +92,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Heavy tiles first, in groups: the 1-D grid takes the (sequence, KV head)
-  // pairs four at a time and, inside a group, walks the query-tile index
+  // pairs sixteen at a time and, inside a group, walks the query-tile index
   // from the last (the most keys under the causal mask) down with the pairs
   // fastest.  The block scheduler then starts every group's longest CTAs
   // first, so short CTAs fill the end of the grid, while the CTAs running at
   // once still share the K/V of only a few pairs in L2.
-  constexpr int kGroupPairs = 4;
+  constexpr int kGroupPairs = 16;
   const int pairs = p.n_kv_heads * p.batch;
   const int nx = static_cast<int>(gridDim.x) / pairs;
   const int grp = static_cast<int>(blockIdx.x) / (kGroupPairs * nx);
