@@ -51,6 +51,8 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "GB/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    host = d["cpu_baseline"]["host"]
+    assert host["logical_cpus"] == os.cpu_count() and host["machine"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0
 
 
