@@ -16,7 +16,7 @@
 //    whole rows per load instruction.
 //  * Keys run in tiles of 128 tokens (8 or 4 pool blocks).  Two producer
 //    warps gather each tile's K rows and V rows with one TMA box per block
-//    and column half, K into a 3-stage ring and V into a 2-stage ring: a K
+//    and column half, K into a 2-stage ring and V into a 3-stage ring: a K
 //    stage is refilled as soon as the S products of its tile are done, a V
 //    stage once its P V products are.  Blocks outside the attended range or
 //    with a bad id are left out and their rows masked.
@@ -55,8 +55,8 @@ constexpr int kD = 128;
 constexpr int kRows = 128;           // query rows per tile (M)
 constexpr int kTiles = 2;            // query tiles per CTA, alternating over the same keys
 constexpr int kKv = 128;             // keys per key tile (N of S, K of P V)
-constexpr int kKStages = 3;          // K ring
-constexpr int kVStages = 2;          // V ring
+constexpr int kKStages = 2;          // K ring
+constexpr int kVStages = 3;          // V ring
 constexpr int kSoftmax = kTiles * kRows;      // one softmax thread per query row
 constexpr int kThreads = kSoftmax + 96;       // + K producer, V producer, MMA warps
 constexpr int kKWarp = kSoftmax / 32, kVWarp = kKWarp + 1, kMmaWarp = kVWarp + 1;
@@ -70,7 +70,7 @@ constexpr int kKvStage = 2 * kKv * 128;               // 2 column halves x [128 
 constexpr int kK = kQ + kTiles * kQTile;
 constexpr int kV = kK + kKStages * kKvStage;
 constexpr int kBars = kV + kVStages * kKvStage;
-// barriers: k_full[3], k_empty[3], v_full[2], v_empty[2], per tile s_full, p_full,
+// barriers: k_full[2], k_empty[2], v_full[3], v_empty[3], per tile s_full, p_full,
 // pv_done, o_final; q_full, mma_done
 constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 4 * kTiles + 2;
 constexpr int kTmemSlot = kBars + kNumBars * 8;
