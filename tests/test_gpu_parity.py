@@ -295,3 +295,8 @@ def test_host_argument_checks():
                                                          dtype=torch.bfloat16), t, c, 0.1,
                                        max_context_len=64)
     assert e.value.status == 4
+    # an output that is not 16-byte aligned (the reduce stores float4) is refused
+    unaligned = torch.empty(2 * 6 * 128 + 1, device="cuda")[1:].view(2, 6, 128)
+    with pytest.raises(pagedkv.KVError) as e:
+        pagedkv.paged_decode_attention(pool, q, t, c, 0.1, max_context_len=64, out=unaligned)
+    assert e.value.status == 1
