@@ -11,6 +11,9 @@ token's K or V row, on top of the per-KV-head fp32 scale.  The pins:
   * the row quantizer against torch: torch.max for the group maximum, torch's
     own E4M3 conversion for the block scale, torch float32 arithmetic for the
     divisor and the quotient, and the grid rule above for the codes;
+  * the block-scale rule (largest magnitude onto E2M1's 6) by the format
+    itself: rows already on the FP4 grid come back losslessly, a group's
+    maximum decodes to itself, and 6·448·G is the largest unsaturated group;
   * attention over an FP4 pool against dense fp64 attention (torch) on the
     values decoded from the stored codes and scales with the golden tables.
 """
@@ -228,3 +231,79 @@ def test_fp4_block_copy_moves_codes_and_scales():
     for dst, src in ((4, 1), (0, 1)):
         assert np.array_equal(a2[dst], arr[src]) and np.array_equal(s2[dst], sc[src])
     assert np.array_equal(a2[[2, 3, 5]], arr[[2, 3, 5]])
+
+
+# -- the block-scale rule, pinned by the format's own grid --------------------
+#
+# NVFP4 picks each 16-element block's scale so that the block's largest
+# magnitude maps onto the largest E2M1 magnitude, 6.  Data that already lies
+# on the format's grid -- 16 E2M1 values with at least one of magnitude 6,
+# times a representable E4M3 scale s, times a power-of-two head scale G --
+# must therefore come back with exactly those codes and that scale: every step
+# (6·G, amax / (6·G), E4M3(s), s·G, x / S) is exact, and the quantiser is
+# lossless on it.  A divisor of 4·G or 8·G (or a missing G) puts the largest
+# element at 4 or 12 and breaks the round trip.
+
+def _on_grid_row(rng, s_code: int, G: float):
+    """A 128-element row whose every group is on the FP4 grid with scale code
+    s_code; returns (bf16 row, element codes, scale code)."""
+    ev = _e4m3_values()
+    s = ev[s_code]
+    codes = rng.integers(0, 16, 128).astype(np.uint8)
+    for j in range(8):                                   # one ±6 per group
+        codes[16 * j + rng.integers(0, 16)] = 0x7 | (8 * int(rng.integers(0, 2)))
+    vals = E2M1[codes] * s * G
+    x = torch.from_numpy(vals.astype(np.float32)).bfloat16()
+    assert np.array_equal(x.double().numpy(), vals)      # exact in bf16 (<= 5 significant bits)
+    return x, codes, s_code
+
+
+@pytest.mark.parametrize("G", [1.0, 2.0 ** -7, 2.0 ** -11, 2.0 ** 3])
+def test_fp4_on_grid_groups_round_trip_exactly(G):
+    rng = np.random.default_rng(int(-math.log2(G)) + 40)
+    ev = _e4m3_values()
+    # normal E4M3 scales across the whole range, subnormal ones, and 448
+    for s_code in [0x08, 0x11, 0x2A, 0x38, 0x3F, 0x40, 0x55, 0x6D, 0x7E, 0x01, 0x05]:
+        x, codes, sc = _on_grid_row(rng, s_code, G)
+        got_c, got_s = oracle.fp4_quantize_row(x, G)
+        # -0 and +0 both decode to 0: compare values for zeros, codes otherwise
+        assert np.array_equal(got_s, np.full(8, sc, np.uint8)), (hex(s_code), got_s)
+        dec = E2M1[got_c] * np.repeat(ev[got_s], 16) * G
+        assert np.array_equal(dec, x.double().numpy()), hex(s_code)
+        nz = E2M1[codes] != 0
+        assert np.array_equal(got_c[nz], codes[nz])
+
+
+def test_fp4_group_maximum_decodes_to_itself():
+    # For any group whose amax / (6 G) is an E4M3 value the largest element
+    # is stored as code ±6 and decodes to exactly ±amax.
+    rng = np.random.default_rng(77)
+    ev = _e4m3_values()
+    G = 2.0 ** -9
+    for s_code in range(0x08, 0x7F, 3):                  # normal E4M3 scales up to 448
+        s = ev[s_code]
+        amax = 6 * s * G
+        x = rng.uniform(-amax, amax, 128)
+        x[rng.integers(0, 16) + 16 * np.arange(8)] = amax * rng.choice([-1, 1], 8)
+        xb = torch.from_numpy(x.astype(np.float32)).bfloat16()
+        xv = xb.double().numpy()
+        got_c, got_s = oracle.fp4_quantize_row(xb, G)
+        for j in range(8):
+            grp = xv[16 * j:16 * j + 16]
+            i = int(np.argmax(np.abs(grp)))
+            if np.abs(grp[i]) != amax:                   # bf16 rounding moved the maximum
+                continue
+            assert got_s[j] == s_code, (hex(s_code), j)
+            assert got_c[16 * j + i] & 0x7 == 0x7
+            assert E2M1[got_c[16 * j + i]] * ev[got_s[j]] * G == grp[i]
+
+
+def test_fp4_largest_scale_does_not_saturate_elements():
+    # amax = 6 · 448 · G is the largest group the scale represents without
+    # saturation: the scale is 448 (0x7E) and the maximum decodes exactly.
+    G = 2.0 ** -4
+    x = torch.zeros(16).bfloat16()
+    x[3], x[9] = 6 * 448 * G, -3 * 448 * G
+    codes, scales = oracle.fp4_quantize_row(x, G)
+    assert scales[0] == 0x7E
+    assert codes[3] == 0x7 and codes[9] == 0xD
