@@ -79,7 +79,10 @@ typedef enum {
   KV_ERR_BAD_BLOCK_ID = 5,  /* device: a block-table entry outside the pool  */
   KV_ERR_TIMEOUT = 6,       /* device: a bounded wait on a copy ran out      */
   KV_ERR_BAD_SLOT = 7,      /* device: a slot_mapping entry outside the pool */
-  KV_ERR_BAD_CONTEXT = 8    /* device: context_lens[b] < 0 or above a bound  */
+  KV_ERR_BAD_CONTEXT = 8,   /* device: context_lens[b] < 0 or above a bound  */
+  KV_ERR_DRAIN_TIMEOUT = 9  /* device: a kernel gave up waiting for its own   */
+                            /* copies while leaving; treat the context as     */
+                            /* suspect (see kv_pool_check_status)             */
 } kv_status;
 
 typedef enum { KV_BF16 = 0, KV_FP8_E4M3 = 1, KV_FP4_E2M1 = 2 } kv_dtype;
@@ -244,13 +247,17 @@ kv_status paged_decode_step(kv_pool* pool, const void* k_dev, const void* v_dev,
  *   PAGED_DECODE_STATIC_SCRATCH_BYTES that this library holds on every GPU
  *   that loads it, until the process exits.  The call itself allocates
  *   nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *   out_dev may be pinned host memory, as for paged_decode_attention.
  *   Returns KV_ERR_INVALID_ARG when paged_decode_workspace_bytes() for these
- *   sizes exceeds PAGED_DECODE_STATIC_SCRATCH_BYTES; use a larger partition
- *   (kv_pool_set_partition_blocks) or the workspace entry point then.
- *   The first call on a device looks up the array's device address (once,
- *   with that device current); make that first call before any stream
- *   capture.  All calls on a device share the array: calls that may overlap
- *   on the GPU (different streams, no ordering between them) race on it.
+ *   sizes exceeds PAGED_DECODE_STATIC_SCRATCH_BYTES (use a larger partition,
+ *   kv_pool_set_partition_blocks, or the workspace entry point then), else
+ *   what paged_decode_attention returns for the same arguments.
+ *   The first call on a device looks up the array's device address (once
+ *   per device and CUDA context, with that device current; again after the
+ *   context was destroyed and made anew, e.g. by cudaDeviceReset); make that
+ *   first call before any stream capture.  All calls on a device share the
+ *   array: calls that may overlap on the GPU (different streams, no ordering
+ *   between them) race on it.
  */
 #define PAGED_DECODE_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 kv_status paged_decode_attention_noalloc(kv_pool* pool, const void* q_dev, int32_t n_q_heads,
@@ -316,7 +323,10 @@ kv_status kv_pool_set_timing_events(kv_pool* pool, void* start_event, void* stop
  * kv_pool_set_wait_limit -- bound, in nanoseconds of wall time, of every wait
  * the pool's kernels make on a copy or on another warp (default 1 s; 1e5 ..
  * 1e10).  A wait that runs out records KV_ERR_TIMEOUT, the kernel drains
- * what it issued and returns; nothing traps.
+ * what it issued and returns; nothing traps.  The drain is bounded too: if a
+ * wait for one of its own copies (or, in the prefill, for its tensor-core
+ * products) also runs out, the kernel records KV_ERR_DRAIN_TIMEOUT and exits
+ * with that work possibly still in flight.
  *
  * kv_pool_set_test_stall -- test instrumentation for the timeout path: while
  * enabled, the first copy of worker 0 in each decode launch expects 16 more
@@ -330,8 +340,13 @@ kv_status kv_pool_set_test_stall(kv_pool* pool, int32_t enable);
 /*
  * kv_pool_check_status -- synchronise `stream`, read and clear the pool's
  * device error word.  Returns KV_OK, or the first recorded problem in the
- * order KV_ERR_TIMEOUT, KV_ERR_BAD_BLOCK_ID, KV_ERR_BAD_SLOT,
- * KV_ERR_BAD_CONTEXT; KV_ERR_CUDA if the stream itself failed.
+ * order KV_ERR_DRAIN_TIMEOUT, KV_ERR_TIMEOUT, KV_ERR_BAD_BLOCK_ID,
+ * KV_ERR_BAD_SLOT, KV_ERR_BAD_CONTEXT; KV_ERR_CUDA if the stream itself
+ * failed.  After KV_ERR_TIMEOUT the context stays usable (every copy the
+ * kernel issued was seen to land).  After KV_ERR_DRAIN_TIMEOUT it is not
+ * known to be: copies may still have been writing shared memory when the
+ * kernel exited, so the caller should stop issuing work on it, synchronise
+ * and tear the context down rather than keep using it.
  */
 kv_status kv_pool_check_status(kv_pool* pool, void* stream);
 

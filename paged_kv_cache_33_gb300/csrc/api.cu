@@ -135,6 +135,7 @@ const char* kv_status_str(kv_status s) {
     case KV_ERR_UNSUPPORTED: return "KV_ERR_UNSUPPORTED";
     case KV_ERR_BAD_BLOCK_ID: return "KV_ERR_BAD_BLOCK_ID";
     case KV_ERR_TIMEOUT: return "KV_ERR_TIMEOUT";
+    case KV_ERR_DRAIN_TIMEOUT: return "KV_ERR_DRAIN_TIMEOUT";
     case KV_ERR_BAD_SLOT: return "KV_ERR_BAD_SLOT";
     case KV_ERR_BAD_CONTEXT: return "KV_ERR_BAD_CONTEXT";
   }
@@ -493,6 +494,7 @@ kv_status kv_pool_check_status(kv_pool* p, void* stream) {
     cudaGetLastError();
     return KV_ERR_CUDA;
   }
+  if (word & pkv::kErrDrainTimeout) return KV_ERR_DRAIN_TIMEOUT;
   if (word & pkv::kErrTimeout) return KV_ERR_TIMEOUT;
   if (word & pkv::kErrBadBlock) return KV_ERR_BAD_BLOCK_ID;
   if (word & pkv::kErrBadSlot) return KV_ERR_BAD_SLOT;

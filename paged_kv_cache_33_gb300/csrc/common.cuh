@@ -20,6 +20,9 @@ enum : uint32_t {
   kErrBadSlot = 2u,
   kErrTimeout = 4u,
   kErrBadContext = 8u,
+  // A wait ran out while the kernel was leaving: copies (or tensor-core
+  // products) it issued may still be writing its shared memory.
+  kErrDrainTimeout = 16u,
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

@@ -837,9 +837,10 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : (KIND == kFp4 ? PKV_FP
     // leave no copy in flight: wait (bounded) for every stage holding one
     atomicOr(p.err, kErrTimeout);
     for (int k = it; k < it + STAGES; ++k)
-      if ((tma_stages >> (k % STAGES)) & 1u)
-        mbar_wait_bounded(smem_addr(&bars[k % STAGES]), (k / STAGES) & 1, p.wait_limit_ns, p.err,
-                          kErrTimeout, kShortWaitNs);
+      if ((tma_stages >> (k % STAGES)) & 1u &&
+          !mbar_wait_bounded(smem_addr(&bars[k % STAGES]), (k / STAGES) & 1, p.wait_limit_ns,
+                             p.err, kErrTimeout, kShortWaitNs))
+        atomicOr(p.err, kErrDrainTimeout);
   }
 }
 

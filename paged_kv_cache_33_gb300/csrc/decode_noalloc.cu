@@ -29,18 +29,50 @@ namespace {
 constexpr int kMaxDevices = 256;
 std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};  // context the address belongs to
 
-// Device address of g_decode_scratch on `device`, looked up once per device
-// with that device current.  In host code the symbol is only a host-side
-// stand-in, so a kernel must be given this address, never the symbol itself.
+// Unique id of the calling thread's current CUDA context (cuCtxGetId, reached
+// through the runtime's driver entry point).  False when it cannot be told.
+// Called with g_scratch_mutex held.
+bool current_context_id(unsigned long long* id) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+    looked_up = true;
+  }
+  CUcontext ctx = nullptr;
+  return get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx &&
+         get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_decode_scratch on `device`, which must be current.  In
+// host code the symbol is only a host-side stand-in, so a kernel must be given
+// this address, never the symbol itself.  The address is looked up once per
+// device and context: if the device's context was destroyed and made again
+// (cudaDeviceReset), the module is loaded anew and the address is looked up
+// again; if the context cannot be identified it is looked up on every call.
 cudaError_t scratch_address(int device, void** out) {
   if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_addr[device]) {
+  unsigned long long ctx = 0;
+  const bool known = current_context_id(&ctx);
+  if (!g_scratch_addr[device] || !known || g_scratch_ctx[device] != ctx) {
     void* addr = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&addr, g_decode_scratch);
     if (e != cudaSuccess) return e;
     g_scratch_addr[device] = addr;
+    g_scratch_ctx[device] = known ? ctx : 0;
   }
   *out = g_scratch_addr[device];
   return cudaSuccess;

@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       }
       // leave no copy in flight: wait (bounded) for the stages not yet consumed
       for (int jt = max(0, issued - stages); jt < issued; ++jt)
-        wait(full(jt % stages), (jt / stages) & 1);
+        if (!wait(full(jt % stages), (jt / stages) & 1)) atomicOr(p.err, kErrDrainTimeout);
     }
     __syncwarp();
   } else {
@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       }
       // every product issued has completed before the tensor memory is freed
       umma_commit(mma_done);
-      wait(mma_done, 0);
+      if (!wait(mma_done, 0)) atomicOr(p.err, kErrDrainTimeout);
     }
     __syncwarp();
   }

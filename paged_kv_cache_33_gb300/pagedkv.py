@@ -21,7 +21,7 @@ from . import build as _build
 KV_OK = 0
 STATUS = {0: "KV_OK", 1: "KV_ERR_INVALID_ARG", 2: "KV_ERR_OOM", 3: "KV_ERR_CUDA",
           4: "KV_ERR_UNSUPPORTED", 5: "KV_ERR_BAD_BLOCK_ID", 6: "KV_ERR_TIMEOUT",
-          7: "KV_ERR_BAD_SLOT", 8: "KV_ERR_BAD_CONTEXT"}
+          7: "KV_ERR_BAD_SLOT", 8: "KV_ERR_BAD_CONTEXT", 9: "KV_ERR_DRAIN_TIMEOUT"}
 DTYPES = {"bf16": 0, "fp8": 1, "fp4": 2}
 FP4_RECORD_BYTES = 2304  # one 16-token sub-tile of a (block, KV head) in an FP4 pool
 
@@ -293,6 +293,25 @@ def _fp4_maps(device):
     return byte.to(device), shift.to(device), sbyte.to(device)
 
 
+def _check_decode_shapes(pool: KVPool, q: torch.Tensor, block_tables: torch.Tensor,
+                         context_lens: torch.Tensor, out: torch.Tensor | None) -> tuple:
+    """The sizes the C ABI cannot see: it reads q at the pool's head_dim,
+    context_lens and block_tables with the batch of q, and writes out as
+    [B, Hq, D].  Raises ValueError on any mismatch; returns (B, Hq, D)."""
+    if q.dim() != 3:
+        raise ValueError("q must be [B, Hq, D]")
+    B, Hq, D = q.shape
+    if D != pool.head_dim:
+        raise ValueError(f"q has head_dim {D}, the pool {pool.head_dim}")
+    if tuple(context_lens.shape) != (B,):
+        raise ValueError(f"context_lens must be [{B}]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be [B, max_blocks_per_seq]")
+    if out is not None and tuple(out.shape) != (B, Hq, D):
+        raise ValueError(f"out must be {(B, Hq, D)}")
+    return B, Hq, D
+
+
 # ----------------------------------------------------- C ABI named functions --
 
 def kv_pool_create(num_blocks: int, block_size: int, n_kv_heads: int, head_dim: int,
@@ -349,20 +368,16 @@ def paged_decode_attention(pool: KVPool, q: torch.Tensor, block_tables: torch.Te
     it); when omitted it is read from context_lens, which synchronises.  `out`
     may be a pinned host tensor: the kernels then write the result into host
     memory directly."""
-    B, Hq, D = q.shape
+    B, Hq, D = _check_decode_shapes(pool, q, block_tables, context_lens, out)
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if B else 0
     if out is None:
         out = torch.empty(B, Hq, D, dtype=torch.float32, device=q.device)
-    if tuple(out.shape) != (B, Hq, D):
-        raise ValueError(f"out must be {(B, Hq, D)}")
     need = paged_decode_workspace_bytes(pool, B, Hq, max_context_len, sliding_window)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    if block_tables.dim() != 2 or block_tables.shape[0] != B:
-        raise ValueError("block_tables must be [B, max_blocks_per_seq]")
     _check(load().paged_decode_attention(
         pool.handle, _dev(q, torch.bfloat16, "q"), Hq,
         _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
@@ -385,20 +400,16 @@ def paged_decode_step(pool: KVPool, k: torch.Tensor, v: torch.Tensor, slot_mappi
     shape = (T, pool.n_kv_heads, pool.head_dim)
     if tuple(k.shape) != shape or tuple(v.shape) != shape:
         raise ValueError(f"k and v must be {shape}")
-    B, Hq, D = q.shape
+    B, Hq, D = _check_decode_shapes(pool, q, block_tables, context_lens, out)
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if B else 0
     if out is None:
         out = torch.empty(B, Hq, D, dtype=torch.float32, device=q.device)
-    if tuple(out.shape) != (B, Hq, D):
-        raise ValueError(f"out must be {(B, Hq, D)}")
     need = paged_decode_workspace_bytes(pool, B, Hq, max_context_len, sliding_window)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    if block_tables.dim() != 2 or block_tables.shape[0] != B:
-        raise ValueError("block_tables must be [B, max_blocks_per_seq]")
     _check(load().paged_decode_step(
         pool.handle, _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
         _dev(slot_mapping, torch.int64, "slot_mapping"), T,
@@ -441,16 +452,16 @@ def paged_decode_attention_noalloc(pool: KVPool, q: torch.Tensor, block_tables: 
                                    context_lens: torch.Tensor, scale: float, sliding_window: int,
                                    max_context_len: int, out: torch.Tensor, stream=None) -> None:
     """Decode attention whose split-K scratch is the library's static device
-    array: nothing is allocated, so `out` ([B, Hq, D] fp32) and
-    `max_context_len` must come from the caller."""
-    B, Hq, _ = q.shape
-    if block_tables.dim() != 2 or block_tables.shape[0] != B:
-        raise ValueError("block_tables must be [B, max_blocks_per_seq]")
+    array: nothing is allocated, so `out` ([B, Hq, D] fp32, a CUDA tensor or
+    a pinned host tensor) and `max_context_len` must come from the caller."""
+    if out is None:
+        raise ValueError("out is required: this entry point allocates nothing")
+    _, Hq, _ = _check_decode_shapes(pool, q, block_tables, context_lens, out)
     _check(load().paged_decode_attention_noalloc(
         pool.handle, _dev(q, torch.bfloat16, "q"), Hq,
         _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
         _dev(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
-        int(sliding_window), _dev(out, torch.float32, "out"), _stream(stream)),
+        int(sliding_window), _out(out, "out"), _stream(stream)),
         "paged_decode_attention_noalloc")
 
 

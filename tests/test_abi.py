@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from paged_kv_cache_33_gb300 import pagedkv
 
@@ -86,3 +87,53 @@ def test_create_without_a_device_fails_cleanly():
     h = ctypes.c_void_p()
     assert L.kv_pool_create(10, 16, 8, 128, 0, ctypes.byref(h)) in (2, 3)
     assert not h.value
+
+
+class _FakePool:
+    """Only the sizes the bindings check before any call into the library."""
+    n_kv_heads, head_dim = 2, 128
+
+
+def _decode_args(B=3, Hq=8, D=128, mbs=4):
+    return (torch.zeros(B, Hq, D, dtype=torch.bfloat16), torch.zeros(B, mbs, dtype=torch.int32),
+            torch.ones(B, dtype=torch.int32), torch.zeros(B, Hq, D))
+
+
+@pytest.mark.parametrize("bad", ["head_dim", "lens_short", "lens_2d", "tables", "out_small",
+                                 "q_2d"])
+@pytest.mark.parametrize("entry", ["attention", "step", "noalloc"])
+def test_decode_bindings_check_the_sizes_the_abi_cannot_see(entry, bad):
+    q, tables, lens, out = _decode_args()
+    if bad == "head_dim":
+        q = torch.zeros(3, 8, 64, dtype=torch.bfloat16)
+    elif bad == "lens_short":
+        lens = lens[:2]
+    elif bad == "lens_2d":
+        lens = lens.view(3, 1)
+    elif bad == "tables":
+        tables = tables[:2]
+    elif bad == "out_small":
+        out = out[:, :4]
+    elif bad == "q_2d":
+        q = q[0]
+    pool = _FakePool()
+    with pytest.raises(ValueError):
+        if entry == "attention":
+            pagedkv.paged_decode_attention(pool, q, tables, lens, 0.1, out=out, max_context_len=16)
+        elif entry == "noalloc":
+            pagedkv.paged_decode_attention_noalloc(pool, q, tables, lens, 0.1, 0, 16, out)
+        else:
+            kv = torch.zeros(3, 2, 128, dtype=torch.bfloat16)
+            pagedkv.paged_decode_step(pool, kv, kv, torch.zeros(3, dtype=torch.int64), q, tables,
+                                      lens, 0.1, out=out, max_context_len=16)
+
+
+def test_noalloc_binding_requires_out():
+    q, tables, lens, _ = _decode_args()
+    with pytest.raises(ValueError):
+        pagedkv.paged_decode_attention_noalloc(_FakePool(), q, tables, lens, 0.1, 0, 16, None)
+
+
+def test_drain_timeout_status_is_named():
+    assert pagedkv.STATUS[9] == "KV_ERR_DRAIN_TIMEOUT"
+    assert pagedkv.kv_status_str(9) == "KV_ERR_DRAIN_TIMEOUT"

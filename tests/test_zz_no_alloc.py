@@ -64,3 +64,28 @@ def test_refuses_sizes_beyond_the_static_scratch():
     torch.cuda.synchronize()
     assert not out.any()   # nothing was launched
     pool.destroy()
+
+
+def test_pinned_host_output_and_undersized_output():
+    w = W.make("8b", "small")
+    pool = make_gpu_pool(w)
+    pool.set_partition_blocks(8)
+    fill_both(w, pool, None)
+    tables = torch.from_numpy(w.block_tables).cuda()
+    lens = torch.from_numpy(w.context_lens).cuda()
+    q = torch.randn(w.batch, w.n_q_heads, w.head_dim,
+                    generator=torch.Generator().manual_seed(7)).bfloat16().cuda()
+    ref = pagedkv.paged_decode_attention(pool, q, tables, lens, w.scale, w.window,
+                                         max_context_len=w.max_context_len)
+    host = torch.full(tuple(ref.shape), float("nan")).pin_memory()
+    pagedkv.paged_decode_attention_noalloc(pool, q, tables, lens, w.scale, w.window,
+                                           w.max_context_len, host)
+    torch.cuda.synchronize()
+    assert pool.check_status() == pagedkv.KV_OK
+    max_abs, rel = errors(host.numpy(), ref.cpu().numpy())
+    assert max_abs <= BF16_MAX_ABS and rel <= BF16_REL_L2
+    small = torch.zeros(w.batch, w.n_q_heads - 1, w.head_dim, device="cuda")
+    with pytest.raises(ValueError):
+        pagedkv.paged_decode_attention_noalloc(pool, q, tables, lens, w.scale, w.window,
+                                               w.max_context_len, small)
+    pool.destroy()
