@@ -9,7 +9,14 @@ memory and the output read back inside the timed region.  `roofline` gives the
 decode kernel alone against the measured HBM copy bandwidth.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 8b|70b|sw|tiny]
-                  [--impl ours|reference] [--part-blocks P]
+                  [--configs 70b,sw,fp8,fp4,tiny|none] [--impl ours|reference]
+                  [--part-blocks P]
+
+The headline workload (--config, default 8b) gives the top-level figures;
+every workload named by --configs is then measured the same way (device
+steps, decode kernel roofline, cold L2, end to end, clocks) and reported
+under "configs", each with the oracle timed on a sample of its sequences
+and the sample's error against the oracle.
 
 Under torchrun every rank runs an independent replica on its own GPU (the
 path has no exchange step); ranks meet at barriers around the timed region.
@@ -70,6 +77,11 @@ def parse_args(argv=None):
                     help="skip the block-copy, prefill and host block-manager measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    ap.add_argument("--configs", default="70b,sw,fp8,fp4,tiny",
+                    help="comma-separated workloads measured after the headline one and "
+                         "reported under 'configs' ('none' = only the headline)")
+    ap.add_argument("--config-oracle-seconds", type=float, default=3.0,
+                    help="oracle CPU time per workload under 'configs' (timing + parity sample)")
     return ap.parse_args(argv)
 
 
@@ -169,6 +181,128 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(r["sm"] for r in sel),
                 "sm_max_mhz": max(r["max"] for r in sel), "reasons": reasons,
                 "samples": len(sel), "window": window}
+
+
+# ------------------------------------------------- bytes of one decode launch --
+
+# The decode kernel's split of a launch's units into segments (decode.cu,
+# struct Split): 25% of the units go to dynamic chunks once there are at least
+# 8 per worker; the chunk regions take 60%, 30% and 10% of them in chunks of
+# 16, 8 and 4 units, the rest in chunks of 4.
+SPLIT_DYN_PCT = 25
+SPLIT_CHUNKS = (16, 8, 4, 4)
+SPLIT_REGION_PCT = (60, 30, 10)
+MAX_DECODE_BATCH = 512          # sequences per decode launch
+NOMINAL_HBM_GBS = 7900.0        # GB300 HBM3e spec-sheet bandwidth
+
+
+def decode_workers(w, sm_count: int) -> int:
+    """Warps of the persistent decode grid: 3 CTAs per SM, 4 warps each
+    (2 for bf16 with 32-token blocks, with 6 CTAs per SM)."""
+    return sm_count * 12
+
+
+def blocks_per_unit(w) -> int:
+    if w.block_size == 32:
+        return 1
+    return {"bf16": 1, "fp8": 2, "fp4": 3}[w.dtype]
+
+
+def _split_segments(T: int, P: int):
+    """seg_of(u) of the kernel's split of T units over P workers."""
+    Td = T * SPLIT_DYN_PCT // 100 if T >= 8 * P else 0
+    Ts = T - Td
+    Ps = min(P, Ts)
+    c0, c1, c2, c3 = SPLIT_CHUNKS
+    r0 = Td * SPLIT_REGION_PCT[0] // 100 // c0 * c0
+    r1 = Td * SPLIT_REGION_PCT[1] // 100 // c1 * c1
+    r2 = Td * SPLIT_REGION_PCT[2] // 100 // c2 * c2
+    s1, s2, s3 = Ts + r0, Ts + r0 + r1, Ts + r0 + r1 + r2
+    t1, t2, t3 = r0 // c0, r0 // c0 + r1 // c1, r0 // c0 + r1 // c1 + r2 // c2
+
+    def seg_of(u: int) -> int:
+        if u < Ts:
+            return ((u + 1) * Ps - 1) // Ts
+        if u < s1:
+            return Ps + (u - Ts) // c0
+        if u < s2:
+            return Ps + t1 + (u - s1) // c1
+        if u < s3:
+            return Ps + t2 + (u - s2) // c2
+        return Ps + t3 + (u - s3) // c3
+    return seg_of
+
+
+def decode_launch_bytes(w, sm_count: int) -> dict:
+    """Algorithmic bytes of the decode kernel and of its reduce, summed over
+    the launches of one call.
+
+    Decode: K/V of the attended tokens (the shared prefix once) + the queries
+    + 4 B per block-table entry read per KV head + the outputs of pairs
+    finished inside one segment + one partial (g*D unnormalised outputs and
+    g (max, sum) pairs, fp32) per segment of a pair cut between segments.
+    Reduce: reads those partials, writes the cut pairs' outputs.  Block-
+    rounded K/V (whole blocks of every attended range) is given beside the
+    exact figure."""
+    bs, g, D = w.block_size, w.group, w.head_dim
+    bpu = blocks_per_unit(w)
+    P = decode_workers(w, sm_count)
+    tok = w.kv_bytes_per_token_head() * w.n_kv_heads
+    pieces = cut = whole = entries = blocks = 0
+    for b0 in range(0, w.batch, MAX_DECODE_BATCH):
+        nunits = []
+        for b in range(b0, min(w.batch, b0 + MAX_DECODE_BATCH)):
+            lo, ctx = w.attended_range(b)
+            nblk = (ctx - 1) // bs - lo // bs + 1 if ctx > lo else 0
+            blocks += nblk
+            entries += nblk * w.n_kv_heads
+            nunits.append(-(-nblk // bpu))
+        T = sum(n * w.n_kv_heads for n in nunits)
+        if T == 0:
+            continue
+        seg_of = _split_segments(T, P)
+        u = 0
+        for n in nunits:
+            for _ in range(w.n_kv_heads):
+                if n == 0:
+                    continue
+                c = seg_of(u + n - 1) - seg_of(u) + 1
+                if c == 1:
+                    whole += 1
+                else:
+                    cut += 1
+                    pieces += c
+                u += n
+    piece_bytes = (g * D + 2 * g) * 4
+    out_pair = g * D * 4
+    q_bytes = w.batch * w.n_q_heads * D * 2
+    decode = (w.kv_bytes_unique() + q_bytes + 4 * entries + whole * out_pair
+              + pieces * piece_bytes + 8 * (whole + cut))
+    return {"decode": decode, "reduce": pieces * piece_bytes + cut * out_pair,
+            "kv_exact": w.kv_bytes_unique(), "kv_block_rounded": _block_rounded_unique(w),
+            "partials": pieces, "cut_pairs": cut, "whole_pairs": whole,
+            "partial_bytes": pieces * piece_bytes, "table_bytes": 4 * entries,
+            "workers": P}
+
+
+def _block_rounded_unique(w) -> int:
+    """K/V bytes of every block an attended range touches, whole (the shared
+    prefix's blocks once)."""
+    bs = w.block_size
+    per_block = bs * w.kv_bytes_per_token_head() * w.n_kv_heads
+    prefix_blocks = w.shared_prefix_tokens // bs
+    seen_prefix = 0
+    n = 0
+    for b in range(w.batch):
+        lo, ctx = w.attended_range(b)
+        if ctx <= lo:
+            continue
+        first, last = lo // bs, (ctx - 1) // bs
+        if prefix_blocks:
+            seen_prefix = max(seen_prefix, min(last + 1, prefix_blocks) if first < prefix_blocks else 0)
+            first = max(first, prefix_blocks)
+        n += max(0, last - first + 1)
+    return (n + seen_prefix) * per_block
 
 
 # ----------------------------------------------------------------- the step --
@@ -494,50 +628,82 @@ class OracleSampler:
     """Times the oracle (single-threaded fp64) on bounded samples of the
     workload: sequences in seeded order, each filled into the oracle's pool on
     its first visit (untimed) and decoded (timed), cycling through the batch
-    again when it is exhausted."""
+    again when it is exhausted.  Given the GPU's output of the same step, it
+    also compares every sequence it decodes with it (outside the timing)."""
 
-    def __init__(self, w):
+    def __init__(self, w, gpu_out=None, gen_device="cpu"):
         import numpy as np
 
         import oracle
 
         self.w = w
+        # inputs drawn by the workload's seeded generators on this device (the
+        # GPU leg draws its inputs on the GPU: the same seeds on another
+        # device's generator give other numbers)
+        self.gen_device = gen_device
         self.order = np.random.default_rng(0).permutation(w.batch)
         self.pool = oracle.Pool(w.num_blocks, w.block_size, w.n_kv_heads, w.head_dim, w.dtype)
         if w.dtype in ("fp8", "fp4"):
             self.pool.set_scales(w.k_scale, w.v_scale)
-        self.q = w.query()
+        self.q = w.query(device=gen_device).cpu()
         self.filled: set[int] = set()
         self.decodes = 0
         self.token_bytes = w.n_kv_heads * w.kv_bytes_per_token_head()
+        self.gpu_out = gpu_out
+        self.checked: set[int] = set()
+        self.err_max = 0.0
+        self.err_sq = 0.0
+        self.ref_sq = 0.0
+        self.finite = True
 
     def _fill(self, b: int) -> None:
         w = self.w
-        setup, (k_new, v_new, s_new) = w.fill_plan(seqs=[b])
+        setup, (k_new, v_new, s_new) = w.fill_plan(seqs=[b], device=self.gen_device)
         for k, v, s in setup:
-            self.pool.write(k, v, s.numpy())
+            self.pool.write(k.cpu(), v.cpu(), s.numpy())
         keep = s_new.clone()
         keep[[i for i in range(w.batch) if i != b]] = -1
-        self.pool.write(k_new, v_new, keep.numpy())
+        self.pool.write(k_new.cpu(), v_new.cpu(), keep.numpy())
         self.filled.add(b)
 
-    def run(self, budget_s: float) -> tuple[int, float, int]:
-        """Decode sequences until ~budget_s of timed work (at least one);
-        returns (K/V bytes read, seconds, sequences decoded)."""
+    def run(self, budget_s: float, max_seqs: int | None = None) -> tuple[int, float, int]:
+        """Decode sequences until ~budget_s of timed work (at least one, at
+        most max_seqs); returns (K/V bytes read, seconds, sequences decoded)."""
+        import numpy as np
         w = self.w
         done, t, n = 0, 0.0, 0
-        while n == 0 or t < budget_s:
+        while (n == 0 or t < budget_s) and (max_seqs is None or n < max_seqs):
             b = int(self.order[self.decodes % w.batch])
             if b not in self.filled:
                 self._fill(b)
             t0 = time.perf_counter()
-            self.pool.decode(self.q, w.block_tables, w.context_lens, w.scale, w.window, seqs=[b])
+            o = self.pool.decode(self.q, w.block_tables, w.context_lens, w.scale, w.window,
+                                 seqs=[b])
             t += time.perf_counter() - t0
+            if self.gpu_out is not None and b not in self.checked:
+                ref = o[b].astype(np.float64)
+                got = self.gpu_out[b].astype(np.float64)
+                self.finite = self.finite and bool(np.isfinite(got).all())
+                d = got - ref
+                self.err_max = max(self.err_max, float(np.abs(d).max()) if d.size else 0.0)
+                self.err_sq += float((d * d).sum())
+                self.ref_sq += float((ref * ref).sum())
+                self.checked.add(b)
             lo, ctx = w.attended_range(b)
             done += (ctx - lo) * self.token_bytes
             self.decodes += 1
             n += 1
         return done, t, n
+
+    def parity(self) -> dict | None:
+        if self.gpu_out is None:
+            return None
+        tol = {"bf16": (2e-3, 1e-3), "fp8": (3e-2, None), "fp4": (2e-3, 1e-3)}[self.w.dtype]
+        rel = (self.err_sq / self.ref_sq) ** 0.5 if self.ref_sq > 0 else 0.0
+        ok = self.finite and self.err_max <= tol[0] and (tol[1] is None or rel <= tol[1])
+        return {"sequences": len(self.checked), "max_abs_err": self.err_max, "rel_l2_err": rel,
+                "tol_max_abs": tol[0], "tol_rel_l2": tol[1], "pass": ok,
+                "against": "fp64 oracle on the same seeded inputs, sequences in the sample"}
 
 
 def host_info() -> dict:
@@ -561,14 +727,37 @@ def host_info() -> dict:
     return {"logical_cpus": os.cpu_count(), "machine": platform.machine(), "model": model}
 
 
-def oracle_sample(w, budget_s: float) -> dict:
-    """The cpu_baseline object: the oracle on ~budget_s of the workload."""
-    done, t, n = OracleSampler(w).run(budget_s)
-    return {"value": done / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "host": host_info(),
-            "sample": f"{n} sequence decodes in seeded order ({n / w.batch:.2f} passes over the "
-                      f"{w.batch} sequences, {done / 1e6:.1f} MB of K/V), single-threaded fp64 "
-                      f"oracle, {t:.1f} s"}
+def oracle_workload(name: str, block_size: int, gpu_w=None):
+    """The workload rebuilt from its seeds with the oracle's own allocator
+    (for the churned pools), so the CPU legs depend on oracle/ alone; when
+    the GPU leg's workload is given, its block tables must be identical."""
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_33_gb300 import workloads as W
+    w = W.make(name, "full", make_allocator=oracle.Allocator, block_size=block_size)
+    if gpu_w is not None and not (np.array_equal(w.block_tables, gpu_w.block_tables) and
+                                  np.array_equal(w.context_lens, gpu_w.context_lens)):
+        raise RuntimeError(f"{name}: the oracle allocator's tables differ from the GPU leg's")
+    return w
+
+
+def oracle_sample(w, budget_s: float, gpu_out=None, max_seqs: int | None = None,
+                  gen_device="cpu") -> dict:
+    """The cpu_baseline object: the oracle on ~budget_s of the workload, and
+    (given the GPU output of the step, whose inputs were drawn on
+    `gen_device`) the error of that output on the sampled sequences."""
+    sampler = OracleSampler(w, gpu_out, gen_device)
+    done, t, n = sampler.run(budget_s, max_seqs)
+    out = {"value": done / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "host": host_info(),
+           "sample": f"{n} sequence decodes in seeded order ({n / w.batch:.2f} passes over the "
+                     f"{w.batch} sequences, {done / 1e6:.1f} MB of K/V), single-threaded fp64 "
+                     f"oracle, {t:.1f} s"}
+    par = sampler.parity()
+    if par is not None:
+        out["parity"] = par
+    return out
 
 
 def _fanout_worker(rank: int, n: int, config: str, block_size: int, budget_s: float, queue) -> None:
@@ -578,9 +767,7 @@ def _fanout_worker(rank: int, n: int, config: str, block_size: int, budget_s: fl
     import numpy as np
 
     sys.path.insert(0, ROOT)
-    from paged_kv_cache_33_gb300 import pagedkv
-    from paged_kv_cache_33_gb300 import workloads as W
-    w = W.make(config, "full", make_allocator=pagedkv.BlockManager, block_size=block_size)
+    w = oracle_workload(config, block_size)
     sampler = OracleSampler(w)
     sampler.order = np.roll(sampler.order, -(rank * w.batch) // n)
     queue.put(sampler.run(budget_s))
@@ -651,58 +838,52 @@ def run_reference(args) -> None:
 
 # ------------------------------------------------------------------- main --
 
-def main(argv=None) -> None:
-    args = parse_args(argv)
-    if args.impl == "reference":
-        run_reference(args)
-        return
+def measure(name: str, args, dist_ctx: DistCtx, device, peaks: dict) -> tuple[dict, "Step"]:
+    """One workload on this rank's GPU: device-resident steps (value, step
+    time, the decode kernel's own time and roofline), cold-L2 steps, end to
+    end through the public API with host buffers, and the clocks seen."""
     import torch
 
     from paged_kv_cache_33_gb300 import pagedkv
     from paged_kv_cache_33_gb300 import workloads as W
-
-    dist_ctx = DistCtx(args.gpus)
-    torch.cuda.set_device(dist_ctx.local_rank)
-    device = torch.device("cuda", dist_ctx.local_rank)
-    pagedkv.load()
-    # the fp8 workload's tables come from the library's own block manager
-    w = W.make(args.config, "full", make_allocator=pagedkv.BlockManager,
-               block_size=args.block_size)
+    # the churned pools' tables come from the library's own block manager
+    w = W.make(name, "full", make_allocator=pagedkv.BlockManager, block_size=args.block_size)
     step = Step(w, device, args.part_blocks)
     sampler = ClockSampler(dist_ctx.local_rank)
     dev = timed_device(step, args.steps, args.warmup, dist_ctx, sampler)
     clocks = sampler.stop()
-    e2e = timed_e2e(step, max(10, min(args.steps, 500)), min(args.warmup, 10), dist_ctx)
+    e2e_steps = max(10, min(args.steps, 500))
+    e2e = timed_e2e(step, e2e_steps, min(args.warmup, 10), dist_ctx)
     cold_s = dist_ctx.max(timed_cold(step, max(5, min(args.steps, 50))))
 
     kv_bytes = w.kv_bytes_attended()
     unique = w.kv_bytes_unique()
     total_bytes, elapsed = aggregate(dist_ctx, kv_bytes * args.steps, dev["elapsed_s"])
-    e2e_steps = max(10, min(args.steps, 500))
     e2e_bytes, e2e_elapsed = aggregate(dist_ctx, kv_bytes * e2e_steps, e2e["elapsed_s"])
     kernel_s = dist_ctx.max(dev["decode_kernel_s"])
-    peaks = measured_peaks()
-    # algorithmic bytes of one decode launch: attended K/V (shared prefix once),
-    # the queries, the outputs and the block-table entries read
-    bsz = w.block_size
-    tables_read = 4 * w.n_kv_heads * sum(
-        (hi - 1) // bsz - lo // bsz + 1 for lo, hi in map(w.attended_range, range(w.batch)) if hi > lo)
-    algo = unique + w.batch * w.n_q_heads * w.head_dim * (2 + 4) + tables_read
+    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    lb = decode_launch_bytes(w, sm_count)
+    algo = lb["decode"]
     achieved = algo / kernel_s / 1e9
     step_s = elapsed / args.steps
+    key = name if w.block_size == 16 else f"{name}-bs{w.block_size}"
+    traffic = recorded_traffic(key)
     result = {
         "metric": METRIC, "value": total_bytes / elapsed / 1e9, "unit": "GB/s",
         "n_gpus": dist_ctx.world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": f"{DESCRIPTIONS[args.config]}, {w.block_size}-token blocks",
-                   "name": args.config,
+        "config": {"workload": f"{DESCRIPTIONS[name]}, {w.block_size}-token blocks",
+                   "name": name,
                    "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
                    "head_dim": w.head_dim, "block_size": w.block_size,
                    "num_blocks": w.num_blocks, "window": w.window,
                    "kv_bytes_attended_per_step": kv_bytes, "kv_bytes_unique_per_step": unique,
-                   "l2": f"inputs larger than L2: {unique / 1e6:.0f} MB of distinct K/V per "
-                         f"step vs {L2_BYTES / 1e6:.0f} MB L2, no flush",
+                   "kv_bytes_block_rounded_per_step": lb["kv_block_rounded"],
+                   "l2": (f"inputs larger than L2: {unique / 1e6:.0f} MB of distinct K/V per "
+                          f"step vs {L2_BYTES / 1e6:.0f} MB L2, no flush" if unique > L2_BYTES
+                          else f"{unique / 1e6:.3f} MB of K/V per step fits in L2: back-to-back "
+                               "steps are L2-resident; cold_l2 flushes before every step"),
                    "parallelism": f"replicas x{dist_ctx.world} (no collective on the path)"},
         "cold_l2": {"ms_per_step": cold_s * 1e3,
                     "value": dist_ctx.world * kv_bytes / cold_s / 1e9, "unit": "GB/s",
@@ -714,22 +895,78 @@ def main(argv=None) -> None:
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy)",
+                     "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                     "nominal_peak": NOMINAL_HBM_GBS,
                      "algorithmic_bytes_per_launch": algo,
+                     "algorithmic_bytes_detail": {
+                         "kv_exact": lb["kv_exact"], "kv_block_rounded": lb["kv_block_rounded"],
+                         "queries": w.batch * w.n_q_heads * w.head_dim * 2,
+                         "table_entries": lb["table_bytes"],
+                         "partials_written": lb["partial_bytes"], "partial_pieces": lb["partials"],
+                         "cut_pairs": lb["cut_pairs"], "whole_pairs": lb["whole_pairs"]},
+                     "reduce_bytes_per_launch": lb["reduce"],
                      "kernel_ms": kernel_s * 1e3,
-                     "traffic": recorded_traffic(args.config if w.block_size == 16
-                                                 else f"{args.config}-bs{w.block_size}")},
+                     "traffic": traffic,
+                     "traffic_over_algorithmic": traffic / algo if traffic else None},
         "e2e": {"value": e2e_bytes / e2e_elapsed / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "steps": e2e_steps},
         "clocks": clocks,
         "gpu_launches": step.launches * args.steps,
     }
+    return result, step
+
+
+def config_entry(r: dict) -> dict:
+    """The per-workload object under "configs": the headline keys that
+    describe one workload's measurement."""
+    keys = ("value", "unit", "ms_per_step", "dtype", "config", "cold_l2", "pct_of_hbm_peak",
+            "tokens_per_s_per_layer", "roofline", "e2e", "clocks", "gpu_launches",
+            "cpu_baseline")
+    return {k: r[k] for k in keys if k in r}
+
+
+def main(argv=None) -> None:
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+
+    from paged_kv_cache_33_gb300 import pagedkv
+
+    dist_ctx = DistCtx(args.gpus)
+    torch.cuda.set_device(dist_ctx.local_rank)
+    device = torch.device("cuda", dist_ctx.local_rank)
+    pagedkv.load()
+    peaks = measured_peaks()
+    result, step = measure(args.config, args, dist_ctx, device, peaks)
     if dist_ctx.rank == 0 and not args.no_extras:
         result["extras"] = measure_extras(step, peaks, device)
     if dist_ctx.rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = oracle_sample(w, args.cpu_baseline_seconds)
-        result["cpu_baseline_all_cores"] = oracle_fanout(args.config, w.block_size,
+        gpu_out = step.out.cpu().numpy()
+        ow = oracle_workload(args.config, step.w.block_size, step.w)
+        result["cpu_baseline"] = oracle_sample(ow, args.cpu_baseline_seconds, gpu_out,
+                                               gen_device=device)
+        result["cpu_baseline_all_cores"] = oracle_fanout(args.config, step.w.block_size,
                                                          args.cpu_baseline_seconds)
+    step.pool.destroy()
+    del step
+    names = [] if args.configs in ("", "none") else [c for c in args.configs.split(",")
+                                                      if c and c != args.config]
+    if names:
+        result["configs"] = {}
+    for name in names:
+        torch.cuda.empty_cache()
+        r, st = measure(name, args, dist_ctx, device, peaks)
+        if dist_ctx.rank == 0 and not args.no_cpu_baseline:
+            gpu_out = st.out.cpu().numpy()
+            ow = oracle_workload(name, st.w.block_size, st.w)
+            r["cpu_baseline"] = oracle_sample(ow, args.config_oracle_seconds, gpu_out,
+                                              max_seqs=32, gen_device=device)
+        st.pool.destroy()
+        del st
+        result["configs"][name] = config_entry(r)
     dist_ctx.barrier()
     if dist_ctx.rank == 0:
         print(json.dumps(result))

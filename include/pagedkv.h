@@ -287,10 +287,12 @@ kv_status paged_decode_attention_noalloc(kv_pool* pool, const void* q_dev, int32
  *                      softmax(scale q K^T) V over positions [lo, pos], lo =
  *                      max(0, pos + 1 - sliding_window) when the window is on.
  * bf16 pools with head_dim 128 and a query group of at most 8 heads per KV
- * head (KV_ERR_UNSUPPORTED otherwise).  Runs on the tcgen05 tensor cores
- * (P rounded to bf16).  A sequence with q_len > context_len or a context
- * above a bound sets KV_ERR_BAD_CONTEXT and is skipped.  Asynchronous on
- * `stream`; no workspace.
+ * head (KV_ERR_UNSUPPORTED otherwise).  Runs on the tcgen05 tensor cores;
+ * P enters the P V product as a bf16 high part plus the bf16 rounding of
+ * its remainder (two products into the same accumulator), so the result
+ * meets the decode's bf16 accuracy.  A sequence with q_len > context_len or
+ * a context above a bound sets KV_ERR_BAD_CONTEXT and is skipped.
+ * Asynchronous on `stream`; no workspace.
  */
 kv_status paged_prefill_attention(kv_pool* pool, const void* q_dev, int32_t n_q_heads,
                                   const int32_t* cu_q_lens_dev, const int32_t* block_tables_dev,
@@ -331,8 +333,10 @@ kv_status kv_pool_set_timing_events(kv_pool* pool, void* start_event, void* stop
  * kv_pool_set_test_stall -- test instrumentation for the timeout path: while
  * enabled, the first copy of worker 0 in each decode launch expects 16 more
  * bytes than it brings, so that warp's bounded wait runs out and the call
- * reports KV_ERR_TIMEOUT (its outputs are then undefined).  No copy is left
- * in flight and the context stays usable.  0 disables it (the default).
+ * reports KV_ERR_TIMEOUT (its outputs are then undefined).  Having recorded
+ * the timeout, the kernel supplies the 16 bytes itself, so its drain
+ * completes: no copy is left in flight and the context stays usable.
+ * 0 disables it (the default).
  */
 kv_status kv_pool_set_wait_limit(kv_pool* pool, uint64_t limit_ns);
 kv_status kv_pool_set_test_stall(kv_pool* pool, int32_t enable);

@@ -358,6 +358,7 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : (KIND == kFp4 ? PKV_FP
   // test hook: the first copy of worker 0 expects more bytes than it brings,
   // so its (bounded) wait runs out
   uint32_t stall = worker == 0 ? p.stall_tx : 0u;
+  uint32_t stall_bar = 0;  // the barrier that expects the extra bytes
   auto next_segment = [&]() {
     const int t = atomicAdd(p.ticket, 1);
     if (t >= sp.Nc) {
@@ -400,6 +401,7 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : (KIND == kFp4 ? PKV_FP
     info[s] = StageInfo{iu, ic.b, ic.h, ic.k, iu_end, iseg};
     const uint32_t dst = smem_addr(ring + s * G::kStageBytes);
     mbar_arrive_expect_tx(bar, nload * G::kBlockBytes + stall);
+    if (stall) stall_bar = bar;
     stall = 0;
 #pragma unroll
     for (int i = 0; i < BPU; ++i) {
@@ -834,8 +836,11 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : (KIND == kFp4 ? PKV_FP
   }
 
   if (timed_out && lane == 0) {
-    // leave no copy in flight: wait (bounded) for every stage holding one
+    // leave no copy in flight: wait (bounded) for every stage holding one.
+    // Under the test stall the missing bytes are supplied here, so that the
+    // stalled stage completes once its real copy has landed.
     atomicOr(p.err, kErrTimeout);
+    if (stall_bar) mbar_complete_tx(stall_bar, p.stall_tx);
     for (int k = it; k < it + STAGES; ++k)
       if ((tma_stages >> (k % STAGES)) & 1u &&
           !mbar_wait_bounded(smem_addr(&bars[k % STAGES]), (k / STAGES) & 1, p.wait_limit_ns,

@@ -21,8 +21,11 @@
 //    stage once its P V products are.  Blocks outside the attended range or
 //    with a bad id are left out and their rows masked.
 //  * One thread issues tcgen05.mma: S = Q K^T (128 x 128, fp32 in tensor
-//    memory), then O += P V (128 x 128, fp32 in tensor memory) with P read
-//    from tensor memory and V read MN-major straight from its pool rows.
+//    memory), then O += P_hi V + P_lo V (128 x 128, fp32 in tensor memory)
+//    with P read from tensor memory and V read MN-major straight from its
+//    pool rows.  P is a bf16 high part plus the bf16 rounding of its
+//    remainder: one bf16 P alone (2^-9 relative per weight) would put the
+//    output ~1e-3 (relative) off the exact attention.
 //    128-key products run the tensor pipe at its full rate; 64-key ones
 //    reach two thirds of it.
 //  * Two query tiles share every key tile and alternate on the tensor pipe:
@@ -34,7 +37,7 @@
 //    tensor-memory load of the row of S (128 columns), masking (causal, window, sequence end, missing blocks),
 //    online softmax in the exp2 domain with a lazy maximum (O in tensor
 //    memory is rescaled only when a row's maximum grows by more than 2^8),
-//    P in bf16 back over the first columns of S (P never touches shared
+//    P's two bf16 parts back over the columns of S (P never touches shared
 //    memory, whose bandwidth the products' operand reads use), and zeros into
 //    the V rows the product must not see (slots past the sequence's end,
 //    blocks not loaded).  The epilogue divides O by the row sum and stores
@@ -76,7 +79,8 @@ constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 4 * kTiles + 2;
 constexpr int kTmemSlot = kBars + kNumBars * 8;
 constexpr int kSmemBytes = kTmemSlot + 16 + 1024;     // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
-// tensor memory per query tile: S [0,128) (P over its first 64 columns), O [128,256)
+// tensor memory per query tile: S [0,128) (P_hi over its first 64 columns, P_lo over
+// the last 64), O [128,256)
 constexpr uint32_t kOCol = kKv;
 constexpr uint32_t kTmemTile = 256;
 constexpr uint32_t kTmemCols = kTiles * kTmemTile;
@@ -267,19 +271,32 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       if (m_run == -INFINITY || rescale) m_run = m_new;
       const float mu = m_run == -INFINITY ? 0.f : m_run;
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nmu2 = make_float2(-mu, -mu);
-      // the exponentials; P (bf16 pairs) over the first kKv/2 columns of S,
-      // one tensor-memory store
+      // the exponentials; P as a bf16 high part (pairs over the first kKv/2
+      // columns of S) and the bf16 rounding of its remainder (the last kKv/2
+      // columns), so ~16 significant bits of every weight reach the products.
+      // Each quarter of the keys is stored as soon as it is done (its S
+      // columns were read into registers above), which keeps few registers
+      // live; one wait covers the stores.
       float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      uint32_t w[kKv / 2];
+      constexpr int kQuarter = kKv / 8;  // bf16 pairs per quarter of the keys
 #pragma unroll
-      for (int e = 0; e < kKv / 2; ++e) {
-        const float2 arg = ffma2(make_float2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])),
-                                 sc2, nmu2);
-        const float2 pe = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
-        l2[e & 1] = fadd2(l2[e & 1], pe);
-        w[e] = pack_bf16x2(pe.x, pe.y);
+      for (int kq = 0; kq < 4; ++kq) {
+        uint32_t wh[kQuarter], wl[kQuarter];
+#pragma unroll
+        for (int i = 0; i < kQuarter; ++i) {
+          const int e = kq * kQuarter + i;
+          const float2 arg = ffma2(make_float2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])),
+                                   sc2, nmu2);
+          const float2 pe = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
+          l2[i & 1] = fadd2(l2[i & 1], pe);
+          wh[i] = pack_bf16x2(pe.x, pe.y);
+          const float2 rem = fsub2(pe, make_float2(bf16_lo(wh[i]), bf16_hi(wh[i])));
+          wl[i] = pack_bf16x2(rem.x, rem.y);
+        }
+        tmem_st16_nowait(lane_base + kq * kQuarter, wh);
+        tmem_st16_nowait(lane_base + kKv / 2 + kq * kQuarter, wl);
       }
-      tmem_st64(lane_base, w);
+      tmem_wait_st();
       // O is stable: S of this key tile was issued only after the tile's
       // previous P V product had completed
       if (__any_sync(0xffffffffu, rescale)) {  // tensor-memory access is warp-wide
@@ -457,10 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         const uint32_t va = v_lo + (jt % kVStages) * kStageUnits;
         const uint32_t pt = tmem + t * kTmemTile;  // P over the S columns
         const uint32_t d = tmem + t * kTmemTile + kOCol;
+        // O += P_hi V, then O += P_lo V (the remainders, kKv/2 columns on)
 #pragma unroll
-        for (int k = 0; k < kKv / 16; ++k)
-          umma_bf16_ta_w(d, pt + k * 8, va + ((k * 16 * 128) >> 4), v_hi, idO,
-                         (jt > 0 || k > 0) ? 1u : 0u);
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int k = 0; k < kKv / 16; ++k)
+            umma_bf16_ta_w(d, pt + part * (kKv / 2) + k * 8, va + ((k * 16 * 128) >> 4), v_hi, idO,
+                           (jt > 0 || part > 0 || k > 0) ? 1u : 0u);
       };
       for (int jt = 0; ok && jt <= n_tiles; ++jt) {
         bool v_ready = false, k_ready = false;

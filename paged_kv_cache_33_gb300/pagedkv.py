@@ -456,7 +456,7 @@ def paged_decode_attention_noalloc(pool: KVPool, q: torch.Tensor, block_tables: 
     a pinned host tensor) and `max_context_len` must come from the caller."""
     if out is None:
         raise ValueError("out is required: this entry point allocates nothing")
-    _, Hq, _ = _check_decode_shapes(pool, q, block_tables, context_lens, out)
+    B, Hq, _ = _check_decode_shapes(pool, q, block_tables, context_lens, out)
     _check(load().paged_decode_attention_noalloc(
         pool.handle, _dev(q, torch.bfloat16, "q"), Hq,
         _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],

@@ -137,3 +137,33 @@ def test_noalloc_binding_requires_out():
 def test_drain_timeout_status_is_named():
     assert pagedkv.STATUS[9] == "KV_ERR_DRAIN_TIMEOUT"
     assert pagedkv.kv_status_str(9) == "KV_ERR_DRAIN_TIMEOUT"
+
+
+def test_decode_bindings_marshal_their_arguments(monkeypatch):
+    # The library replaced by a recorder (no GPU here): each binding must
+    # pass the sizes taken from the tensors, in the C ABI's order.
+    calls = {}
+
+    class _Lib:
+        def __getattr__(self, name):
+            def f(*args):
+                calls[name] = args
+                return 0
+            return f
+
+    monkeypatch.setattr(pagedkv, "load", lambda: _Lib())
+    monkeypatch.setattr(pagedkv, "_dev", lambda t, dtype, name: (name, tuple(t.shape)))
+    monkeypatch.setattr(pagedkv, "_out", lambda t, name: (name, tuple(t.shape)))
+    monkeypatch.setattr(pagedkv, "_stream", lambda s: "stream")
+    pool = _FakePool()
+    pool.handle = "pool"
+    q, tables, lens, out = _decode_args(B=3, Hq=8, mbs=4)
+    pagedkv.paged_decode_attention_noalloc(pool, q, tables, lens, 0.5, 7, 16, out)
+    assert calls["paged_decode_attention_noalloc"] == (
+        "pool", ("q", (3, 8, 128)), 8, ("block_tables", (3, 4)), 4, ("context_lens", (3,)), 3, 16,
+        0.5, 7, ("out", (3, 8, 128)), "stream")
+    monkeypatch.setattr(pagedkv, "paged_decode_workspace_bytes", lambda *a: 0)
+    pagedkv.paged_decode_attention(pool, q, tables, lens, 0.5, 7, max_context_len=16, out=out)
+    args = calls["paged_decode_attention"]
+    assert args[:10] == ("pool", ("q", (3, 8, 128)), 8, ("block_tables", (3, 4)), 4,
+                         ("context_lens", (3,)), 3, 16, 0.5, 7)

@@ -1,13 +1,12 @@
 """GPU parity of paged prefill (extend) attention on tcgen05 against the fp64
 oracle.
 
-Tolerance: the kernel rounds the softmax weights P to bf16 (8 significant
-bits, relative rounding error <= 2^-9) before the P V product, accumulating
-in fp32; every output is a convex combination of V rows, so its error is at
-most ~2^-9 * max|V| plus fp32 rounding.  With N(0,1) data (max|V| ~ 5) that
-gives max |err| <= 1e-2; the errors are independent over the attended
-tokens, so the relative L2 error stays near 2^-9 / sqrt(3) ~ 1.1e-3: the bar
-is 3e-3.
+Tolerance: the bf16 KV bar of the decode (max |err| <= 2e-3, relative L2
+<= 1e-3).  The kernel hands P to the P V product as a bf16 high part plus
+the bf16 rounding of its remainder, so each weight keeps ~16 significant
+bits (relative error <= 2^-17), and accumulates in fp32; the residual is the
+fp32 arithmetic of S, the exponentials and the accumulation, far below the
+bar.
 """
 
 import numpy as np
@@ -17,12 +16,11 @@ import torch
 import oracle
 from paged_kv_cache_33_gb300 import pagedkv
 
+from _parity import BF16_MAX_ABS as MAX_ABS
+from _parity import BF16_REL_L2 as REL_L2
 from _parity import compare_pools, errors, poison
 
 pytestmark = pytest.mark.gpu
-
-MAX_ABS = 1e-2
-REL_L2 = 3e-3
 
 
 def _build(ctx_lens, q_lens, hq, hkv, bs=16, seed=0, extra_blocks=5):

@@ -2,9 +2,10 @@
 
 With the pool's test stall enabled, the first copy of worker 0 expects 16
 bytes more than it brings, so that warp's wait (bounded to 2 ms here) runs
-out: the kernel records KV_ERR_TIMEOUT, drains the copies it issued (every
-copy lands; only the expected count is off) and returns.  The host reads
-the status, and the same context then computes a correct step.
+out: the kernel records KV_ERR_TIMEOUT, supplies the 16 missing bytes to
+that barrier itself, drains the copies it issued (every copy lands, so the
+drain completes and no KV_ERR_DRAIN_TIMEOUT is recorded) and returns.  The
+host reads the status, and the same context then computes a correct step.
 """
 
 import pytest
