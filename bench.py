@@ -498,21 +498,45 @@ def _event_time(torch, fn, iters: int) -> float:
 def measure_extras(step: Step, peaks: dict, device) -> dict:
     """The other operations of the library, each against its own roofline:
     copy-on-write block copies (HBM), prefill attention (tensor cores), and
-    the host block manager's per-step work.  Runs after the timed steps (the
-    block copies overwrite blocks of the bench pool)."""
+    the host block manager's per-step work.  Runs after the timed steps, each
+    on pools of its own."""
     import numpy as np
     torch, pk, w = step.torch, step.pk, step.w
     out = {}
-    # -- paged_kv_copy_blocks: disjoint random pairs over the whole pool
-    n = min(2048, w.num_blocks // 2)
-    pairs = np.random.default_rng(9).permutation(w.num_blocks)[:2 * n].astype(np.int32).reshape(n, 2)
-    blk_bytes = w.n_kv_heads * w.block_size * w.kv_bytes_per_token_head()
-    t = _event_time(torch, lambda: pk.paged_kv_copy_blocks(step.pool, pairs), 20)
-    gbs = 2 * blk_bytes * n / t / 1e9
-    out["paged_kv_copy_blocks"] = {
-        "pairs": n, "block_bytes": blk_bytes, "us_per_call": t * 1e6, "achieved": gbs,
-        "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
-        "bytes_per_pair": 2 * blk_bytes}
+    # -- paged_kv_copy_blocks: disjoint random pairs, 268 MB moved per call
+    #    (134 MB read, 134 MB written), each call timed alone after an L2
+    #    flush, on a bf16 pool (64 KB blocks) and on an FP8 pool (32 KB blocks)
+    flush_w = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    flush_r = torch.ones(64 * 1024 * 1024, dtype=torch.int32, device=device)
+    for key, dt, nblocks, npairs in (("paged_kv_copy_blocks", "bf16", 4096, 2048),
+                                     ("paged_kv_copy_blocks_fp8", "fp8", 8192, 4096)):
+        cpool = pk.KVPool(nblocks, 16, 8, 128, dt)
+        pairs = (np.random.default_rng(9).permutation(nblocks)[:2 * npairs].astype(np.int32)
+                 .reshape(npairs, 2))
+        blk = 8 * 16 * 128 * 2 * (2 if dt == "bf16" else 1)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(20)]
+        for i in range(23):
+            flush_w.fill_(1)
+            flush_r.sum()
+            if i >= 3:
+                ev[i - 3][0].record()
+            pk.paged_kv_copy_blocks(cpool, pairs)
+            if i >= 3:
+                ev[i - 3][1].record()
+        torch.cuda.synchronize()
+        t = statistics.median(a.elapsed_time(b) for a, b in ev) / 1e3
+        gbs = 2 * blk * npairs / t / 1e9
+        out[key] = {
+            "dtype": dt, "pairs": npairs, "block_bytes": blk, "launches": -(-npairs // 2048),
+            "us_per_call": t * 1e6, "achieved": gbs, "unit": "GB/s", "bound": "hbm",
+            "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"], "bytes_per_pair": 2 * blk,
+            "note": "median of 20 calls, each after an L2 flush (256 MB written, another 256 MB "
+                    "read); 268 MB moved per call"}
+        if cpool.check_status() != pk.KV_OK:
+            raise RuntimeError("device error in the block copies")
+        cpool.destroy()
+    del flush_w, flush_r
     # -- paged_prefill_attention: 8B-shaped full causal prefill, 4 x 2048 tokens
     #    (short prompts: per-CTA set-up weighs more) and 4 x 8192 tokens
     bf16_peak = peaks["bf16_tflops"]

@@ -251,6 +251,17 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : (KIND == kFp4 ? PKV_FP
   const int worker = blockIdx.x * NW + warp;
   // the reduce kernel may be scheduled now; it waits for this grid to finish
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Pull the block tables into L2 (one line per thread across the grid), so
+  // that the first table entries every warp reads, right after the batch
+  // table below, do not wait on DRAM.
+  {
+    const char* tb = reinterpret_cast<const char*>(p.block_tables);
+    const int64_t tbytes = static_cast<int64_t>(p.batch) * p.mbs * 4;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * (NW * 32) * 128;
+    for (int64_t off = (static_cast<int64_t>(blockIdx.x) * (NW * 32) + threadIdx.x) * 128;
+         off < tbytes; off += stride)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(tb + off));
+  }
 
   // ---- the batch table: usable context lengths and units before each sequence
   {
@@ -302,12 +313,6 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : (KIND == kFp4 ? PKV_FP
       }
     }
   }
-
-  // Launched after the KV write of the same step as its programmatic
-  // dependent, this kernel has built its table while the write ran; the pool
-  // and the ticket counter are read only after the write has completed.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("fence.proxy.async;" ::: "memory");
 
   // ---- the split of this call's units into segments
   Split sp;
@@ -433,16 +438,26 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : (KIND == kFp4 ? PKV_FP
       next_segment();
     }
   };
+  // A static share's first unit and its table entries come from inputs of
+  // the call alone, so they are resolved before the wait below.
+  if (lane == 0 && worker < sp.Ps) {
+    iu = static_cast<int>(static_cast<int64_t>(sp.Ts) * worker / sp.Ps);
+    iu_end = static_cast<int>(static_cast<int64_t>(sp.Ts) * (worker + 1) / sp.Ps);
+    iseg = worker;
+    ic = locate(iu);
+    table_entries(ic, next_phys);
+  }
+
+  // Launched after the KV write of the same step as its programmatic
+  // dependent, this kernel has built its table and found its first units
+  // while the write ran (the write lets it start only once every kernel
+  // before the write has completed, so the tables and lengths are final);
+  // the pool and the ticket counter are touched only after the write has
+  // completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("fence.proxy.async;" ::: "memory");
   if (lane == 0) {
-    if (worker < sp.Ps) {
-      iu = static_cast<int>(static_cast<int64_t>(sp.Ts) * worker / sp.Ps);
-      iu_end = static_cast<int>(static_cast<int64_t>(sp.Ts) * (worker + 1) / sp.Ps);
-      iseg = worker;
-      ic = locate(iu);
-      table_entries(ic, next_phys);
-    } else {
-      next_segment();
-    }
+    if (worker >= sp.Ps) next_segment();
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) issue(s);
   }
