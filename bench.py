@@ -433,12 +433,15 @@ def timed_cold(step: Step, iters: int) -> float:
 
 
 def timed_e2e(step: Step, steps: int, warmup: int, dist_ctx) -> dict:
-    """Same steps through the public API with host inputs and a host result:
-    every step copies q, the new K/V, slots, block tables and context lengths
-    from pinned host memory (laid out back to back in one pinned buffer, so
-    one copy moves them all), and the kernels write the step's output into a
-    pinned host buffer (mapped host memory: the device-to-host transfer of the
-    result happens inside the step, with no separate copy)."""
+    """Same steps through the public API with host inputs and a host result.
+    Every step's inputs -- q, the new K/V, slots, block tables and context
+    lengths, laid out back to back in one pinned host buffer -- are passed to
+    paged_decode_step as host memory, which the kernels read in place over
+    the host link, and the kernels write the step's output into a pinned host
+    buffer: the whole host-to-device and device-to-host traffic of the step
+    happens inside the call, with no separate copy.  `staged_s` times the
+    same steps with the inputs first copied to device memory by one
+    host-to-device copy per step (torch), for comparison."""
     torch, w = step.torch, step.w
     srcs = {"q": step.q, "k": step.k_new, "v": step.v_new, "slots": step.slots,
             "tables": step.tables, "lens": step.lens}
@@ -456,27 +459,34 @@ def timed_e2e(step: Step, steps: int, warmup: int, dist_ctx) -> dict:
 
     for name, t in srcs.items():
         view(host_buf, name).copy_(t.cpu())
+    host = {name: view(host_buf, name) for name in srcs}
     dev = {name: view(dev_buf, name) for name in srcs}
     out_host = torch.empty(step.out.shape, dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in srcs.values())
     d2h = out_host.numel() * out_host.element_size()
 
-    def one():
+    def in_place():
+        step.run(q=host["q"], tables=host["tables"], lens=host["lens"], k=host["k"],
+                 v=host["v"], slots=host["slots"], out=out_host)
+
+    def staged():
         dev_buf.copy_(host_buf, non_blocking=True)
         step.run(q=dev["q"], tables=dev["tables"], lens=dev["lens"], k=dev["k"], v=dev["v"],
                  slots=dev["slots"], out=out_host)
 
-    for _ in range(warmup):
-        one()
-    torch.cuda.synchronize()
-    dist_ctx.barrier()
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
-    torch.cuda.synchronize()
-    elapsed = time.perf_counter() - t0
-    dist_ctx.barrier()
-    return {"elapsed_s": elapsed, "h2d": h2d, "d2h": d2h}
+    times = {}
+    for label, one in (("in_place", in_place), ("staged", staged)):
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        dist_ctx.barrier()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one()
+        torch.cuda.synchronize()
+        times[label] = time.perf_counter() - t0
+        dist_ctx.barrier()
+    return {"elapsed_s": times["in_place"], "staged_s": times["staged"], "h2d": h2d, "d2h": d2h}
 
 
 # ----------------------------------------------------------------- extras --
@@ -934,7 +944,12 @@ def measure(name: str, args, dist_ctx: DistCtx, device, peaks: dict) -> tuple[di
                      "traffic_over_algorithmic": traffic / algo if traffic else None},
         "e2e": {"value": e2e_bytes / e2e_elapsed / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "steps": e2e_steps},
+                "steps": e2e_steps,
+                "how": "paged_decode_step with every per-step input in pinned host memory, read "
+                       "in place by the kernels, and the output written into pinned host memory",
+                "staged_value": e2e_bytes / dist_ctx.max(e2e["staged_s"]) / 1e9,
+                "staged_how": "the same with the inputs copied to device memory first (one "
+                              "host-to-device copy per step)"},
         "clocks": clocks,
         "gpu_launches": step.launches * args.steps,
     }

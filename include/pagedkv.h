@@ -22,6 +22,14 @@
  * Conventions used by every call:
  *  - Pointers named *_dev, and all tensor arguments, are DEVICE pointers on
  *    the pool's device, owned by the caller, unless stated otherwise.
+ *  - The per-step inputs of paged_kv_write, paged_decode_attention,
+ *    paged_decode_step and paged_decode_attention_noalloc (k, v,
+ *    slot_mapping, q, block_tables, context_lens) may instead be pinned host
+ *    memory the device can address (cudaHostAlloc, or cudaHostRegister with
+ *    cudaHostRegisterMapped, under unified addressing), like out_dev: the
+ *    kernels then read them in place over the host link (NVLink-C2C on
+ *    Grace-Blackwell), with no separate copy.  The host must not modify them
+ *    until the call's work on `stream` has completed.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls that
  *    take a stream are asynchronous: they validate their host-side arguments,
  *    enqueue kernels and return.  Device-side problems (a table entry outside

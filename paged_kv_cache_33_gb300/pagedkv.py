@@ -133,6 +133,20 @@ def _dev(t: torch.Tensor, dtype: torch.dtype, name: str) -> ctypes.c_void_p:
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _in(t: torch.Tensor, dtype: torch.dtype, name: str) -> ctypes.c_void_p:
+    """A per-step input: a CUDA tensor, or a pinned host tensor, which the
+    kernels read in place (mapped host memory; no host-to-device copy)."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda:
+        if not t.is_pinned():
+            raise TypeError(f"{name} must be a CUDA tensor or a pinned host tensor")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        return ctypes.c_void_p(t.data_ptr())
+    return _dev(t, dtype, name)
+
+
 def _out(t: torch.Tensor, name: str) -> ctypes.c_void_p:
     """An fp32 result buffer: a CUDA tensor, or a pinned host tensor, which
     the kernels write directly (mapped host memory; no device-to-host copy)."""
@@ -155,6 +169,7 @@ class KVPool:
         _check(L.kv_pool_create(int(num_blocks), int(block_size), int(n_kv_heads),
                                 int(head_dim), DTYPES[dtype], ctypes.byref(h)), "kv_pool_create")
         self._h = h
+        self.device = torch.device("cuda", torch.cuda.current_device())  # the pool's GPU
         self.num_blocks, self.block_size = int(num_blocks), int(block_size)
         self.n_kv_heads, self.head_dim, self.dtype = int(n_kv_heads), int(head_dim), dtype
         self._events = None
@@ -338,9 +353,9 @@ def paged_kv_write(pool: KVPool, k: torch.Tensor, v: torch.Tensor, slot_mapping:
     shape = (T, pool.n_kv_heads, pool.head_dim)
     if tuple(k.shape) != shape or tuple(v.shape) != shape:
         raise ValueError(f"k and v must be {shape}")
-    _check(load().paged_kv_write(pool.handle, _dev(k, torch.bfloat16, "k"),
-                                 _dev(v, torch.bfloat16, "v"),
-                                 _dev(slot_mapping, torch.int64, "slot_mapping"), T,
+    _check(load().paged_kv_write(pool.handle, _in(k, torch.bfloat16, "k"),
+                                 _in(v, torch.bfloat16, "v"),
+                                 _in(slot_mapping, torch.int64, "slot_mapping"), T,
                                  _stream(stream)), "paged_kv_write")
 
 
@@ -372,16 +387,16 @@ def paged_decode_attention(pool: KVPool, q: torch.Tensor, block_tables: torch.Te
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if B else 0
     if out is None:
-        out = torch.empty(B, Hq, D, dtype=torch.float32, device=q.device)
+        out = torch.empty(B, Hq, D, dtype=torch.float32, device=pool.device)
     need = paged_decode_workspace_bytes(pool, B, Hq, max_context_len, sliding_window)
     if workspace is None and need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=pool.device)
     ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().paged_decode_attention(
-        pool.handle, _dev(q, torch.bfloat16, "q"), Hq,
-        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
-        _dev(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
+        pool.handle, _in(q, torch.bfloat16, "q"), Hq,
+        _in(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _in(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
         int(sliding_window), _out(out, "out"), ws_ptr, ws_bytes, _stream(stream)),
         "paged_decode_attention")
     return out
@@ -404,18 +419,18 @@ def paged_decode_step(pool: KVPool, k: torch.Tensor, v: torch.Tensor, slot_mappi
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if B else 0
     if out is None:
-        out = torch.empty(B, Hq, D, dtype=torch.float32, device=q.device)
+        out = torch.empty(B, Hq, D, dtype=torch.float32, device=pool.device)
     need = paged_decode_workspace_bytes(pool, B, Hq, max_context_len, sliding_window)
     if workspace is None and need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=pool.device)
     ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().paged_decode_step(
-        pool.handle, _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
-        _dev(slot_mapping, torch.int64, "slot_mapping"), T,
-        _dev(q, torch.bfloat16, "q"), Hq,
-        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
-        _dev(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
+        pool.handle, _in(k, torch.bfloat16, "k"), _in(v, torch.bfloat16, "v"),
+        _in(slot_mapping, torch.int64, "slot_mapping"), T,
+        _in(q, torch.bfloat16, "q"), Hq,
+        _in(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _in(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
         int(sliding_window), _out(out, "out"), ws_ptr, ws_bytes, _stream(stream)),
         "paged_decode_step")
     return out
@@ -458,9 +473,9 @@ def paged_decode_attention_noalloc(pool: KVPool, q: torch.Tensor, block_tables: 
         raise ValueError("out is required: this entry point allocates nothing")
     B, Hq, _ = _check_decode_shapes(pool, q, block_tables, context_lens, out)
     _check(load().paged_decode_attention_noalloc(
-        pool.handle, _dev(q, torch.bfloat16, "q"), Hq,
-        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
-        _dev(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
+        pool.handle, _in(q, torch.bfloat16, "q"), Hq,
+        _in(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _in(context_lens, torch.int32, "context_lens"), B, int(max_context_len), float(scale),
         int(sliding_window), _out(out, "out"), _stream(stream)),
         "paged_decode_attention_noalloc")
 

@@ -153,6 +153,7 @@ def test_decode_bindings_marshal_their_arguments(monkeypatch):
 
     monkeypatch.setattr(pagedkv, "load", lambda: _Lib())
     monkeypatch.setattr(pagedkv, "_dev", lambda t, dtype, name: (name, tuple(t.shape)))
+    monkeypatch.setattr(pagedkv, "_in", lambda t, dtype, name: (name, tuple(t.shape)))
     monkeypatch.setattr(pagedkv, "_out", lambda t, name: (name, tuple(t.shape)))
     monkeypatch.setattr(pagedkv, "_stream", lambda s: "stream")
     pool = _FakePool()
@@ -167,3 +168,10 @@ def test_decode_bindings_marshal_their_arguments(monkeypatch):
     args = calls["paged_decode_attention"]
     assert args[:10] == ("pool", ("q", (3, 8, 128)), 8, ("block_tables", (3, 4)), 4,
                          ("context_lens", (3,)), 3, 16, 0.5, 7)
+
+
+def test_inputs_must_be_device_or_pinned_host_tensors():
+    # a pageable host tensor cannot be read by the kernels in place
+    t = torch.zeros(4, dtype=torch.int32)
+    with pytest.raises(TypeError, match="pinned"):
+        pagedkv._in(t, torch.int32, "context_lens")

@@ -226,3 +226,33 @@ def test_step_reports_a_bad_slot():
     torch.cuda.synchronize()
     assert pool.check_status() == 7              # KV_ERR_BAD_SLOT
     pool.destroy()
+
+
+@pytest.mark.parametrize("name", ["tiny", "8b", "sw", "fp8", "fp4"])
+def test_inputs_in_pinned_host_memory_give_the_same_step(name):
+    # Every per-step input (new K/V, slots, queries, tables, lengths) read in
+    # place from pinned host memory, the output written into pinned host
+    # memory: same pool and, bit for bit, the same output as device inputs.
+    w = _workload(name, "small")
+    q, tables, lens = _inputs(w)
+    dev_pool, host_pool = make_gpu_pool(w), make_gpu_pool(w)
+    _, (k, v, s) = _setup(w, dev_pool)
+    _setup(w, host_pool)
+    ref = pagedkv.paged_decode_step(dev_pool, k.cuda(), v.cuda(), s.cuda(), q, tables, lens,
+                                    w.scale, w.window, max_context_len=w.max_context_len)
+    pin = lambda t: t.cpu().contiguous().pin_memory()
+    out = torch.full(tuple(ref.shape), float("nan")).pin_memory()
+    pagedkv.paged_decode_step(host_pool, pin(k), pin(v), pin(s), pin(q), pin(tables), pin(lens),
+                              w.scale, w.window, max_context_len=w.max_context_len, out=out)
+    torch.cuda.synchronize()
+    assert dev_pool.check_status() == pagedkv.KV_OK and host_pool.check_status() == pagedkv.KV_OK
+    assert torch.equal(out, ref.cpu())
+    bits = lambda t: t.view(torch.int16) if t.dtype == torch.bfloat16 else t   # NaN-poisoned
+    assert torch.equal(bits(host_pool.view()), bits(dev_pool.view()))
+    # and the attention alone, reading host inputs
+    out2 = pagedkv.paged_decode_attention(host_pool, pin(q), pin(tables), pin(lens), w.scale,
+                                          w.window, max_context_len=w.max_context_len)
+    torch.cuda.synchronize()
+    assert torch.equal(out2.cpu(), ref.cpu())
+    dev_pool.destroy()
+    host_pool.destroy()
