@@ -9,7 +9,7 @@ memory and the output read back inside the timed region.  `roofline` gives the
 decode kernel alone against the measured HBM copy bandwidth.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 8b|70b|sw|tiny]
-                  [--configs 70b,sw,fp8,fp4,tiny|none] [--impl ours|reference]
+                  [--configs 70b,sw,fp8,fp4,long,tiny|none] [--impl ours|reference]
                   [--part-blocks P]
 
 The headline workload (--config, default 8b) gives the top-level figures;
@@ -77,7 +77,7 @@ def parse_args(argv=None):
                     help="skip the block-copy, prefill and host block-manager measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
-    ap.add_argument("--configs", default="70b,sw,fp8,fp4,tiny",
+    ap.add_argument("--configs", default="70b,sw,fp8,fp4,long,tiny",
                     help="comma-separated workloads measured after the headline one and "
                          "reported under 'configs' ('none' = only the headline)")
     ap.add_argument("--config-oracle-seconds", type=float, default=3.0,
