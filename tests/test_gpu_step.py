@@ -256,3 +256,42 @@ def test_inputs_in_pinned_host_memory_give_the_same_step(name):
     assert torch.equal(out2.cpu(), ref.cpu())
     dev_pool.destroy()
     host_pool.destroy()
+
+
+def test_step_replays_from_a_cuda_graph():
+    # The fused step (write, decode as its programmatic dependent, reduce)
+    # has no host synchronisation: captured once into a CUDA graph it
+    # replays with whatever the captured input buffers hold, bit for bit as
+    # a direct call on the same inputs.
+    w = _workload("8b", "small")
+    q, tables, lens = _inputs(w)
+    pool, ref_pool = make_gpu_pool(w), make_gpu_pool(w)
+    _, (k, v, s) = _setup(w, pool)
+    _setup(w, ref_pool)
+    k, v, s = k.cuda(), v.cuda(), s.cuda()
+    need = pagedkv.paged_decode_workspace_bytes(pool, w.batch, w.n_q_heads, w.max_context_len,
+                                                w.window)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    out = torch.empty(w.batch, w.n_q_heads, w.head_dim, device="cuda")
+    run = lambda: pagedkv.paged_decode_step(pool, k, v, s, q, tables, lens, w.scale, w.window,
+                                            max_context_len=w.max_context_len, out=out,
+                                            workspace=ws)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run()                                   # first call outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    gen = torch.Generator().manual_seed(11)
+    for _ in range(3):
+        q.copy_(torch.randn(q.shape, generator=gen).bfloat16())   # new queries, same buffer
+        graph.replay()
+        ref = pagedkv.paged_decode_step(ref_pool, k, v, s, q, tables, lens, w.scale, w.window,
+                                        max_context_len=w.max_context_len)
+        torch.cuda.synchronize()
+        assert pool.check_status() == pagedkv.KV_OK and ref_pool.check_status() == pagedkv.KV_OK
+        assert torch.equal(out, ref)
+    pool.destroy()
+    ref_pool.destroy()
