@@ -233,7 +233,10 @@ kv_status paged_decode_attention(kv_pool* pool, const void* q_dev, int32_t n_q_h
  *   a programmatic dependent of the kernel before it on the stream: it may be
  *   scheduled while that kernel runs and waits for it to complete before it
  *   reads or writes anything (so inputs produced by any earlier kernel are
- *   safe).  batch == 0 performs the write alone.
+ *   safe).  batch == 0 performs the write alone.  The call neither
+ *   synchronises nor allocates: with the pool, the workspace and the output
+ *   in place it can be captured into a CUDA graph (stream capture), whose
+ *   replays read whatever the captured input buffers then hold.
  */
 kv_status paged_decode_step(kv_pool* pool, const void* k_dev, const void* v_dev,
                             const int64_t* slot_mapping_dev, int64_t num_tokens,
