@@ -189,7 +189,10 @@ size_t paged_decode_workspace_bytes(const kv_pool* pool, int32_t batch, int32_t 
  * paged_decode_attention -- one decode step of attention over the pool.
  *   q_dev:               bf16 [batch][n_q_heads][head_dim]; query head hq uses
  *                        KV head hq / (n_q_heads / n_kv_heads); n_q_heads must
- *                        be a multiple of n_kv_heads with a group of at most 8.
+ *                        be a multiple of n_kv_heads with a group of at most
+ *                        64 (KV_ERR_UNSUPPORTED above).  A group of more than
+ *                        8 runs as passes over 8 query heads at a time, each
+ *                        reading the attended K/V again.
  *   block_tables_dev:    int32 [batch][max_blocks_per_seq]; only entries of
  *                        blocks holding an attended position are read.
  *   context_lens_dev:    int32 [batch]; each in [0, max_context_len] and

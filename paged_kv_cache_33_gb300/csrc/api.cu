@@ -109,7 +109,7 @@ DecodePlan plan_decode(const kv_pool* pool, int32_t batch, int32_t n_q_heads,
   }
   plan.ctas = static_cast<int32_t>(ctas);
   plan.workers = static_cast<int32_t>(ctas * nw);
-  const int64_t g = n_q_heads / pool->n_kv_heads;
+  const int64_t g = std::min<int64_t>(n_q_heads / pool->n_kv_heads, 8);  // heads per pass
   const int64_t pairs = static_cast<int64_t>(plan.batch) * pool->n_kv_heads;
   // partial slot of (segment s, pair p) is s + p: segments + pairs slots
   const int64_t slots = plan.workers + decode_max_chunks(t_max) + pairs;
@@ -296,7 +296,7 @@ kv_status decode_call(kv_pool* p, const StepWrite* w, const void* q, int32_t n_q
   if (!p || batch < 0 || n_q_heads <= 0) return KV_ERR_INVALID_ARG;
   if (n_q_heads % p->n_kv_heads != 0) return KV_ERR_INVALID_ARG;
   const int32_t g = n_q_heads / p->n_kv_heads;
-  if (g > 8) return KV_ERR_UNSUPPORTED;
+  if (g > pkv::kMaxDecodeGroup) return KV_ERR_UNSUPPORTED;
   if (w) {
     if (w->num_tokens < 0 || w->num_tokens > (int64_t(1) << 40)) return KV_ERR_INVALID_ARG;
     if (w->num_tokens > 0 && (!w->k || !w->v || !w->slots || !aligned16(w->k) || !aligned16(w->v)))
@@ -341,7 +341,7 @@ kv_status decode_call(kv_pool* p, const StepWrite* w, const void* q, int32_t n_q
   d.mbs = max_blocks_per_seq;
   d.n_q_heads = n_q_heads;
   d.n_kv_heads = p->n_kv_heads;
-  d.group = g;
+  d.group_stride = g;
   d.max_ctx = max_context_len;
   d.window = sliding_window > 0 ? sliding_window : 0;
   d.num_workers = plan.workers;
@@ -352,17 +352,22 @@ kv_status decode_call(kv_pool* p, const StepWrite* w, const void* q, int32_t n_q
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool timed = p->ev_start != nullptr;
-  // batches beyond one launch's table run as consecutive launches
-  for (int32_t b0 = 0; b0 < batch; b0 += plan.batch) {
+  // batches beyond one launch's table run as consecutive launches, and a
+  // group of more than 8 query heads per KV head as passes over 8 of them
+  // at a time (each pass reads the K/V again)
+  for (int32_t b0 = 0; b0 < batch; b0 += plan.batch)
+  for (int32_t h0 = 0; h0 < g; h0 += 8) {
     const int32_t nb = std::min(plan.batch, batch - b0);
-    d.q = static_cast<const uint16_t*>(q) + static_cast<int64_t>(b0) * n_q_heads * p->head_dim;
+    const int64_t first = static_cast<int64_t>(b0) * n_q_heads + h0;  // the pass's first q row
+    d.q = static_cast<const uint16_t*>(q) + first * p->head_dim;
     d.block_tables = block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq;
     d.context_lens = context_lens + b0;
-    d.out = out + static_cast<int64_t>(b0) * n_q_heads * p->head_dim;
+    d.out = out + first * p->head_dim;
     d.batch = nb;
+    d.group = std::min(8, g - h0);
     // The fused step's write kernel clears the ticket and lets the first
     // decode launch start while it runs; otherwise a memset clears it.
-    const bool fused = w != nullptr && b0 == 0;
+    const bool fused = w != nullptr && b0 == 0 && h0 == 0;
     if (fused) {
       if (pkv::launch_kv_write(p, w->k, w->v, w->slots, w->num_tokens, s, d.ticket) != cudaSuccess)
         return KV_ERR_CUDA;

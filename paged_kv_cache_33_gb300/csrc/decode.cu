@@ -305,11 +305,16 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : (KIND == kFp4 ? PKV_FP
     }
     if (threadIdx.x == kThreads - 1) s_pre[p.batch] = base;
     __syncthreads();
-    // zero the outputs of sequences with nothing to attend to (CTA-strided)
+    // zero the outputs of sequences with nothing to attend to (CTA-strided;
+    // this call's heads of every KV head)
     for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
       if (s_pre[b + 1] == s_pre[b]) {
         float* o = p.out + static_cast<int64_t>(b) * p.n_q_heads * D;
-        for (int x = threadIdx.x; x < p.n_q_heads * D; x += kThreads) o[x] = 0.f;
+        const int per_kv = p.group * D;
+        for (int x = threadIdx.x; x < p.n_kv_heads * per_kv; x += kThreads) {
+          const int hk = x / per_kv;
+          o[static_cast<int64_t>(hk) * p.group_stride * D + (x - hk * per_kv)] = 0.f;
+        }
       }
     }
   }
@@ -487,7 +492,8 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 2 ? 6 : (KIND == kFp4 ? PKV_FP
     const StageInfo si = info[s];
     if (si.u < 0) break;
     const SeqRange r = seq_from_ctx<BS, BPU>(s_ctx[si.b], p.window);
-    const int64_t row0 = static_cast<int64_t>(si.b) * p.n_q_heads + static_cast<int64_t>(si.h) * g;
+    const int64_t row0 = static_cast<int64_t>(si.b) * p.n_q_heads +
+                         static_cast<int64_t>(si.h) * p.group_stride;
     if (si.u != prev_u + 1 || si.k == 0) {
       // ---- a new piece of a (b, h) pair: its query fragments, a fresh state
       const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) + row0 * D;
@@ -963,7 +969,7 @@ __global__ void __launch_bounds__(kReduceThreads, kReduceCtas) paged_decode_redu
   }
   const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
   float4* dst = reinterpret_cast<float4*>(
-      p.out + (static_cast<int64_t>(b) * p.n_q_heads + static_cast<int64_t>(h) * g + hd) * D) + c4;
+      p.out + (static_cast<int64_t>(b) * p.n_q_heads + static_cast<int64_t>(h) * p.group_stride + hd) * D) + c4;
   *dst = make_float4(Ot.x * inv, Ot.y * inv, Ot.z * inv, Ot.w * inv);
 }
 

@@ -30,6 +30,9 @@ namespace pkv {
 // Sequences per decode launch: every CTA keeps a table of the batch in shared
 // memory.  Larger batches are split into several launches by the host.
 constexpr int kMaxDecodeBatch = 512;
+// Query heads per KV head the decode accepts; groups above 8 run as passes
+// of at most 8 heads.
+constexpr int kMaxDecodeGroup = 64;
 
 // Arguments of the stream-K decode, shared by all variants.
 //
@@ -55,6 +58,9 @@ struct DecodeParams {
   const float* v_scale;
   int64_t num_blocks;
   int32_t mbs, batch, n_q_heads, n_kv_heads, group;
+  int32_t group_stride;         // query heads per KV head in q and out (>= group: a call
+                                // with more than 8 runs as passes of <= 8 heads, q and out
+                                // offset to the pass's first head)
   int32_t max_ctx, window, num_workers;
   int64_t num_slots;            // partial slots in the workspace (bounds the reduce's reads)
   float scale_log2;             // softmax scale * log2(e)

@@ -81,7 +81,8 @@ def _custom(lens, hq=8, hkv=2, d=128, window=0, dtype="bf16", extra_blocks=7, se
 
 @pytest.mark.parametrize("bs", [16, 32])
 @pytest.mark.parametrize("hq,hkv,d", [(8, 8, 128), (4, 2, 128), (16, 4, 128), (16, 2, 128),
-                                      (2, 1, 64), (8, 1, 64), (7, 7, 64), (24, 3, 128)])
+                                      (2, 1, 64), (8, 1, 64), (7, 7, 64), (24, 3, 128),
+                                      (32, 2, 128), (24, 2, 128), (18, 2, 64), (64, 1, 128)])
 def test_head_grouping_and_head_dim(hq, hkv, d, bs):
     lens = [1, 15, 16, 17, 31, 32, 33, 47, 48, 49, 200, 513]
     run_parity(_custom(lens, hq, hkv, d, seed=hq + hkv + d, bs=bs))
@@ -290,8 +291,8 @@ def test_host_argument_checks():
                                                          dtype=torch.bfloat16), t, c, 0.1,
                                        max_context_len=64)
     assert e.value.status == 1
-    with pytest.raises(pagedkv.KVError) as e:
-        pagedkv.paged_decode_attention(pool, torch.zeros(2, 18, 128, device="cuda",
+    with pytest.raises(pagedkv.KVError) as e:                          # group 65 > 64
+        pagedkv.paged_decode_attention(pool, torch.zeros(2, 130, 128, device="cuda",
                                                          dtype=torch.bfloat16), t, c, 0.1,
                                        max_context_len=64)
     assert e.value.status == 4
@@ -300,3 +301,12 @@ def test_host_argument_checks():
     with pytest.raises(pagedkv.KVError) as e:
         pagedkv.paged_decode_attention(pool, q, t, c, 0.1, max_context_len=64, out=unaligned)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("dtype", ["fp8", "fp4"])
+@pytest.mark.parametrize("window", [0, 40])
+def test_groups_above_eight_quantised_and_windowed(dtype, window):
+    # 16 query heads per KV head (two passes of 8) on the quantised pools,
+    # with and without a window, and a forced small partition so pairs are cut
+    w = _custom([1, 16, 17, 100, 333, 700], 32, 2, 128, seed=5, bs=16, dtype=dtype, window=window)
+    run_parity(w, part_blocks=4)

@@ -295,3 +295,26 @@ def test_step_replays_from_a_cuda_graph():
         assert torch.equal(out, ref)
     pool.destroy()
     ref_pool.destroy()
+
+
+def test_step_with_sixteen_query_heads_per_kv_head():
+    # a group of 16 runs the decode as two passes of 8 heads; the fused call
+    # must match the write followed by the attention, bit for bit, and the
+    # oracle within the bf16 bar
+    lens = np.array([3, 16, 40, 129, 500], dtype=np.int32)
+    bs, hkv, hq = 16, 2, 32
+    nblk = [-(-int(c) // bs) for c in lens]
+    nb = sum(nblk) + 3
+    perm = np.random.default_rng(21).permutation(nb).astype(np.int32)
+    tables = np.full((len(lens), max(nblk)), -1, dtype=np.int32)
+    off = 0
+    for b, n in enumerate(nblk):
+        tables[b, :n] = perm[off:off + n]
+        off += n
+    w = W.Workload("g16", "small", len(lens), hq, hkv, 128, bs, nb, 0, "bf16", 128 ** -0.5, lens,
+                   tables, (lens - 1).astype(np.int64), data_seed=4242)
+    out_f, out_s, fused, opool, written = _two_ways(w)
+    assert torch.equal(out_f, out_s)
+    ref = opool.decode(w.query(), w.block_tables, w.context_lens, w.scale, w.window)
+    assert_close(w, out_f.cpu().numpy(), ref, "g16 fused")
+    fused.destroy()
