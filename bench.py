@@ -548,13 +548,22 @@ def measure_extras(step: Step, peaks: dict, device) -> dict:
         cpool.destroy()
     del flush_w, flush_r
     # -- paged_prefill_attention: 8B-shaped full causal prefill, 4 x 2048 tokens
-    #    (short prompts: per-CTA set-up weighs more) and 4 x 8192 tokens
+    #    (short prompts: per-CTA set-up weighs more) and 4 x 8192 tokens, over
+    #    bf16 and FP8 pools.  The FP8 products run at twice the bf16 rate
+    #    (the nominal ratio, 4.5 / 2.25 PFLOP/s dense, applied to the measured
+    #    bf16 peak).  Issued tensor work per algorithmic flop: bf16 1.5 (P V
+    #    twice: P's high part and remainder), FP8 2 (Q K^T and P V twice each)
     bf16_peak = peaks["bf16_tflops"]
-    for key, (B, ctx) in (("paged_prefill_attention", (4, 2048)),
-                          ("paged_prefill_attention_long", (4, 8192))):
+    for key, dt, (B, ctx) in (("paged_prefill_attention", "bf16", (4, 2048)),
+                              ("paged_prefill_attention_long", "bf16", (4, 8192)),
+                              ("paged_prefill_attention_fp8", "fp8", (4, 2048)),
+                              ("paged_prefill_attention_fp8_long", "fp8", (4, 8192))):
         hq, hkv = 32, 8
         nblk = ctx // 16
-        ppool = pk.KVPool(B * nblk, 16, hkv, 128, "bf16")
+        ppool = pk.KVPool(B * nblk, 16, hkv, 128, dt)
+        if dt == "fp8":   # randn keys and values: |x| < 4.5 for these sizes
+            sc = torch.full((hkv,), 4.5 / 448, device=device)
+            ppool.set_scales(sc, sc)
         tables = torch.from_numpy(np.random.default_rng(3).permutation(B * nblk).astype(np.int32)
                                   .reshape(B, nblk)).to(device)
         g = torch.Generator(device=device).manual_seed(5)
@@ -571,12 +580,17 @@ def measure_extras(step: Step, peaks: dict, device) -> dict:
             out=pout), 20)
         flops = 4.0 * 128 * hq * B * (ctx * (ctx + 1) // 2)   # QK and PV over the causal keys
         tf = flops / t / 1e12
+        peak = bf16_peak * (2.0 if dt == "fp8" else 1.0)
+        issued = 2.0 if dt == "fp8" else 1.5
         out[key] = {
             "workload": f"full causal prefill, {B} x {ctx} tokens, {hq} q / {hkv} KV heads, "
-                        "head_dim 128, 16-token blocks",
+                        f"head_dim 128, 16-token blocks, {dt} pool",
+            "dtype": dt,
             "us_per_call": t * 1e6, "achieved": tf, "unit": "TFLOP/s", "bound": "tensor",
-            "peak": bf16_peak, "frac": tf / bf16_peak, "flops_per_call": flops,
-            "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"}
+            "peak": peak, "frac": tf / peak, "flops_per_call": flops,
+            "issued_tensor_flops_per_call": issued * flops, "issued_frac": issued * tf / peak,
+            "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst"
+                           + (", x 2 for E4M3 operands)" if dt == "fp8" else ")")}
         if ppool.check_status() != pk.KV_OK or step.pool.check_status() != pk.KV_OK:
             raise RuntimeError("device error in the extra measurements")
         ppool.destroy()

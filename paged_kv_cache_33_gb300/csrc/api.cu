@@ -66,13 +66,15 @@ bool encode_pool_map(kv_pool* p) {
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
-  if (p->dtype == KV_BF16) {
-    // the prefill gathers the K rows and the V rows of a block separately
-    cuuint32_t box_rows[4] = {64, static_cast<cuuint32_t>(p->block_size), 1, 1};
-    r = encode(&p->tmap_rows, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p->base, dims, strides, box_rows,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  }
+  // the prefill gathers the K rows and the V rows of a block separately: one
+  // box is the 128 bytes of every row of one tile (bf16: half a row)
+  cuuint32_t box_rows[4] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(p->block_size),
+                            1, 1};
+  r = encode(&p->tmap_rows,
+             p->dtype == KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+             p->base, dims, strides, box_rows, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -419,7 +421,7 @@ kv_status paged_prefill_attention(kv_pool* p, const void* q, int32_t n_q_heads,
     return KV_ERR_INVALID_ARG;
   if (n_q_heads % p->n_kv_heads != 0) return KV_ERR_INVALID_ARG;
   const int32_t g = n_q_heads / p->n_kv_heads;
-  if (g > 8 || p->dtype != KV_BF16 || p->head_dim != 128) return KV_ERR_UNSUPPORTED;
+  if (g > 8 || p->dtype == KV_FP4_E2M1 || p->head_dim != 128) return KV_ERR_UNSUPPORTED;
   if (batch == 0 || max_q_len == 0) return KV_OK;
   if (!q || !cu_q_lens || !block_tables || !context_lens || !out || !aligned16(q) || !aligned16(out))
     return KV_ERR_INVALID_ARG;
@@ -440,6 +442,9 @@ kv_status paged_prefill_attention(kv_pool* p, const void* q, int32_t n_q_heads,
   d.context_lens = context_lens;
   d.out = out;
   d.err = p->err;
+  d.pool = static_cast<const uint8_t*>(p->base);
+  d.k_scale = p->scales;
+  d.v_scale = p->scales + p->n_kv_heads;
   d.num_blocks = p->num_blocks;
   d.mbs = max_blocks_per_seq;
   d.batch = batch;
@@ -449,9 +454,15 @@ kv_status paged_prefill_attention(kv_pool* p, const void* q, int32_t n_q_heads,
   d.group_pow2 = gp;
   d.max_ctx = max_context_len;
   d.window = sliding_window > 0 ? sliding_window : 0;
-  d.scale_log2 = scale * 1.4426950408889634f;
+  // The kernels take the row maximum of the unscaled scores and mask with
+  // -inf, so they need a positive scale: a negative one negates q instead,
+  // and zero (equal weights) becomes a scale too small to change any weight.
+  d.q_sign = scale < 0.f ? 0x80008000u : 0u;
+  d.scale_log2 = std::max(std::fabs(scale) * 1.4426950408889634f, 1e-30f);
   d.wait_limit_ns = p->wait_limit_ns;
-  const cudaError_t e = pkv::launch_prefill(p, d, max_q_len, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = p->dtype == KV_FP8_E4M3
+                            ? pkv::launch_prefill_fp8(p, d, max_q_len, static_cast<cudaStream_t>(stream))
+                            : pkv::launch_prefill(p, d, max_q_len, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return KV_ERR_CUDA;

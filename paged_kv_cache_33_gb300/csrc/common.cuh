@@ -201,6 +201,48 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n, bool b_mn) 
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B, fp32 accumulate,
+// M x N, A K-major, B K-major (b_mn = false) or MN-major (b_mn = true).
+__host__ __device__ constexpr uint32_t umma_idesc_e4m3(int m, int n, bool b_mn) {
+  return (1u << 4) | ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor without swizzle: core matrices of 8 rows
+// x 16 bytes, each 128 contiguous bytes.  K-major operands: lbo = the byte
+// distance between core matrices adjacent in K, sbo = between core matrices
+// adjacent in M / N.
+__device__ __forceinline__ uint64_t umma_desc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// D[tmem] (+)= A[smem] * B[smem] (kind::f8f6f4), issued by one thread, the
+// shared-memory descriptors given as 32-bit halves.
+__device__ __forceinline__ void umma_e4m3_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                            uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "mov.b64 ad, {%1, %2};\n\tmov.b64 bd, {%3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem] (kind::f8f6f4): A four 8-bit elements per
+// 32-bit column.
+__device__ __forceinline__ void umma_e4m3_ta_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                               uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem] (kind::f16, bf16 operands), issued by one
 // thread, with the shared-memory descriptors given as 32-bit halves (the
 // start address lives in the low half, so a stage or k-step offset is one

@@ -18,7 +18,7 @@ struct kv_pool {
   float* scales = nullptr;     // device [2][Hkv]: K scales then V scales
   uint32_t* err = nullptr;     // device error word
   CUtensorMap tmap;            // pool viewed as [NB*Hkv][2][BS][D] for TMA
-  CUtensorMap tmap_rows;       // bf16 pools: the same view, boxes of one tile (K or V)
+  CUtensorMap tmap_rows;       // bf16 / FP8 pools: the same view, boxes of one tile (K or V)
   int32_t partition_blocks = 0;  // 0 = automatic
   uint64_t wait_limit_ns = 1000000000ull;  // bound of every wait in the kernels
   uint32_t stall_tx = 0;       // test hook (kv_pool_set_test_stall)
@@ -117,10 +117,15 @@ struct PrefillParams {
   const int32_t* context_lens;  // [B]
   float* out;                   // [T][Hq][D]
   uint32_t* err;
+  const uint8_t* pool;          // FP8: pool base (the V sub-tiles are staged with bulk copies)
+  const float* k_scale;         // FP8: [Hkv]
+  const float* v_scale;
   int64_t num_blocks;
   int32_t mbs, batch, n_q_heads, n_kv_heads, group, group_pow2;
   int32_t max_ctx, window;
-  float scale_log2;
+  uint32_t q_sign;              // xor into every word of q: 0x80008000 negates it (the
+                                // kernels work with |scale|)
+  float scale_log2;             // |softmax scale| * log2(e), at least 1e-30
   uint64_t wait_limit_ns;
 };
 
@@ -128,6 +133,9 @@ struct PrefillParams {
 int prefill_smem_bytes();
 cudaError_t launch_prefill(const kv_pool* pool, const PrefillParams& p, int32_t max_q_len,
                            cudaStream_t stream);
+// The same over an FP8 (E4M3) pool, with E4M3 tensor-core products.
+cudaError_t launch_prefill_fp8(const kv_pool* pool, const PrefillParams& p, int32_t max_q_len,
+                               cudaStream_t stream);
 
 // The merge of cut pairs, launched as a programmatic dependent of the decode.
 cudaError_t launch_reduce(const kv_pool* pool, const DecodeParams& p, cudaStream_t stream);

@@ -203,9 +203,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         const int tt = row / kRows, rr = row % kRows;
         const int tq2 = rr >> log2_gp, jh2 = rr & (Gp - 1);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (tq2 < (tt ? ntok1 : ntok0) && jh2 < g)
+        if (tq2 < (tt ? ntok1 : ntok0) && jh2 < g) {
           v = qg[(static_cast<int64_t>(q0 + tok0 + tt * tpt + tq2) * p.n_q_heads + h * g + jh2) *
                      kChunks + ch];
+          v = make_uint4(v.x ^ p.q_sign, v.y ^ p.q_sign, v.z ^ p.q_sign, v.w ^ p.q_sign);
+        }
         *reinterpret_cast<uint4*>(smem + kQ + tt * kQTile + (ch >> 3) * (kRows * 128) +
                                   swz128(rr, ch & 7)) = v;
       }

@@ -1,0 +1,592 @@
+// Paged prefill / extend attention over an FP8 (E4M3) pool, on the
+// 5th-generation tensor cores with E4M3 operands.
+//
+// What it computes is the bf16 prefill's ("Optimizing KV Cache Memory
+// Management in vLLM with PagedAttention and Dynamic Block Allocation", "The
+// Prefill Phase"; prefix caching from "PagedAttention", "Walking through two
+// requests"), every key and value being its E4M3 code times the KV head's
+// scale: new token i of sequence b sits at position pos = ctx - q_len + i and
+// attends causally to [lo, pos], lo = max(0, pos + 1 - W) under a window W,
+// keys resolved through the block table; query head hq reads KV head hq / g.
+//
+// How.  The CTA geometry, warp roles, barriers and the alternation of two
+// 128-row query tiles over shared key tiles are those of the bf16 kernel;
+// the products run on kind::f8f6f4 (twice the bf16 rate, half the operand
+// bytes):
+//  * Q: every row is scaled by a power of two that puts its largest
+//    magnitude in [128, 256), then split into an E4M3 code and the E4M3 code
+//    of its remainder (about 8 significant bits); S = Q_hi K^T + Q_lo K^T
+//    over the K codes exactly as stored (one TMA box per block, 128-byte
+//    swizzle).  The row's power, k_scale and the softmax scale fold into the
+//    exponent's coefficient.
+//  * V: an FP8 pool stores each V tile transposed, as 16-token sub-tiles of
+//    [D][16] codes.  They are copied verbatim (one bulk copy per block) and
+//    read as the K-major B operand without swizzle: a sub-tile's 16-byte
+//    rows are the rows of its core matrices (8 dims each, 128 bytes apart),
+//    and consecutive sub-tiles, 2 KB apart, follow along the keys.
+//  * P: 128 p, with p <= 2 under a lazy maximum of threshold 2^1, as an E4M3
+//    high code and the E4M3 code of its remainder, packed four keys per
+//    tensor-memory column in the sub-tile's token order (column c of a
+//    sub-tile: tokens 2c, 2c+1, 2c+8, 2c+9), high codes over the first 32
+//    columns of S and remainders over the next 32.  O += P_hi V + P_lo V.
+//    The row sum l adds the unrounded 128 p; out = O v_scale / l.
+//  * Keys a product must not see in V (past the sequence's end, blocks not
+//    loaded) have their codes zeroed in the stage before P is handed over.
+//  * Every wait is bounded in wall time; on a timeout the CTA records
+//    KV_ERR_TIMEOUT, drains what it issued and frees its tensor memory.
+
+#include <math.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kRows = 128;           // query rows per tile (M)
+constexpr int kTiles = 2;            // query tiles per CTA, alternating over the same keys
+constexpr int kKv = 128;             // keys per key tile (N of S, K of P V)
+constexpr int kSub = 16;             // tokens per transposed V sub-tile
+constexpr int kKStages = 4;          // K ring
+constexpr int kVStages = 5;          // V ring
+constexpr int kSoftmax = kTiles * kRows;
+constexpr int kThreads = kSoftmax + 96;       // + K producer, V producer, MMA warps
+constexpr int kKWarp = kSoftmax / 32, kVWarp = kKWarp + 1, kMmaWarp = kVWarp + 1;
+constexpr float kLazy = 1.f;         // rescale O when a row maximum grows by more than this (log2)
+constexpr float kPLog2 = 7.f;        // P is handed over as 2^7 p (<= 256 < 448)
+constexpr uint64_t kShortWaitNs = 200000;
+
+// Shared memory (offsets from a 1024-aligned base).  The V ring sits below
+// the K ring, so every byte the V descriptor can address stays inside the
+// allocation.
+constexpr int kQPart = kRows * 128;                   // [128 rows][128 codes], 128-byte swizzle
+constexpr int kQTile = 2 * kQPart;                    // high codes, then remainder codes
+constexpr int kStage = kKv * 128;                     // 128 keys x 128 codes
+constexpr int kQ = 0;
+constexpr int kV = kQ + kTiles * kQTile;
+constexpr int kK = kV + kVStages * kStage;
+constexpr int kRs = kK + kKStages * kStage;           // float [kTiles][kRows]: 2^-(row power)
+constexpr int kBars = kRs + kTiles * kRows * 4;
+constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 4 * kTiles + 2;
+constexpr int kTmemSlot = kBars + kNumBars * 8;
+constexpr int kSmemBytes = kTmemSlot + 16 + 1024;     // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
+static_assert(kTiles * kRows * 256 <= kTiles * kQTile, "output staging fits in the Q buffers");
+// tensor memory per query tile: S [0,128) (P high codes over columns [0,32),
+// remainders over [32,64)), O [128,256)
+constexpr uint32_t kOCol = kKv;
+constexpr uint32_t kTmemTile = 256;
+constexpr uint32_t kTmemCols = kTiles * kTmemTile;
+
+__device__ __forceinline__ int swz128(int row, int chunk) {
+  return row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+// Byte mask of the first `nv` tokens of a transposed V sub-tile row (token t
+// at byte 4 ((t mod 8) / 2) + t mod 2 + 2 (t / 8)).
+__device__ __forceinline__ uint4 sub_tile_mask(int nv) {
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int t = 0; t < kSub; ++t)
+    if (t < nv) w[(t & 7) >> 1] |= 0xFFu << (8 * ((t & 1) + 2 * (t >> 3)));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <int BS>
+__global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
+    const __grid_constant__ CUtensorMap tmap, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // CTA order as in the bf16 kernel: (sequence, KV head) pairs sixteen at a
+  // time, the query tiles with the most keys first inside a group.
+  constexpr int kGroupPairs = 16;
+  const int pairs = p.n_kv_heads * p.batch;
+  const int nx = static_cast<int>(gridDim.x) / pairs;
+  const int grp = static_cast<int>(blockIdx.x) / (kGroupPairs * nx);
+  const int rb = static_cast<int>(blockIdx.x) - grp * kGroupPairs * nx;
+  const int kc = min(kGroupPairs, pairs - grp * kGroupPairs);
+  const int qx = nx - 1 - rb / kc;
+  const int hb = grp * kGroupPairs + rb % kc;
+  const int b = hb / p.n_kv_heads, h = hb - b * p.n_kv_heads;
+  const int Gp = p.group_pow2, g = p.group;
+  const int log2_gp = __ffs(Gp) - 1;
+  const int tpt = kRows / Gp;  // query tokens per tile
+
+  const int32_t q0 = p.cu_q_lens[b];
+  const int32_t qn = p.cu_q_lens[b + 1] - q0;
+  const int32_t ctx = p.context_lens[b];
+  if (qn < 0 || qn > ctx || ctx > p.max_ctx || static_cast<int64_t>(ctx) > static_cast<int64_t>(p.mbs) * BS) {
+    if (qn != 0 && qx == 0 && h == 0 && tid == 0) atomicOr(p.err, kErrBadContext);
+    return;
+  }
+  const int tok0 = qx * (kTiles * tpt);
+  if (tok0 >= qn) return;
+  const int pos_base = ctx - qn;
+  const int kv_begin = p.window > 0 ? max(0, pos_base + tok0 + 1 - p.window) : 0;
+  const int jt0 = kv_begin / kKv;
+  const int ntok0 = min(tpt, qn - tok0), ntok1 = max(0, min(tpt, qn - tok0 - tpt));
+  const int last0 = pos_base + tok0 + ntok0 - 1;
+  const int last1 = pos_base + tok0 + tpt + ntok1 - 1;
+  const int n_kv0 = last0 / kKv - jt0 + 1;
+  const int n_kv1 = ntok1 > 0 ? last1 / kKv - jt0 + 1 : 0;
+  const int kv_end = (ntok1 > 0 ? last1 : last0) + 1;
+  const int n_tiles = max(n_kv0, n_kv1);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBars);
+  const uint32_t bar0 = smem_addr(bars);
+  auto k_full = [&](int s) { return bar0 + 8u * s; };
+  auto k_empty = [&](int s) { return bar0 + 8u * (kKStages + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (2 * kKStages + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (2 * kKStages + kVStages + s); };
+  constexpr int kTileBars = 2 * kKStages + 2 * kVStages;
+  auto s_full = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t); };
+  auto p_full = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t + 1); };
+  auto pv_done = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t + 2); };
+  auto o_final = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t + 3); };
+  const uint32_t q_full = bar0 + 8u * (kTileBars + 4 * kTiles);
+  const uint32_t mma_done = q_full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
+  float* row_rs = reinterpret_cast<float*>(smem + kRs);
+
+  if (tid == 0) {
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
+    }
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(s_full(t), 1);
+      mbar_init(p_full(t), kRows);
+      mbar_init(pv_done(t), 1);
+      mbar_init(o_final(t), 1);
+    }
+    mbar_init(q_full, kSoftmax);
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    return mbar_wait_bounded(bar, parity, p.wait_limit_ns, p.err, kErrTimeout, kShortWaitNs);
+  };
+
+  if (warp < kKWarp) {
+    // ====== softmax warps: warps 4t..4t+3 serve query tile t, one row per thread
+    const int t = warp >> 2;
+    const int r = tid & (kRows - 1);
+    const int tq = r / Gp, jh = r - tq * Gp;
+    const bool row_ok = tq < (t ? ntok1 : ntok0) && jh < g;
+    const int tok = tok0 + t * tpt + tq;
+    const int pos = pos_base + tok;
+    const int lo = p.window > 0 ? max(0, pos + 1 - p.window) : 0;
+    // Q of both tiles -> E4M3 high and remainder codes in shared memory, 16
+    // threads per row (one 16-byte chunk of bf16 each), the row's power of
+    // two from a maximum over those 16 lanes
+    {
+      const uint4* qg = static_cast<const uint4*>(p.q);
+      constexpr int kChunks = kD / 8;
+#pragma unroll 2
+      for (int it = 0; it < kTiles * kRows * kChunks / kSoftmax; ++it) {
+        const int idx = it * kSoftmax + tid;
+        const int row = idx / kChunks, ch = idx % kChunks;
+        const int tt = row / kRows, rr = row % kRows;
+        const int tq2 = rr >> log2_gp, jh2 = rr & (Gp - 1);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (tq2 < (tt ? ntok1 : ntok0) && jh2 < g)
+          v = qg[(static_cast<int64_t>(q0 + tok0 + tt * tpt + tq2) * p.n_q_heads + h * g + jh2) *
+                     kChunks + ch];
+        const uint32_t w[4] = {v.x ^ p.q_sign, v.y ^ p.q_sign, v.z ^ p.q_sign, v.w ^ p.q_sign};
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+#pragma unroll
+        for (int o = 1; o < kChunks; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        // amax in [2^e, 2^(e+1)); the row is scaled by 2^(7 - e)
+        int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127;
+        e = amax > 0.f ? max(-100, min(100, e)) : 0;
+        const float qs = __uint_as_float(static_cast<uint32_t>(127 + 7 - e) << 23);
+        uint32_t hv[4], rv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) hv[i] = pack_f16x2(bf16_lo(w[i]) * qs, bf16_hi(w[i]) * qs);
+        const uint32_t c0 = f16x2x2_to_e4m3x4(hv[0], hv[1]), c1 = f16x2x2_to_e4m3x4(hv[2], hv[3]);
+        e4m3x4_to_f16x2(c0, rv[0], rv[1]);
+        e4m3x4_to_f16x2(c1, rv[2], rv[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rv[i] = hsub2_bits(hv[i], rv[i]);
+        const uint32_t d0 = f16x2x2_to_e4m3x4(rv[0], rv[1]), d1 = f16x2x2_to_e4m3x4(rv[2], rv[3]);
+        const int off = tt * kQTile + swz128(rr, ch >> 1) + (ch & 1) * 8;
+        *reinterpret_cast<uint2*>(smem + kQ + off) = make_uint2(c0, c1);
+        *reinterpret_cast<uint2*>(smem + kQ + kQPart + off) = make_uint2(d0, d1);
+        if (ch == 0) row_rs[tt * kRows + rr] = __uint_as_float(static_cast<uint32_t>(127 - 7 + e) << 23);
+      }
+      fence_proxy_async_smem();
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(q_full) : "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(kSoftmax) : "memory");  // the row powers
+    }
+    const uint32_t lane_base = tmem + t * kTmemTile + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    // coefficient of the exponent: softmax scale (log2) x k_scale x the row's power
+    const float coef = p.scale_log2 * p.k_scale[h] * row_rs[t * kRows + r];
+    constexpr uint32_t kAllBlocks = (1u << (kKv / BS)) - 1u;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    const int nt = t ? n_kv1 : n_kv0;
+    const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.mbs;
+    auto needed = [&](int jt, int i) {
+      const int k0 = (jt0 + jt) * kKv + i * BS;
+      return k0 + BS > kv_begin && k0 < kv_end;
+    };
+    int next[kKv / BS];
+    auto fetch = [&](int jt) {
+#pragma unroll
+      for (int i = 0; i < kKv / BS; ++i)
+        next[i] = needed(jt, i) ? trow[((jt0 + jt) * kKv + i * BS) / BS] : -1;
+    };
+    if (nt > 0) fetch(0);
+    for (int jt = 0; jt < nt && ok; ++jt) {
+      uint32_t mask = 0;
+#pragma unroll
+      for (int i = 0; i < kKv / BS; ++i)
+        if (next[i] >= 0 && next[i] < p.num_blocks) mask |= 1u << i;
+      if (jt + 1 < nt) fetch(jt + 1);
+      const int sv = jt % kVStages;
+      ok = wait(s_full(t), jt & 1);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      const int key0 = (jt0 + jt) * kKv;
+      uint32_t x[kKv];
+      tmem_ld128(lane_base, x);
+      if (!__all_sync(0xffffffffu, row_ok && key0 >= lo && key0 + kKv - 1 <= pos &&
+                                       mask == kAllBlocks)) {
+#pragma unroll
+        for (int c = 0; c < kKv; ++c) {
+          const int key = key0 + c;
+          const bool valid = row_ok && key >= lo && key <= pos && ((mask >> (c / BS)) & 1u);
+          if (!valid) x[c] = __float_as_uint(-INFINITY);
+        }
+      }
+      float mt4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < kKv; ++c) mt4[c & 3] = fmaxf(mt4[c & 3], __uint_as_float(x[c]));
+      const float mt_raw = fmaxf(fmaxf(mt4[0], mt4[1]), fmaxf(mt4[2], mt4[3]));
+      const float mt = mt_raw == -INFINITY ? -INFINITY : mt_raw * coef;
+      const float m_new = fmaxf(m_run, mt);
+      const bool rescale = m_run != -INFINITY && m_new > m_run + kLazy;
+      const float m_old = m_run;
+      if (m_run == -INFINITY || rescale) m_run = m_new;
+      const float mu = m_run == -INFINITY ? 0.f : m_run;
+      const float2 sc2 = make_float2(coef, coef), nmu2 = make_float2(kPLog2 - mu, kPLog2 - mu);
+      // 2^7 p for the sixteen keys of each sub-tile, as four columns of four
+      // E4M3 codes (tokens 2c, 2c+1, 2c+8, 2c+9) and the codes of their
+      // remainders; each half of the key tile is stored as soon as it is done.
+      // In exact arithmetic the exponent is at most kLazy + 7 (2^8 = 256);
+      // fp32 holds it to within ulp(mu), so rows whose maximum reaches 2^21
+      // (scores beyond any real model's) clamp it there, keeping l and P alike.
+      float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      auto emit = [&](auto clamp) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t wh[16], wl[16];
+#pragma unroll
+          for (int sl = 0; sl < 4; ++sl) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int k0 = 64 * hf + kSub * sl + 2 * c;
+              float2 a0 = ffma2(make_float2(__uint_as_float(x[k0]), __uint_as_float(x[k0 + 1])), sc2, nmu2);
+              float2 a1 = ffma2(make_float2(__uint_as_float(x[k0 + 8]), __uint_as_float(x[k0 + 9])), sc2, nmu2);
+              if (decltype(clamp)::value) {
+                constexpr float kTop = kLazy + kPLog2;
+                a0 = make_float2(fminf(a0.x, kTop), fminf(a0.y, kTop));
+                a1 = make_float2(fminf(a1.x, kTop), fminf(a1.y, kTop));
+              }
+              const float2 p0 = make_float2(fast_exp2(a0.x), fast_exp2(a0.y));
+              const float2 p1 = make_float2(fast_exp2(a1.x), fast_exp2(a1.y));
+              l2[0] = fadd2(l2[0], p0);
+              l2[1] = fadd2(l2[1], p1);
+              const uint32_t h0 = pack_f16x2(p0.x, p0.y), h1 = pack_f16x2(p1.x, p1.y);
+              const uint32_t cw = f16x2x2_to_e4m3x4(h0, h1);
+              uint32_t b0, b1;
+              e4m3x4_to_f16x2(cw, b0, b1);
+              wh[4 * sl + c] = cw;
+              wl[4 * sl + c] = f16x2x2_to_e4m3x4(hsub2_bits(h0, b0), hsub2_bits(h1, b1));
+            }
+          }
+          tmem_st16_nowait(lane_base + 16 * hf, wh);
+          tmem_st16_nowait(lane_base + 32 + 16 * hf, wl);
+        }
+      };
+      if (__any_sync(0xffffffffu, fabsf(mu) >= 0x1p21f))
+        emit(std::true_type{});
+      else
+        emit(std::false_type{});
+      tmem_wait_st();
+      if (__any_sync(0xffffffffu, rescale)) {
+        const float alpha = rescale ? fast_exp2(m_old - m_new) : 1.f;
+        l_run *= alpha;
+#pragma unroll
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + kOCol + c0, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(lane_base + kOCol + c0, o);
+        }
+      }
+      l_run += (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
+      // V codes the products must not see: tokens past the sequence's end and
+      // blocks that were not loaded.  Thread r clears dim row r of each
+      // sub-tile that needs it (the same sub-tiles for the whole warp).
+      const int zero_tile = jt < n_kv0 ? 0 : 1;
+      if (t == zero_tile && (mask != kAllBlocks || key0 + kKv > ctx)) {
+        ok = wait(v_full(sv), (jt / kVStages) & 1);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        uint8_t* vst = smem + kV + sv * kStage;
+#pragma unroll 1
+        for (int st = 0; st < kKv / kSub; ++st) {
+          const int kb = key0 + kSub * st;
+          const int nv = ((mask >> ((kSub * st) / BS)) & 1u) ? min(kSub, max(0, ctx - kb)) : 0;
+          if (nv < kSub) {
+            uint4* rowp = reinterpret_cast<uint4*>(vst + st * (kD * kSub) + r * kSub);
+            const uint4 m = sub_tile_mask(nv);
+            const uint4 cur = *rowp;
+            *rowp = make_uint4(cur.x & m.x, cur.y & m.y, cur.z & m.z, cur.w & m.w);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(p_full(t)) : "memory");
+    }
+    if (ok && nt > 0) ok = __all_sync(0xffffffffu, wait(o_final(t), 0));
+    if (ok && nt > 0) {
+      tc_fence_after();
+      const float inv = l_run > 0.f ? p.v_scale[h] / l_run : 0.f;
+      // O v_scale / l -> out through a per-warp staging area in the tile's Q
+      // buffer (free once the tile's last product is done), whole rows per store
+      uint8_t* stg = smem + kQ + t * kQTile + (warp & 3) * (32 * 256);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + kOCol + hh * 64 + c0, o);
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const int ch = (c0 + i) >> 2;
+            *reinterpret_cast<float4*>(stg + lane * 256 + ((ch ^ (lane & 15)) << 4)) =
+                make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
+                            __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+          }
+        }
+        __syncwarp();
+#pragma unroll 4
+        for (int rr = 0; rr < 32; rr += 2) {
+          const int row = rr + (lane >> 4), ch = lane & 15;
+          const int r_t = 32 * (warp & 3) + row;
+          const int tq2 = r_t >> log2_gp, jh2 = r_t & (Gp - 1);
+          if (tq2 < (t ? ntok1 : ntok0) && jh2 < g) {
+            const float4 v = *reinterpret_cast<const float4*>(stg + row * 256 + ((ch ^ (row & 15)) << 4));
+            *reinterpret_cast<float4*>(
+                p.out + (static_cast<int64_t>(q0 + tok0 + t * tpt + tq2) * p.n_q_heads + h * g + jh2) * kD +
+                hh * 64 + ch * 4) = v;
+          }
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp == kKWarp || warp == kVWarp) {
+    // =========================== producers: K rows by TMA (swizzled boxes),
+    // the transposed V sub-tiles of each block by one bulk copy
+    if (lane == 0) {
+      const bool is_v = warp == kVWarp;
+      const int stages = is_v ? kVStages : kKStages;
+      uint8_t* ring = smem + (is_v ? kV : kK);
+      auto full = [&](int s) { return is_v ? v_full(s) : k_full(s); };
+      auto empty = [&](int s) { return is_v ? v_empty(s) : k_empty(s); };
+      const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.mbs;
+      auto needed = [&](int jt, int i) {
+        const int k0 = (jt0 + jt) * kKv + i * BS;
+        return k0 + BS > kv_begin && k0 < kv_end;
+      };
+      int next[kKv / BS];
+      auto fetch = [&](int jt) {
+#pragma unroll
+        for (int i = 0; i < kKv / BS; ++i)
+          next[i] = needed(jt, i) ? trow[((jt0 + jt) * kKv + i * BS) / BS] : 0;
+      };
+      if (n_tiles > 0) fetch(0);
+      int issued = 0;
+      for (int jt = 0; jt < n_tiles; ++jt) {
+        const int s = jt % stages;
+        int cur[kKv / BS];
+#pragma unroll
+        for (int i = 0; i < kKv / BS; ++i) cur[i] = next[i];
+        if (jt + 1 < n_tiles) fetch(jt + 1);
+        if (jt >= stages && !wait(empty(s), ((jt / stages) - 1) & 1)) break;
+        uint32_t mask = 0;
+        int phys[kKv / BS];
+#pragma unroll
+        for (int i = 0; i < kKv / BS; ++i) {
+          phys[i] = -1;
+          if (!needed(jt, i)) continue;
+          const int e = cur[i];
+          if (e < 0 || e >= p.num_blocks) {
+            if (!is_v) atomicOr(p.err, kErrBadBlock);
+            continue;
+          }
+          phys[i] = e;
+          mask |= 1u << i;
+        }
+        const uint32_t bar = full(s);
+        const int nblk = __popc(mask);
+        if (nblk == 0) {
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+        } else {
+          mbar_arrive_expect_tx(bar, nblk * BS * 128);
+          const uint32_t st = smem_addr(ring + s * kStage);
+#pragma unroll
+          for (int i = 0; i < kKv / BS; ++i) {
+            if (phys[i] < 0) continue;
+            const int64_t tile = static_cast<int64_t>(phys[i]) * p.n_kv_heads + h;
+            if (is_v)
+              bulk_load(st + i * BS * 128, p.pool + (2 * tile + 1) * (BS * 128), BS * 128, bar);
+            else
+              tma_load_4d(st + i * BS * 128, &tmap, bar, 0, 0, 0, static_cast<int>(tile));
+          }
+        }
+        ++issued;
+      }
+      for (int jt = max(0, issued - stages); jt < issued; ++jt)
+        if (!wait(full(jt % stages), (jt / stages) & 1)) atomicOr(p.err, kErrDrainTimeout);
+    }
+    __syncwarp();
+  } else {
+    // =========================== MMA issuer, in the bf16 kernel's order: per
+    // key tile and query tile, P V of the previous key tile, then S
+    if (lane == 0) {
+      constexpr uint32_t idS = umma_idesc_e4m3(kRows, kKv, false);
+      constexpr uint32_t idO = umma_idesc_e4m3(kRows, kD, false);
+      const uint64_t q_desc = umma_desc_sw128(smem_addr(smem + kQ), 16, 1024);
+      const uint64_t k_desc = umma_desc_sw128(smem_addr(smem + kK), 16, 1024);
+      // V: core matrices 8 dims x 16 tokens; 128 bytes to the next 8 dims,
+      // one sub-tile (2 KB) to the next 16 tokens
+      const uint64_t v_desc = umma_desc_noswz(smem_addr(smem + kV), kD * kSub, 128);
+      const uint32_t q_lo = static_cast<uint32_t>(q_desc), q_hi = static_cast<uint32_t>(q_desc >> 32);
+      const uint32_t k_lo = static_cast<uint32_t>(k_desc), k_hi = static_cast<uint32_t>(k_desc >> 32);
+      const uint32_t v_lo = static_cast<uint32_t>(v_desc), v_hi = static_cast<uint32_t>(v_desc >> 32);
+      constexpr uint32_t kStageUnits = kStage >> 4;
+      bool ok = wait(q_full, 0);
+      if (ok) tc_fence_after();
+      auto issue_s = [&](int t, int jt) {
+        const uint32_t ka = k_lo + (jt % kKStages) * kStageUnits;
+        const uint32_t qa = q_lo + t * (kQTile >> 4);
+        const uint32_t d = tmem + t * kTmemTile;
+        // S = Q_hi K^T + Q_lo K^T, 32 dims per product
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int k = 0; k < kD / 32; ++k)
+            umma_e4m3_w(d, qa + ((part * kQPart + k * 32) >> 4), q_hi, ka + ((k * 32) >> 4), k_hi, idS,
+                        (part > 0 || k > 0) ? 1u : 0u);
+        umma_commit(s_full(t));
+      };
+      auto issue_pv = [&](int t, int jt) {
+        const uint32_t va = v_lo + (jt % kVStages) * kStageUnits;
+        const uint32_t pt = tmem + t * kTmemTile;
+        const uint32_t d = pt + kOCol;
+        // O += P_hi V + P_lo V, 32 keys (two sub-tiles, eight columns of P) per product
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int k = 0; k < kKv / 32; ++k)
+            umma_e4m3_ta_w(d, pt + part * 32 + k * 8, va + ((k * 2 * kD * kSub) >> 4), v_hi, idO,
+                           (jt > 0 || part > 0 || k > 0) ? 1u : 0u);
+      };
+      for (int jt = 0; ok && jt <= n_tiles; ++jt) {
+        bool v_ready = false, k_ready = false;
+        for (int t = 0; t < kTiles && ok; ++t) {
+          const int nt = t ? n_kv1 : n_kv0;
+          if (jt > 0 && jt - 1 < nt) {
+            if (!v_ready) {
+              ok = wait(v_full((jt - 1) % kVStages), ((jt - 1) / kVStages) & 1);
+              if (!ok) break;
+              v_ready = true;
+            }
+            ok = wait(p_full(t), (jt - 1) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, jt - 1);
+            umma_commit(jt == nt ? o_final(t) : pv_done(t));
+          }
+          if (jt < nt) {
+            // S of this key tile overwrites the P the previous product reads
+            // (products with different accumulators are not ordered)
+            if (jt > 0) {
+              ok = wait(pv_done(t), (jt - 1) & 1);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            if (!k_ready) {
+              ok = wait(k_full(jt % kKStages), (jt / kKStages) & 1);
+              if (!ok) break;
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_s(t, jt);
+          }
+        }
+        if (!ok) break;
+        if (k_ready) umma_commit(k_empty(jt % kKStages));
+        if (v_ready) umma_commit(v_empty((jt - 1) % kVStages));
+      }
+      umma_commit(mma_done);
+      if (!wait(mma_done, 0)) atomicOr(p.err, kErrDrainTimeout);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int BS>
+int smem_opt_in() {
+  static int done = -1;
+  if (done < 0)
+    done = cudaFuncSetAttribute(paged_prefill_fp8_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemBytes) == cudaSuccess ? 1 : 0;
+  return done;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_fp8(const kv_pool* pool, const PrefillParams& p, int32_t max_q_len,
+                               cudaStream_t stream) {
+  const int tok_per_cta = kTiles * (kRows / p.group_pow2);
+  const int64_t ntiles = (max_q_len + tok_per_cta - 1) / tok_per_cta;
+  const int64_t ctas = ntiles * p.n_kv_heads * p.batch;
+  if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(ctas));
+  if (pool->block_size == 32) {
+    if (!smem_opt_in<32>()) return cudaErrorInvalidValue;
+    paged_prefill_fp8_kernel<32><<<grid, kThreads, kSmemBytes, stream>>>(pool->tmap_rows, p);
+  } else {
+    if (!smem_opt_in<16>()) return cudaErrorInvalidValue;
+    paged_prefill_fp8_kernel<16><<<grid, kThreads, kSmemBytes, stream>>>(pool->tmap_rows, p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -160,11 +160,11 @@ def test_prefill_host_checks():
     c = torch.tensor([4], dtype=torch.int32, device="cuda")
     with pytest.raises(pagedkv.KVError):
         pagedkv.paged_prefill_attention(pool, q, cu, t, c, 0.1, max_q_len=4, max_context_len=64)
-    fp8 = pagedkv.KVPool(8, 16, 2, 128, "fp8")
+    fp4 = pagedkv.KVPool(8, 16, 2, 128, "fp4")              # FP4 pools have no prefill
     with pytest.raises(pagedkv.KVError):
-        pagedkv.paged_prefill_attention(fp8, q, cu, t, c, 0.1, max_q_len=4, max_context_len=4)
+        pagedkv.paged_prefill_attention(fp4, q, cu, t, c, 0.1, max_q_len=4, max_context_len=4)
     pool.destroy()
-    fp8.destroy()
+    fp4.destroy()
 
 
 @pytest.mark.parametrize("bs", [16, 32])
@@ -199,4 +199,17 @@ def test_prefill_rescales_on_every_key_tile(bs):
     assert pool.check_status() == pagedkv.KV_OK
     ref = opool.prefill(q, cu, tables, lens, 1.0)
     _check(out, ref, f"rescale bs={bs}")
+    pool.destroy()
+
+
+@pytest.mark.parametrize("scale", [-0.09, 0.0])
+def test_prefill_negative_and_zero_scale(scale):
+    """A negative softmax scale favours the keys least aligned with the
+    query; scale 0 weighs every attended key alike (masked keys still out)."""
+    pool, opool, q, cu, tables, lens = _build([77, 300], [20, 150], 8, 2, seed=17)
+    out = _run(pool, q, cu, tables, lens, scale, 100)
+    torch.cuda.synchronize()
+    assert pool.check_status() == pagedkv.KV_OK
+    ref = opool.prefill(q, cu, tables, lens, scale, 100)
+    _check(out, ref, f"scale={scale}")
     pool.destroy()
