@@ -304,12 +304,13 @@ kv_status paged_decode_attention_noalloc(kv_pool* pool, const void* q_dev, int32
  * per KV head (FP4 pools and other shapes: KV_ERR_UNSUPPORTED).  Runs on the
  * tcgen05 tensor cores.  bf16: P enters the P V product as a bf16 high part
  * plus the bf16 rounding of its remainder (two products into the same
- * accumulator), so the result meets the decode's bf16 accuracy.  FP8: the
- * products take E4M3 operands -- the K and V codes as stored, each query row
- * scaled by a power of two and split into an E4M3 code and the code of its
- * remainder, P (as 128 p) likewise -- with k_scale and v_scale applied in
- * fp32 (for scores of magnitude 2^21 or more, in log2 units, the weights are
- * only as exact as fp32 holds the row maximum).  A sequence with q_len > context_len or a context above a
+ * accumulator), so the result meets the decode's bf16 accuracy.  FP8: Q K^T
+ * takes E4M3 operands -- the K codes as stored, each query row scaled by a
+ * power of two and split into an E4M3 code and the code of its remainder --
+ * and P V f16 ones (P rounded once to f16, the V codes converted exactly),
+ * with k_scale and v_scale applied in fp32 (for scores of magnitude 2^21 or
+ * more, in log2 units, the weights are only as exact as fp32 holds the row
+ * maximum).  A sequence with q_len > context_len or a context above a
  * bound sets KV_ERR_BAD_CONTEXT and is skipped.  Asynchronous on `stream`;
  * no workspace.
  */

@@ -9,29 +9,26 @@
 // attends causally to [lo, pos], lo = max(0, pos + 1 - W) under a window W,
 // keys resolved through the block table; query head hq reads KV head hq / g.
 //
-// How.  The CTA geometry, warp roles, barriers and the alternation of two
-// 128-row query tiles over shared key tiles are those of the bf16 kernel;
-// the products run on kind::f8f6f4 (twice the bf16 rate, half the operand
-// bytes):
-//  * Q: every row is scaled by a power of two that puts its largest
-//    magnitude in [128, 256), then split into an E4M3 code and the E4M3 code
-//    of its remainder (about 8 significant bits); S = Q_hi K^T + Q_lo K^T
-//    over the K codes exactly as stored (one TMA box per block, 128-byte
-//    swizzle).  The row's power, k_scale and the softmax scale fold into the
+// How.  The CTA geometry, barriers and the alternation of two 128-row query
+// tiles over shared key tiles are those of the bf16 kernel.
+//  * S = Q K^T on kind::f8f6f4 (E4M3 operands, twice the bf16 rate): every
+//    query row is scaled by a power of two that puts its largest magnitude
+//    in [128, 256), then split into an E4M3 code and the E4M3 code of its
+//    remainder (about 8 significant bits); S = Q_hi K^T + Q_lo K^T over the
+//    K codes exactly as stored (one TMA box per block, 128-byte swizzle).
+//    The row's power, k_scale and the softmax scale fold into the
 //    exponent's coefficient.
-//  * V: an FP8 pool stores each V tile transposed, as 16-token sub-tiles of
-//    [D][16] codes.  They are copied verbatim (one bulk copy per block) and
-//    read as the K-major B operand without swizzle: a sub-tile's 16-byte
-//    rows are the rows of its core matrices (8 dims each, 128 bytes apart),
-//    and consecutive sub-tiles, 2 KB apart, follow along the keys.
-//  * P: 128 p, with p <= 2 under a lazy maximum of threshold 2^1, as an E4M3
-//    high code and the E4M3 code of its remainder, packed four keys per
-//    tensor-memory column in the sub-tile's token order (column c of a
-//    sub-tile: tokens 2c, 2c+1, 2c+8, 2c+9), high codes over the first 32
-//    columns of S and remainders over the next 32.  O += P_hi V + P_lo V.
-//    The row sum l adds the unrounded 128 p; out = O v_scale / l.
-//  * Keys a product must not see in V (past the sequence's end, blocks not
-//    loaded) have their codes zeroed in the stage before P is handed over.
+//  * P V on kind::f16: P is one f16 per weight (relative rounding 2^-11,
+//    finer than a bf16 high part plus remainder needs two products for), so
+//    V must be f16 too, which E4M3 codes convert to exactly.  A fourth
+//    warpgroup converts: the pool's transposed V sub-tiles ([D][16] codes
+//    per 16 tokens, one bulk copy per block) become f16 sub-tiles in natural
+//    token order, read as the K-major B operand without swizzle (core
+//    matrices of 8 dims x 8 tokens, 128 bytes apart along the dims, 2 KB
+//    along the keys), with tokens past the sequence's end and blocks not
+//    loaded written as zeros.  O += P V, out = O v_scale / l.
+//  * Registers: the two softmax warpgroups take 192 per thread, the
+//    producer / issuer and converter warpgroups give theirs up to 64.
 //  * Every wait is bounded in wall time; on a timeout the CTA records
 //    KV_ERR_TIMEOUT, drains what it issued and frees its tensor memory.
 
@@ -50,33 +47,42 @@ constexpr int kRows = 128;           // query rows per tile (M)
 constexpr int kTiles = 2;            // query tiles per CTA, alternating over the same keys
 constexpr int kKv = 128;             // keys per key tile (N of S, K of P V)
 constexpr int kSub = 16;             // tokens per transposed V sub-tile
-constexpr int kKStages = 4;          // K ring
-constexpr int kVStages = 5;          // V ring
+constexpr int kKStages = 4;          // K ring (E4M3 rows)
+constexpr int kV8Stages = 2;         // V ring as copied (E4M3 sub-tiles)
+constexpr int kV16Stages = 2;        // V ring converted (f16 sub-tiles)
 constexpr int kSoftmax = kTiles * kRows;
-constexpr int kThreads = kSoftmax + 96;       // + K producer, V producer, MMA warps
 constexpr int kKWarp = kSoftmax / 32, kVWarp = kKWarp + 1, kMmaWarp = kVWarp + 1;
-constexpr float kLazy = 1.f;         // rescale O when a row maximum grows by more than this (log2)
-constexpr float kPLog2 = 7.f;        // P is handed over as 2^7 p (<= 256 < 448)
+constexpr int kCvtWarp = kKWarp + 4;          // converter warpgroup (warp kKWarp + 3 is idle)
+constexpr int kCvt = 128;
+constexpr int kThreads = kSoftmax + 128 + kCvt;
+constexpr int kLaunchRegs = 65536 / kThreads;
+constexpr int kSoftmaxRegs = 192, kOtherRegs = 64;
+static_assert(2 * kSoftmaxRegs + 2 * kOtherRegs <= 4 * kLaunchRegs,
+              "register increases must be covered by the decreases");
+constexpr float kLazy = 8.f;         // rescale O when a row maximum grows by more than this (log2)
 constexpr uint64_t kShortWaitNs = 200000;
 
-// Shared memory (offsets from a 1024-aligned base).  The V ring sits below
-// the K ring, so every byte the V descriptor can address stays inside the
-// allocation.
+// Shared memory (offsets from a 1024-aligned base).  The f16 V ring sits
+// lowest after Q, so every byte its descriptor can address stays inside
+// the allocation.
 constexpr int kQPart = kRows * 128;                   // [128 rows][128 codes], 128-byte swizzle
 constexpr int kQTile = 2 * kQPart;                    // high codes, then remainder codes
-constexpr int kStage = kKv * 128;                     // 128 keys x 128 codes
+constexpr int kK8Stage = kKv * 128;                   // 128 keys x 128 codes
+constexpr int kV8Stage = kKv * 128;                   // 8 sub-tiles x [128 dims][16 codes]
+constexpr int kV16Stage = kKv * kD * 2;               // 8 sub-tiles x 2 x [128 dims][8 f16]
+constexpr int kV16Sub = kSub * kD * 2;                // 4 KB per 16 tokens
 constexpr int kQ = 0;
-constexpr int kV = kQ + kTiles * kQTile;
-constexpr int kK = kV + kVStages * kStage;
-constexpr int kRs = kK + kKStages * kStage;           // float [kTiles][kRows]: 2^-(row power)
+constexpr int kV16 = kQ + kTiles * kQTile;
+constexpr int kV8 = kV16 + kV16Stages * kV16Stage;
+constexpr int kK = kV8 + kV8Stages * kV8Stage;
+constexpr int kRs = kK + kKStages * kK8Stage;         // float [kTiles][kRows]: 2^-(row power)
 constexpr int kBars = kRs + kTiles * kRows * 4;
-constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 4 * kTiles + 2;
+constexpr int kNumBars = 2 * kKStages + 2 * kV8Stages + 2 * kV16Stages + 4 * kTiles + 2;
 constexpr int kTmemSlot = kBars + kNumBars * 8;
 constexpr int kSmemBytes = kTmemSlot + 16 + 1024;     // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
 static_assert(kTiles * kRows * 256 <= kTiles * kQTile, "output staging fits in the Q buffers");
-// tensor memory per query tile: S [0,128) (P high codes over columns [0,32),
-// remainders over [32,64)), O [128,256)
+// tensor memory per query tile: S [0,128) (P as f16 pairs over columns [0,64)), O [128,256)
 constexpr uint32_t kOCol = kKv;
 constexpr uint32_t kTmemTile = 256;
 constexpr uint32_t kTmemCols = kTiles * kTmemTile;
@@ -85,14 +91,9 @@ __device__ __forceinline__ int swz128(int row, int chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
-// Byte mask of the first `nv` tokens of a transposed V sub-tile row (token t
-// at byte 4 ((t mod 8) / 2) + t mod 2 + 2 (t / 8)).
-__device__ __forceinline__ uint4 sub_tile_mask(int nv) {
-  uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-  for (int t = 0; t < kSub; ++t)
-    if (t < nv) w[(t & 7) >> 1] |= 0xFFu << (8 * ((t & 1) + 2 * (t >> 3)));
-  return make_uint4(w[0], w[1], w[2], w[3]);
+// f16 pair word of tokens (2k, 2k+1) with the tokens from `nv` on zeroed.
+__device__ __forceinline__ uint32_t keep_tokens(uint32_t w, int k, int nv) {
+  return 2 * k + 1 < nv ? w : (2 * k < nv ? (w & 0xFFFFu) : 0u);
 }
 
 template <int BS>
@@ -140,14 +141,16 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
   const uint32_t bar0 = smem_addr(bars);
   auto k_full = [&](int s) { return bar0 + 8u * s; };
   auto k_empty = [&](int s) { return bar0 + 8u * (kKStages + s); };
-  auto v_full = [&](int s) { return bar0 + 8u * (2 * kKStages + s); };
-  auto v_empty = [&](int s) { return bar0 + 8u * (2 * kKStages + kVStages + s); };
-  constexpr int kTileBars = 2 * kKStages + 2 * kVStages;
-  auto s_full = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t); };
-  auto p_full = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t + 1); };
-  auto pv_done = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t + 2); };
-  auto o_final = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t + 3); };
-  const uint32_t q_full = bar0 + 8u * (kTileBars + 4 * kTiles);
+  constexpr int kB8 = 2 * kKStages, kB16 = kB8 + 2 * kV8Stages, kBT = kB16 + 2 * kV16Stages;
+  auto v8_full = [&](int s) { return bar0 + 8u * (kB8 + s); };
+  auto v8_empty = [&](int s) { return bar0 + 8u * (kB8 + kV8Stages + s); };
+  auto v16_full = [&](int s) { return bar0 + 8u * (kB16 + s); };
+  auto v16_empty = [&](int s) { return bar0 + 8u * (kB16 + kV16Stages + s); };
+  auto s_full = [&](int t) { return bar0 + 8u * (kBT + 4 * t); };
+  auto p_full = [&](int t) { return bar0 + 8u * (kBT + 4 * t + 1); };
+  auto pv_done = [&](int t) { return bar0 + 8u * (kBT + 4 * t + 2); };
+  auto o_final = [&](int t) { return bar0 + 8u * (kBT + 4 * t + 3); };
+  const uint32_t q_full = bar0 + 8u * (kBT + 4 * kTiles);
   const uint32_t mma_done = q_full + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
   float* row_rs = reinterpret_cast<float*>(smem + kRs);
@@ -157,9 +160,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
     }
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(v_full(s), 1);
-      mbar_init(v_empty(s), 1);
+    for (int s = 0; s < kV8Stages; ++s) {
+      mbar_init(v8_full(s), 1);
+      mbar_init(v8_empty(s), kCvt);
+    }
+    for (int s = 0; s < kV16Stages; ++s) {
+      mbar_init(v16_full(s), kCvt);
+      mbar_init(v16_empty(s), 1);
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(s_full(t), 1);
@@ -179,8 +186,16 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
   auto wait = [&](uint32_t bar, uint32_t parity) {
     return mbar_wait_bounded(bar, parity, p.wait_limit_ns, p.err, kErrTimeout, kShortWaitNs);
   };
+  // Which blocks of key tile jt are loaded (inside [kv_begin, kv_end), a
+  // table entry inside the pool): the rule every role applies.
+  const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.mbs;
+  auto needed = [&](int jt, int i) {
+    const int k0 = (jt0 + jt) * kKv + i * BS;
+    return k0 + BS > kv_begin && k0 < kv_end;
+  };
 
   if (warp < kKWarp) {
+    warpgroup_regs_inc<kSoftmaxRegs>();
     // ====== softmax warps: warps 4t..4t+3 serve query tile t, one row per thread
     const int t = warp >> 2;
     const int r = tid & (kRows - 1);
@@ -241,11 +256,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     const int nt = t ? n_kv1 : n_kv0;
-    const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.mbs;
-    auto needed = [&](int jt, int i) {
-      const int k0 = (jt0 + jt) * kKv + i * BS;
-      return k0 + BS > kv_begin && k0 < kv_end;
-    };
     int next[kKv / BS];
     auto fetch = [&](int jt) {
 #pragma unroll
@@ -259,13 +269,16 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
       for (int i = 0; i < kKv / BS; ++i)
         if (next[i] >= 0 && next[i] < p.num_blocks) mask |= 1u << i;
       if (jt + 1 < nt) fetch(jt + 1);
-      const int sv = jt % kVStages;
       ok = wait(s_full(t), jt & 1);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       const int key0 = (jt0 + jt) * kKv;
+      // the row of S, two loads of 64 columns (an instruction may not name
+      // more registers than the launch gives a thread) and one wait
       uint32_t x[kKv];
-      tmem_ld128(lane_base, x);
+      tmem_ld64_nowait(lane_base, *reinterpret_cast<uint32_t(*)[64]>(&x[0]));
+      tmem_ld64_nowait(lane_base + 64, *reinterpret_cast<uint32_t(*)[64]>(&x[64]));
+      tmem_wait_ld();
       if (!__all_sync(0xffffffffu, row_ok && key0 >= lo && key0 + kKv - 1 <= pos &&
                                        mask == kAllBlocks)) {
 #pragma unroll
@@ -285,44 +298,28 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
       const float m_old = m_run;
       if (m_run == -INFINITY || rescale) m_run = m_new;
       const float mu = m_run == -INFINITY ? 0.f : m_run;
-      const float2 sc2 = make_float2(coef, coef), nmu2 = make_float2(kPLog2 - mu, kPLog2 - mu);
-      // 2^7 p for the sixteen keys of each sub-tile, as four columns of four
-      // E4M3 codes (tokens 2c, 2c+1, 2c+8, 2c+9) and the codes of their
-      // remainders; each half of the key tile is stored as soon as it is done.
-      // In exact arithmetic the exponent is at most kLazy + 7 (2^8 = 256);
-      // fp32 holds it to within ulp(mu), so rows whose maximum reaches 2^21
-      // (scores beyond any real model's) clamp it there, keeping l and P alike.
+      const float2 sc2 = make_float2(coef, coef), nmu2 = make_float2(-mu, -mu);
+      // P as f16 pairs over the first 64 columns of S, a quarter of the keys
+      // per store.  In exact arithmetic the exponent is at most kLazy (p <=
+      // 256); fp32 holds it to within ulp(mu), so rows whose maximum reaches
+      // 2^21 (scores beyond any real model's) clamp it there, keeping l and
+      // P alike and P finite.
       float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       auto emit = [&](auto clamp) {
+        constexpr int kQuarter = kKv / 8;  // f16 pairs per quarter of the keys
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t wh[16], wl[16];
+        for (int kq = 0; kq < 4; ++kq) {
+          uint32_t wp[kQuarter];
 #pragma unroll
-          for (int sl = 0; sl < 4; ++sl) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int k0 = 64 * hf + kSub * sl + 2 * c;
-              float2 a0 = ffma2(make_float2(__uint_as_float(x[k0]), __uint_as_float(x[k0 + 1])), sc2, nmu2);
-              float2 a1 = ffma2(make_float2(__uint_as_float(x[k0 + 8]), __uint_as_float(x[k0 + 9])), sc2, nmu2);
-              if (decltype(clamp)::value) {
-                constexpr float kTop = kLazy + kPLog2;
-                a0 = make_float2(fminf(a0.x, kTop), fminf(a0.y, kTop));
-                a1 = make_float2(fminf(a1.x, kTop), fminf(a1.y, kTop));
-              }
-              const float2 p0 = make_float2(fast_exp2(a0.x), fast_exp2(a0.y));
-              const float2 p1 = make_float2(fast_exp2(a1.x), fast_exp2(a1.y));
-              l2[0] = fadd2(l2[0], p0);
-              l2[1] = fadd2(l2[1], p1);
-              const uint32_t h0 = pack_f16x2(p0.x, p0.y), h1 = pack_f16x2(p1.x, p1.y);
-              const uint32_t cw = f16x2x2_to_e4m3x4(h0, h1);
-              uint32_t b0, b1;
-              e4m3x4_to_f16x2(cw, b0, b1);
-              wh[4 * sl + c] = cw;
-              wl[4 * sl + c] = f16x2x2_to_e4m3x4(hsub2_bits(h0, b0), hsub2_bits(h1, b1));
-            }
+          for (int i = 0; i < kQuarter; ++i) {
+            const int e2 = kq * kQuarter + i;
+            float2 a = ffma2(make_float2(__uint_as_float(x[2 * e2]), __uint_as_float(x[2 * e2 + 1])), sc2, nmu2);
+            if (decltype(clamp)::value) a = make_float2(fminf(a.x, kLazy), fminf(a.y, kLazy));
+            const float2 pe = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+            l2[i & 1] = fadd2(l2[i & 1], pe);
+            wp[i] = pack_f16x2(pe.x, pe.y);
           }
-          tmem_st16_nowait(lane_base + 16 * hf, wh);
-          tmem_st16_nowait(lane_base + 32 + 16 * hf, wl);
+          tmem_st16_nowait(lane_base + kq * kQuarter, wp);
         }
       };
       if (__any_sync(0xffffffffu, fabsf(mu) >= 0x1p21f))
@@ -343,27 +340,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
         }
       }
       l_run += (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
-      // V codes the products must not see: tokens past the sequence's end and
-      // blocks that were not loaded.  Thread r clears dim row r of each
-      // sub-tile that needs it (the same sub-tiles for the whole warp).
-      const int zero_tile = jt < n_kv0 ? 0 : 1;
-      if (t == zero_tile && (mask != kAllBlocks || key0 + kKv > ctx)) {
-        ok = wait(v_full(sv), (jt / kVStages) & 1);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        uint8_t* vst = smem + kV + sv * kStage;
-#pragma unroll 1
-        for (int st = 0; st < kKv / kSub; ++st) {
-          const int kb = key0 + kSub * st;
-          const int nv = ((mask >> ((kSub * st) / BS)) & 1u) ? min(kSub, max(0, ctx - kb)) : 0;
-          if (nv < kSub) {
-            uint4* rowp = reinterpret_cast<uint4*>(vst + st * (kD * kSub) + r * kSub);
-            const uint4 m = sub_tile_mask(nv);
-            const uint4 cur = *rowp;
-            *rowp = make_uint4(cur.x & m.x, cur.y & m.y, cur.z & m.z, cur.w & m.w);
-          }
-        }
-      }
-      fence_proxy_async_smem();
       tc_fence_before();
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(p_full(t)) : "memory");
     }
@@ -404,155 +380,197 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
         __syncwarp();
       }
     }
-  } else if (warp == kKWarp || warp == kVWarp) {
-    // =========================== producers: K rows by TMA (swizzled boxes),
-    // the transposed V sub-tiles of each block by one bulk copy
-    if (lane == 0) {
-      const bool is_v = warp == kVWarp;
-      const int stages = is_v ? kVStages : kKStages;
-      uint8_t* ring = smem + (is_v ? kV : kK);
-      auto full = [&](int s) { return is_v ? v_full(s) : k_full(s); };
-      auto empty = [&](int s) { return is_v ? v_empty(s) : k_empty(s); };
-      const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.mbs;
-      auto needed = [&](int jt, int i) {
-        const int k0 = (jt0 + jt) * kKv + i * BS;
-        return k0 + BS > kv_begin && k0 < kv_end;
-      };
-      int next[kKv / BS];
-      auto fetch = [&](int jt) {
+  } else if (warp >= kCvtWarp) {
+    warpgroup_regs_dec<kOtherRegs>();
+    // ====== converters: thread ct turns dim row ct of every V sub-tile of a
+    // key tile into f16, tokens in natural order: the word of code positions
+    // 4c..4c+3 holds tokens 2c, 2c+1, 2c+8, 2c+9, so its low f16 pair goes
+    // to the first 8 tokens and its high pair to the last 8.
+    const int ct = tid - kCvtWarp * 32;
+    bool ok = true;
+    for (int jt = 0; jt < n_tiles && ok; ++jt) {
+      const int s8 = jt % kV8Stages, s16 = jt % kV16Stages;
+      uint32_t mask = 0;
 #pragma unroll
-        for (int i = 0; i < kKv / BS; ++i)
-          next[i] = needed(jt, i) ? trow[((jt0 + jt) * kKv + i * BS) / BS] : 0;
-      };
-      if (n_tiles > 0) fetch(0);
-      int issued = 0;
-      for (int jt = 0; jt < n_tiles; ++jt) {
-        const int s = jt % stages;
-        int cur[kKv / BS];
-#pragma unroll
-        for (int i = 0; i < kKv / BS; ++i) cur[i] = next[i];
-        if (jt + 1 < n_tiles) fetch(jt + 1);
-        if (jt >= stages && !wait(empty(s), ((jt / stages) - 1) & 1)) break;
-        uint32_t mask = 0;
-        int phys[kKv / BS];
-#pragma unroll
-        for (int i = 0; i < kKv / BS; ++i) {
-          phys[i] = -1;
-          if (!needed(jt, i)) continue;
-          const int e = cur[i];
-          if (e < 0 || e >= p.num_blocks) {
-            if (!is_v) atomicOr(p.err, kErrBadBlock);
-            continue;
+      for (int i = 0; i < kKv / BS; ++i) {
+        if (!needed(jt, i)) continue;
+        const int e = trow[((jt0 + jt) * kKv + i * BS) / BS];
+        if (e >= 0 && e < p.num_blocks) mask |= 1u << i;
+      }
+      ok = wait(v8_full(s8), (jt / kV8Stages) & 1);
+      if (ok && jt >= kV16Stages) ok = wait(v16_empty(s16), ((jt / kV16Stages) - 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      const int key0 = (jt0 + jt) * kKv;
+      const uint8_t* src = smem + kV8 + s8 * kV8Stage + ct * 16;
+      uint8_t* dst = smem + kV16 + s16 * kV16Stage + ct * 16;
+#pragma unroll 2
+      for (int st = 0; st < kKv / kSub; ++st) {
+        const int nv = ((mask >> ((kSub * st) / BS)) & 1u) ? min(kSub, max(0, ctx - (key0 + kSub * st))) : 0;
+        uint4 a = make_uint4(0u, 0u, 0u, 0u), c = make_uint4(0u, 0u, 0u, 0u);
+        if (nv > 0) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + st * (kD * kSub));
+          e4m3x4_to_f16x2(v.x, a.x, c.x);
+          e4m3x4_to_f16x2(v.y, a.y, c.y);
+          e4m3x4_to_f16x2(v.z, a.z, c.z);
+          e4m3x4_to_f16x2(v.w, a.w, c.w);
+          if (nv < kSub) {
+            a = make_uint4(keep_tokens(a.x, 0, nv), keep_tokens(a.y, 1, nv), keep_tokens(a.z, 2, nv),
+                           keep_tokens(a.w, 3, nv));
+            c = make_uint4(keep_tokens(c.x, 4, nv), keep_tokens(c.y, 5, nv), keep_tokens(c.z, 6, nv),
+                           keep_tokens(c.w, 7, nv));
           }
-          phys[i] = e;
-          mask |= 1u << i;
         }
-        const uint32_t bar = full(s);
-        const int nblk = __popc(mask);
-        if (nblk == 0) {
-          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-        } else {
-          mbar_arrive_expect_tx(bar, nblk * BS * 128);
-          const uint32_t st = smem_addr(ring + s * kStage);
+        *reinterpret_cast<uint4*>(dst + st * kV16Sub) = a;
+        *reinterpret_cast<uint4*>(dst + st * kV16Sub + kV16Sub / 2) = c;
+      }
+      fence_proxy_async_smem();
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(v16_full(s16)) : "memory");
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(v8_empty(s8)) : "memory");
+    }
+  } else {
+    warpgroup_regs_dec<kOtherRegs>();
+    if (warp == kKWarp || warp == kVWarp) {
+      // ======================= producers: K rows by TMA (swizzled boxes), the
+      // transposed V sub-tiles of each block by one bulk copy
+      if (lane == 0) {
+        const bool is_v = warp == kVWarp;
+        const int stages = is_v ? kV8Stages : kKStages;
+        uint8_t* ring = smem + (is_v ? kV8 : kK);
+        auto full = [&](int s) { return is_v ? v8_full(s) : k_full(s); };
+        auto empty = [&](int s) { return is_v ? v8_empty(s) : k_empty(s); };
+        int next[kKv / BS];
+        auto fetch = [&](int jt) {
+#pragma unroll
+          for (int i = 0; i < kKv / BS; ++i)
+            next[i] = needed(jt, i) ? trow[((jt0 + jt) * kKv + i * BS) / BS] : 0;
+        };
+        if (n_tiles > 0) fetch(0);
+        int issued = 0;
+        for (int jt = 0; jt < n_tiles; ++jt) {
+          const int s = jt % stages;
+          int cur[kKv / BS];
+#pragma unroll
+          for (int i = 0; i < kKv / BS; ++i) cur[i] = next[i];
+          if (jt + 1 < n_tiles) fetch(jt + 1);
+          if (jt >= stages && !wait(empty(s), ((jt / stages) - 1) & 1)) break;
+          uint32_t mask = 0;
+          int phys[kKv / BS];
 #pragma unroll
           for (int i = 0; i < kKv / BS; ++i) {
-            if (phys[i] < 0) continue;
-            const int64_t tile = static_cast<int64_t>(phys[i]) * p.n_kv_heads + h;
-            if (is_v)
-              bulk_load(st + i * BS * 128, p.pool + (2 * tile + 1) * (BS * 128), BS * 128, bar);
-            else
-              tma_load_4d(st + i * BS * 128, &tmap, bar, 0, 0, 0, static_cast<int>(tile));
-          }
-        }
-        ++issued;
-      }
-      for (int jt = max(0, issued - stages); jt < issued; ++jt)
-        if (!wait(full(jt % stages), (jt / stages) & 1)) atomicOr(p.err, kErrDrainTimeout);
-    }
-    __syncwarp();
-  } else {
-    // =========================== MMA issuer, in the bf16 kernel's order: per
-    // key tile and query tile, P V of the previous key tile, then S
-    if (lane == 0) {
-      constexpr uint32_t idS = umma_idesc_e4m3(kRows, kKv, false);
-      constexpr uint32_t idO = umma_idesc_e4m3(kRows, kD, false);
-      const uint64_t q_desc = umma_desc_sw128(smem_addr(smem + kQ), 16, 1024);
-      const uint64_t k_desc = umma_desc_sw128(smem_addr(smem + kK), 16, 1024);
-      // V: core matrices 8 dims x 16 tokens; 128 bytes to the next 8 dims,
-      // one sub-tile (2 KB) to the next 16 tokens
-      const uint64_t v_desc = umma_desc_noswz(smem_addr(smem + kV), kD * kSub, 128);
-      const uint32_t q_lo = static_cast<uint32_t>(q_desc), q_hi = static_cast<uint32_t>(q_desc >> 32);
-      const uint32_t k_lo = static_cast<uint32_t>(k_desc), k_hi = static_cast<uint32_t>(k_desc >> 32);
-      const uint32_t v_lo = static_cast<uint32_t>(v_desc), v_hi = static_cast<uint32_t>(v_desc >> 32);
-      constexpr uint32_t kStageUnits = kStage >> 4;
-      bool ok = wait(q_full, 0);
-      if (ok) tc_fence_after();
-      auto issue_s = [&](int t, int jt) {
-        const uint32_t ka = k_lo + (jt % kKStages) * kStageUnits;
-        const uint32_t qa = q_lo + t * (kQTile >> 4);
-        const uint32_t d = tmem + t * kTmemTile;
-        // S = Q_hi K^T + Q_lo K^T, 32 dims per product
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int k = 0; k < kD / 32; ++k)
-            umma_e4m3_w(d, qa + ((part * kQPart + k * 32) >> 4), q_hi, ka + ((k * 32) >> 4), k_hi, idS,
-                        (part > 0 || k > 0) ? 1u : 0u);
-        umma_commit(s_full(t));
-      };
-      auto issue_pv = [&](int t, int jt) {
-        const uint32_t va = v_lo + (jt % kVStages) * kStageUnits;
-        const uint32_t pt = tmem + t * kTmemTile;
-        const uint32_t d = pt + kOCol;
-        // O += P_hi V + P_lo V, 32 keys (two sub-tiles, eight columns of P) per product
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int k = 0; k < kKv / 32; ++k)
-            umma_e4m3_ta_w(d, pt + part * 32 + k * 8, va + ((k * 2 * kD * kSub) >> 4), v_hi, idO,
-                           (jt > 0 || part > 0 || k > 0) ? 1u : 0u);
-      };
-      for (int jt = 0; ok && jt <= n_tiles; ++jt) {
-        bool v_ready = false, k_ready = false;
-        for (int t = 0; t < kTiles && ok; ++t) {
-          const int nt = t ? n_kv1 : n_kv0;
-          if (jt > 0 && jt - 1 < nt) {
-            if (!v_ready) {
-              ok = wait(v_full((jt - 1) % kVStages), ((jt - 1) / kVStages) & 1);
-              if (!ok) break;
-              v_ready = true;
+            phys[i] = -1;
+            if (!needed(jt, i)) continue;
+            const int e = cur[i];
+            if (e < 0 || e >= p.num_blocks) {
+              if (!is_v) atomicOr(p.err, kErrBadBlock);
+              continue;
             }
-            ok = wait(p_full(t), (jt - 1) & 1);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(t, jt - 1);
-            umma_commit(jt == nt ? o_final(t) : pv_done(t));
+            phys[i] = e;
+            mask |= 1u << i;
           }
-          if (jt < nt) {
-            // S of this key tile overwrites the P the previous product reads
-            // (products with different accumulators are not ordered)
-            if (jt > 0) {
-              ok = wait(pv_done(t), (jt - 1) & 1);
+          const uint32_t bar = full(s);
+          const int nblk = __popc(mask);
+          if (nblk == 0) {
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+          } else {
+            mbar_arrive_expect_tx(bar, nblk * BS * 128);
+            const uint32_t st = smem_addr(ring + s * kK8Stage);
+#pragma unroll
+            for (int i = 0; i < kKv / BS; ++i) {
+              if (phys[i] < 0) continue;
+              const int64_t tile = static_cast<int64_t>(phys[i]) * p.n_kv_heads + h;
+              if (is_v)
+                bulk_load(st + i * BS * 128, p.pool + (2 * tile + 1) * (BS * 128), BS * 128, bar);
+              else
+                tma_load_4d(st + i * BS * 128, &tmap, bar, 0, 0, 0, static_cast<int>(tile));
+            }
+          }
+          ++issued;
+        }
+        for (int jt = max(0, issued - stages); jt < issued; ++jt)
+          if (!wait(full(jt % stages), (jt / stages) & 1)) atomicOr(p.err, kErrDrainTimeout);
+      }
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ===================== MMA issuer, in the bf16 kernel's order: per key
+      // tile and query tile, P V of the previous key tile, then S
+      if (lane == 0) {
+        constexpr uint32_t idS = umma_idesc_e4m3(kRows, kKv, false);
+        constexpr uint32_t idO = umma_idesc_f16(kRows, kD, false);
+        const uint64_t q_desc = umma_desc_sw128(smem_addr(smem + kQ), 16, 1024);
+        const uint64_t k_desc = umma_desc_sw128(smem_addr(smem + kK), 16, 1024);
+        // f16 V: core matrices 8 dims x 8 tokens; 128 bytes to the next 8
+        // dims, 2 KB to the next 8 tokens
+        const uint64_t v_desc = umma_desc_noswz(smem_addr(smem + kV16), kV16Sub / 2, 128);
+        const uint32_t q_lo = static_cast<uint32_t>(q_desc), q_hi = static_cast<uint32_t>(q_desc >> 32);
+        const uint32_t k_lo = static_cast<uint32_t>(k_desc), k_hi = static_cast<uint32_t>(k_desc >> 32);
+        const uint32_t v_lo = static_cast<uint32_t>(v_desc), v_hi = static_cast<uint32_t>(v_desc >> 32);
+        bool ok = wait(q_full, 0);
+        if (ok) tc_fence_after();
+        auto issue_s = [&](int t, int jt) {
+          const uint32_t ka = k_lo + (jt % kKStages) * (kK8Stage >> 4);
+          const uint32_t qa = q_lo + t * (kQTile >> 4);
+          const uint32_t d = tmem + t * kTmemTile;
+          // S = Q_hi K^T + Q_lo K^T, 32 dims per product
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int k = 0; k < kD / 32; ++k)
+              umma_e4m3_w(d, qa + ((part * kQPart + k * 32) >> 4), q_hi, ka + ((k * 32) >> 4), k_hi, idS,
+                          (part > 0 || k > 0) ? 1u : 0u);
+          umma_commit(s_full(t));
+        };
+        auto issue_pv = [&](int t, int jt) {
+          const uint32_t va = v_lo + (jt % kV16Stages) * (kV16Stage >> 4);
+          const uint32_t pt = tmem + t * kTmemTile;
+          const uint32_t d = pt + kOCol;
+          // O += P V, 16 keys (one sub-tile, eight columns of P) per product
+#pragma unroll
+          for (int k = 0; k < kKv / 16; ++k)
+            umma_bf16_ta_w(d, pt + k * 8, va + ((k * kV16Sub) >> 4), v_hi, idO, (jt > 0 || k > 0) ? 1u : 0u);
+        };
+        for (int jt = 0; ok && jt <= n_tiles; ++jt) {
+          bool v_ready = false, k_ready = false;
+          for (int t = 0; t < kTiles && ok; ++t) {
+            const int nt = t ? n_kv1 : n_kv0;
+            if (jt > 0 && jt - 1 < nt) {
+              if (!v_ready) {
+                ok = wait(v16_full((jt - 1) % kV16Stages), ((jt - 1) / kV16Stages) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                v_ready = true;
+              }
+              ok = wait(p_full(t), (jt - 1) & 1);
               if (!ok) break;
               tc_fence_after();
+              issue_pv(t, jt - 1);
+              umma_commit(jt == nt ? o_final(t) : pv_done(t));
             }
-            if (!k_ready) {
-              ok = wait(k_full(jt % kKStages), (jt / kKStages) & 1);
-              if (!ok) break;
-              tc_fence_after();
-              k_ready = true;
+            if (jt < nt) {
+              // S of this key tile overwrites the P the previous product reads
+              // (products with different accumulators are not ordered)
+              if (jt > 0) {
+                ok = wait(pv_done(t), (jt - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              if (!k_ready) {
+                ok = wait(k_full(jt % kKStages), (jt / kKStages) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                k_ready = true;
+              }
+              issue_s(t, jt);
             }
-            issue_s(t, jt);
           }
+          if (!ok) break;
+          if (k_ready) umma_commit(k_empty(jt % kKStages));
+          if (v_ready) umma_commit(v16_empty((jt - 1) % kV16Stages));
         }
-        if (!ok) break;
-        if (k_ready) umma_commit(k_empty(jt % kKStages));
-        if (v_ready) umma_commit(v_empty((jt - 1) % kVStages));
+        umma_commit(mma_done);
+        if (!wait(mma_done, 0)) atomicOr(p.err, kErrDrainTimeout);
       }
-      umma_commit(mma_done);
-      if (!wait(mma_done, 0)) atomicOr(p.err, kErrDrainTimeout);
+      __syncwarp();
     }
-    __syncwarp();
   }
 
   tc_fence_before();

@@ -1,12 +1,12 @@
 """GPU parity of paged prefill (extend) attention over FP8 (E4M3) pools, on
-the E4M3 tensor-core products, against the fp64 oracle on the same codes.
+the tensor cores, against the fp64 oracle on the same codes.
 
 Tolerance: the FP8 bar of the decode, max |err| <= 3e-2, and a relative L2
 bound of 1e-2 derived from the kernel's arithmetic: K and V enter as their
-codes (exact), each query row as a power-of-two scaled E4M3 code plus the
-code of its remainder (relative error <= 2^-8 per element), each weight as
-the same two-code split of 128 p (<= 2^-8), accumulation in fp32.  Errors of
-2^-8 per term give a few 1e-3 on the output at most.
+codes (exact; V converted to f16, exactly), each query row as a power-of-two
+scaled E4M3 code plus the code of its remainder (relative error <= 2^-8 per
+element), each weight as one f16 (<= 2^-11), accumulation in fp32.  Errors
+of 2^-8 per term give a few 1e-3 on the output at most.
 """
 
 import numpy as np
@@ -130,8 +130,8 @@ def test_prefill_fp8_long_prompt_many_tiles():
 @pytest.mark.parametrize("bs", [16, 32])
 def test_prefill_fp8_rescales_often(bs):
     """Keys aligned with the queries and growing along the sequence raise each
-    row's maximum on nearly every key tile, past the (small) lazy threshold
-    this kernel uses to keep 128 p inside the E4M3 range."""
+    row's maximum on nearly every key tile, past the lazy-rescale threshold,
+    so O in tensor memory is rescaled again and again."""
     hkv, hq, ctx, ql = 2, 8, 900, 700
     g0 = torch.Generator().manual_seed(8)
     direction = torch.randn(hkv, 128, generator=g0)
