@@ -22,7 +22,7 @@
 //    finer than a bf16 high part plus remainder needs two products for), so
 //    V must be f16 too, which E4M3 codes convert to exactly.  A fourth
 //    warpgroup converts: the pool's transposed V sub-tiles ([D][16] codes
-//    per 16 tokens, one bulk copy per block) become f16 sub-tiles in natural
+//    per 16 tokens, one TMA box per block) become f16 sub-tiles in natural
 //    token order, read as the K-major B operand without swizzle (core
 //    matrices of 8 dims x 8 tokens, 128 bytes apart along the dims, 2 KB
 //    along the keys), with tokens past the sequence's end and blocks not
@@ -76,7 +76,9 @@ constexpr int kV16 = kQ + kTiles * kQTile;
 constexpr int kV8 = kV16 + kV16Stages * kV16Stage;
 constexpr int kK = kV8 + kV8Stages * kV8Stage;
 constexpr int kRs = kK + kKStages * kK8Stage;         // float [kTiles][kRows]: 2^-(row power)
-constexpr int kBars = kRs + kTiles * kRows * 4;
+constexpr int kV8Mask = kRs + kTiles * kRows * 4;     // uint32 [kV8Stages]: blocks each V stage holds
+constexpr int kBars = kV8Mask + 16;
+static_assert(kV8Stages * 4 <= 16, "the V stages' block masks fit");
 constexpr int kNumBars = 2 * kKStages + 2 * kV8Stages + 2 * kV16Stages + 4 * kTiles + 2;
 constexpr int kTmemSlot = kBars + kNumBars * 8;
 constexpr int kSmemBytes = kTmemSlot + 16 + 1024;     // + alignment slack
@@ -154,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
   const uint32_t mma_done = q_full + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
   float* row_rs = reinterpret_cast<float*>(smem + kRs);
+  uint32_t* v8_mask = reinterpret_cast<uint32_t*>(smem + kV8Mask);
 
   if (tid == 0) {
     for (int s = 0; s < kKStages; ++s) {
@@ -390,18 +393,17 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
     bool ok = true;
     for (int jt = 0; jt < n_tiles && ok; ++jt) {
       const int s8 = jt % kV8Stages, s16 = jt % kV16Stages;
-      uint32_t mask = 0;
-#pragma unroll
-      for (int i = 0; i < kKv / BS; ++i) {
-        if (!needed(jt, i)) continue;
-        const int e = trow[((jt0 + jt) * kKv + i * BS) / BS];
-        if (e >= 0 && e < p.num_blocks) mask |= 1u << i;
-      }
       ok = wait(v8_full(s8), (jt / kV8Stages) & 1);
       if (ok && jt >= kV16Stages) ok = wait(v16_empty(s16), ((jt / kV16Stages) - 1) & 1);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      // the blocks the stage holds, left there by the V producer
+      const uint32_t mask = v8_mask[s8];
       const int key0 = (jt0 + jt) * kKv;
-      const uint8_t* src = smem + kV8 + s8 * kV8Stage + ct * 16;
+      // the stage holds the sub-tiles as rows of 128 bytes (8 dims), 128-byte
+      // swizzled: dim row ct of every sub-tile sits in row ct / 8 of it, at
+      // chunk (ct mod 8) ^ (ct / 8 mod 8)
+      const uint8_t* src =
+          smem + kV8 + s8 * kV8Stage + (ct >> 3) * 128 + (((ct & 7) ^ ((ct >> 3) & 7)) << 4);
       uint8_t* dst = smem + kV16 + s16 * kV16Stage + ct * 16;
 #pragma unroll 2
       for (int st = 0; st < kKv / kSub; ++st) {
@@ -431,7 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
     warpgroup_regs_dec<kOtherRegs>();
     if (warp == kKWarp || warp == kVWarp) {
       // ======================= producers: K rows by TMA (swizzled boxes), the
-      // transposed V sub-tiles of each block by one bulk copy
+      // transposed V sub-tiles of each block, seen as rows of 128 bytes (8
+      // dims each), by one swizzled TMA box too
       if (lane == 0) {
         const bool is_v = warp == kVWarp;
         const int stages = is_v ? kV8Stages : kKStages;
@@ -469,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
           }
           const uint32_t bar = full(s);
           const int nblk = __popc(mask);
+          if (is_v) v8_mask[s] = mask;  // for the converters (published by the arrive below)
           if (nblk == 0) {
             asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
           } else {
@@ -478,10 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
             for (int i = 0; i < kKv / BS; ++i) {
               if (phys[i] < 0) continue;
               const int64_t tile = static_cast<int64_t>(phys[i]) * p.n_kv_heads + h;
-              if (is_v)
-                bulk_load(st + i * BS * 128, p.pool + (2 * tile + 1) * (BS * 128), BS * 128, bar);
-              else
-                tma_load_4d(st + i * BS * 128, &tmap, bar, 0, 0, 0, static_cast<int>(tile));
+              tma_load_4d(st + i * BS * 128, &tmap, bar, 0, 0, is_v ? 1 : 0, static_cast<int>(tile));
             }
           }
           ++issued;
