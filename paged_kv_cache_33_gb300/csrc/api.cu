@@ -442,7 +442,6 @@ kv_status paged_prefill_attention(kv_pool* p, const void* q, int32_t n_q_heads,
   d.context_lens = context_lens;
   d.out = out;
   d.err = p->err;
-  d.pool = static_cast<const uint8_t*>(p->base);
   d.k_scale = p->scales;
   d.v_scale = p->scales + p->n_kv_heads;
   d.num_blocks = p->num_blocks;

@@ -117,7 +117,6 @@ struct PrefillParams {
   const int32_t* context_lens;  // [B]
   float* out;                   // [T][Hq][D]
   uint32_t* err;
-  const uint8_t* pool;          // FP8: pool base (the V sub-tiles are staged with bulk copies)
   const float* k_scale;         // FP8: [Hkv]
   const float* v_scale;
   int64_t num_blocks;
