@@ -551,8 +551,9 @@ def measure_extras(step: Step, peaks: dict, device) -> dict:
     #    (short prompts: per-CTA set-up weighs more) and 4 x 8192 tokens, over
     #    bf16 and FP8 pools.  The FP8 products run at twice the bf16 rate
     #    (the nominal ratio, 4.5 / 2.25 PFLOP/s dense, applied to the measured
-    #    bf16 peak).  Issued tensor work per algorithmic flop: bf16 1.5 (P V
-    #    twice: P's high part and remainder), FP8 2 (Q K^T and P V twice each)
+    #    bf16 peak).  Issued tensor work per algorithmic flop, in units of the
+    #    pool's own rate: bf16 1.5 (P V twice: P's high part and remainder),
+    #    FP8 2 (Q K^T twice on E4M3; P V once on f16, at half the E4M3 rate)
     bf16_peak = peaks["bf16_tflops"]
     for key, dt, (B, ctx) in (("paged_prefill_attention", "bf16", (4, 2048)),
                               ("paged_prefill_attention_long", "bf16", (4, 8192)),
