@@ -549,21 +549,24 @@ def measure_extras(step: Step, peaks: dict, device) -> dict:
     del flush_w, flush_r
     # -- paged_prefill_attention: 8B-shaped full causal prefill, 4 x 2048 tokens
     #    (short prompts: per-CTA set-up weighs more) and 4 x 8192 tokens, over
-    #    bf16 and FP8 pools.  The FP8 products run at twice the bf16 rate
+    #    bf16, FP8 and FP4 pools.  The FP8 products run at twice the bf16 rate
     #    (the nominal ratio, 4.5 / 2.25 PFLOP/s dense, applied to the measured
-    #    bf16 peak).  Issued tensor work per algorithmic flop, in units of the
-    #    pool's own rate: bf16 1.5 (P V twice: P's high part and remainder),
-    #    FP8 2 (Q K^T twice on E4M3; P V once on f16, at half the E4M3 rate)
+    #    bf16 peak); the FP4 kernel's are f16 ones (the bf16 rate).  Issued
+    #    tensor work per algorithmic flop, in units of the peak used: bf16 1.5
+    #    (P V twice: P's high part and remainder), FP8 2 (Q K^T twice on E4M3;
+    #    P V once on f16, at half the E4M3 rate), FP4 1
     bf16_peak = peaks["bf16_tflops"]
     for key, dt, (B, ctx) in (("paged_prefill_attention", "bf16", (4, 2048)),
                               ("paged_prefill_attention_long", "bf16", (4, 8192)),
                               ("paged_prefill_attention_fp8", "fp8", (4, 2048)),
-                              ("paged_prefill_attention_fp8_long", "fp8", (4, 8192))):
+                              ("paged_prefill_attention_fp8_long", "fp8", (4, 8192)),
+                              ("paged_prefill_attention_fp4", "fp4", (4, 2048)),
+                              ("paged_prefill_attention_fp4_long", "fp4", (4, 8192))):
         hq, hkv = 32, 8
         nblk = ctx // 16
         ppool = pk.KVPool(B * nblk, 16, hkv, 128, dt)
-        if dt == "fp8":   # randn keys and values: |x| < 4.5 for these sizes
-            sc = torch.full((hkv,), 4.5 / 448, device=device)
+        if dt in ("fp8", "fp4"):   # randn keys and values: |x| < 4.5 for these sizes
+            sc = torch.full((hkv,), 4.5 / (448 if dt == "fp8" else 6 * 448), device=device)
             ppool.set_scales(sc, sc)
         tables = torch.from_numpy(np.random.default_rng(3).permutation(B * nblk).astype(np.int32)
                                   .reshape(B, nblk)).to(device)
@@ -582,7 +585,7 @@ def measure_extras(step: Step, peaks: dict, device) -> dict:
         flops = 4.0 * 128 * hq * B * (ctx * (ctx + 1) // 2)   # QK and PV over the causal keys
         tf = flops / t / 1e12
         peak = bf16_peak * (2.0 if dt == "fp8" else 1.0)
-        issued = 2.0 if dt == "fp8" else 1.5
+        issued = {"bf16": 1.5, "fp8": 2.0, "fp4": 1.0}[dt]
         out[key] = {
             "workload": f"full causal prefill, {B} x {ctx} tokens, {hq} q / {hkv} KV heads, "
                         f"head_dim 128, 16-token blocks, {dt} pool",

@@ -300,19 +300,22 @@ kv_status paged_decode_attention_noalloc(kv_pool* pool, const void* q_dev, int32
  *                      position pos = ctx - q_len + i) gets
  *                      softmax(scale q K^T) V over positions [lo, pos], lo =
  *                      max(0, pos + 1 - sliding_window) when the window is on.
- * bf16 and FP8 pools with head_dim 128 and a query group of at most 8 heads
- * per KV head (FP4 pools and other shapes: KV_ERR_UNSUPPORTED).  Runs on the
- * tcgen05 tensor cores.  bf16: P enters the P V product as a bf16 high part
+ * bf16, FP8 and FP4 pools with head_dim 128 and a query group of at most 8
+ * heads per KV head (other shapes: KV_ERR_UNSUPPORTED).  Runs on the tcgen05
+ * tensor cores.  bf16: P enters the P V product as a bf16 high part
  * plus the bf16 rounding of its remainder (two products into the same
  * accumulator), so the result meets the decode's bf16 accuracy.  FP8: Q K^T
  * takes E4M3 operands -- the K codes as stored, each query row scaled by a
  * power of two and split into an E4M3 code and the code of its remainder --
  * and P V f16 ones (P rounded once to f16, the V codes converted exactly),
- * with k_scale and v_scale applied in fp32 (for scores of magnitude 2^21 or
- * more, in log2 units, the weights are only as exact as fp32 holds the row
- * maximum).  A sequence with q_len > context_len or a context above a
- * bound sets KV_ERR_BAD_CONTEXT and is skipped.  Asynchronous on `stream`;
- * no workspace.
+ * with k_scale and v_scale applied in fp32.  FP4: keys and values
+ * dequantised exactly into f16 (an E2M1 value times an E4M3 group scale),
+ * each query row scaled by a power of two into f16, P one f16 per weight,
+ * the head scales applied in fp32; the result meets the decode's bf16
+ * accuracy.  Scores of any magnitude are handled (the softmax maximum is
+ * kept in raw score units).  A sequence with q_len > context_len or a
+ * context above a bound sets KV_ERR_BAD_CONTEXT and is skipped.
+ * Asynchronous on `stream`; no workspace.
  */
 kv_status paged_prefill_attention(kv_pool* pool, const void* q_dev, int32_t n_q_heads,
                                   const int32_t* cu_q_lens_dev, const int32_t* block_tables_dev,

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libpagedkv.so")
 SOURCES = ["api.cu", "kv_write.cu", "decode.cu", "decode_noalloc.cu", "kv_copy.cu", "prefill.cu",
-           "prefill_fp8.cu",
+           "prefill_fp8.cu", "prefill_fp4.cu",
            "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",

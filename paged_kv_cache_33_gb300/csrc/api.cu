@@ -45,9 +45,22 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // K+V pair: 64 bf16 columns (head_dim 128 takes two boxes) or 128 E4M3
 // columns, 16 token rows, both K and V; 128-byte swizzle in shared memory.
 bool encode_pool_map(kv_pool* p) {
-  if (p->dtype == KV_FP4_E2M1) return true;  // FP4 records are staged with plain bulk copies
   auto encode = tensor_map_encoder();
   if (!encode) return false;
+  if (p->dtype == KV_FP4_E2M1) {
+    // The decode stages FP4 records with plain bulk copies; the prefill takes
+    // the records of one (block, head), contiguous, as rows of 128 bytes, all
+    // of them in one box, verbatim (no swizzle).
+    const uint64_t rec = static_cast<uint64_t>(p->block_size / 16) * pkv::kFp4SubBytes;
+    cuuint64_t dims[3] = {128, rec / 128, static_cast<cuuint64_t>(p->num_blocks) * p->n_kv_heads};
+    cuuint64_t strides[2] = {128, rec};
+    cuuint32_t box[3] = {128, static_cast<cuuint32_t>(rec / 128), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return encode(&p->tmap_rows, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, p->base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+  }
   const uint64_t esz = p->dtype == KV_BF16 ? 2 : 1;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(p->head_dim),
                         static_cast<cuuint64_t>(p->block_size), 2,
@@ -421,7 +434,7 @@ kv_status paged_prefill_attention(kv_pool* p, const void* q, int32_t n_q_heads,
     return KV_ERR_INVALID_ARG;
   if (n_q_heads % p->n_kv_heads != 0) return KV_ERR_INVALID_ARG;
   const int32_t g = n_q_heads / p->n_kv_heads;
-  if (g > 8 || p->dtype == KV_FP4_E2M1 || p->head_dim != 128) return KV_ERR_UNSUPPORTED;
+  if (g > 8 || p->head_dim != 128) return KV_ERR_UNSUPPORTED;
   if (batch == 0 || max_q_len == 0) return KV_OK;
   if (!q || !cu_q_lens || !block_tables || !context_lens || !out || !aligned16(q) || !aligned16(out))
     return KV_ERR_INVALID_ARG;
@@ -459,9 +472,10 @@ kv_status paged_prefill_attention(kv_pool* p, const void* q, int32_t n_q_heads,
   d.q_sign = scale < 0.f ? 0x80008000u : 0u;
   d.scale_log2 = std::max(std::fabs(scale) * 1.4426950408889634f, 1e-30f);
   d.wait_limit_ns = p->wait_limit_ns;
-  const cudaError_t e = p->dtype == KV_FP8_E4M3
-                            ? pkv::launch_prefill_fp8(p, d, max_q_len, static_cast<cudaStream_t>(stream))
-                            : pkv::launch_prefill(p, d, max_q_len, static_cast<cudaStream_t>(stream));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = p->dtype == KV_FP8_E4M3   ? pkv::launch_prefill_fp8(p, d, max_q_len, s)
+                        : p->dtype == KV_FP4_E2M1 ? pkv::launch_prefill_fp4(p, d, max_q_len, s)
+                                                  : pkv::launch_prefill(p, d, max_q_len, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return KV_ERR_CUDA;

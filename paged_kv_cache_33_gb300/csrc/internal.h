@@ -18,7 +18,8 @@ struct kv_pool {
   float* scales = nullptr;     // device [2][Hkv]: K scales then V scales
   uint32_t* err = nullptr;     // device error word
   CUtensorMap tmap;            // pool viewed as [NB*Hkv][2][BS][D] for TMA
-  CUtensorMap tmap_rows;       // bf16 / FP8 pools: the same view, boxes of one tile (K or V)
+  CUtensorMap tmap_rows;       // bf16 / FP8 pools: the same view, boxes of one tile (K or V);
+                               // FP4 pools: each (block, head)'s records as rows of 128 bytes
   int32_t partition_blocks = 0;  // 0 = automatic
   uint64_t wait_limit_ns = 1000000000ull;  // bound of every wait in the kernels
   uint32_t stall_tx = 0;       // test hook (kv_pool_set_test_stall)
@@ -134,6 +135,9 @@ cudaError_t launch_prefill(const kv_pool* pool, const PrefillParams& p, int32_t 
                            cudaStream_t stream);
 // The same over an FP8 (E4M3) pool, with E4M3 tensor-core products.
 cudaError_t launch_prefill_fp8(const kv_pool* pool, const PrefillParams& p, int32_t max_q_len,
+                               cudaStream_t stream);
+// The same over an FP4 pool, its values dequantised exactly into f16.
+cudaError_t launch_prefill_fp4(const kv_pool* pool, const PrefillParams& p, int32_t max_q_len,
                                cudaStream_t stream);
 
 // The merge of cut pairs, launched as a programmatic dependent of the decode.

@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     }
     const uint32_t lane_base = tmem + t * kTmemTile + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     constexpr uint32_t kAllBlocks = (1u << (kKv / BS)) - 1u;
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_raw = -INFINITY, l_run = 0.f;  // running maximum in raw score units
     bool ok = true;
     const int nt = t ? n_kv1 : n_kv0;
     // Which blocks of a key tile hold keys: the same rule the producers use
@@ -264,15 +264,32 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
 #pragma unroll
       for (int c = 0; c < kKv; ++c) mt4[c & 3] = fmaxf(mt4[c & 3], __uint_as_float(x[c]));
       const float mt_raw = fmaxf(fmaxf(mt4[0], mt4[1]), fmaxf(mt4[2], mt4[3]));
-      const float mt = mt_raw == -INFINITY ? -INFINITY : mt_raw * p.scale_log2;
       // A row with nothing accumulated yet (O's row is zero) takes the new
-      // maximum; others keep theirs unless it grew by more than 2^kLazy.
-      const float m_new = fmaxf(m_run, mt);
-      const bool rescale = m_run != -INFINITY && m_new > m_run + kLazy;
-      const float m_old = m_run;
-      if (m_run == -INFINITY || rescale) m_run = m_new;
-      const float mu = m_run == -INFINITY ? 0.f : m_run;
-      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nmu2 = make_float2(-mu, -mu);
+      // maximum; others keep theirs unless it grew by more than 2^kLazy.  The
+      // maximum is kept in raw score units (the scale is positive), so the
+      // rescale and, for large scores, the exponents come from exact
+      // differences of raw scores.
+      const float coef = p.scale_log2;
+      const bool rescale = m_raw != -INFINITY && mt_raw != -INFINITY && (mt_raw - m_raw) * coef > kLazy;
+      const float m_old = m_raw;
+      if (m_raw == -INFINITY || rescale) m_raw = mt_raw;
+      const float mr = m_raw == -INFINITY ? 0.f : m_raw;
+      float mu = mr * coef;
+      // The exponent (x - m) coef is at most kLazy, taken as one FMA against
+      // m coef.  Once |m coef| reaches 2^13 fp32 holds it only to within
+      // 2^-11 (scores of no real model get there): such warps first subtract
+      // m from their raw scores, exactly near the maximum, and use no offset.
+      if (__any_sync(0xffffffffu, fabsf(mu) >= 0x1p13f)) {
+        const float2 nmr2 = make_float2(-mr, -mr);
+#pragma unroll
+        for (int c = 0; c < kKv; c += 2) {
+          const float2 d = fadd2(make_float2(__uint_as_float(x[c]), __uint_as_float(x[c + 1])), nmr2);
+          x[c] = __float_as_uint(d.x);
+          x[c + 1] = __float_as_uint(d.y);
+        }
+        mu = 0.f;
+      }
+      const float2 sc2 = make_float2(coef, coef), nmu2 = make_float2(-mu, -mu);
       // the exponentials; P as a bf16 high part (pairs over the first kKv/2
       // columns of S) and the bf16 rounding of its remainder (the last kKv/2
       // columns), so ~16 significant bits of every weight reach the products.
@@ -302,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       // O is stable: S of this key tile was issued only after the tile's
       // previous P V product had completed
       if (__any_sync(0xffffffffu, rescale)) {  // tensor-memory access is warp-wide
-        const float alpha = rescale ? fast_exp2(m_old - m_new) : 1.f;
+        const float alpha = rescale ? fast_exp2((m_old - m_raw) * coef) : 1.f;
         l_run *= alpha;
 #pragma unroll
         for (int c0 = 0; c0 < kD; c0 += 32) {

@@ -34,8 +34,6 @@
 
 #include <math.h>
 
-#include <type_traits>
-
 #include "common.cuh"
 #include "internal.h"
 
@@ -256,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
     // coefficient of the exponent: softmax scale (log2) x k_scale x the row's power
     const float coef = p.scale_log2 * p.k_scale[h] * row_rs[t * kRows + r];
     constexpr uint32_t kAllBlocks = (1u << (kKv / BS)) - 1u;
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_raw = -INFINITY, l_run = 0.f;  // running maximum in raw score units
     bool ok = true;
     const int nt = t ? n_kv1 : n_kv0;
     int next[kKv / BS];
@@ -295,20 +293,34 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
 #pragma unroll
       for (int c = 0; c < kKv; ++c) mt4[c & 3] = fmaxf(mt4[c & 3], __uint_as_float(x[c]));
       const float mt_raw = fmaxf(fmaxf(mt4[0], mt4[1]), fmaxf(mt4[2], mt4[3]));
-      const float mt = mt_raw == -INFINITY ? -INFINITY : mt_raw * coef;
-      const float m_new = fmaxf(m_run, mt);
-      const bool rescale = m_run != -INFINITY && m_new > m_run + kLazy;
-      const float m_old = m_run;
-      if (m_run == -INFINITY || rescale) m_run = m_new;
-      const float mu = m_run == -INFINITY ? 0.f : m_run;
+      // The running maximum is kept in raw score units (coef > 0 keeps the
+      // order), so the lazy rescale and, for large scores, the exponents come
+      // from exact differences of raw scores.
+      const bool rescale = m_raw != -INFINITY && mt_raw != -INFINITY && (mt_raw - m_raw) * coef > kLazy;
+      const float m_old = m_raw;
+      if (m_raw == -INFINITY || rescale) m_raw = mt_raw;
+      const float mr = m_raw == -INFINITY ? 0.f : m_raw;
+      float mu = mr * coef;
+      // The exponent (x - m) coef is at most kLazy (p <= 256), taken as one
+      // FMA against m coef.  Once |m coef| reaches 2^13 fp32 holds it only
+      // to within 2^-11 (scores of no real model get there): such warps
+      // first subtract m from their raw scores, exactly near the maximum,
+      // and use no offset.
+      if (__any_sync(0xffffffffu, fabsf(mu) >= 0x1p13f)) {
+        const float2 nmr2 = make_float2(-mr, -mr);
+#pragma unroll
+        for (int c = 0; c < kKv; c += 2) {
+          const float2 d = fadd2(make_float2(__uint_as_float(x[c]), __uint_as_float(x[c + 1])), nmr2);
+          x[c] = __float_as_uint(d.x);
+          x[c + 1] = __float_as_uint(d.y);
+        }
+        mu = 0.f;
+      }
       const float2 sc2 = make_float2(coef, coef), nmu2 = make_float2(-mu, -mu);
       // P as f16 pairs over the first 64 columns of S, a quarter of the keys
-      // per store.  In exact arithmetic the exponent is at most kLazy (p <=
-      // 256); fp32 holds it to within ulp(mu), so rows whose maximum reaches
-      // 2^21 (scores beyond any real model's) clamp it there, keeping l and
-      // P alike and P finite.
+      // per store
       float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      auto emit = [&](auto clamp) {
+      {
         constexpr int kQuarter = kKv / 8;  // f16 pairs per quarter of the keys
 #pragma unroll
         for (int kq = 0; kq < 4; ++kq) {
@@ -316,22 +328,18 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp8_kernel(
 #pragma unroll
           for (int i = 0; i < kQuarter; ++i) {
             const int e2 = kq * kQuarter + i;
-            float2 a = ffma2(make_float2(__uint_as_float(x[2 * e2]), __uint_as_float(x[2 * e2 + 1])), sc2, nmu2);
-            if (decltype(clamp)::value) a = make_float2(fminf(a.x, kLazy), fminf(a.y, kLazy));
+            const float2 a = ffma2(make_float2(__uint_as_float(x[2 * e2]), __uint_as_float(x[2 * e2 + 1])),
+                                   sc2, nmu2);
             const float2 pe = make_float2(fast_exp2(a.x), fast_exp2(a.y));
             l2[i & 1] = fadd2(l2[i & 1], pe);
             wp[i] = pack_f16x2(pe.x, pe.y);
           }
           tmem_st16_nowait(lane_base + kq * kQuarter, wp);
         }
-      };
-      if (__any_sync(0xffffffffu, fabsf(mu) >= 0x1p21f))
-        emit(std::true_type{});
-      else
-        emit(std::false_type{});
+      }
       tmem_wait_st();
       if (__any_sync(0xffffffffu, rescale)) {
-        const float alpha = rescale ? fast_exp2(m_old - m_new) : 1.f;
+        const float alpha = rescale ? fast_exp2((m_old - m_raw) * coef) : 1.f;
         l_run *= alpha;
 #pragma unroll
         for (int c0 = 0; c0 < kD; c0 += 32) {

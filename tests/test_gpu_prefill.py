@@ -160,11 +160,12 @@ def test_prefill_host_checks():
     c = torch.tensor([4], dtype=torch.int32, device="cuda")
     with pytest.raises(pagedkv.KVError):
         pagedkv.paged_prefill_attention(pool, q, cu, t, c, 0.1, max_q_len=4, max_context_len=64)
-    fp4 = pagedkv.KVPool(8, 16, 2, 128, "fp4")              # FP4 pools have no prefill
+    d64 = pagedkv.KVPool(8, 16, 2, 64)                      # head_dim 64: no prefill
+    q64 = torch.zeros(4, 4, 64, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(pagedkv.KVError):
-        pagedkv.paged_prefill_attention(fp4, q, cu, t, c, 0.1, max_q_len=4, max_context_len=4)
+        pagedkv.paged_prefill_attention(d64, q64, cu, t, c, 0.1, max_q_len=4, max_context_len=4)
     pool.destroy()
-    fp4.destroy()
+    d64.destroy()
 
 
 @pytest.mark.parametrize("bs", [16, 32])
@@ -212,4 +213,21 @@ def test_prefill_negative_and_zero_scale(scale):
     assert pool.check_status() == pagedkv.KV_OK
     ref = opool.prefill(q, cu, tables, lens, scale, 100)
     _check(out, ref, f"scale={scale}")
+    pool.destroy()
+
+
+def test_prefill_query_rows_of_any_magnitude():
+    """Rows of q scaled by 2^-30 .. 2^30 (and an all-zero row): scores up to
+    ~2^32 in log2 units, where the exponent of the maximum key must still
+    come out exact (the row is then its maximum key's value)."""
+    pool, opool, q, cu, tables, lens = _build([300], [64], 8, 2, seed=21)
+    f = torch.tensor([2.0 ** e for e in range(-30, 31, 4)] + [0.0])
+    rows = q.float().view(64 * 8, 128)
+    rows[: f.numel()] *= f.view(-1, 1)
+    q = rows.view(64, 8, 128).bfloat16()
+    out = _run(pool, q, cu, tables, lens, 0.05)
+    torch.cuda.synchronize()
+    assert pool.check_status() == pagedkv.KV_OK
+    ref = opool.prefill(q, cu, tables, lens, 0.05)
+    _check(out, ref, "query magnitudes")
     pool.destroy()

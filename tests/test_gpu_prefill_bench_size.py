@@ -1,14 +1,14 @@
 """Prefill parity at the sizes bench.py times: full causal prefills of 4 x 2,048
 and 4 x 8,192 tokens with 32 query / 8 KV heads, head_dim 128, 16-token
-blocks in shuffled tables, over bf16 and FP8 pools, launched as the bench
+blocks in shuffled tables, over bf16, FP8 and FP4 pools, launched as the bench
 launches them (one call for the whole batch).
 
 The oracle computes sampled output rows one by one: token i of sequence b is
 the last (only) new token of a prefill whose context ends at its position, so
 a one-token oracle prefill over the same pool and table gives its row.  The
 samples cover the first and last tokens, block edges and 128-key tile edges.
-Bars: bf16 the decode's (max |err| 2e-3, relative L2 1e-3); FP8 the FP8 bar
-(3e-2) and the relative L2 bound of its tests (1e-2).
+Bars: bf16 and FP4 the decode's bf16 bar (max |err| 2e-3, relative L2 1e-3);
+FP8 the FP8 bar (3e-2) and the relative L2 bound of its tests (1e-2).
 """
 
 import numpy as np
@@ -26,7 +26,7 @@ HQ, HKV, D, BS = 32, 8, 128, 16
 
 
 @pytest.mark.parametrize("ctx", [2048, 8192])
-@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "fp4"])
 def test_prefill_bench_size_sampled_rows(dtype, ctx):
     B = 4
     nblk = ctx // BS
@@ -39,8 +39,8 @@ def test_prefill_bench_size_sampled_rows(dtype, ctx):
     slots = (tables[:, pos // BS].astype(np.int64) * BS + pos % BS).reshape(-1)
     pool = pagedkv.KVPool(B * nblk, BS, HKV, D, dtype)
     opool = oracle.Pool(B * nblk, BS, HKV, D, dtype)
-    if dtype == "fp8":
-        sc = np.full(HKV, 4.5 / 448, np.float32)   # randn bf16: |x| < 4.5 at these sizes
+    if dtype in ("fp8", "fp4"):   # randn bf16: |x| < 4.5 at these sizes
+        sc = np.full(HKV, 4.5 / (448 if dtype == "fp8" else 6 * 448), np.float32)
         pool.set_scales(torch.from_numpy(sc).cuda(), torch.from_numpy(sc).cuda())
         opool.set_scales(sc, sc)
     pagedkv.paged_kv_write(pool, k.cuda(), v.cuda(), torch.from_numpy(slots).cuda())
@@ -67,8 +67,8 @@ def test_prefill_bench_size_sampled_rows(dtype, ctx):
     max_abs, rel = errors(got, ref)
     print(f"PARITY prefill bench-size {dtype} 4x{ctx} ({len(samples)} rows) "
           f"max_abs={max_abs:.3e} rel_l2={rel:.3e}")
-    if dtype == "bf16":
-        assert max_abs <= BF16_MAX_ABS and rel <= BF16_REL_L2
-    else:
+    if dtype == "fp8":
         assert max_abs <= FP8_MAX_ABS and rel <= 1e-2
+    else:   # bf16, and FP4 (values exact in f16)
+        assert max_abs <= BF16_MAX_ABS and rel <= BF16_REL_L2
     pool.destroy()
