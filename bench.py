@@ -551,10 +551,10 @@ def measure_extras(step: Step, peaks: dict, device) -> dict:
     #    (short prompts: per-CTA set-up weighs more) and 4 x 8192 tokens, over
     #    bf16, FP8 and FP4 pools.  The FP8 products run at twice the bf16 rate
     #    (the nominal ratio, 4.5 / 2.25 PFLOP/s dense, applied to the measured
-    #    bf16 peak); the FP4 kernel's are f16 ones (the bf16 rate).  Issued
-    #    tensor work per algorithmic flop, in units of the peak used: bf16 1.5
-    #    (P V twice: P's high part and remainder), FP8 2 (Q K^T twice on E4M3;
-    #    P V once on f16, at half the E4M3 rate), FP4 1
+    #    bf16 peak); the bf16 and FP4 kernels' are bf16 / f16 ones (the bf16
+    #    rate).  Issued tensor work per algorithmic flop, in units of the peak
+    #    used: bf16 1, FP8 2 (Q K^T twice on E4M3; P V once on f16, at half
+    #    the E4M3 rate), FP4 1
     bf16_peak = peaks["bf16_tflops"]
     for key, dt, (B, ctx) in (("paged_prefill_attention", "bf16", (4, 2048)),
                               ("paged_prefill_attention_long", "bf16", (4, 8192)),
@@ -585,7 +585,7 @@ def measure_extras(step: Step, peaks: dict, device) -> dict:
         flops = 4.0 * 128 * hq * B * (ctx * (ctx + 1) // 2)   # QK and PV over the causal keys
         tf = flops / t / 1e12
         peak = bf16_peak * (2.0 if dt == "fp8" else 1.0)
-        issued = {"bf16": 1.5, "fp8": 2.0, "fp4": 1.0}[dt]
+        issued = {"bf16": 1.0, "fp8": 2.0, "fp4": 1.0}[dt]
         out[key] = {
             "workload": f"full causal prefill, {B} x {ctx} tokens, {hq} q / {hkv} KV heads, "
                         f"head_dim 128, 16-token blocks, {dt} pool",

@@ -302,9 +302,12 @@ kv_status paged_decode_attention_noalloc(kv_pool* pool, const void* q_dev, int32
  *                      max(0, pos + 1 - sliding_window) when the window is on.
  * bf16, FP8 and FP4 pools with head_dim 128 and a query group of at most 8
  * heads per KV head (other shapes: KV_ERR_UNSUPPORTED).  Runs on the tcgen05
- * tensor cores.  bf16: P enters the P V product as a bf16 high part
- * plus the bf16 rounding of its remainder (two products into the same
- * accumulator), so the result meets the decode's bf16 accuracy.  FP8: Q K^T
+ * tensor cores.  bf16: Q K^T on bf16 operands; P V on f16 ones, P rounded
+ * once to f16 and V converted to f16 scaled by a power of two (set from the
+ * largest V of the key tiles seen so far, raised when a later tile would
+ * overflow), which keeps every V value exact whose magnitude is at least
+ * 2^-31 times that largest one (smaller ones are off by at most 2^-39 of
+ * it); the result meets the decode's bf16 accuracy.  FP8: Q K^T
  * takes E4M3 operands -- the K codes as stored, each query row scaled by a
  * power of two and split into an E4M3 code and the code of its remainder --
  * and P V f16 ones (P rounded once to f16, the V codes converted exactly),

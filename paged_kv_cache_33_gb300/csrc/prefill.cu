@@ -20,12 +20,17 @@
 //    stage is refilled as soon as the S products of its tile are done, a V
 //    stage once its P V products are.  Blocks outside the attended range or
 //    with a bad id are left out and their rows masked.
-//  * One thread issues tcgen05.mma: S = Q K^T (128 x 128, fp32 in tensor
-//    memory), then O += P_hi V + P_lo V (128 x 128, fp32 in tensor memory)
-//    with P read from tensor memory and V read MN-major straight from its
-//    pool rows.  P is a bf16 high part plus the bf16 rounding of its
-//    remainder: one bf16 P alone (2^-9 relative per weight) would put the
-//    output ~1e-3 (relative) off the exact attention.
+//  * S = Q K^T on kind::f16 with bf16 operands (128 x 128, fp32 in tensor
+//    memory).  P V on kind::f16 with f16 operands: P is one f16 per weight
+//    (relative rounding 2^-12 on average, where one bf16 P, 2^-9, would put
+//    the output ~1e-3 off the exact attention), so V is converted to f16 in
+//    place in its stage by a converter warpgroup, scaled by a power of two
+//    2^-e: every bf16 value whose magnitude lies within 2^29 below the
+//    largest V the CTA has seen is exact in f16 then.  e is set from the
+//    first key tile's largest exponent (0 when its values sit in f16's own
+//    range) and raised when a later tile would overflow; the softmax
+//    warps rescale O by the change, and the output by 2^e.  Rows past the
+//    sequence's end and of blocks not loaded become zeros.
 //    128-key products run the tensor pipe at its full rate; 64-key ones
 //    reach two thirds of it.
 //  * Two query tiles share every key tile and alternate on the tensor pipe:
@@ -33,16 +38,17 @@
 //    Each tile has one S buffer: S of the next key tile is issued once the
 //    P V product that reads P from it has completed (products with different
 //    accumulators are not ordered), so a finished S also means O is stable.
-//  * Four softmax warps per query tile own one row each per thread: one
-//    tensor-memory load of the row of S (128 columns), masking (causal, window, sequence end, missing blocks),
-//    online softmax in the exp2 domain with a lazy maximum (O in tensor
-//    memory is rescaled only when a row's maximum grows by more than 2^8),
-//    P's two bf16 parts back over the columns of S (P never touches shared
-//    memory, whose bandwidth the products' operand reads use), and zeros into
-//    the V rows the product must not see (slots past the sequence's end,
-//    blocks not loaded).  The epilogue divides O by the row sum and stores
-//    the valid rows through a per-warp staging area in the tile's (then
-//    unused) Q buffer, so that every store instruction writes whole rows.
+//  * Four softmax warps per query tile own one row each per thread: two
+//    tensor-memory loads of the row of S (128 columns), masking (causal,
+//    window, sequence end, missing blocks), online softmax in the exp2
+//    domain with a lazy maximum (O in tensor memory is rescaled only when a
+//    row's maximum grows by more than 2^8), P as f16 pairs back over the
+//    first 64 columns of S.  The epilogue divides O by the row sum and
+//    stores the valid rows through a per-warp staging area in the tile's
+//    (then unused) Q buffer, so that every store instruction writes whole
+//    rows.
+//  * Registers: the two softmax warpgroups take 192 per thread, the
+//    producer / issuer and converter warpgroups give theirs up to 64.
 //  * Every wait is bounded in wall time; on a timeout the CTA records
 //    KV_ERR_TIMEOUT, drains what it issued and frees its tensor memory.
 
@@ -59,11 +65,20 @@ constexpr int kRows = 128;           // query rows per tile (M)
 constexpr int kTiles = 2;            // query tiles per CTA, alternating over the same keys
 constexpr int kKv = 128;             // keys per key tile (N of S, K of P V)
 constexpr int kKStages = 2;          // K ring
-constexpr int kVStages = 3;          // V ring
+constexpr int kVStages = 3;          // V ring (bf16 as copied, then f16 in place)
 constexpr int kSoftmax = kTiles * kRows;      // one softmax thread per query row
-constexpr int kThreads = kSoftmax + 96;       // + K producer, V producer, MMA warps
 constexpr int kKWarp = kSoftmax / 32, kVWarp = kKWarp + 1, kMmaWarp = kVWarp + 1;
+constexpr int kCvtWarp = kKWarp + 4;          // converter warpgroup (warp kKWarp + 3 is idle)
+constexpr int kCvt = 128;
+constexpr int kThreads = kSoftmax + 128 + kCvt;
+constexpr int kLaunchRegs = 65536 / kThreads;
+constexpr int kSoftmaxRegs = 192, kOtherRegs = 64;
+static_assert(2 * kSoftmaxRegs + 2 * kOtherRegs <= 4 * kLaunchRegs,
+              "register increases must be covered by the decreases");
 constexpr float kLazy = 8.f;         // rescale O when a row maximum grows by more than this (log2)
+// V's power of two: e = E - kVBias for a largest biased bf16 exponent E puts
+// the largest magnitude in [2^14, 2^15)
+constexpr int kVBias = 141, kVMin = -126, kVMax = 113;
 constexpr uint64_t kShortWaitNs = 200000;
 
 // Shared memory (offsets from a 1024-aligned base).
@@ -72,15 +87,19 @@ constexpr int kQTile = 2 * kRows * 128;
 constexpr int kKvStage = 2 * kKv * 128;               // 2 column halves x [128 keys][64] bf16
 constexpr int kK = kQ + kTiles * kQTile;
 constexpr int kV = kK + kKStages * kKvStage;
-constexpr int kBars = kV + kVStages * kKvStage;
-// barriers: k_full[2], k_empty[2], v_full[3], v_empty[3], per tile s_full, p_full,
-// pv_done, o_final; q_full, mma_done
-constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 4 * kTiles + 2;
+constexpr int kVe = kV + kVStages * kKvStage;         // int32 [kVStages]: each stage's e
+constexpr int kVMask = kVe + 16;                      // uint32 [kVStages]: blocks each V stage holds
+constexpr int kEx = kVMask + 16;                      // uint32 [2][4]: converter warps' maxima
+constexpr int kBars = kEx + 32;
+static_assert(kVStages * 4 <= 16, "the V stages' exponents and block masks fit");
+// barriers: k_full[2], k_empty[2], v_full[3], v_empty[3], v16_full[3], per tile
+// s_full, p_full, pv_done, o_final; q_full, mma_done, ex_full
+constexpr int kNumBars = 2 * kKStages + 3 * kVStages + 4 * kTiles + 3;
 constexpr int kTmemSlot = kBars + kNumBars * 8;
 constexpr int kSmemBytes = kTmemSlot + 16 + 1024;     // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
-// tensor memory per query tile: S [0,128) (P_hi over its first 64 columns, P_lo over
-// the last 64), O [128,256)
+// tensor memory per query tile: S [0,128) (P as f16 pairs over its first 64 columns),
+// O [128,256)
 constexpr uint32_t kOCol = kKv;
 constexpr uint32_t kTmemTile = 256;
 constexpr uint32_t kTmemCols = kTiles * kTmemTile;
@@ -88,6 +107,32 @@ constexpr uint32_t kTmemCols = kTiles * kTmemTile;
 __device__ __forceinline__ int swz128(int row, int chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
 }
+
+// Lane-wise larger magnitude of two bf16 pairs (the sign bits are not used).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// a * b on two fp32 lanes at once.
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(reinterpret_cast<const uint64_t&>(a)), "l"(reinterpret_cast<const uint64_t&>(b)));
+  return reinterpret_cast<const float2&>(d);
+}
+
+// The two bf16 of a word, times s, as an f16 pair (exact while the products
+// are normal in f16).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, float2 s) {
+  const float2 f = fmul2(make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)), s);
+  return pack_f16x2(f.x, f.y);
+}
+
+// 2^e as a float, e in [-126, 127].
+__device__ __forceinline__ float pow2i(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
 
 template <int BS>
 __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
@@ -143,14 +188,18 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   auto k_empty = [&](int s) { return bar0 + 8u * (kKStages + s); };
   auto v_full = [&](int s) { return bar0 + 8u * (2 * kKStages + s); };
   auto v_empty = [&](int s) { return bar0 + 8u * (2 * kKStages + kVStages + s); };
-  constexpr int kTileBars = 2 * kKStages + 2 * kVStages;
+  auto v16_full = [&](int s) { return bar0 + 8u * (2 * kKStages + 2 * kVStages + s); };
+  constexpr int kTileBars = 2 * kKStages + 3 * kVStages;
   auto s_full = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t); };
   auto p_full = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t + 1); };
   auto pv_done = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t + 2); };
   auto o_final = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t + 3); };
   const uint32_t q_full = bar0 + 8u * (kTileBars + 4 * kTiles);
   const uint32_t mma_done = q_full + 8;
+  const uint32_t ex_full = q_full + 16;  // the converter warps' maxima are in
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
+  int* v_e = reinterpret_cast<int*>(smem + kVe);
+  uint32_t* v_mask = reinterpret_cast<uint32_t*>(smem + kVMask);
 
   if (tid == 0) {
     for (int s = 0; s < kKStages; ++s) {
@@ -160,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
+      mbar_init(v16_full(s), kCvt);
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(s_full(t), 1);
@@ -169,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     }
     mbar_init(q_full, kSoftmax);
     mbar_init(mma_done, 1);
+    mbar_init(ex_full, kCvt);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -179,8 +230,16 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   auto wait = [&](uint32_t bar, uint32_t parity) {
     return mbar_wait_bounded(bar, parity, p.wait_limit_ns, p.err, kErrTimeout, kShortWaitNs);
   };
+  // Which blocks of key tile jt are loaded (inside [kv_begin, kv_end), a
+  // table entry inside the pool): the rule every role applies.
+  const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.mbs;
+  auto needed = [&](int jt, int i) {
+    const int k0 = (jt0 + jt) * kKv + i * BS;
+    return k0 + BS > kv_begin && k0 < kv_end;
+  };
 
   if (warp < kKWarp) {
+    warpgroup_regs_inc<kSoftmaxRegs>();
     // ====== softmax warps: warps 4t..4t+3 serve query tile t, one row per thread
     const int t = warp >> 2;
     const int r = tid & (kRows - 1);
@@ -189,7 +248,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     const int tok = tok0 + t * tpt + tq;
     const int pos = pos_base + tok;
     const int lo = p.window > 0 ? max(0, pos + 1 - p.window) : 0;
-    const int hq = h * g + jh;
     // Q of both tiles -> shared memory (zeros for padding rows), coalesced:
     // 16 threads per row, so one load instruction reads two whole 256-byte
     // rows of q
@@ -215,19 +273,16 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(q_full) : "memory");
     }
     const uint32_t lane_base = tmem + t * kTmemTile + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const float coef = p.scale_log2;
     constexpr uint32_t kAllBlocks = (1u << (kKv / BS)) - 1u;
     float m_raw = -INFINITY, l_run = 0.f;  // running maximum in raw score units
+    int ve = 0;                            // V's power of two in the products so far
     bool ok = true;
     const int nt = t ? n_kv1 : n_kv0;
     // Which blocks of a key tile hold keys: the same rule the producers use
     // (inside [kv_begin, kv_end), a table entry inside the pool), from the
     // table entries read one key tile ahead, so the softmax never waits for
     // the V copy it does not read.
-    const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.mbs;
-    auto needed = [&](int jt, int i) {
-      const int k0 = (jt0 + jt) * kKv + i * BS;
-      return k0 + BS > kv_begin && k0 < kv_end;
-    };
     int next[kKv / BS];
     auto fetch = [&](int jt) {
 #pragma unroll
@@ -241,14 +296,16 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       for (int i = 0; i < kKv / BS; ++i)
         if (next[i] >= 0 && next[i] < p.num_blocks) mask |= 1u << i;
       if (jt + 1 < nt) fetch(jt + 1);
-      const int sv = jt % kVStages;
       ok = wait(s_full(t), jt & 1);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       const int key0 = (jt0 + jt) * kKv;
-      // the row of S: one tensor-memory load of all kKv columns
+      // the row of S, two loads of 64 columns (an instruction may not name
+      // more registers than the launch gives a thread) and one wait
       uint32_t x[kKv];
-      tmem_ld128(lane_base, x);
+      tmem_ld64_nowait(lane_base, *reinterpret_cast<uint32_t(*)[64]>(&x[0]));
+      tmem_ld64_nowait(lane_base + 64, *reinterpret_cast<uint32_t(*)[64]>(&x[64]));
+      tmem_wait_ld();
       // rows of this warp that see every key of the tile need no mask;
       // masked keys become -inf (the scale is applied in the exp)
       if (!__all_sync(0xffffffffu, row_ok && key0 >= lo && key0 + kKv - 1 <= pos &&
@@ -269,16 +326,16 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       // maximum is kept in raw score units (the scale is positive), so the
       // rescale and, for large scores, the exponents come from exact
       // differences of raw scores.
-      const float coef = p.scale_log2;
       const bool rescale = m_raw != -INFINITY && mt_raw != -INFINITY && (mt_raw - m_raw) * coef > kLazy;
       const float m_old = m_raw;
       if (m_raw == -INFINITY || rescale) m_raw = mt_raw;
       const float mr = m_raw == -INFINITY ? 0.f : m_raw;
       float mu = mr * coef;
-      // The exponent (x - m) coef is at most kLazy, taken as one FMA against
-      // m coef.  Once |m coef| reaches 2^13 fp32 holds it only to within
-      // 2^-11 (scores of no real model get there): such warps first subtract
-      // m from their raw scores, exactly near the maximum, and use no offset.
+      // The exponent (x - m) coef is at most kLazy (p <= 256), taken as one
+      // FMA against m coef.  Once |m coef| reaches 2^13 fp32 holds it only
+      // to within 2^-11 (scores of no real model get there): such warps
+      // first subtract m from their raw scores, exactly near the maximum,
+      // and use no offset.
       if (__any_sync(0xffffffffu, fabsf(mu) >= 0x1p13f)) {
         const float2 nmr2 = make_float2(-mr, -mr);
 #pragma unroll
@@ -290,76 +347,60 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         mu = 0.f;
       }
       const float2 sc2 = make_float2(coef, coef), nmu2 = make_float2(-mu, -mu);
-      // the exponentials; P as a bf16 high part (pairs over the first kKv/2
-      // columns of S) and the bf16 rounding of its remainder (the last kKv/2
-      // columns), so ~16 significant bits of every weight reach the products.
-      // Each quarter of the keys is stored as soon as it is done (its S
-      // columns were read into registers above), which keeps few registers
-      // live; one wait covers the stores.
+      // P as f16 pairs over the first 64 columns of S, a quarter of the keys
+      // per store
       float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      constexpr int kQuarter = kKv / 8;  // bf16 pairs per quarter of the keys
+      {
+        constexpr int kQuarter = kKv / 8;  // f16 pairs per quarter of the keys
 #pragma unroll
-      for (int kq = 0; kq < 4; ++kq) {
-        uint32_t wh[kQuarter], wl[kQuarter];
+        for (int kq = 0; kq < 4; ++kq) {
+          uint32_t wp[kQuarter];
 #pragma unroll
-        for (int i = 0; i < kQuarter; ++i) {
-          const int e = kq * kQuarter + i;
-          const float2 arg = ffma2(make_float2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])),
+          for (int i = 0; i < kQuarter; ++i) {
+            const int e2 = kq * kQuarter + i;
+            const float2 a = ffma2(make_float2(__uint_as_float(x[2 * e2]), __uint_as_float(x[2 * e2 + 1])),
                                    sc2, nmu2);
-          const float2 pe = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
-          l2[i & 1] = fadd2(l2[i & 1], pe);
-          wh[i] = pack_bf16x2(pe.x, pe.y);
-          const float2 rem = fsub2(pe, make_float2(bf16_lo(wh[i]), bf16_hi(wh[i])));
-          wl[i] = pack_bf16x2(rem.x, rem.y);
+            const float2 pe = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+            l2[i & 1] = fadd2(l2[i & 1], pe);
+            wp[i] = pack_f16x2(pe.x, pe.y);
+          }
+          tmem_st16_nowait(lane_base + kq * kQuarter, wp);
         }
-        tmem_st16_nowait(lane_base + kq * kQuarter, wh);
-        tmem_st16_nowait(lane_base + kKv / 2 + kq * kQuarter, wl);
       }
       tmem_wait_st();
-      // O is stable: S of this key tile was issued only after the tile's
-      // previous P V product had completed
-      if (__any_sync(0xffffffffu, rescale)) {  // tensor-memory access is warp-wide
+      // V's power of two for this key tile (its P V product cannot be issued
+      // before the conversion anyway); a raised one scales what O holds down
+      const int sv = jt % kVStages;
+      ok = wait(v16_full(sv), (jt / kVStages) & 1);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      const int ve_j = v_e[sv];
+      const bool vchange = jt > 0 && ve_j != ve;
+      if (__any_sync(0xffffffffu, rescale) || vchange) {  // tensor-memory access is warp-wide
         const float alpha = rescale ? fast_exp2((m_old - m_raw) * coef) : 1.f;
         l_run *= alpha;
+        const float f = vchange ? alpha * pow2i(max(ve - ve_j, kVMin)) : alpha;
 #pragma unroll
         for (int c0 = 0; c0 < kD; c0 += 32) {
           uint32_t o[32];
           tmem_ld32(lane_base + kOCol + c0, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
           tmem_st32(lane_base + kOCol + c0, o);
         }
       }
+      ve = ve_j;
       l_run += (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
-      // V rows the products must not see: slots past the sequence's end and
-      // blocks that were not loaded (stale or never-written shared memory).
-      // The first query tile that uses this key tile does it before handing
-      // its P over; the product of the other tile is issued after that.
-      const int zero_tile = jt < n_kv0 ? 0 : 1;
-      if (t == zero_tile && (mask != kAllBlocks || key0 + kKv > ctx)) {
-        // the V stage of this key tile cannot be refilled before this tile's
-        // P of it is consumed, so its phase is safe to wait on here
-        ok = wait(v_full(sv), (jt / kVStages) & 1);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        for (int idx = r; idx < kKv * 2 * 8; idx += kRows) {
-          const int key = idx >> 4, half = (idx >> 3) & 1, chunk = idx & 7;
-          if (key0 + key >= ctx || !((mask >> (key / BS)) & 1u))
-            *reinterpret_cast<uint4*>(smem + kV + sv * kKvStage + half * (kKv * 128) + key * 128 +
-                                      chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      fence_proxy_async_smem();
       tc_fence_before();
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(p_full(t)) : "memory");
     }
     if (ok && nt > 0) ok = __all_sync(0xffffffffu, wait(o_final(t), 0));
     if (ok && nt > 0) {
       tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      // O / l -> out, coalesced: each warp stages its 32 rows, 64 columns at a
-      // time, in shared memory (the tile's Q buffer, free once the tile's last
-      // product is done; 16-byte chunk c of row r at slot c ^ (r & 15)), then
-      // stores two whole 256-byte row halves per instruction.
+      const float inv = l_run > 0.f ? pow2i(ve) / l_run : 0.f;
+      // O 2^e / l -> out, coalesced: each warp stages its 32 rows, 64 columns
+      // at a time, in shared memory (the tile's Q buffer, free once the tile's
+      // last product is done; 16-byte chunk c of row r at slot c ^ (r & 15)),
+      // then stores two whole 256-byte row halves per instruction.
       uint8_t* stg = smem + kQ + t * kQTile + (warp & 3) * (32 * 256);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -391,161 +432,226 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         __syncwarp();
       }
     }
-  } else if (warp == kKWarp || warp == kVWarp) {
-    // =========================== producers: the K rows (one warp) and the V
-    // rows (the other) of each key tile, each into its own ring
-    if (lane == 0) {
-      const bool is_v = warp == kVWarp;
-      const int stages = is_v ? kVStages : kKStages;
-      const int rows = is_v ? 1 : 0;  // the pool's K / V index
-      uint8_t* ring = smem + (is_v ? kV : kK);
-      auto full = [&](int s) { return is_v ? v_full(s) : k_full(s); };
-      auto empty = [&](int s) { return is_v ? v_empty(s) : k_empty(s); };
-      // The block-table entries of a key tile are read one tile ahead, so
-      // their global-memory latency overlaps the wait for a free stage.
-      const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.mbs;
-      auto needed = [&](int jt, int i) {
-        const int k0 = (jt0 + jt) * kKv + i * BS;
-        return k0 + BS > kv_begin && k0 < kv_end;
+  } else if (warp >= kCvtWarp) {
+    warpgroup_regs_dec<kOtherRegs>();
+    // ====== converters: each V stage, bf16 as copied, into f16 in place.
+    // Thread ct takes the 16-byte chunks ct + 128 i (i < 16) of the stage's
+    // two column halves: key row ct / 8 + 16 (i mod 8), a whole 512-byte run
+    // of the stage per warp and instruction.  Two passes: the largest
+    // exponent of the rows that hold keys, then the conversion, scaled by
+    // the power of two that keeps it exact; rows without a key are zeroed.
+    const int ct = tid - kCvtWarp * 32;
+    uint32_t* ex = reinterpret_cast<uint32_t*>(smem + kEx);
+    int e = 0, nred = 0;
+    bool ok = true;
+    for (int jt = 0; jt < n_tiles && ok; ++jt) {
+      const int s = jt % kVStages;
+      ok = wait(v_full(s), (jt / kVStages) & 1);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      const uint32_t mask = v_mask[s];  // the blocks the stage holds, left by the V producer
+      const int key0 = (jt0 + jt) * kKv;
+      constexpr uint32_t kAllBlocks = (1u << (kKv / BS)) - 1u;
+      const bool full = mask == kAllBlocks && key0 + kKv <= ctx;
+      const uint32_t st = smem_addr(smem + kV + s * kKvStage) + 16 * ct;
+      auto row_ok = [&](int i) {
+        const int key = (ct >> 3) + 16 * (i & 7);
+        return full || (((mask >> (key / BS)) & 1u) && key0 + key < ctx);
       };
-      int next[kKv / BS];
-      auto fetch = [&](int jt) {
-#pragma unroll
-        for (int i = 0; i < kKv / BS; ++i)
-          next[i] = needed(jt, i) ? trow[((jt0 + jt) * kKv + i * BS) / BS] : 0;
-      };
-      if (n_tiles > 0) fetch(0);
-      int issued = 0;
-      for (int jt = 0; jt < n_tiles; ++jt) {
-        const int s = jt % stages;
-        int cur[kKv / BS];
-#pragma unroll
-        for (int i = 0; i < kKv / BS; ++i) cur[i] = next[i];
-        if (jt + 1 < n_tiles) fetch(jt + 1);
-        if (jt >= stages && !wait(empty(s), ((jt / stages) - 1) & 1)) break;
-        uint32_t mask = 0;
-        int phys[kKv / BS];
-#pragma unroll
-        for (int i = 0; i < kKv / BS; ++i) {
-          phys[i] = -1;
-          if (!needed(jt, i)) continue;
-          const int e = cur[i];
-          if (e < 0 || e >= p.num_blocks) {
-            if (!is_v) atomicOr(p.err, kErrBadBlock);
-            continue;
-          }
-          phys[i] = e;
-          mask |= 1u << i;
+      uint32_t em = 0;
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        if (!row_ok(i)) continue;
+        const uint4 v = lds128(st + 2048 * i);
+        em = absmax_bf16x2(em, absmax_bf16x2(absmax_bf16x2(v.x, v.y), absmax_bf16x2(v.z, v.w)));
+      }
+      em &= 0x7F807F80u;
+      em = __reduce_max_sync(0xffffffffu, max(em & 0xFFFFu, em >> 16));
+      if (lane == 0) ex[(nred & 1) * 4 + (warp - kCvtWarp)] = em;
+      // every converter thread arrives; a phase completes once all four
+      // warps' maxima are written (two slots alternate, so a warp already on
+      // the next tile cannot overwrite the slot a slower one still reads)
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ex_full) : "memory");
+      ok = wait(ex_full, nred & 1);
+      ++nred;
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      {
+        const uint32_t* xr = ex + ((nred - 1) & 1) * 4;
+        const int E = static_cast<int>(max(max(xr[0], xr[1]), max(xr[2], xr[3])) >> 7);
+        // the first tile sets e; later tiles only raise it, when they would
+        // overflow
+        if (jt == 0)
+          e = min(max(E - kVBias, kVMin), kVMax);
+        else if (E - kVBias > e)
+          e = min(E - kVBias, kVMax);
+      }
+      const float2 sc = make_float2(pow2i(-e), pow2i(-e));
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (row_ok(i)) {
+          const uint4 v = lds128(st + 2048 * i);
+          o = make_uint4(bf16x2_to_f16x2(v.x, sc), bf16x2_to_f16x2(v.y, sc), bf16x2_to_f16x2(v.z, sc),
+                         bf16x2_to_f16x2(v.w, sc));
         }
-        const uint32_t bar = full(s);
-        const int nblk = __popc(mask);
-        if (nblk == 0) {
-          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-        } else {
-          mbar_arrive_expect_tx(bar, nblk * 2 * BS * 128);
-          const uint32_t st = smem_addr(ring + s * kKvStage);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + 2048 * i), "r"(o.x), "r"(o.y),
+                     "r"(o.z), "r"(o.w) : "memory");
+      }
+      if (ct == 0) v_e[s] = e;
+      fence_proxy_async_smem();
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(v16_full(s)) : "memory");
+    }
+  } else {
+    warpgroup_regs_dec<kOtherRegs>();
+    if (warp == kKWarp || warp == kVWarp) {
+      // ========================= producers: the K rows (one warp) and the V
+      // rows (the other) of each key tile, each into its own ring
+      if (lane == 0) {
+        const bool is_v = warp == kVWarp;
+        const int stages = is_v ? kVStages : kKStages;
+        const int rows = is_v ? 1 : 0;  // the pool's K / V index
+        uint8_t* ring = smem + (is_v ? kV : kK);
+        auto full = [&](int s) { return is_v ? v_full(s) : k_full(s); };
+        auto empty = [&](int s) { return is_v ? v_empty(s) : k_empty(s); };
+        // The block-table entries of a key tile are read one tile ahead, so
+        // their global-memory latency overlaps the wait for a free stage.
+        int next[kKv / BS];
+        auto fetch = [&](int jt) {
+#pragma unroll
+          for (int i = 0; i < kKv / BS; ++i)
+            next[i] = needed(jt, i) ? trow[((jt0 + jt) * kKv + i * BS) / BS] : 0;
+        };
+        if (n_tiles > 0) fetch(0);
+        int issued = 0;
+        for (int jt = 0; jt < n_tiles; ++jt) {
+          const int s = jt % stages;
+          int cur[kKv / BS];
+#pragma unroll
+          for (int i = 0; i < kKv / BS; ++i) cur[i] = next[i];
+          if (jt + 1 < n_tiles) fetch(jt + 1);
+          if (jt >= stages && !wait(empty(s), ((jt / stages) - 1) & 1)) break;
+          uint32_t mask = 0;
+          int phys[kKv / BS];
 #pragma unroll
           for (int i = 0; i < kKv / BS; ++i) {
-            if (phys[i] < 0) continue;
-            const int tile = phys[i] * p.n_kv_heads + h;
-#pragma unroll
-            for (int half = 0; half < 2; ++half)
-              tma_load_4d(st + half * (kKv * 128) + i * BS * 128, &tmap, bar, half * 64, 0, rows,
-                          tile);
+            phys[i] = -1;
+            if (!needed(jt, i)) continue;
+            const int e = cur[i];
+            if (e < 0 || e >= p.num_blocks) {
+              if (!is_v) atomicOr(p.err, kErrBadBlock);
+              continue;
+            }
+            phys[i] = e;
+            mask |= 1u << i;
           }
+          const uint32_t bar = full(s);
+          const int nblk = __popc(mask);
+          if (is_v) v_mask[s] = mask;  // for the converters (published by the arrive below)
+          if (nblk == 0) {
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+          } else {
+            mbar_arrive_expect_tx(bar, nblk * 2 * BS * 128);
+            const uint32_t st = smem_addr(ring + s * kKvStage);
+#pragma unroll
+            for (int i = 0; i < kKv / BS; ++i) {
+              if (phys[i] < 0) continue;
+              const int tile = phys[i] * p.n_kv_heads + h;
+#pragma unroll
+              for (int half = 0; half < 2; ++half)
+                tma_load_4d(st + half * (kKv * 128) + i * BS * 128, &tmap, bar, half * 64, 0, rows,
+                            tile);
+            }
+          }
+          ++issued;
         }
-        ++issued;
+        // leave no copy in flight: wait (bounded) for the stages not yet consumed
+        for (int jt = max(0, issued - stages); jt < issued; ++jt)
+          if (!wait(full(jt % stages), (jt / stages) & 1)) atomicOr(p.err, kErrDrainTimeout);
       }
-      // leave no copy in flight: wait (bounded) for the stages not yet consumed
-      for (int jt = max(0, issued - stages); jt < issued; ++jt)
-        if (!wait(full(jt % stages), (jt / stages) & 1)) atomicOr(p.err, kErrDrainTimeout);
-    }
-    __syncwarp();
-  } else {
-    // =========================== MMA issuer.  Key tile jt: for each query
-    // tile, the P V product of key tile jt - 1 (which reads P from the S
-    // buffer), then S of key tile jt into that buffer.
-    if (lane == 0) {
-      constexpr uint32_t idS = umma_idesc_bf16(kRows, kKv, false);
-      constexpr uint32_t idO = umma_idesc_bf16(kRows, kD, true);
-      // Descriptors as 32-bit halves, computed once: a stage or k-step moves
-      // only the start address (16-byte units, low half).
-      const uint64_t q_desc = umma_desc_sw128(smem_addr(smem + kQ), 16, 1024);
-      const uint64_t k_desc = umma_desc_sw128(smem_addr(smem + kK), 16, 1024);
-      const uint64_t v_desc = umma_desc_sw128(smem_addr(smem + kV), kKv * 128, 1024);
-      const uint32_t q_lo = static_cast<uint32_t>(q_desc), q_hi = static_cast<uint32_t>(q_desc >> 32);
-      const uint32_t k_lo = static_cast<uint32_t>(k_desc), k_hi = static_cast<uint32_t>(k_desc >> 32);
-      const uint32_t v_lo = static_cast<uint32_t>(v_desc), v_hi = static_cast<uint32_t>(v_desc >> 32);
-      constexpr uint32_t kStageUnits = kKvStage >> 4;
-      bool ok = wait(q_full, 0);
-      if (ok) tc_fence_after();
-      auto issue_s = [&](int t, int jt) {
-        const uint32_t ka = k_lo + (jt % kKStages) * kStageUnits;
-        const uint32_t qa = q_lo + t * (kQTile >> 4);
-        const uint32_t d = tmem + t * kTmemTile;
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ========================= MMA issuer.  Key tile jt: for each query
+      // tile, the P V product of key tile jt - 1 (which reads P from the S
+      // buffer), then S of key tile jt into that buffer.
+      if (lane == 0) {
+        constexpr uint32_t idS = umma_idesc_bf16(kRows, kKv, false);
+        constexpr uint32_t idO = umma_idesc_f16(kRows, kD, true);
+        // Descriptors as 32-bit halves, computed once: a stage or k-step moves
+        // only the start address (16-byte units, low half).
+        const uint64_t q_desc = umma_desc_sw128(smem_addr(smem + kQ), 16, 1024);
+        const uint64_t k_desc = umma_desc_sw128(smem_addr(smem + kK), 16, 1024);
+        const uint64_t v_desc = umma_desc_sw128(smem_addr(smem + kV), kKv * 128, 1024);
+        const uint32_t q_lo = static_cast<uint32_t>(q_desc), q_hi = static_cast<uint32_t>(q_desc >> 32);
+        const uint32_t k_lo = static_cast<uint32_t>(k_desc), k_hi = static_cast<uint32_t>(k_desc >> 32);
+        const uint32_t v_lo = static_cast<uint32_t>(v_desc), v_hi = static_cast<uint32_t>(v_desc >> 32);
+        constexpr uint32_t kStageUnits = kKvStage >> 4;
+        bool ok = wait(q_full, 0);
+        if (ok) tc_fence_after();
+        auto issue_s = [&](int t, int jt) {
+          const uint32_t ka = k_lo + (jt % kKStages) * kStageUnits;
+          const uint32_t qa = q_lo + t * (kQTile >> 4);
+          const uint32_t d = tmem + t * kTmemTile;
 #pragma unroll
-        for (int k = 0; k < kD / 16; ++k)
-          umma_bf16_w(d, qa + (((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4), q_hi,
-                      ka + (((k >> 2) * (kKv * 128) + (k & 3) * 32) >> 4), k_hi, idS, k > 0);
-        umma_commit(s_full(t));
-      };
-      auto issue_pv = [&](int t, int jt) {
-        const uint32_t va = v_lo + (jt % kVStages) * kStageUnits;
-        const uint32_t pt = tmem + t * kTmemTile;  // P over the S columns
-        const uint32_t d = tmem + t * kTmemTile + kOCol;
-        // O += P_hi V, then O += P_lo V (the remainders, kKv/2 columns on)
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
+          for (int k = 0; k < kD / 16; ++k)
+            umma_bf16_w(d, qa + (((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4), q_hi,
+                        ka + (((k >> 2) * (kKv * 128) + (k & 3) * 32) >> 4), k_hi, idS, k > 0);
+          umma_commit(s_full(t));
+        };
+        auto issue_pv = [&](int t, int jt) {
+          const uint32_t va = v_lo + (jt % kVStages) * kStageUnits;
+          const uint32_t pt = tmem + t * kTmemTile;  // P over the S columns
+          const uint32_t d = tmem + t * kTmemTile + kOCol;
+          // O += P V, 16 keys (eight columns of P) per product
 #pragma unroll
           for (int k = 0; k < kKv / 16; ++k)
-            umma_bf16_ta_w(d, pt + part * (kKv / 2) + k * 8, va + ((k * 16 * 128) >> 4), v_hi, idO,
-                           (jt > 0 || part > 0 || k > 0) ? 1u : 0u);
-      };
-      for (int jt = 0; ok && jt <= n_tiles; ++jt) {
-        bool v_ready = false, k_ready = false;
-        for (int t = 0; t < kTiles && ok; ++t) {
-          const int nt = t ? n_kv1 : n_kv0;
-          if (jt > 0 && jt - 1 < nt) {
-            if (!v_ready) {
-              ok = wait(v_full((jt - 1) % kVStages), ((jt - 1) / kVStages) & 1);
-              if (!ok) break;
-              v_ready = true;
-            }
-            ok = wait(p_full(t), (jt - 1) & 1);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(t, jt - 1);
-            umma_commit(jt == nt ? o_final(t) : pv_done(t));
-          }
-          if (jt < nt) {
-            // tcgen05 products with different accumulators are not ordered:
-            // S of this key tile overwrites the P the previous product reads,
-            // and the softmax rescales O once this S is done, so that product
-            // must have completed first (the tensor pipe is busy with it
-            // meanwhile)
-            if (jt > 0) {
-              ok = wait(pv_done(t), (jt - 1) & 1);
+            umma_bf16_ta_w(d, pt + k * 8, va + ((k * 16 * 128) >> 4), v_hi, idO, (jt > 0 || k > 0) ? 1u : 0u);
+        };
+        for (int jt = 0; ok && jt <= n_tiles; ++jt) {
+          bool v_ready = false, k_ready = false;
+          for (int t = 0; t < kTiles && ok; ++t) {
+            const int nt = t ? n_kv1 : n_kv0;
+            if (jt > 0 && jt - 1 < nt) {
+              if (!v_ready) {
+                ok = wait(v16_full((jt - 1) % kVStages), ((jt - 1) / kVStages) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                v_ready = true;
+              }
+              ok = wait(p_full(t), (jt - 1) & 1);
               if (!ok) break;
               tc_fence_after();
+              issue_pv(t, jt - 1);
+              umma_commit(jt == nt ? o_final(t) : pv_done(t));
             }
-            if (!k_ready) {
-              ok = wait(k_full(jt % kKStages), (jt / kKStages) & 1);
-              if (!ok) break;
-              tc_fence_after();
-              k_ready = true;
+            if (jt < nt) {
+              // tcgen05 products with different accumulators are not ordered:
+              // S of this key tile overwrites the P the previous product reads,
+              // and the softmax rescales O once this S is done, so that product
+              // must have completed first (the tensor pipe is busy with it
+              // meanwhile)
+              if (jt > 0) {
+                ok = wait(pv_done(t), (jt - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              if (!k_ready) {
+                ok = wait(k_full(jt % kKStages), (jt / kKStages) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                k_ready = true;
+              }
+              issue_s(t, jt);
             }
-            issue_s(t, jt);
           }
+          if (!ok) break;
+          if (k_ready) umma_commit(k_empty(jt % kKStages));  // free once these products are done
+          if (v_ready) umma_commit(v_empty((jt - 1) % kVStages));
         }
-        if (!ok) break;
-        if (k_ready) umma_commit(k_empty(jt % kKStages));  // free once these products are done
-        if (v_ready) umma_commit(v_empty((jt - 1) % kVStages));
+        // every product issued has completed before the tensor memory is freed
+        umma_commit(mma_done);
+        if (!wait(mma_done, 0)) atomicOr(p.err, kErrDrainTimeout);
       }
-      // every product issued has completed before the tensor memory is freed
-      umma_commit(mma_done);
-      if (!wait(mma_done, 0)) atomicOr(p.err, kErrDrainTimeout);
+      __syncwarp();
     }
-    __syncwarp();
   }
 
   tc_fence_before();
