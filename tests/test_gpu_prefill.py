@@ -233,13 +233,15 @@ def test_prefill_query_rows_of_any_magnitude():
     pool.destroy()
 
 
-@pytest.mark.parametrize("profile", ["mixed", "tiny", "huge"])
-def test_prefill_values_of_any_magnitude(profile):
+@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("profile", ["mixed", "tiny", "huge", "zero_first"])
+def test_prefill_values_of_any_magnitude(profile, bs):
     """V rows scaled per 128-key tile (mixed: 2^-12 .. 2^8 in one sequence,
-    the largest arriving late), or all by 2^-40 or 2^60: the output matches
-    the oracle in units of its own largest magnitude (relative L2 and max
-    |err| / max |ref| within the bar)."""
-    hkv, hq, ctx, ql, bs = 2, 8, 700, 300, 16
+    the largest arriving late), all by 2^-40 or 2^60, or zero over the first
+    key tile and N(0,1) after it: the output matches the oracle in units of
+    its own largest magnitude (relative L2 and max |err| / max |ref| within
+    the bar)."""
+    hkv, hq, ctx, ql = 2, 8, 700, 300
     nblk = -(-ctx // bs)
     rng = np.random.default_rng(31)
     tables = rng.permutation(nblk + 3)[:nblk].astype(np.int32).reshape(1, nblk)
@@ -248,8 +250,10 @@ def test_prefill_values_of_any_magnitude(profile):
     opool = oracle.Pool(nblk + 3, bs, hkv, 128, "bf16")
     g = torch.Generator().manual_seed(32)
     k = torch.randn(ctx, hkv, 128, generator=g).bfloat16()
-    powers = {"mixed": [-12, 8, 0, -4, 3, 6], "tiny": [-40] * 6, "huge": [60] * 6}[profile]
-    tile_scale = torch.tensor([2.0 ** powers[i // 128] for i in range(ctx)]).view(ctx, 1, 1)
+    powers = {"mixed": [-12, 8, 0, -4, 3, 6], "tiny": [-40] * 6, "huge": [60] * 6,
+              "zero_first": [None, 0, 0, 0, 0, 0]}[profile]
+    tile_scale = torch.tensor([0.0 if powers[i // 128] is None else 2.0 ** powers[i // 128]
+                               for i in range(ctx)]).view(ctx, 1, 1)
     v = (torch.randn(ctx, hkv, 128, generator=g) * tile_scale).bfloat16()
     pos = np.arange(ctx)
     slots = tables[0, pos // bs].astype(np.int64) * bs + pos % bs
@@ -266,6 +270,6 @@ def test_prefill_values_of_any_magnitude(profile):
     assert np.isfinite(got).all()
     unit = float(np.abs(ref).max())
     max_abs, rel = errors(got / unit, ref / unit)
-    print(f"PARITY prefill V {profile} max_abs/unit={max_abs:.3e} rel_l2={rel:.3e}")
+    print(f"PARITY prefill V {profile} bs={bs} max_abs/unit={max_abs:.3e} rel_l2={rel:.3e}")
     assert max_abs <= MAX_ABS and rel <= REL_L2, (profile, max_abs, rel)
     pool.destroy()
