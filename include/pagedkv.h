@@ -300,8 +300,9 @@ kv_status paged_decode_attention_noalloc(kv_pool* pool, const void* q_dev, int32
  *                      position pos = ctx - q_len + i) gets
  *                      softmax(scale q K^T) V over positions [lo, pos], lo =
  *                      max(0, pos + 1 - sliding_window) when the window is on.
- * bf16, FP8 and FP4 pools with head_dim 128 and a query group of at most 8
- * heads per KV head (other shapes: KV_ERR_UNSUPPORTED).  Runs on the tcgen05
+ * bf16, FP8 and FP4 pools with head_dim 128 and a query group of at most
+ * 128 heads per KV head (a query tile's 128 rows are (token, head) pairs with
+ * the group padded to a power of two; other shapes: KV_ERR_UNSUPPORTED).  Runs on the tcgen05
  * tensor cores.  bf16: Q K^T on bf16 operands; P V on f16 ones, P rounded
  * once to f16 and V converted to f16 scaled by a power of two (set from the
  * largest V of the key tiles seen so far, raised when a later tile would

@@ -434,7 +434,8 @@ kv_status paged_prefill_attention(kv_pool* p, const void* q, int32_t n_q_heads,
     return KV_ERR_INVALID_ARG;
   if (n_q_heads % p->n_kv_heads != 0) return KV_ERR_INVALID_ARG;
   const int32_t g = n_q_heads / p->n_kv_heads;
-  if (g > 8 || p->head_dim != 128) return KV_ERR_UNSUPPORTED;
+  // a query tile holds 128 (token, head) rows: groups up to 128 heads
+  if (g > 128 || p->head_dim != 128) return KV_ERR_UNSUPPORTED;
   if (batch == 0 || max_q_len == 0) return KV_OK;
   if (!q || !cu_q_lens || !block_tables || !context_lens || !out || !aligned16(q) || !aligned16(out))
     return KV_ERR_INVALID_ARG;

@@ -273,3 +273,16 @@ def test_prefill_values_of_any_magnitude(profile, bs):
     print(f"PARITY prefill V {profile} bs={bs} max_abs/unit={max_abs:.3e} rel_l2={rel:.3e}")
     assert max_abs <= MAX_ABS and rel <= REL_L2, (profile, max_abs, rel)
     pool.destroy()
+
+
+@pytest.mark.parametrize("hq,hkv", [(16, 1), (48, 2), (128, 1)])
+def test_prefill_large_groups(hq, hkv):
+    """Groups of 16, 24 (padded to 32) and 128 query heads per KV head: a
+    query tile then holds 8, 4 or 1 tokens."""
+    pool, opool, q, cu, tables, lens = _build([150, 300], [150, 77], hq, hkv, seed=hq + hkv)
+    out = _run(pool, q, cu, tables, lens, 128 ** -0.5, 200)
+    torch.cuda.synchronize()
+    assert pool.check_status() == pagedkv.KV_OK
+    ref = opool.prefill(q, cu, tables, lens, 128 ** -0.5, 200)
+    _check(out, ref, f"group hq={hq} hkv={hkv}")
+    pool.destroy()

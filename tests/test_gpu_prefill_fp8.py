@@ -209,3 +209,15 @@ def test_prefill_fp8_negative_and_zero_scale(scale):
     ref = opool.prefill(q, cu, tables, lens, scale, 100)
     _check(out, ref, f"scale={scale}")
     pool.destroy()
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 2), (96, 1)])
+def test_prefill_fp8_large_groups(hq, hkv):
+    """Groups of 16 and 96 (padded to 128) query heads per KV head."""
+    pool, opool, q, cu, tables, lens = _build([150, 300], [150, 77], hq, hkv, seed=hq + hkv)
+    out = _run(pool, q, cu, tables, lens, 128 ** -0.5)
+    torch.cuda.synchronize()
+    assert pool.check_status() == pagedkv.KV_OK
+    ref = opool.prefill(q, cu, tables, lens, 128 ** -0.5)
+    _check(out, ref, f"group hq={hq} hkv={hkv}")
+    pool.destroy()
