@@ -88,9 +88,12 @@ typedef enum {
   KV_ERR_TIMEOUT = 6,       /* device: a bounded wait on a copy ran out      */
   KV_ERR_BAD_SLOT = 7,      /* device: a slot_mapping entry outside the pool */
   KV_ERR_BAD_CONTEXT = 8,   /* device: context_lens[b] < 0 or above a bound  */
-  KV_ERR_DRAIN_TIMEOUT = 9  /* device: a kernel gave up waiting for its own   */
+  KV_ERR_DRAIN_TIMEOUT = 9, /* device: a kernel gave up waiting for its own   */
                             /* copies while leaving; treat the context as     */
                             /* suspect (see kv_pool_check_status)             */
+  KV_ERR_STALE_EXPONENT_MAP = 10 /* device: a bf16 prefill read a V row the      */
+                            /* exponent map has no entry for (written other   */
+                            /* than by paged_kv_write; see kv_pool_exponent_map) */
 } kv_status;
 
 typedef enum { KV_BF16 = 0, KV_FP8_E4M3 = 1, KV_FP4_E2M1 = 2 } kv_dtype;
@@ -130,6 +133,31 @@ kv_status kv_pool_destroy(kv_pool* pool);
 kv_status kv_pool_info(const kv_pool* pool, kv_pool_desc* out);
 
 /*
+ * kv_pool_exponent_map -- bf16 pools keep, next to the blocks, one byte per
+ * (block, KV head, token): the largest biased exponent field of the token's
+ * V row as paged_kv_write stored it (at least 1), 0 for a row no write has
+ * recorded.  Layout [num_blocks][n_kv_heads][block_size] uint8, owned by the
+ * pool.  paged_kv_write sets it, paged_kv_copy_blocks moves it with the
+ * blocks, and paged_prefill_attention reads it to scale its f16 copy of V
+ * without a pass over each key tile.  V rows changed by other means (the
+ * memory kv_pool_info describes) keep their old entries, or 0: call
+ * kv_pool_refresh_exponent_map afterwards.  A prefill that attends to a row
+ * whose entry is 0 records KV_ERR_STALE_EXPONENT_MAP (its output is then
+ * undefined); an entry below the row's true exponent makes its f16 copy of V
+ * overflow.
+ *   map_dev, bytes: out; the map's device address and size (NULL and 0 for
+ *                   FP8 and FP4 pools).
+ */
+kv_status kv_pool_exponent_map(const kv_pool* pool, void** map_dev, int64_t* bytes);
+
+/*
+ * kv_pool_refresh_exponent_map -- bf16 pools: recompute every entry from the
+ * V rows the pool holds (one pass over the pool), ordered on `stream`; a
+ * no-op for FP8 and FP4 pools.
+ */
+kv_status kv_pool_refresh_exponent_map(kv_pool* pool, void* stream);
+
+/*
  * kv_pool_set_scales -- FP8 and FP4 pools: copy per-KV-head scales (device
  * float[Hkv] each) into the pool, ordered on `stream`.  A stored FP8 code c of
  * KV head h stands for c * k_scale[h] (K) or c * v_scale[h] (V); the write
@@ -152,9 +180,10 @@ kv_status kv_pool_set_scales(kv_pool* pool, const float* k_scale_dev, const floa
  *   slot_mapping_dev:    int64 [num_tokens]; slot = physical_block * block_size
  *                        + offset; slot < 0 marks a padded token (skipped);
  *                        slot >= num_blocks * block_size sets KV_ERR_BAD_SLOT.
- * BF16 pools receive a bit copy; FP8 and FP4 pools the quantised codes (see
- * kv_pool_set_scales).  Two tokens with the same slot in one call is
- * undefined.  num_tokens == 0 is a no-op.
+ * BF16 pools receive a bit copy, and each written V row's largest exponent
+ * field goes into the pool's exponent map (see kv_pool_exponent_map); FP8 and
+ * FP4 pools the quantised codes (see kv_pool_set_scales).  Two tokens with the
+ * same slot in one call is undefined.  num_tokens == 0 is a no-op.
  */
 kv_status paged_kv_write(kv_pool* pool, const void* k_dev, const void* v_dev,
                          const int64_t* slot_mapping_dev, int64_t num_tokens, void* stream);
@@ -171,8 +200,9 @@ kv_status paged_kv_write(kv_pool* pool, const void* k_dev, const void* v_dev,
  * The result is that of applying the pairs one after another (chains, a
  * block written twice, a block read after it is written all behave so): the
  * host cuts the list into waves without conflicts, one kernel per wave, the
- * pairs passed in the launch parameters.  `pairs` may be reused when the
- * call returns.  Asynchronous on `stream`.
+ * pairs passed in the launch parameters.  A bf16 block's rows of the V
+ * exponent map move with it.  `pairs` may be reused when the call returns.
+ * Asynchronous on `stream`.
  */
 kv_status paged_kv_copy_blocks(kv_pool* pool, const int32_t* pairs, int64_t num_pairs,
                                void* stream);
@@ -305,10 +335,11 @@ kv_status paged_decode_attention_noalloc(kv_pool* pool, const void* q_dev, int32
  * the group padded to a power of two; other shapes: KV_ERR_UNSUPPORTED).  Runs on the tcgen05
  * tensor cores.  bf16: Q K^T on bf16 operands; P V on f16 ones, P rounded
  * once to f16 and V converted to f16 scaled by a power of two (set from the
- * largest V of the key tiles seen so far, raised when a later tile would
- * overflow), which keeps every V value exact whose magnitude is at least
- * 2^-31 times that largest one (smaller ones are off by at most 2^-39 of
- * it); the result meets the decode's bf16 accuracy.  FP8: Q K^T
+ * largest V of the key tiles seen so far, as the pool's exponent map
+ * records it, raised when a later tile would overflow), which keeps every V
+ * value exact whose magnitude is at least 2^-31 times that largest one
+ * (smaller ones are off by at most 2^-39 of it); the result meets the
+ * decode's bf16 accuracy.  FP8: Q K^T
  * takes E4M3 operands -- the K codes as stored, each query row scaled by a
  * power of two and split into an E4M3 code and the code of its remainder --
  * and P V f16 ones (P rounded once to f16, the V codes converted exactly),
@@ -372,7 +403,7 @@ kv_status kv_pool_set_test_stall(kv_pool* pool, int32_t enable);
  * kv_pool_check_status -- synchronise `stream`, read and clear the pool's
  * device error word.  Returns KV_OK, or the first recorded problem in the
  * order KV_ERR_DRAIN_TIMEOUT, KV_ERR_TIMEOUT, KV_ERR_BAD_BLOCK_ID,
- * KV_ERR_BAD_SLOT, KV_ERR_BAD_CONTEXT; KV_ERR_CUDA if the stream itself
+ * KV_ERR_BAD_SLOT, KV_ERR_BAD_CONTEXT, KV_ERR_STALE_EXPONENT_MAP; KV_ERR_CUDA if the stream itself
  * failed.  After KV_ERR_TIMEOUT the context stays usable (every copy the
  * kernel issued was seen to land).  After KV_ERR_DRAIN_TIMEOUT it is not
  * known to be: copies may still have been writing shared memory when the

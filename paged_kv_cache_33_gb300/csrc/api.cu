@@ -153,6 +153,7 @@ const char* kv_status_str(kv_status s) {
     case KV_ERR_DRAIN_TIMEOUT: return "KV_ERR_DRAIN_TIMEOUT";
     case KV_ERR_BAD_SLOT: return "KV_ERR_BAD_SLOT";
     case KV_ERR_BAD_CONTEXT: return "KV_ERR_BAD_CONTEXT";
+    case KV_ERR_STALE_EXPONENT_MAP: return "KV_ERR_STALE_EXPONENT_MAP";
   }
   return "KV_ERR_UNKNOWN";
 }
@@ -203,11 +204,17 @@ kv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_he
     ok = ok && cudaMemset(p->err, 0, sizeof(uint32_t)) == cudaSuccess;
   }
   ok = ok && encode_pool_map(p);
+  if (ok && dtype == KV_BF16) {
+    const size_t n = static_cast<size_t>(num_blocks) * n_kv_heads * block_size;
+    ok = cudaMalloc(reinterpret_cast<void**>(&p->vexp), n) == cudaSuccess &&
+         cudaMemset(p->vexp, 0, n) == cudaSuccess;
+  }
   if (!ok) {
     cudaGetLastError();
     cudaFree(p->base);
     cudaFree(p->scales);
     cudaFree(p->err);
+    cudaFree(p->vexp);
     delete p;
     return KV_ERR_CUDA;
   }
@@ -222,8 +229,27 @@ kv_status kv_pool_destroy(kv_pool* p) {
   cudaFree(p->base);
   cudaFree(p->scales);
   cudaFree(p->err);
+  cudaFree(p->vexp);
   delete p;
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+kv_status kv_pool_exponent_map(const kv_pool* p, void** map_dev, int64_t* bytes) {
+  if (!p || !map_dev || !bytes) return KV_ERR_INVALID_ARG;
+  *map_dev = p->vexp;
+  *bytes = p->vexp ? p->num_blocks * p->n_kv_heads * p->block_size : 0;
+  return KV_OK;
+}
+
+kv_status kv_pool_refresh_exponent_map(kv_pool* p, void* stream) {
+  if (!p) return KV_ERR_INVALID_ARG;
+  if (!p->vexp) return KV_OK;
+  DeviceGuard guard(p->device);
+  if (pkv::launch_refresh_exponent_map(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return KV_ERR_CUDA;
+  }
+  return KV_OK;
 }
 
 kv_status kv_pool_info(const kv_pool* p, kv_pool_desc* out) {
@@ -456,6 +482,7 @@ kv_status paged_prefill_attention(kv_pool* p, const void* q, int32_t n_q_heads,
   d.context_lens = context_lens;
   d.out = out;
   d.err = p->err;
+  d.vexp = p->vexp;
   d.k_scale = p->scales;
   d.v_scale = p->scales + p->n_kv_heads;
   d.num_blocks = p->num_blocks;
@@ -529,6 +556,7 @@ kv_status kv_pool_check_status(kv_pool* p, void* stream) {
   if (word & pkv::kErrBadBlock) return KV_ERR_BAD_BLOCK_ID;
   if (word & pkv::kErrBadSlot) return KV_ERR_BAD_SLOT;
   if (word & pkv::kErrBadContext) return KV_ERR_BAD_CONTEXT;
+  if (word & pkv::kErrStaleMap) return KV_ERR_STALE_EXPONENT_MAP;
   return KV_OK;
 }
 

@@ -23,6 +23,8 @@ enum : uint32_t {
   // A wait ran out while the kernel was leaving: copies (or tensor-core
   // products) it issued may still be writing its shared memory.
   kErrDrainTimeout = 16u,
+  // A bf16 prefill met a V row without an exponent-map entry.
+  kErrStaleMap = 32u,
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

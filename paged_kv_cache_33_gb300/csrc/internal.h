@@ -17,6 +17,8 @@ struct kv_pool {
   uint64_t bytes = 0;
   float* scales = nullptr;     // device [2][Hkv]: K scales then V scales
   uint32_t* err = nullptr;     // device error word
+  uint8_t* vexp = nullptr;     // bf16 pools: [NB][Hkv][BS], the largest exponent field of each
+                               // V row as paged_kv_write stored it (0: not known)
   CUtensorMap tmap;            // pool viewed as [NB*Hkv][2][BS][D] for TMA
   CUtensorMap tmap_rows;       // bf16 / FP8 pools: the same view, boxes of one tile (K or V);
                                // FP4 pools: each (block, head)'s records as rows of 128 bytes
@@ -92,6 +94,8 @@ int64_t decode_max_chunks(int64_t max_units);
 
 // The KV write; with `zero_word` it also clears that int (the decode's ticket
 // counter) and lets a programmatic dependent launch early.
+// bf16 pools: recompute the V exponent map from the pool's V rows.
+cudaError_t launch_refresh_exponent_map(const kv_pool* pool, cudaStream_t stream);
 cudaError_t launch_kv_write(const kv_pool* pool, const void* k, const void* v,
                             const int64_t* slots, int64_t num_tokens, cudaStream_t stream,
                             int32_t* zero_word = nullptr);
@@ -118,6 +122,7 @@ struct PrefillParams {
   const int32_t* context_lens;  // [B]
   float* out;                   // [T][Hq][D]
   uint32_t* err;
+  const uint8_t* vexp;          // bf16: the pool's V exponent map (kv_pool::vexp)
   const float* k_scale;         // FP8: [Hkv]
   const float* v_scale;
   int64_t num_blocks;

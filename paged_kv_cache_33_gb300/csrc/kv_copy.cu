@@ -7,7 +7,8 @@
 // block that the sequence then owns.
 //
 // A physical block is one contiguous run of the pool ([Hkv][2][BS][D], or
-// [Hkv][BS/16] FP4 records), so a copy is a flat move of block_bytes.  The (src, dst) pairs come from the
+// [Hkv][BS/16] FP4 records), so a copy is a flat move of block_bytes (plus,
+// for bf16 pools, its Hkv x BS bytes of the V exponent map).  The (src, dst) pairs come from the
 // host block manager; the host cuts them into waves in which no block is
 // both read and written, so every wave runs fully parallel and the result is
 // that of applying the pairs one after another.  Each wave's pairs travel in
@@ -35,10 +36,14 @@ struct CopyWave {
 
 __global__ void __launch_bounds__(kCopyThreads) kv_copy_blocks_kernel(
     const __grid_constant__ CopyWave wave, int slices, int64_t chunks_per_block,
-    uint4* __restrict__ pool) {
+    uint4* __restrict__ pool, uint4* __restrict__ map, int map_chunks) {
   const int pair = blockIdx.x / slices;
   const int slice = blockIdx.x - pair * slices;
   const int2 pr = wave.pairs[pair];
+  // bf16 pools: the block's rows of the V exponent map move with it
+  if (slice == 0)
+    for (int m = threadIdx.x; m < map_chunks; m += kCopyThreads)
+      map[static_cast<int64_t>(pr.y) * map_chunks + m] = map[static_cast<int64_t>(pr.x) * map_chunks + m];
   const uint4* src = pool + static_cast<int64_t>(pr.x) * chunks_per_block;
   uint4* dst = pool + static_cast<int64_t>(pr.y) * chunks_per_block;
   const int64_t base = static_cast<int64_t>(slice) * kChunksPerCta + threadIdx.x;
@@ -67,6 +72,8 @@ int64_t block_bytes(const kv_pool* pool) {
 cudaError_t launch_copy_blocks(const kv_pool* pool, const int32_t* pairs, int64_t n,
                                cudaStream_t stream) {
   const int64_t chunks = block_bytes(pool) / 16;
+  // exponent-map bytes per block: Hkv x block_size, a multiple of 16
+  const int map_chunks = pool->vexp ? pool->n_kv_heads * pool->block_size / 16 : 0;
   const int slices = static_cast<int>((chunks + kChunksPerCta - 1) / kChunksPerCta);
   static thread_local CopyWave wave;
   int count = 0;
@@ -90,7 +97,8 @@ cudaError_t launch_copy_blocks(const kv_pool* pool, const int32_t* pairs, int64_
   auto flush = [&]() -> cudaError_t {
     if (count == 0) return cudaSuccess;
     kv_copy_blocks_kernel<<<count * slices, kCopyThreads, 0, stream>>>(
-        wave, slices, chunks, static_cast<uint4*>(pool->base));
+        wave, slices, chunks, static_cast<uint4*>(pool->base), reinterpret_cast<uint4*>(pool->vexp),
+        map_chunks);
     count = 0;
     next_wave();
     return cudaGetLastError();

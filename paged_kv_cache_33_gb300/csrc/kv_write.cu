@@ -32,12 +32,35 @@ __device__ __forceinline__ void wait_for_prerequisites() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// BF16 pool: bit copy.  Thread i handles chunk c of row (t, h, kv).
+// Lane-wise maximum of two pairs of unsigned 16-bit halves.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// The largest exponent field of a bf16 row held 16 bytes per thread by
+// kChunks consecutive lanes (all in `lanes`), at least 1 (0 marks a row the
+// exponent map has no entry for).
+template <int kChunks>
+__device__ __forceinline__ uint32_t row_exponent(const uint4 val, uint32_t lanes) {
+  constexpr uint32_t kE = 0x7F807F80u;
+  uint32_t m = max_u16x2(max_u16x2(val.x & kE, val.y & kE), max_u16x2(val.z & kE, val.w & kE));
+  m = max(m & 0xFFFFu, m >> 16) >> 7;
+#pragma unroll
+  for (int o = 1; o < kChunks; o <<= 1) m = max(m, __shfl_xor_sync(lanes, m, o));
+  return max(m, 1u);
+}
+
+// BF16 pool: bit copy.  Thread i handles chunk c of row (t, h, kv).  The
+// threads of a V row also record the row's largest exponent field in the
+// pool's exponent map (at least 1: 0 stands for a row never written here),
+// which the prefill reads to scale its f16 copy of V.
 template <int D>
 __global__ void __launch_bounds__(256) kv_write_bf16_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
     int64_t num_tokens, int hkv, int bs, int64_t num_slots, uint4* __restrict__ pool,
-    uint32_t* __restrict__ err, int32_t* __restrict__ zero_word) {
+    uint8_t* __restrict__ vexp, uint32_t* __restrict__ err, int32_t* __restrict__ zero_word) {
   constexpr int kChunks = D / 8;  // 16-byte chunks per row
   // Once the kernels before this one are complete, a decode launched as this
   // kernel's programmatic dependent may start (it reads its inputs at once,
@@ -65,6 +88,30 @@ __global__ void __launch_bounds__(256) kv_write_bf16_kernel(
   const uint4 val = (kv ? v : k)[(t * hkv + h) * kChunks + c];
   const int64_t row = ((blk * hkv + h) * 2 + kv) * bs + off;
   pool[row * kChunks + c] = val;
+  if (kv && vexp) {
+    // the kChunks threads of the row are consecutive lanes, all present
+    const uint32_t m = row_exponent<kChunks>(val, __activemask());
+    if (c == 0) vexp[(blk * hkv + h) * bs + off] = static_cast<uint8_t>(m);
+  }
+}
+
+// bf16 pools: every V row's exponent-map entry again, from the pool itself
+// (after V was written other than through paged_kv_write).  Thread i reads
+// chunk c of V row r = i / kChunks of the pool.
+template <int D>
+__global__ void __launch_bounds__(256) refresh_exponent_map_kernel(const uint4* __restrict__ pool,
+                                                                   int64_t rows, int bs,
+                                                                   uint8_t* __restrict__ vexp) {
+  constexpr int kChunks = D / 8;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= rows * kChunks) return;
+  const int64_t r = i / kChunks;  // (block, head) * bs + offset
+  const int c = static_cast<int>(i % kChunks);
+  const int64_t bh = r / bs;
+  const int off = static_cast<int>(r % bs);
+  const uint4 val = pool[((bh * 2 + 1) * bs + off) * kChunks + c];
+  const uint32_t m = row_exponent<kChunks>(val, __activemask());
+  if (c == 0) vexp[r] = static_cast<uint8_t>(m);
 }
 
 // Byte position of token `off` (0..15) inside a row of a transposed FP8 V
@@ -239,6 +286,20 @@ cudaError_t launch_write(Kernel kernel, int64_t blocks, cudaStream_t stream, boo
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+cudaError_t launch_refresh_exponent_map(const kv_pool* pool, cudaStream_t stream) {
+  const int64_t rows = pool->num_blocks * pool->n_kv_heads * pool->block_size;
+  const int64_t total = rows * (pool->head_dim / 8);
+  const int64_t blocks = (total + 255) / 256;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  if (pool->head_dim == 128)
+    refresh_exponent_map_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint4*>(pool->base), rows, pool->block_size, pool->vexp);
+  else
+    refresh_exponent_map_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint4*>(pool->base), rows, pool->block_size, pool->vexp);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_kv_write(const kv_pool* pool, const void* k, const void* v,
                             const int64_t* slots, int64_t num_tokens, cudaStream_t stream,
                             int32_t* zero_word) {
@@ -253,11 +314,11 @@ cudaError_t launch_kv_write(const kv_pool* pool, const void* k, const void* v,
       return launch_write(kv_write_bf16_kernel<128>, blocks, stream, dependent,
                           static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots,
                           num_tokens, hkv, pool->block_size, num_slots,
-                          static_cast<uint4*>(pool->base), pool->err, zero_word);
+                          static_cast<uint4*>(pool->base), pool->vexp, pool->err, zero_word);
     return launch_write(kv_write_bf16_kernel<64>, blocks, stream, dependent,
                         static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots,
                         num_tokens, hkv, pool->block_size, num_slots,
-                        static_cast<uint4*>(pool->base), pool->err, zero_word);
+                        static_cast<uint4*>(pool->base), pool->vexp, pool->err, zero_word);
   }
   if (pool->dtype == KV_FP4_E2M1) {
     const int64_t total = num_tokens * hkv * 2 * 32;  // one warp per row

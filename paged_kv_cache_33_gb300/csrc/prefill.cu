@@ -25,12 +25,14 @@
 //    (relative rounding 2^-12 on average, where one bf16 P, 2^-9, would put
 //    the output ~1e-3 off the exact attention), so V is converted to f16 in
 //    place in its stage by a converter warpgroup, scaled by a power of two
-//    2^-e: every bf16 value whose magnitude lies within 2^29 below the
-//    largest V the CTA has seen is exact in f16 then.  e is set from the
-//    first key tile's largest exponent (0 when its values sit in f16's own
-//    range) and raised when a later tile would overflow; the softmax
-//    warps rescale O by the change, and the output by 2^e.  Rows past the
-//    sequence's end and of blocks not loaded become zeros.
+//    2^-e: every bf16 value at least 2^-31 times the largest V the CTA has
+//    seen is exact in f16 then.  e is set from the first key tile's largest
+//    exponent and raised when a later tile would overflow; the largest
+//    exponent of a tile comes from the pool's V exponent map (one byte per
+//    V row, kept by paged_kv_write), read a tile ahead, not from a pass over
+//    the tile.  The softmax warps rescale O by a change of e, and the output
+//    by 2^e.  Rows past the sequence's end and of blocks not loaded become
+//    zeros.
 //    128-key products run the tensor pipe at its full rate; 64-key ones
 //    reach two thirds of it.
 //  * Two query tiles share every key tile and alternate on the tensor pipe:
@@ -89,12 +91,11 @@ constexpr int kK = kQ + kTiles * kQTile;
 constexpr int kV = kK + kKStages * kKvStage;
 constexpr int kVe = kV + kVStages * kKvStage;         // int32 [kVStages]: each stage's e
 constexpr int kVMask = kVe + 16;                      // uint32 [kVStages]: blocks each V stage holds
-constexpr int kEx = kVMask + 16;                      // uint32 [2][4]: converter warps' maxima
-constexpr int kBars = kEx + 32;
+constexpr int kBars = kVMask + 16;
 static_assert(kVStages * 4 <= 16, "the V stages' exponents and block masks fit");
 // barriers: k_full[2], k_empty[2], v_full[3], v_empty[3], v16_full[3], per tile
-// s_full, p_full, pv_done, o_final; q_full, mma_done, ex_full
-constexpr int kNumBars = 2 * kKStages + 3 * kVStages + 4 * kTiles + 3;
+// s_full, p_full, pv_done, o_final; q_full, mma_done
+constexpr int kNumBars = 2 * kKStages + 3 * kVStages + 4 * kTiles + 2;
 constexpr int kTmemSlot = kBars + kNumBars * 8;
 constexpr int kSmemBytes = kTmemSlot + 16 + 1024;     // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
@@ -106,13 +107,6 @@ constexpr uint32_t kTmemCols = kTiles * kTmemTile;
 
 __device__ __forceinline__ int swz128(int row, int chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
-}
-
-// Lane-wise larger magnitude of two bf16 pairs (the sign bits are not used).
-__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
 }
 
 // a * b on two fp32 lanes at once.
@@ -196,7 +190,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   auto o_final = [&](int t) { return bar0 + 8u * (kTileBars + 4 * t + 3); };
   const uint32_t q_full = bar0 + 8u * (kTileBars + 4 * kTiles);
   const uint32_t mma_done = q_full + 8;
-  const uint32_t ex_full = q_full + 16;  // the converter warps' maxima are in
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
   int* v_e = reinterpret_cast<int*>(smem + kVe);
   uint32_t* v_mask = reinterpret_cast<uint32_t*>(smem + kVMask);
@@ -219,7 +212,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     }
     mbar_init(q_full, kSoftmax);
     mbar_init(mma_done, 1);
-    mbar_init(ex_full, kCvt);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -437,14 +429,29 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     // ====== converters: each V stage, bf16 as copied, into f16 in place.
     // Thread ct takes the 16-byte chunks ct + 128 i (i < 16) of the stage's
     // two column halves: key row ct / 8 + 16 (i mod 8), a whole 512-byte run
-    // of the stage per warp and instruction.  Two passes: the largest
-    // exponent of the rows that hold keys, then the conversion, scaled by
-    // the power of two that keeps it exact; rows without a key are zeroed.
+    // of the stage per warp and instruction.  The largest exponent of the
+    // rows that hold keys comes from the pool's exponent map: lane l reads
+    // the entries of keys 4l .. 4l + 3, loaded a key tile ahead (the table
+    // entry two tiles ahead), and every warp reads all 128 and comes to the
+    // same answer.  Then the conversion, scaled by the power of two that
+    // keeps it exact; rows without a key are zeroed.
     const int ct = tid - kCvtWarp * 32;
-    uint32_t* ex = reinterpret_cast<uint32_t*>(smem + kEx);
-    int e = 0, nred = 0;
+    const int mblk = (4 * lane) / BS, moff = (4 * lane) % BS;
+    auto table_entry = [&](int jt) -> int {
+      return jt < n_tiles && needed(jt, mblk) ? trow[((jt0 + jt) * kKv) / BS + mblk] : -1;
+    };
+    auto map_word = [&](int phys) -> uint32_t {
+      if (phys < 0 || phys >= p.num_blocks) return 0u;
+      return __ldg(reinterpret_cast<const uint32_t*>(
+          p.vexp + (static_cast<int64_t>(phys) * p.n_kv_heads + h) * BS + moff));
+    };
+    int tab1 = table_entry(1);
+    uint32_t map0 = map_word(table_entry(0));
+    int e = 0;
     bool ok = true;
     for (int jt = 0; jt < n_tiles && ok; ++jt) {
+      const int tab2 = table_entry(jt + 2);
+      const uint32_t map1 = map_word(tab1);
       const int s = jt % kVStages;
       ok = wait(v_full(s), (jt / kVStages) & 1);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -452,43 +459,34 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       const int key0 = (jt0 + jt) * kKv;
       constexpr uint32_t kAllBlocks = (1u << (kKv / BS)) - 1u;
       const bool full = mask == kAllBlocks && key0 + kKv <= ctx;
-      const uint32_t st = smem_addr(smem + kV + s * kKvStage) + 16 * ct;
-      auto row_ok = [&](int i) {
-        const int key = (ct >> 3) + 16 * (i & 7);
-        return full || (((mask >> (key / BS)) & 1u) && key0 + key < ctx);
-      };
-      uint32_t em = 0;
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        if (!row_ok(i)) continue;
-        const uint4 v = lds128(st + 2048 * i);
-        em = absmax_bf16x2(em, absmax_bf16x2(absmax_bf16x2(v.x, v.y), absmax_bf16x2(v.z, v.w)));
+      auto row_ok = [&](int key) { return full || (((mask >> (key / BS)) & 1u) && key0 + key < ctx); };
+      uint32_t E = 0;
+      bool stale = false;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t x = (map0 >> (8 * b)) & 0xFFu;
+        if (row_ok(4 * lane + b)) {
+          stale = stale || x == 0u;
+          E = max(E, x);
+        }
       }
-      em &= 0x7F807F80u;
-      em = __reduce_max_sync(0xffffffffu, max(em & 0xFFFFu, em >> 16));
-      if (lane == 0) ex[(nred & 1) * 4 + (warp - kCvtWarp)] = em;
-      // every converter thread arrives; a phase completes once all four
-      // warps' maxima are written (two slots alternate, so a warp already on
-      // the next tile cannot overwrite the slot a slower one still reads)
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ex_full) : "memory");
-      ok = wait(ex_full, nred & 1);
-      ++nred;
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      {
-        const uint32_t* xr = ex + ((nred - 1) & 1) * 4;
-        const int E = static_cast<int>(max(max(xr[0], xr[1]), max(xr[2], xr[3])) >> 7);
-        // the first tile sets e; later tiles only raise it, when they would
-        // overflow
-        if (jt == 0)
-          e = min(max(E - kVBias, kVMin), kVMax);
-        else if (E - kVBias > e)
-          e = min(E - kVBias, kVMax);
-      }
+      if (stale && warp == kCvtWarp) atomicOr(p.err, kErrStaleMap);
+      E = __reduce_max_sync(0xffffffffu, E);
+      map0 = map1;
+      tab1 = tab2;
+      // the first tile sets e; later tiles only raise it, when they would
+      // overflow
+      const int need = static_cast<int>(E) - kVBias;
+      if (jt == 0)
+        e = min(max(need, kVMin), kVMax);
+      else if (need > e)
+        e = min(need, kVMax);
       const float2 sc = make_float2(pow2i(-e), pow2i(-e));
+      const uint32_t st = smem_addr(smem + kV + s * kKvStage) + 16 * ct;
 #pragma unroll 4
       for (int i = 0; i < 16; ++i) {
         uint4 o = make_uint4(0u, 0u, 0u, 0u);
-        if (row_ok(i)) {
+        if (row_ok((ct >> 3) + 16 * (i & 7))) {
           const uint4 v = lds128(st + 2048 * i);
           o = make_uint4(bf16x2_to_f16x2(v.x, sc), bf16x2_to_f16x2(v.y, sc), bf16x2_to_f16x2(v.z, sc),
                          bf16x2_to_f16x2(v.w, sc));

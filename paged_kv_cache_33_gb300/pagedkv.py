@@ -21,7 +21,8 @@ from . import build as _build
 KV_OK = 0
 STATUS = {0: "KV_OK", 1: "KV_ERR_INVALID_ARG", 2: "KV_ERR_OOM", 3: "KV_ERR_CUDA",
           4: "KV_ERR_UNSUPPORTED", 5: "KV_ERR_BAD_BLOCK_ID", 6: "KV_ERR_TIMEOUT",
-          7: "KV_ERR_BAD_SLOT", 8: "KV_ERR_BAD_CONTEXT", 9: "KV_ERR_DRAIN_TIMEOUT"}
+          7: "KV_ERR_BAD_SLOT", 8: "KV_ERR_BAD_CONTEXT", 9: "KV_ERR_DRAIN_TIMEOUT",
+          10: "KV_ERR_STALE_EXPONENT_MAP"}
 DTYPES = {"bf16": 0, "fp8": 1, "fp4": 2}
 FP4_RECORD_BYTES = 2304  # one 16-token sub-tile of a (block, KV head) in an FP4 pool
 
@@ -62,6 +63,8 @@ def load() -> ctypes.CDLL:
                                          c.POINTER(P)]),
             "kv_pool_destroy": (c.c_int, [P]),
             "kv_pool_info": (c.c_int, [P, c.POINTER(_Desc)]),
+            "kv_pool_exponent_map": (c.c_int, [P, c.POINTER(P), c.POINTER(c.c_int64)]),
+            "kv_pool_refresh_exponent_map": (c.c_int, [P, P]),
             "kv_pool_set_scales": (c.c_int, [P, P, P, P]),
             "paged_kv_write": (c.c_int, [P, P, P, P, c.c_int64, P]),
             "paged_kv_copy_blocks": (c.c_int, [P, P, c.c_int64, P]),
@@ -214,6 +217,26 @@ class KVPool:
                                         "version": 3, "strides": None}
         t = torch.as_tensor(_Buf(), device=f"cuda:{i['device']}")
         return t.view(tdt) if tdt == torch.bfloat16 else t
+
+    def exponent_map(self) -> torch.Tensor | None:
+        """bf16 pools: the V exponent map as a uint8 tensor view
+        [NB, Hkv, BS] (no copy); None for FP8 and FP4 pools."""
+        ptr, n = ctypes.c_void_p(), ctypes.c_int64()
+        _check(load().kv_pool_exponent_map(self.handle, ctypes.byref(ptr), ctypes.byref(n)),
+               "kv_pool_exponent_map")
+        if not ptr.value:
+            return None
+        shape = (self.num_blocks, self.n_kv_heads, self.block_size)
+
+        class _Buf:
+            __cuda_array_interface__ = {"shape": shape, "typestr": "|u1", "data": (ptr.value, False),
+                                        "version": 3, "strides": None}
+        return torch.as_tensor(_Buf(), device=f"cuda:{self.info()['device']}")
+
+    def refresh_exponent_map(self, stream=None) -> None:
+        """Recompute the V exponent map from the pool (after writing V through view())."""
+        _check(load().kv_pool_refresh_exponent_map(self.handle, _stream(stream)),
+               "kv_pool_refresh_exponent_map")
 
     def rows(self) -> torch.Tensor:
         """Inspection: the pool as [NB, Hkv, 2, BS, D] with every V tile in
