@@ -24,10 +24,12 @@
 //    verbatim, one TMA box per block, into a 2-stage ring.  A converter
 //    warpgroup turns each key tile into an f16 K tile (thread = key: its 64
 //    code bytes are four 16-byte rows whose byte c holds dims 8c + 2i, +1 of
-//    row i; 128-byte swizzled, K-major, one stage) and an f16 V tile (thread
-//    = dim: per 16 tokens four code words and four scale words, tokens in
-//    natural order; K-major without swizzle, 2 stages), zeros for tokens
-//    past the sequence's end and for blocks not loaded.
+//    row i; 128-byte swizzled, K-major, one stage), and at the same time two
+//    more warps turn it into an f16 V tile (thread = two dims: per 16 tokens
+//    four code words and four scale words, tokens in natural order; K-major
+//    without swizzle, 2 stages), zeros for tokens past the sequence's end and
+//    for blocks not loaded.  K feeds the S products, which wait on it, so
+//    the converter warpgroup's four warps convert K alone.
 //  * S = Q K^T, O += P V with P one f16 per weight (relative rounding
 //    2^-11); out = O v_scale / l.
 //  * Registers: the two softmax warpgroups take 192 per thread, the others
@@ -51,8 +53,10 @@ constexpr int kSub = 16;             // tokens per FP4 record
 constexpr int kRawStages = 2;        // ring of the records as copied
 constexpr int kV16Stages = 2;        // V ring converted (f16 sub-tiles); K has one f16 stage
 constexpr int kSoftmax = kTiles * kRows;
-constexpr int kRawWarp = kSoftmax / 32, kMmaWarp = kRawWarp + 2;  // warps 9 and 11 idle
-constexpr int kCvtWarp = kRawWarp + 4;       // converter warpgroup
+constexpr int kRawWarp = kSoftmax / 32, kMmaWarp = kRawWarp + 2;
+constexpr int kVCvtWarpA = kRawWarp + 1, kVCvtWarpB = kRawWarp + 3;  // V converters
+constexpr int kVCvt = 64;
+constexpr int kCvtWarp = kRawWarp + 4;       // K converter warpgroup
 constexpr int kCvt = 128;
 constexpr int kThreads = kSoftmax + 128 + kCvt;
 constexpr int kLaunchRegs = 65536 / kThreads;
@@ -176,12 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp4_kernel(
   if (tid == 0) {
     for (int s = 0; s < kRawStages; ++s) {
       mbar_init(raw_full(s), 1);
-      mbar_init(raw_empty(s), kCvt);
+      mbar_init(raw_empty(s), kCvt + kVCvt);
     }
     mbar_init(k16_full, kCvt);
     mbar_init(k16_empty, 1);
     for (int s = 0; s < kV16Stages; ++s) {
-      mbar_init(v16_full(s), kCvt);
+      mbar_init(v16_full(s), kVCvt);
       mbar_init(v16_empty(s), 1);
     }
     for (int t = 0; t < kTiles; ++t) {
@@ -401,15 +405,14 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp4_kernel(
     }
   } else if (warp >= kCvtWarp) {
     warpgroup_regs_dec<kOtherRegs>();
-    // ====== converters: from each stage of records, the f16 K tile (thread
-    // ct = key ct of the tile) and the f16 V tile (thread ct = dim ct)
+    // ====== K converters: from each stage of records, the f16 K tile
+    // (thread ct = key ct of the tile)
     const int ct = tid - kCvtWarp * 32;
     bool ok = true;
     for (int jt = 0; jt < n_tiles && ok; ++jt) {
-      const int sr = jt % kRawStages, s16 = jt % kV16Stages;
+      const int sr = jt % kRawStages;
       ok = wait(raw_full(sr), (jt / kRawStages) & 1);
       if (ok && jt >= 1) ok = wait(k16_empty, (jt - 1) & 1);
-      if (ok && jt >= kV16Stages) ok = wait(v16_empty(s16), ((jt / kV16Stages) - 1) & 1);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       const uint32_t mask = raw_mask[sr];  // the blocks the stage holds (from the producer)
       const int key0 = (jt0 + jt) * kKv;
@@ -455,48 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp4_kernel(
           }
         }
       }
-      // -- V: dim ct of every record; tokens 2k, 2k+1 (word A_k) and 2k+8,
-      // 2k+9 (word B_k) of record st
-      {
-        const int d = ct;
-        uint8_t* dst = smem + kV16 + s16 * kV16Stage + d * 16;
-        const int code_base = 1024 + 16 * ((d >> 6) * 32 + 4 * (d & 7)) + 4 * ((d >> 4) & 3);
-        const int byte0 = 2 * ((d & 15) >> 3);  // byte of tokens (2k, 2k+1); +1: (2k+8, 2k+9)
-        const int scale_base = 2176 + 4 * (d >> 4);
-#pragma unroll 2
-        for (int st = 0; st < kKv / kSub; ++st) {
-          const int nv = ((mask >> ((kSub * st) / BS)) & 1u) ? min(kSub, max(0, ctx - (key0 + kSub * st))) : 0;
-          uint4 a = make_uint4(0u, 0u, 0u, 0u), c = make_uint4(0u, 0u, 0u, 0u);
-          if (nv > 0) {
-            const uint8_t* rec = raw + st * kFp4SubBytes;
-            uint32_t av[4], bv[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint32_t cw = *reinterpret_cast<const uint32_t*>(rec + code_base + 16 * k);
-              const uint32_t sw = *reinterpret_cast<const uint32_t*>(rec + scale_base + 32 * k);
-              uint32_t slo, shi;  // scales of tokens (2k, 2k+1) and (2k+8, 2k+9)
-              e4m3x4_to_f16x2(sw, slo, shi);
-              uint32_t f[4];
-              fp4x8_to_f16x2(cw >> (8 * byte0), f);  // f[0]: tokens 2k, 2k+1; f[1]: 2k+8, 2k+9
-              av[k] = hmul2_bits(f[0], slo);
-              bv[k] = hmul2_bits(f[1], shi);
-            }
-            a = make_uint4(av[0], av[1], av[2], av[3]);
-            c = make_uint4(bv[0], bv[1], bv[2], bv[3]);
-            if (nv < kSub) {
-              a = make_uint4(keep_tokens(a.x, 0, nv), keep_tokens(a.y, 1, nv), keep_tokens(a.z, 2, nv),
-                             keep_tokens(a.w, 3, nv));
-              c = make_uint4(keep_tokens(c.x, 4, nv), keep_tokens(c.y, 5, nv), keep_tokens(c.z, 6, nv),
-                             keep_tokens(c.w, 7, nv));
-            }
-          }
-          *reinterpret_cast<uint4*>(dst + st * kV16Sub) = a;
-          *reinterpret_cast<uint4*>(dst + st * kV16Sub + kV16Sub / 2) = c;
-        }
-      }
       fence_proxy_async_smem();
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(k16_full) : "memory");
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(v16_full(s16)) : "memory");
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(raw_empty(sr)) : "memory");
     }
   } else {
@@ -556,6 +519,61 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_fp4_kernel(
           if (!wait(raw_full(jt % kRawStages), (jt / kRawStages) & 1)) atomicOr(p.err, kErrDrainTimeout);
       }
       __syncwarp();
+    } else if (warp == kVCvtWarpA || warp == kVCvtWarpB) {
+      // ================== V converters: from each stage of records, the f16
+      // V tile (thread vc makes dims vc and vc + 64)
+      const int vc = lane + (warp == kVCvtWarpB ? 32 : 0);
+      bool ok = true;
+      for (int jt = 0; jt < n_tiles && ok; ++jt) {
+        const int sr = jt % kRawStages, s16 = jt % kV16Stages;
+        ok = wait(raw_full(sr), (jt / kRawStages) & 1);
+        if (ok && jt >= kV16Stages) ok = wait(v16_empty(s16), ((jt / kV16Stages) - 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const uint32_t mask = raw_mask[sr];
+        const int key0 = (jt0 + jt) * kKv;
+        const uint8_t* raw = smem + kRaw + sr * kRawStage;
+        // dim d of every record; tokens 2k, 2k+1 (word A_k) and 2k+8, 2k+9
+        // (word B_k) of record st
+        for (int d = vc; d < kD; d += kVCvt) {
+          uint8_t* dst = smem + kV16 + s16 * kV16Stage + d * 16;
+          const int code_base = 1024 + 16 * ((d >> 6) * 32 + 4 * (d & 7)) + 4 * ((d >> 4) & 3);
+          const int byte0 = 2 * ((d & 15) >> 3);  // byte of tokens (2k, 2k+1); +1: (2k+8, 2k+9)
+          const int scale_base = 2176 + 4 * (d >> 4);
+#pragma unroll 2
+          for (int st = 0; st < kKv / kSub; ++st) {
+            const int nv = ((mask >> ((kSub * st) / BS)) & 1u) ? min(kSub, max(0, ctx - (key0 + kSub * st))) : 0;
+            uint4 a = make_uint4(0u, 0u, 0u, 0u), c = make_uint4(0u, 0u, 0u, 0u);
+            if (nv > 0) {
+              const uint8_t* rec = raw + st * kFp4SubBytes;
+              uint32_t av[4], bv[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint32_t cw = *reinterpret_cast<const uint32_t*>(rec + code_base + 16 * k);
+                const uint32_t sw = *reinterpret_cast<const uint32_t*>(rec + scale_base + 32 * k);
+                uint32_t slo, shi;  // scales of tokens (2k, 2k+1) and (2k+8, 2k+9)
+                e4m3x4_to_f16x2(sw, slo, shi);
+                uint32_t f[4];
+                fp4x8_to_f16x2(cw >> (8 * byte0), f);  // f[0]: tokens 2k, 2k+1; f[1]: 2k+8, 2k+9
+                av[k] = hmul2_bits(f[0], slo);
+                bv[k] = hmul2_bits(f[1], shi);
+              }
+              a = make_uint4(av[0], av[1], av[2], av[3]);
+              c = make_uint4(bv[0], bv[1], bv[2], bv[3]);
+              if (nv < kSub) {
+                a = make_uint4(keep_tokens(a.x, 0, nv), keep_tokens(a.y, 1, nv), keep_tokens(a.z, 2, nv),
+                               keep_tokens(a.w, 3, nv));
+                c = make_uint4(keep_tokens(c.x, 4, nv), keep_tokens(c.y, 5, nv), keep_tokens(c.z, 6, nv),
+                               keep_tokens(c.w, 7, nv));
+              }
+            }
+            *reinterpret_cast<uint4*>(dst + st * kV16Sub) = a;
+            *reinterpret_cast<uint4*>(dst + st * kV16Sub + kV16Sub / 2) = c;
+          }
+        }
+        fence_proxy_async_smem();
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(v16_full(s16)) : "memory");
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(raw_empty(sr)) : "memory");
+      }
     } else if (warp == kMmaWarp) {
       // ===================== MMA issuer, in the bf16 kernel's order: per key
       // tile and query tile, P V of the previous key tile, then S
