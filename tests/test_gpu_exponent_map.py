@@ -26,9 +26,9 @@ def _row_exponents(v: torch.Tensor) -> torch.Tensor:
     return torch.clamp((bits >> 7).amax(dim=2), min=1).to(torch.uint8)
 
 
-@pytest.mark.parametrize("bs", [16, 32])
-def test_write_records_row_exponents(bs):
-    nb, hkv, d = 12, 4, 128
+@pytest.mark.parametrize("bs,d", [(16, 128), (32, 128), (16, 64)])
+def test_write_records_row_exponents(bs, d):
+    nb, hkv = 12, 4
     pool = pagedkv.KVPool(nb, bs, hkv, d)
     emap = pool.exponent_map()
     assert emap is not None and tuple(emap.shape) == (nb, hkv, bs)
@@ -54,6 +54,36 @@ def test_write_records_row_exponents(bs):
             want[s // bs, :, s % bs] = ex[t]
     assert torch.equal(got, want)
     assert int(ex[0].max()) == 1 and int(ex[1, 0]) == 255 and int(ex[2, 1]) == 1
+    pool.destroy()
+
+
+def test_decode_step_records_the_new_rows():
+    """The fused decode step writes through the same kernel: its new tokens'
+    rows get their entries too."""
+    nb, hkv, hq, d, B = 8, 2, 8, 128, 3
+    pool = pagedkv.KVPool(nb, 16, hkv, d)
+    g = torch.Generator().manual_seed(9)
+    lens = torch.tensor([5, 17, 30], dtype=torch.int32)
+    tables = torch.tensor([[0, -1], [1, 2], [3, 4]], dtype=torch.int32)
+    T = int(lens.sum())
+    kv = (torch.randn(T, hkv, d, generator=g) * 3).bfloat16()
+    slots = torch.cat([tables[b, torch.arange(int(lens[b]) - 1) // 16].long() * 16
+                       + torch.arange(int(lens[b]) - 1) % 16 for b in range(B)])
+    pagedkv.paged_kv_write(pool, kv[:slots.numel()].cuda(), kv[:slots.numel()].cuda(), slots.cuda())
+    k_new = torch.randn(B, hkv, d, generator=g).bfloat16()
+    v_new = (torch.randn(B, hkv, d, generator=g) * 2.0 ** 12).bfloat16()
+    pos = lens.long() - 1
+    new_slots = tables[torch.arange(B), pos // 16].long() * 16 + pos % 16
+    q = torch.randn(B, hq, d, generator=g).bfloat16()
+    pagedkv.paged_decode_step(pool, k_new.cuda(), v_new.cuda(), new_slots.cuda(), q.cuda(),
+                              tables.cuda(), lens.cuda(), d ** -0.5, 0)
+    torch.cuda.synchronize()
+    assert pool.check_status() == pagedkv.KV_OK
+    emap = pool.exponent_map().cpu()
+    ex = _row_exponents(v_new)
+    for b in range(B):
+        s_ = int(new_slots[b])
+        assert torch.equal(emap[s_ // 16, :, s_ % 16], ex[b])
     pool.destroy()
 
 
