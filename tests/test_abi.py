@@ -77,6 +77,9 @@ def test_null_handles_are_rejected():
     assert L.kv_pool_set_partition_blocks(None, 8) == 1
     assert L.kv_pool_set_wait_limit(None, 1000000) == 1
     assert L.kv_pool_set_test_stall(None, 1) == 1
+    assert L.kv_pool_refresh_exponent_map(None, None) == 1
+    ptr, n = ctypes.c_void_p(), ctypes.c_int64()
+    assert L.kv_pool_exponent_map(None, ctypes.byref(ptr), ctypes.byref(n)) == 1
 
 
 def test_create_without_a_device_fails_cleanly():
@@ -137,6 +140,11 @@ def test_noalloc_binding_requires_out():
 def test_drain_timeout_status_is_named():
     assert pagedkv.STATUS[9] == "KV_ERR_DRAIN_TIMEOUT"
     assert pagedkv.kv_status_str(9) == "KV_ERR_DRAIN_TIMEOUT"
+
+
+def test_stale_exponent_map_status_is_named():
+    assert pagedkv.STATUS[10] == "KV_ERR_STALE_EXPONENT_MAP"
+    assert pagedkv.kv_status_str(10) == "KV_ERR_STALE_EXPONENT_MAP"
 
 
 def test_decode_bindings_marshal_their_arguments(monkeypatch):
